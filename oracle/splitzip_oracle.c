@@ -1,0 +1,349 @@
+/*
+ * splitzip_oracle.c -- plain, slow, single-threaded CPU oracle of the SplitZip
+ * lossless KV-cache format (BF16 and FP8 E5M2).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the parity reference that the CUDA
+ * path is checked against.  Only the test suite, the smoke check and the
+ * bench's CPU-baseline leg may load it.  It shares no code, header, table or
+ * constant generator with the CUDA library; it includes only the C standard
+ * library.
+ *
+ * Sources (the method is described in prose only; no listing is followed):
+ *  [ABS]  SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
+ *         Serving -- authors' abstract (arXiv 2605.01708v2, fugumt.com page).
+ *  [MET]  same paper, technical summary (gist.science/es), section
+ *         "Metodologia: SplitZip", items "Estrategia de Codificacion" and
+ *         "Estrategia de Decodificacion".
+ *  [EXT]  same summary, "Contribuciones Clave", item 4 "Extensibilidad"
+ *         (FP8 E5M2 variant).
+ *  [CAL]  same summary, "Resultados" > "Estudios de Ablacion" > "Calibracion"
+ *         (one offline codebook).
+ *
+ * Readings of points the pages leave open (each one is listed in the design doc):
+ *  R1  sign|mantissa byte = sign << 7 | mantissa (BF16); 3-bit field
+ *      sign << 2 | mantissa (E5M2).
+ *  R2  two 4-bit codes per byte, the even element in the low nibble.
+ *  R3  codes are given in ascending exponent order (code k = k-th smallest
+ *      codebook exponent).
+ *  R4  top-16 ties break toward the smaller exponent; fewer than 16 seen
+ *      exponents are padded with the smallest unseen ones.
+ *  R5  an escaped element gets code 0 in the dense stream.
+ *  R6  escapes are (position, value) pairs stored in element order, 3 bytes
+ *      each: position as a little-endian u16 within its 65,536-element chunk,
+ *      then the raw exponent as a u8.
+ *  R7  one 8-byte header per chunk: u32 offset (escapes in earlier chunks),
+ *      u32 count (escapes in this chunk), little-endian.
+ *  R8  E5M2: 7-bit field = code | sm3 << 4; element j of a group of 8 sits at
+ *      bits 7j..7j+6 of a 56-bit little-endian word written as 7 bytes; a
+ *      short last group is padded with zero fields.
+ *  R9  stream = [dense][codebook 16 B][headers 8 B x C][escapes 3 B x E];
+ *      BF16 dense = [sign|mantissa byte x N][nibble byte x ceil(N/2)];
+ *      E5M2 dense = [7 bytes x ceil(N/8)].  No global header, no padding.
+ *  R10 zero, subnormal, Inf and NaN need no special case: an exponent field
+ *      is just a value.
+ */
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_INVALID_ARG 1
+#define ORC_CAPACITY 3
+#define ORC_CORRUPT 4
+
+#define ORC_BF16 0
+#define ORC_E5M2 1
+
+#define ORC_CHUNK 65536u   /* a u16 position addresses 65,536 elements [MET] */
+#define ORC_CB 16          /* top-16 codebook, 4-bit codes [MET] */
+#define ORC_NO_CODE 0xFFu
+
+static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+static int exponent_bins(int dt) { return dt == ORC_BF16 ? 256 : 32; }
+
+/* ---- element fields ([MET] field split; [EXT] for E5M2) ---------------- */
+
+/* BF16 element i as a 16-bit pattern (little-endian storage). */
+static unsigned bf16_at(const uint8_t *x, uint64_t i) {
+    return (unsigned)x[2 * i] | ((unsigned)x[2 * i + 1] << 8);
+}
+
+/* Exponent field of element i: bits 14..7 for BF16, bits 6..2 for E5M2. */
+static unsigned exponent_at(int dt, const uint8_t *x, uint64_t i) {
+    if (dt == ORC_BF16) return (bf16_at(x, i) >> 7) & 0xFFu;
+    return ((unsigned)x[i] >> 2) & 0x1Fu;
+}
+
+/* ---- sizes (closed form; [MET] + R9) ----------------------------------- */
+
+uint64_t orc_dense_bytes(int dt, uint64_t n) {
+    if (dt == ORC_BF16) return n + ceil_div(n, 2);
+    return 7 * ceil_div(n, 8);
+}
+
+uint64_t orc_num_chunks(uint64_t n) { return ceil_div(n, ORC_CHUNK); }
+
+uint64_t orc_encoded_size(int dt, uint64_t n, uint64_t n_escapes) {
+    return orc_dense_bytes(dt, n) + ORC_CB + 8 * orc_num_chunks(n) + 3 * n_escapes;
+}
+
+/* ---- calibration ([ABS]: offline top-16; [CAL]) ------------------------ */
+
+/* hist[e] = number of elements whose exponent field equals e. */
+void orc_histogram(int dt, const uint8_t *x, uint64_t n, uint64_t *hist) {
+    for (int e = 0; e < exponent_bins(dt); e++) hist[e] = 0;
+    for (uint64_t i = 0; i < n; i++) hist[exponent_at(dt, x, i)]++;
+}
+
+/* Pick the 16 most frequent exponents (R4: ties toward the smaller exponent,
+ * unseen exponents fill up from the smallest), then list them ascending (R3). */
+int orc_codebook_from_histogram(int dt, const uint64_t *hist, uint8_t *cb) {
+    int taken[256];
+    int bins = exponent_bins(dt);
+    for (int e = 0; e < 256; e++) taken[e] = 0;
+    for (int k = 0; k < ORC_CB; k++) {
+        int best = -1;
+        for (int e = 0; e < bins; e++) {
+            if (taken[e]) continue;
+            if (best < 0 || hist[e] > hist[best]) best = e;
+        }
+        taken[best] = 1;
+    }
+    int k = 0;
+    for (int e = 0; e < bins; e++)
+        if (taken[e]) cb[k++] = (uint8_t)e;
+    return ORC_OK;
+}
+
+/* A codebook is 16 distinct exponents that the dtype can hold. */
+int orc_codebook_valid(int dt, const uint8_t *cb) {
+    for (int a = 0; a < ORC_CB; a++) {
+        if ((int)cb[a] >= exponent_bins(dt)) return 0;
+        for (int b = a + 1; b < ORC_CB; b++)
+            if (cb[a] == cb[b]) return 0;
+    }
+    return 1;
+}
+
+/* inv[e] = code of exponent e, or ORC_NO_CODE when e is outside the codebook. */
+static void inverse_codebook(const uint8_t *cb, uint8_t *inv) {
+    for (int e = 0; e < 256; e++) inv[e] = ORC_NO_CODE;
+    for (int k = 0; k < ORC_CB; k++) inv[cb[k]] = (uint8_t)k;
+}
+
+/* Number of elements whose exponent is outside the codebook. */
+uint64_t orc_count_escapes(int dt, const uint8_t *cb, const uint8_t *x, uint64_t n) {
+    uint8_t inv[256];
+    uint64_t count = 0;
+    inverse_codebook(cb, inv);
+    for (uint64_t i = 0; i < n; i++)
+        if (inv[exponent_at(dt, x, i)] == ORC_NO_CODE) count++;
+    return count;
+}
+
+/* ---- little-endian helpers --------------------------------------------- */
+
+static void put_u16(uint8_t *p, unsigned v) {
+    p[0] = (uint8_t)(v & 0xFFu);
+    p[1] = (uint8_t)((v >> 8) & 0xFFu);
+}
+
+static void put_u32(uint8_t *p, uint64_t v) {
+    for (int b = 0; b < 4; b++) p[b] = (uint8_t)((v >> (8 * b)) & 0xFFu);
+}
+
+static unsigned get_u16(const uint8_t *p) { return (unsigned)p[0] | ((unsigned)p[1] << 8); }
+
+static uint64_t get_u32(const uint8_t *p) {
+    uint64_t v = 0;
+    for (int b = 0; b < 4; b++) v |= (uint64_t)p[b] << (8 * b);
+    return v;
+}
+
+/* ---- encode ([MET] Estrategia de Codificacion; [EXT]) ------------------ */
+
+/*
+ * Encode n elements of x (2n bytes for BF16, n bytes for E5M2) with codebook
+ * cb into out (capacity bytes).  On success writes the stream size to
+ * *out_bytes.  If the stream does not fit, nothing is written except
+ * *out_bytes (the size needed) and ORC_CAPACITY is returned.
+ */
+int orc_encode(int dt, const uint8_t *cb, const uint8_t *x, uint64_t n,
+               uint8_t *out, uint64_t capacity, uint64_t *out_bytes) {
+    if (dt != ORC_BF16 && dt != ORC_E5M2) return ORC_INVALID_ARG;
+    if (n >= ((uint64_t)1 << 32)) return ORC_INVALID_ARG;
+    if (!orc_codebook_valid(dt, cb)) return ORC_INVALID_ARG;
+
+    uint8_t inv[256];
+    inverse_codebook(cb, inv);
+
+    uint64_t n_esc = orc_count_escapes(dt, cb, x, n);
+    uint64_t size = orc_encoded_size(dt, n, n_esc);
+    *out_bytes = size;
+    if (size > capacity) return ORC_CAPACITY;
+
+    uint64_t dense = orc_dense_bytes(dt, n);
+    uint64_t chunks = orc_num_chunks(n);
+    uint8_t *cb_out = out + dense;
+    uint8_t *hdr = cb_out + ORC_CB;
+    uint8_t *rec = hdr + 8 * chunks;
+    memset(out, 0, dense);
+
+    /* Step 1: dense stream, element by element, collecting escapes in order. */
+    uint64_t j = 0; /* escapes written so far */
+    for (uint64_t i = 0; i < n; i++) {
+        unsigned e = exponent_at(dt, x, i);
+        unsigned code = inv[e];
+        if (code == ORC_NO_CODE) {
+            /* Escape: keep position within the chunk and the raw exponent (R6);
+             * the dense stream gets code 0 (R5). */
+            put_u16(rec + 3 * j, (unsigned)(i % ORC_CHUNK));
+            rec[3 * j + 2] = (uint8_t)e;
+            j++;
+            code = 0;
+        }
+        if (dt == ORC_BF16) {
+            unsigned v = bf16_at(x, i);
+            unsigned sign = (v >> 15) & 1u;
+            unsigned mant = v & 0x7Fu;
+            out[i] = (uint8_t)((sign << 7) | mant);          /* R1 */
+            out[n + i / 2] |= (uint8_t)(code << (4 * (i % 2))); /* R2 */
+        } else {
+            unsigned v = x[i];
+            unsigned sign = (v >> 7) & 1u;
+            unsigned mant = v & 0x3u;
+            unsigned field = code | (((sign << 2) | mant) << 4); /* R1, R8 */
+            uint64_t g = i / 8;
+            unsigned bit = 7 * (unsigned)(i % 8);
+            /* Field j of the group occupies bits 7j..7j+6 of the group's
+             * 56-bit little-endian word: spread it over the bytes it touches. */
+            for (unsigned b = 0; b < 7; b++) {
+                unsigned lo = 8 * b;
+                if (bit + 7 <= lo || bit >= lo + 8) continue;
+                if (bit >= lo)
+                    out[7 * g + b] |= (uint8_t)((field << (bit - lo)) & 0xFFu);
+                else
+                    out[7 * g + b] |= (uint8_t)((field >> (lo - bit)) & 0xFFu);
+            }
+        }
+    }
+
+    /* Step 2: codebook, then per-chunk headers (R7). */
+    memcpy(cb_out, cb, ORC_CB);
+    uint64_t offset = 0;
+    for (uint64_t c = 0; c < chunks; c++) {
+        uint64_t lo = c * ORC_CHUNK;
+        uint64_t hi = lo + ORC_CHUNK < n ? lo + ORC_CHUNK : n;
+        uint64_t count = 0;
+        for (uint64_t i = lo; i < hi; i++)
+            if (inv[exponent_at(dt, x, i)] == ORC_NO_CODE) count++;
+        put_u32(hdr + 8 * c, offset);
+        put_u32(hdr + 8 * c + 4, count);
+        offset += count;
+    }
+    return ORC_OK;
+}
+
+/* ---- validation --------------------------------------------------------- */
+
+/*
+ * Check that `in` (in_bytes) is a well-formed stream for n elements: the size
+ * matches the closed form for some escape count E, the codebook is valid, the
+ * header offsets are the running sum of the counts and end at E, every chunk
+ * count fits its chunk, and positions are strictly increasing inside a chunk
+ * and below the chunk's length; E5M2 escape exponents must fit 5 bits.
+ * Returns ORC_OK (and E in *n_escapes) or ORC_CORRUPT.
+ */
+int orc_validate(int dt, const uint8_t *in, uint64_t in_bytes, uint64_t n, uint64_t *n_escapes) {
+    if (dt != ORC_BF16 && dt != ORC_E5M2) return ORC_INVALID_ARG;
+    if (n >= ((uint64_t)1 << 32)) return ORC_INVALID_ARG;
+    uint64_t fixed = orc_encoded_size(dt, n, 0);
+    if (in_bytes < fixed || (in_bytes - fixed) % 3 != 0) return ORC_CORRUPT;
+    uint64_t n_esc = (in_bytes - fixed) / 3;
+
+    uint64_t dense = orc_dense_bytes(dt, n);
+    uint64_t chunks = orc_num_chunks(n);
+    const uint8_t *cb = in + dense;
+    const uint8_t *hdr = cb + ORC_CB;
+    const uint8_t *rec = hdr + 8 * chunks;
+    if (!orc_codebook_valid(dt, cb)) return ORC_CORRUPT;
+
+    uint64_t running = 0;
+    for (uint64_t c = 0; c < chunks; c++) {
+        uint64_t offset = get_u32(hdr + 8 * c);
+        uint64_t count = get_u32(hdr + 8 * c + 4);
+        uint64_t lo = c * ORC_CHUNK;
+        uint64_t len = (lo + ORC_CHUNK < n ? lo + ORC_CHUNK : n) - lo;
+        if (offset != running || count > len || running + count > n_esc) return ORC_CORRUPT;
+        for (uint64_t k = 0; k < count; k++) {
+            unsigned pos = get_u16(rec + 3 * (offset + k));
+            if (pos >= len) return ORC_CORRUPT;
+            if (k > 0 && pos <= get_u16(rec + 3 * (offset + k - 1))) return ORC_CORRUPT;
+            if (dt == ORC_E5M2 && rec[3 * (offset + k) + 2] >= 32) return ORC_CORRUPT;
+        }
+        running += count;
+    }
+    if (running != n_esc) return ORC_CORRUPT;
+    *n_escapes = n_esc;
+    return ORC_OK;
+}
+
+/* ---- decode ([MET] Estrategia de Decodificacion) ------------------------ */
+
+/*
+ * Decode a stream into y (2n bytes for BF16, n bytes for E5M2): validate,
+ * then the dense pass (code -> exponent through the codebook, joined with
+ * the stored sign and mantissa), then overwrite every escaped element's
+ * exponent with its raw value.
+ */
+int orc_decode(int dt, const uint8_t *in, uint64_t in_bytes, uint64_t n, uint8_t *y) {
+    uint64_t n_esc = 0;
+    int st = orc_validate(dt, in, in_bytes, n, &n_esc);
+    if (st != ORC_OK) return st;
+
+    uint64_t dense = orc_dense_bytes(dt, n);
+    uint64_t chunks = orc_num_chunks(n);
+    const uint8_t *cb = in + dense;
+    const uint8_t *hdr = cb + ORC_CB;
+    const uint8_t *rec = hdr + 8 * chunks;
+
+    /* Dense pass. */
+    for (uint64_t i = 0; i < n; i++) {
+        if (dt == ORC_BF16) {
+            unsigned sm = in[i];
+            unsigned code = (in[n + i / 2] >> (4 * (i % 2))) & 0xFu;
+            unsigned v = ((sm >> 7) << 15) | ((unsigned)cb[code] << 7) | (sm & 0x7Fu);
+            y[2 * i] = (uint8_t)(v & 0xFFu);
+            y[2 * i + 1] = (uint8_t)(v >> 8);
+        } else {
+            uint64_t g = i / 8;
+            unsigned bit = 7 * (unsigned)(i % 8);
+            uint64_t word = 0;
+            for (unsigned b = 0; b < 7; b++) word |= (uint64_t)in[7 * g + b] << (8 * b);
+            unsigned field = (unsigned)((word >> bit) & 0x7Fu);
+            unsigned code = field & 0xFu;
+            unsigned sm3 = field >> 4;
+            y[i] = (uint8_t)(((sm3 >> 2) << 7) | ((unsigned)cb[code] << 2) | (sm3 & 0x3u));
+        }
+    }
+
+    /* Escape overwrite: put back the raw exponent of every escaped element. */
+    for (uint64_t c = 0; c < chunks; c++) {
+        uint64_t offset = get_u32(hdr + 8 * c);
+        uint64_t count = get_u32(hdr + 8 * c + 4);
+        for (uint64_t k = 0; k < count; k++) {
+            uint64_t i = c * ORC_CHUNK + get_u16(rec + 3 * (offset + k));
+            unsigned e = rec[3 * (offset + k) + 2];
+            if (dt == ORC_BF16) {
+                unsigned v = (unsigned)y[2 * i] | ((unsigned)y[2 * i + 1] << 8);
+                v = (v & 0x807Fu) | (e << 7);
+                y[2 * i] = (uint8_t)(v & 0xFFu);
+                y[2 * i + 1] = (uint8_t)(v >> 8);
+            } else {
+                y[i] = (uint8_t)((y[i] & 0x83u) | (e << 2));
+            }
+        }
+    }
+    return ORC_OK;
+}
