@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""SplitZip codec bench: encode + decode throughput on GB300.
+
+One step = one pass of the whole hot path over one batch: sz_encode of the
+workload tensor (split, code, pack, ordered escape compaction), then
+sz_decode of the stream (dense LUT pass + escape overwrite).  The default
+workload is the Llama-3-8B-shaped BF16 prefill KV cache [32, 2, 8192, 8, 128]
+(1.07 GB).  Throughput is uncompressed bytes / time.  Inputs (1.07 GB) are
+larger than L2 (129 MB), so no L2 flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host instead.  For N > 1 (torchrun), every rank runs its own copy of the
+workload on its own GPU (independent shards, no data-path collective: weak
+scaling); a barrier and a max-over-ranks of the elapsed time bracket the
+timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "encode / decode GB/s (uncompressed) on 1 GB300, % of codec HBM roofline, ratio"
+UNIT = "GB/s"
+LINKS_GBS = (50.0, 100.0)   # inter-node links of the pages' transfer setting
+PAPER_ENCODE_GBS = 613.3    # pages' encode throughput (hardware not named): context only
+PAPER_DECODE_GBS = 2181.8
+
+KERNEL_SOURCES = {
+    "encode_bf16_kernel": ["sz_bf16.cu", "sz_device.cuh", "sz_params.h"],
+    "decode_bf16_kernel": ["sz_bf16.cu", "sz_device.cuh", "sz_params.h"],
+    "encode_e5m2_kernel": ["sz_e5m2.cu", "sz_device.cuh", "sz_params.h"],
+    "decode_e5m2_kernel": ["sz_e5m2.cu", "sz_device.cuh", "sz_params.h"],
+}
+
+
+# ---- host-side helpers (no GPU needed; covered by CPU tests) -------------------
+
+def kernel_source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "lossless_kv_cache_bf16_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if there is
+    none or the kernel's source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            k, sep, v = line.partition(":")
+            if sep:
+                fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256_16") != kernel_source_hash(kernel):
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def link_model(n_bytes: int, stream_bytes: int, t_enc_s: float, t_dec_s: float):
+    """Modelled transfer over a link of L GB/s: raw = bytes / L; with the codec
+    = encode + stream / L + decode."""
+    out = {}
+    for L in LINKS_GBS:
+        raw = n_bytes / (L * 1e9)
+        coded = t_enc_s + stream_bytes / (L * 1e9) + t_dec_s
+        out[f"{int(L)}GBps"] = {"raw_ms": raw * 1e3, "splitzip_ms": coded * 1e3, "speedup": raw / coded}
+    return out
+
+
+def gather_elapsed(dist, elapsed_s: float, device) -> list[float]:
+    """Every rank's elapsed time (for the max-over-ranks); [elapsed] alone
+    without a process group."""
+    if dist is None:
+        return [elapsed_s]
+    import torch
+
+    parts = [torch.zeros(1, dtype=torch.float64, device=device) for _ in range(dist.get_world_size())]
+    dist.all_gather(parts, torch.tensor([elapsed_s], dtype=torch.float64, device=device))
+    return [float(t.item()) for t in parts]
+
+
+def aggregate(bytes_per_rank: int, elapsed_per_rank_s: list[float]):
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    t = max(elapsed_per_rank_s)
+    return len(elapsed_per_rank_s) * bytes_per_rank / t / 1e9, t
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [[c.strip() for c in line.split(",")] for line in out.splitlines() if line.count(",") >= 7]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        loaded = [s for s in sm if s > 0]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- the reference arm: the CPU oracle ------------------------------------------
+
+def time_oracle(orc, dt_oracle, cb, xb, n):
+    t0 = time.perf_counter()
+    s = orc.encode(dt_oracle, cb, xb)
+    t1 = time.perf_counter()
+    st, y = orc.decode(dt_oracle, s, n)
+    t2 = time.perf_counter()
+    assert st == 0
+    return t1 - t0, t2 - t1, s.size
+
+
+# ---- main ------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["splitzip", "reference"], default="splitzip")
+    ap.add_argument("--config", default="llama8b_prefill",
+                    choices=["llama8b_prefill", "long_ctx_gqa", "fp8_e5m2", "escape_sweep", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    import numpy as np
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+
+    from lossless_kv_cache_bf16_gb300 import workloads as W
+
+    cfg = W.CONFIGS[args.config]
+    is_bf16 = cfg.dtype == "bf16"
+    elem_bytes = 2 if is_bf16 else 1
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        from oracle import oracle as O
+
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        x = W.workload(args.config, dev)
+        sample = W.calibration_sample(args.config, dev, full=x)
+        odt = O.BF16 if is_bf16 else O.E5M2
+        orc = O.default()
+        cb = orc.calibrate(odt, sample.contiguous().view(torch.uint8).reshape(-1).cpu().numpy())
+        # Bounded per-step sample: about 30 s for the whole run at ~0.3 GB/s.
+        budget = int(30 * 0.3e9 / (args.steps + args.warmup))
+        n_s = max(65536, min(cfg.numel, budget // elem_bytes))
+        n_s -= n_s % 65536 if n_s > 65536 else 0
+        xb = x.reshape(-1)[:n_s].contiguous().view(torch.uint8).cpu().numpy()
+        del x
+        for _ in range(args.warmup):
+            time_oracle(orc, odt, cb, xb, n_s)
+        t = 0.0
+        for _ in range(args.steps):
+            te, td, _ = time_oracle(orc, odt, cb, xb, n_s)
+            t += te + td
+        value = args.steps * n_s * elem_bytes / t / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+                "data": "synthetic", "config": {"workload": args.config, "elements_per_step": n_s},
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": f"first {n_s} elements of {args.config} per step (encode + decode)"},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    from lossless_kv_cache_bf16_gb300 import build as B
+
+    B.build()
+    from lossless_kv_cache_bf16_gb300 import splitzip as S
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dt = S.SZ_BF16 if is_bf16 else S.SZ_FP8_E5M2
+    stream = torch.cuda.current_stream()
+
+    x = W.workload(args.config, dev)
+    sample = W.calibration_sample(args.config, dev, full=x)
+    hist = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device=dev)
+    cb = S.sz_calibrate(dt, sample, hist)
+    del sample
+    n = x.numel()
+    n_bytes = n * elem_bytes
+    cap = S.sz_encoded_size(dt, n, n)
+    out = torch.empty(cap, dtype=torch.uint8, device=dev)
+    ws = torch.empty(S.sz_workspace_size(dt, n), dtype=torch.uint8, device=dev)
+    ob = torch.zeros(1, dtype=torch.int64, device=dev)
+    est = torch.zeros(1, dtype=torch.int32, device=dev)
+    dst = torch.zeros(1, dtype=torch.int32, device=dev)
+    y = torch.empty_like(x)
+
+    def encode():
+        S.sz_encode(dt, cb, x, out, ob, est, ws)
+
+    def decode(size):
+        S.sz_decode(dt, out, size, n, y, dst)
+
+    # Size of the stream (fixed for a given input), then check the round trip.
+    encode()
+    torch.cuda.synchronize()
+    size = int(ob.item())
+    decode(size)
+    torch.cuda.synchronize()
+    assert int(est.item()) == 0 and int(dst.item()) == 0, "codec reported an error"
+    assert torch.equal(y.view(torch.uint8), x.view(torch.uint8)), "round trip is not bit-exact"
+    n_esc = (size - S.sz_encoded_size(dt, n, 0)) // 3
+
+    for _ in range(args.warmup):
+        encode()
+        decode(size)
+    # Keep the GPU busy for a moment so the clock sampler sees it under load.
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    t_end = time.time() + 0.6
+    while time.time() < t_end:
+        encode()
+        decode(size)
+        torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        encode()
+        e1.record(stream)
+        decode(size)
+        e2.record(stream)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed = t_start.elapsed_time(t_stop) / 1e3
+    t_enc = [a.elapsed_time(b) / 1e3 for a, b, _ in ev]
+    t_dec = [b.elapsed_time(c) / 1e3 for _, b, c in ev]
+    assert int(est.item()) == 0 and int(dst.item()) == 0
+
+    value, t_max = aggregate(K * n_bytes, gather_elapsed(dist, elapsed, dev))
+
+    # End to end through the C ABI with host buffers: pinned H2D of the input,
+    # encode, decode, D2H of the decoded tensor, every step.
+    xh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
+    xh.copy_(x.view(torch.uint8).reshape(-1))
+    yh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
+    xv = x.view(torch.uint8).reshape(-1)
+    yv = y.view(torch.uint8).reshape(-1)
+    for _ in range(2):
+        xv.copy_(xh, non_blocking=True)
+        encode()
+        decode(size)
+        yh.copy_(yv, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_a.record(stream)
+    for _ in range(args.e2e_steps):
+        xv.copy_(xh, non_blocking=True)
+        encode()
+        decode(size)
+        yh.copy_(yv, non_blocking=True)
+    e_b.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = e_a.elapsed_time(e_b) / 1e3
+    e2e_value, _ = aggregate(args.e2e_steps * n_bytes, gather_elapsed(dist, e2e_t, dev))
+    assert torch.equal(yh, xh), "end-to-end round trip is not bit-exact"
+
+    # Device-to-device copy bandwidth in the same run (bytes = read + write).
+    a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        b.copy_(a)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(10):
+        b.copy_(a)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    memcpy_gbs = 2 * a.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
+    del a, b
+
+    te, td = statistics.mean(t_enc), statistics.mean(t_dec)
+    enc_gbs, dec_gbs = n_bytes / te / 1e9, n_bytes / td / 1e9
+    peak, peak_src = measured_peaks()
+    moved = n_bytes + size
+    suffix = "bf16" if is_bf16 else "e5m2"
+    kernels = {f"encode_{suffix}_kernel": te, f"decode_{suffix}_kernel": td}
+    dominant = max(kernels, key=kernels.get)
+    achieved = moved / kernels[dominant] / 1e9
+    traffic = profiled_traffic(dominant, args.config)
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "algorithmic_bytes_per_launch": moved}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import oracle as O
+
+        orc = O.default()
+        odt = O.BF16 if is_bf16 else O.E5M2
+        xb = x.view(torch.uint8).reshape(-1).cpu().numpy()
+        tenc, tdec, osize = time_oracle(orc, odt, np.array(cb, dtype=np.uint8), xb, n)
+        assert osize == size
+        cpu = {"value": n_bytes / (tenc + tdec) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the whole {args.config} tensor ({n_bytes} bytes), one encode + one decode",
+               "encode_gbs": n_bytes / tenc / 1e9, "decode_gbs": n_bytes / tdec / 1e9}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": t_max / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8" if not is_bf16 else "u16", "data": "synthetic",
+        "config": {"workload": args.config, "elements": n, "input_bytes": n_bytes,
+                   "step": "one sz_encode + one sz_decode of the whole tensor",
+                   "l2": "inputs larger than L2 (129 MB); no flush", "parallelism": f"{world} independent shards"},
+        "encode_gbs": enc_gbs, "decode_gbs": dec_gbs,
+        "encode_frac_of_codec_roofline": (n_bytes + size) / te / 1e9 / peak,
+        "decode_frac_of_codec_roofline": (n_bytes + size) / td / 1e9 / peak,
+        "codec_roofline_gbs": peak * n_bytes / (n_bytes + size),
+        "ratio": n_bytes / size, "escape_rate": n_esc / n, "stream_bytes": size,
+        "memcpy_d2d_gbs": memcpy_gbs, "spec_hbm_gbs": 8000.0,
+        "link_model": link_model(n_bytes, size, te, td),
+        "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
+                          "hardware": "not named on the pages"},
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": n_bytes, "d2h_bytes_per_step": n_bytes,
+                "steps": args.e2e_steps},
+        "gpu_launches": 2 * K, "clocks": clocks,
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,176 @@
+/*
+ * splitzip.h -- C ABI of the SplitZip lossless KV-cache codec for GB300 (sm_103a).
+ *
+ * Method: "SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
+ * Serving" (arXiv 2605.01708v2).  Citations below name the page and section:
+ *   [ABS] authors' abstract (fugumt.com page for arXiv 2605.01708v2);
+ *   [MET] technical summary (gist.science/es), "Metodologia: SplitZip",
+ *         items "Estrategia de Codificacion" / "Estrategia de Decodificacion";
+ *   [EXT] same summary, "Contribuciones Clave", item 4 "Extensibilidad";
+ *   [CAL] same summary, "Resultados" > "Estudios de Ablacion" > "Calibracion".
+ *
+ * What the codec does ([ABS], [MET]): each element is split into its sign and
+ * mantissa bits, stored raw, and its exponent.  An offline-calibrated top-16
+ * codebook maps the exponent to a 4-bit code.  An exponent outside the
+ * codebook is an escape: its element gets code 0 in the dense stream and a
+ * (position, raw exponent) record in a sparse escape stream.  Decode rebuilds
+ * every element from the dense stream, then overwrites the escaped exponents,
+ * which restores the input bit for bit.  FP8 E5M2 works the same way with a
+ * 3-bit sign|mantissa field ([EXT]).
+ *
+ * Encoded stream (all multi-byte integers little-endian, no padding):
+ *   BF16 : [sm u8 x N][nib u8 x ceil(N/2)][cb u8 x 16][hdr x C][esc x E]
+ *   E5M2 : [packed u8 x 7*ceil(N/8)]      [cb u8 x 16][hdr x C][esc x E]
+ *   sm   = sign << 7 | 7-bit mantissa (BF16)
+ *   nib  = code(2k) | code(2k+1) << 4; the unused high nibble of an odd N is 0
+ *   E5M2 = per element a 7-bit field code | (sign << 2 | mantissa) << 4; field j
+ *          of each group of 8 sits at bits 7j..7j+6 of a 56-bit little-endian
+ *          word written as 7 bytes; a short last group is padded with zeros
+ *   cb   = the 16 codebook exponents in ascending order; code k = cb[k]
+ *   C    = ceil(N / 65536) chunks; hdr = { u32 offset, u32 count }: offset =
+ *          escapes in earlier chunks, count = escapes in this chunk
+ *   esc  = 3 bytes per escape, in element order: u16 position inside the
+ *          65,536-element chunk, then the raw exponent (u8)
+ *   size = N + ceil(N/2) + 3E + 16 + 8C (BF16);  7*ceil(N/8) + 3E + 16 + 8C (E5M2)
+ *
+ * Conventions for every call:
+ *  - Pointers named d_* are device pointers, h_* host pointers.  The caller
+ *    owns every buffer; the library allocates no memory and keeps no state
+ *    between calls, so calls on different streams with different buffers may
+ *    run concurrently.
+ *  - Element data needs only its natural alignment (2 bytes for BF16); the
+ *    kernels take a vectorised path when the buffers are 16-byte aligned and
+ *    N is a multiple of 32, and a byte-exact slower path otherwise.
+ *  - Calls are asynchronous on `stream` unless stated otherwise.  Argument
+ *    errors that the host can see are returned at once and nothing is
+ *    launched.  Errors that depend on device data are written to *d_status
+ *    (a device int, nullable) when the kernels finish; no kernel traps.
+ *  - N must be below 2^32 (headers hold u32 escape offsets).
+ */
+#ifndef SPLITZIP_H
+#define SPLITZIP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SZ_CHUNK_ELEMS 65536u /* elements addressed by a u16 escape position */
+#define SZ_CODEBOOK_SIZE 16   /* top-16 exponent codebook, 4-bit codes */
+
+typedef enum sz_status {
+    SZ_OK = 0,
+    SZ_ERR_INVALID_ARG = 1, /* null pointer, bad dtype, N >= 2^32, bad codebook, misaligned element data */
+    SZ_ERR_UNSUPPORTED = 2, /* no usable CUDA device for this build (needs sm_103) */
+    SZ_ERR_CAPACITY = 3,    /* output or workspace too small */
+    SZ_ERR_CORRUPT = 4,     /* encoded stream fails validation */
+    SZ_ERR_TIMEOUT = 5,     /* a bounded inter-block wait in encode gave up */
+    SZ_ERR_CUDA = 6         /* a CUDA runtime call failed */
+} sz_status;
+
+typedef enum sz_dtype {
+    SZ_BF16 = 0,     /* bfloat16: 1 sign, 8 exponent, 7 mantissa bits [MET] */
+    SZ_FP8_E5M2 = 1  /* float8 E5M2: 1 sign, 5 exponent, 2 mantissa bits [EXT] */
+} sz_dtype;
+
+/* The top-16 exponent codebook ([ABS], [MET] "Codificacion de Longitud
+ * Fija"): exp[k] is the exponent that code k stands for.  Entries must be
+ * distinct and below 256 (BF16) or 32 (E5M2).  Encode accepts them in any
+ * order and writes them to the stream in ascending order, so code k is the
+ * k-th smallest exponent. */
+typedef struct sz_codebook {
+    uint8_t exp[SZ_CODEBOOK_SIZE];
+} sz_codebook;
+
+/* Size in bytes of the stream for n elements with n_escapes escapes (the
+ * closed form above; [MET] "Codificacion de Longitud Fija", "Flujo de
+ * Escape").  sz_encoded_size(dt, n, n) bounds every stream of n elements.
+ * Host only; returns 0 for an unknown dtype. */
+size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes);
+
+/* Bytes of device workspace that sz_encode needs for n elements: one status
+ * word per tile for the ordered escape compaction plus a tile counter.  The
+ * workspace is scratch: its contents on entry do not matter (sz_encode
+ * clears what it uses), and it must not be shared by encodes that can run at
+ * the same time.  Host only; returns 0 for an unknown dtype. */
+size_t sz_workspace_size(sz_dtype dt, size_t n);
+
+/* Number of exponent bins: 256 (BF16) or 32 (E5M2); 0 for an unknown dtype. */
+size_t sz_histogram_bins(sz_dtype dt);
+
+/* Exponent histogram of a calibration sample ([ABS]: offline calibration;
+ * [CAL]).  d_sample: n elements of dtype dt.  d_hist: caller-owned device
+ * array of sz_histogram_bins(dt) uint64 counts, overwritten (the call clears
+ * it first).  Asynchronous. */
+sz_status sz_histogram(sz_dtype dt, const void* d_sample, size_t n,
+                       unsigned long long* d_hist, cudaStream_t stream);
+
+/* Top-16 selection on the host ([ABS], [MET]): the 16 exponents with the
+ * largest counts; equal counts go to the smaller exponent; when fewer than 16
+ * exponents occur, the smallest unseen exponents fill the rest.  Writes them in
+ * ascending order.  h_hist holds sz_histogram_bins(dt) counts. */
+sz_status sz_codebook_from_histogram(sz_dtype dt, const unsigned long long* h_hist,
+                                     sz_codebook* h_cb);
+
+/* Offline calibration = sz_histogram, a device-to-host copy of the counts,
+ * and sz_codebook_from_histogram.  Synchronises `stream` (the only call that
+ * does).  d_hist is the same caller-owned scratch as for sz_histogram. */
+sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n,
+                       unsigned long long* d_hist, sz_codebook* h_cb,
+                       cudaStream_t stream);
+
+/* Encode ([MET] "Estrategia de Codificacion"; [EXT] for E5M2).
+ *  h_cb          codebook (host), read during the call only
+ *  d_in          n elements of dtype dt (device)
+ *  d_out         stream buffer (device) of out_capacity bytes; must hold at
+ *                least sz_encoded_size(dt, n, 0) bytes.  When the escapes do
+ *                not fit, *d_status becomes SZ_ERR_CAPACITY and the stream is
+ *                incomplete; sz_encoded_size(dt, n, n) always suffices
+ *  d_out_bytes   device u64, receives the stream size (also on
+ *                SZ_ERR_CAPACITY, where it is the size that was needed)
+ *  d_status      device int or NULL: SZ_OK, SZ_ERR_CAPACITY or SZ_ERR_TIMEOUT
+ *  d_ws          device workspace of ws_bytes >= sz_workspace_size(dt, n)
+ * Asynchronous; the stream is byte-for-byte the layout above. */
+sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n,
+                    void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
+                    int* d_status, void* d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Decode ([MET] "Estrategia de Decodificacion"): dense LUT pass, then the
+ * escape overwrite.
+ *  d_in, in_bytes  the stream (device); in_bytes must match the closed form
+ *                  for n and some escape count, else SZ_ERR_CORRUPT is
+ *                  returned at once
+ *  n               element count (the decoder knows the tensor's shape)
+ *  d_out           n elements of dtype dt (device)
+ *  d_status        device int or NULL: SZ_OK or SZ_ERR_CORRUPT (bad codebook,
+ *                  headers that are not a running sum, a position outside its
+ *                  chunk or out of order, an E5M2 exponent above 31).  On
+ *                  SZ_ERR_CORRUPT the contents of d_out are unspecified, but
+ *                  nothing outside d_out[0, n) is written.
+ * Asynchronous. */
+sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n,
+                    void* d_out, int* d_status, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* sz_status_string(int status);
+
+/* Testing hook, not for production use: sz_encode, except that the tile
+ * counter starts at 1, so tile 0 is never processed and its successors'
+ * bounded wait for its escape count runs out after wait_limit_ns.  Lets a
+ * test check that the wait ends with SZ_ERR_TIMEOUT in *d_status instead of
+ * hanging.  d_status must not be NULL. */
+sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const void* d_in,
+                                  size_t n, void* d_out, size_t out_capacity,
+                                  unsigned long long* d_out_bytes, int* d_status,
+                                  void* d_ws, size_t ws_bytes,
+                                  unsigned long long wait_limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPLITZIP_H */

@@ -1,0 +1,214 @@
+// sz_api.cu -- the C ABI of splitzip.h: argument checks, stream layout and
+// kernel launches.  Host code only; the kernels live in sz_bf16.cu,
+// sz_e5m2.cu and sz_histogram.cu.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "splitzip.h"
+#include "sz_params.h"
+
+namespace {
+
+using namespace sz;
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded inter-block waits: 1 s
+
+bool dtype_ok(int dt) { return dt == SZ_BF16 || dt == SZ_FP8_E5M2; }
+uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+uint64_t dense_bytes(sz_dtype dt, uint64_t n) { return dt == SZ_BF16 ? n + cdiv(n, 2) : 7 * cdiv(n, 8); }
+uint64_t tile_elems(sz_dtype dt) { return dt == SZ_BF16 ? kBf16Tile : kE5Tile; }
+uint64_t tiles_for(sz_dtype dt, uint64_t n) { return std::max<uint64_t>(1, cdiv(n, tile_elems(dt))); }
+uint64_t workspace_bytes(sz_dtype dt, uint64_t n) { return 16 + 8 * tiles_for(dt, n); }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+StreamLayout layout_for(sz_dtype dt, uint64_t n) {
+    StreamLayout L{};
+    L.n = n;
+    L.dense = dense_bytes(dt, n);
+    L.nib_off = dt == SZ_BF16 ? n : 0;
+    L.cb_off = L.dense;
+    L.num_chunks = (uint32_t)cdiv(n, SZ_CHUNK_ELEMS);
+    L.hdr_off = L.cb_off + SZ_CODEBOOK_SIZE;
+    L.rec_off = L.hdr_off + 8ull * L.num_chunks;
+    return L;
+}
+
+sz_status from_cuda(cudaError_t e) {
+    switch (e) {
+        case cudaSuccess:
+            return SZ_OK;
+        case cudaErrorNoKernelImageForDevice:
+        case cudaErrorNoDevice:
+        case cudaErrorInsufficientDriver:
+            return SZ_ERR_UNSUPPORTED;
+        default:
+            return SZ_ERR_CUDA;
+    }
+}
+
+// 16 distinct exponents that the dtype can hold.
+bool codebook_ok(sz_dtype dt, const uint8_t* cb) {
+    const unsigned limit = dt == SZ_BF16 ? 256u : 32u;
+    bool seen[256] = {};
+    for (int k = 0; k < SZ_CODEBOOK_SIZE; k++) {
+        if (cb[k] >= limit || seen[cb[k]]) return false;
+        seen[cb[k]] = true;
+    }
+    return true;
+}
+
+sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
+                      size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
+                      size_t ws_bytes, uint32_t first_ticket, uint64_t wait_ns, cudaStream_t stream) {
+    if (!dtype_ok(dt) || !h_cb || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
+    if ((n > 0 && !d_in) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
+    if (dt == SZ_BF16 && !aligned(d_in, 2)) return SZ_ERR_INVALID_ARG;
+    if (!aligned(d_ws, 16) || !aligned(d_out_bytes, 8) || (d_status && !aligned(d_status, 4))) return SZ_ERR_INVALID_ARG;
+    if (!codebook_ok(dt, h_cb->exp)) return SZ_ERR_INVALID_ARG;
+    if (out_capacity < sz_encoded_size(dt, n, 0)) return SZ_ERR_CAPACITY;
+    const uint64_t ws_need = workspace_bytes(dt, n);
+    if (ws_bytes < ws_need) return SZ_ERR_CAPACITY;
+
+    EncodeParams p{};
+    p.L = layout_for(dt, n);
+    p.in = static_cast<const uint8_t*>(d_in);
+    p.out = static_cast<uint8_t*>(d_out);
+    p.capacity = out_capacity;
+    p.num_tiles = (uint32_t)tiles_for(dt, n);
+    p.ticket = static_cast<uint32_t*>(d_ws);
+    p.tile_status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(d_ws) + 16);
+    p.out_bytes = d_out_bytes;
+    p.status = d_status;
+    p.wait_limit_ns = wait_ns;
+    std::memcpy(p.cb, h_cb->exp, SZ_CODEBOOK_SIZE);
+    std::sort(p.cb, p.cb + SZ_CODEBOOK_SIZE);  // code k = k-th smallest exponent
+    if (dt == SZ_BF16)
+        p.vec = aligned(d_in, 16) && aligned(d_out, 8) && aligned(static_cast<uint8_t*>(d_out) + n, 4);
+    else
+        p.vec = aligned(d_in, 16) && aligned(d_out, 16);
+
+    cudaError_t err = cudaMemsetAsync(d_ws, 0, ws_need, stream);
+    if (err == cudaSuccess && first_ticket) err = cudaMemsetAsync(d_ws, (int)first_ticket, 1, stream);
+    if (err == cudaSuccess && d_status) err = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
+    if (err != cudaSuccess) return from_cuda(err);
+    err = dt == SZ_BF16 ? launch_encode_bf16(p, stream) : launch_encode_e5m2(p, stream);
+    return from_cuda(err);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes) {
+    if (!dtype_ok(dt)) return 0;
+    return dense_bytes(dt, n) + SZ_CODEBOOK_SIZE + 8 * cdiv(n, SZ_CHUNK_ELEMS) + 3 * (uint64_t)n_escapes;
+}
+
+size_t sz_workspace_size(sz_dtype dt, size_t n) {
+    if (!dtype_ok(dt)) return 0;
+    return workspace_bytes(dt, n);
+}
+
+size_t sz_histogram_bins(sz_dtype dt) {
+    if (!dtype_ok(dt)) return 0;
+    return dt == SZ_BF16 ? 256 : 32;
+}
+
+sz_status sz_histogram(sz_dtype dt, const void* d_sample, size_t n, unsigned long long* d_hist,
+                       cudaStream_t stream) {
+    if (!dtype_ok(dt) || !d_hist || (n > 0 && !d_sample)) return SZ_ERR_INVALID_ARG;
+    if (dt == SZ_BF16 && !aligned(d_sample, 2)) return SZ_ERR_INVALID_ARG;
+    if (!aligned(d_hist, 8)) return SZ_ERR_INVALID_ARG;
+    cudaError_t err = cudaMemsetAsync(d_hist, 0, sz_histogram_bins(dt) * sizeof(unsigned long long), stream);
+    if (err != cudaSuccess) return from_cuda(err);
+    if (n == 0) return SZ_OK;
+    HistogramParams p{static_cast<const uint8_t*>(d_sample), n, d_hist, dt == SZ_BF16};
+    return from_cuda(launch_histogram(p, stream));
+}
+
+sz_status sz_codebook_from_histogram(sz_dtype dt, const unsigned long long* h_hist, sz_codebook* h_cb) {
+    if (!dtype_ok(dt) || !h_hist || !h_cb) return SZ_ERR_INVALID_ARG;
+    const int bins = (int)sz_histogram_bins(dt);
+    int order[256];
+    for (int e = 0; e < bins; e++) order[e] = e;
+    // Most frequent first; equal counts keep the smaller exponent first.
+    std::stable_sort(order, order + bins, [&](int a, int b) { return h_hist[a] > h_hist[b]; });
+    uint8_t chosen[SZ_CODEBOOK_SIZE];
+    for (int k = 0; k < SZ_CODEBOOK_SIZE; k++) chosen[k] = (uint8_t)order[k];
+    std::sort(chosen, chosen + SZ_CODEBOOK_SIZE);
+    std::memcpy(h_cb->exp, chosen, SZ_CODEBOOK_SIZE);
+    return SZ_OK;
+}
+
+sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n, unsigned long long* d_hist, sz_codebook* h_cb,
+                       cudaStream_t stream) {
+    if (!h_cb) return SZ_ERR_INVALID_ARG;
+    sz_status st = sz_histogram(dt, d_sample, n, d_hist, stream);
+    if (st != SZ_OK) return st;
+    unsigned long long h_hist[256];
+    const size_t bins = sz_histogram_bins(dt);
+    cudaError_t err = cudaMemcpyAsync(h_hist, d_hist, bins * sizeof(unsigned long long), cudaMemcpyDeviceToHost, stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return from_cuda(err);
+    return sz_codebook_from_histogram(dt, h_hist, h_cb);
+}
+
+sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
+                    size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+    return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
+                       kWaitLimitNs, stream);
+}
+
+sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
+                                  size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
+                                  size_t ws_bytes, unsigned long long wait_limit_ns, cudaStream_t stream) {
+    if (!d_status || wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return SZ_ERR_INVALID_ARG;
+    return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 1,
+                       wait_limit_ns, stream);
+}
+
+sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_out, int* d_status,
+                    cudaStream_t stream) {
+    if (!dtype_ok(dt) || !d_in || (n > 0 && !d_out) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
+    if (dt == SZ_BF16 && !aligned(d_out, 2)) return SZ_ERR_INVALID_ARG;
+    if (d_status && !aligned(d_status, 4)) return SZ_ERR_INVALID_ARG;
+    const uint64_t fixed = sz_encoded_size(dt, n, 0);
+    if (in_bytes < fixed || (in_bytes - fixed) % 3 != 0) return SZ_ERR_CORRUPT;
+    const uint64_t n_esc = (in_bytes - fixed) / 3;
+    if (n_esc > n) return SZ_ERR_CORRUPT;  // at most one escape per element
+
+    DecodeParams p{};
+    p.L = layout_for(dt, n);
+    p.in = static_cast<const uint8_t*>(d_in);
+    p.out = static_cast<uint8_t*>(d_out);
+    p.num_tiles = (uint32_t)tiles_for(dt, n);
+    p.n_esc = (uint32_t)n_esc;
+    p.status = d_status;
+    if (dt == SZ_BF16)
+        p.vec = aligned(d_in, 8) && aligned(static_cast<const uint8_t*>(d_in) + n, 4) && aligned(d_out, 16);
+    else
+        p.vec = aligned(d_in, 16) && aligned(d_out, 16);
+
+    if (d_status) {
+        const cudaError_t err = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
+        if (err != cudaSuccess) return from_cuda(err);
+    }
+    return from_cuda(dt == SZ_BF16 ? launch_decode_bf16(p, stream) : launch_decode_e5m2(p, stream));
+}
+
+const char* sz_status_string(int status) {
+    switch (status) {
+        case SZ_OK: return "SZ_OK";
+        case SZ_ERR_INVALID_ARG: return "SZ_ERR_INVALID_ARG";
+        case SZ_ERR_UNSUPPORTED: return "SZ_ERR_UNSUPPORTED";
+        case SZ_ERR_CAPACITY: return "SZ_ERR_CAPACITY";
+        case SZ_ERR_CORRUPT: return "SZ_ERR_CORRUPT";
+        case SZ_ERR_TIMEOUT: return "SZ_ERR_TIMEOUT";
+        case SZ_ERR_CUDA: return "SZ_ERR_CUDA";
+        default: return "SZ_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,329 @@
+// sz_device.cuh -- device-side building blocks shared by the SplitZip kernels.
+//
+// Ordered escape compaction ([MET] "Flujo de Escape": escapes are written in
+// element order) uses a single-pass decoupled look-back over tiles.  Every
+// tile publishes a 64-bit status word:
+//
+//   [63:62] flag   0 = nothing yet, 1 = aggregate known, 2 = prefix known,
+//                  3 = error (a wait gave up; successors stop waiting)
+//   [61:32] aggregate: escapes inside this tile
+//   [31: 0] exclusive prefix: escapes in all earlier tiles (flag 2 only)
+//
+// The data travels inside the word, so relaxed gpu-scope loads and stores are
+// enough.  Tiles are handed out by an atomic counter in launch order, so every
+// tile a block waits for belongs to a block that is already running: the wait
+// always ends, and it is bounded anyway (globaltimer) so that a fault can only
+// end in SZ_ERR_TIMEOUT, never in a hung GPU.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "sz_params.h"
+
+namespace sz {
+
+constexpr uint32_t kChunk = 65536;  // elements per escape chunk (u16 positions)
+constexpr int kCodes = 16;          // top-16 codebook
+
+constexpr uint64_t kFlagNone = 0;
+constexpr uint64_t kFlagAggregate = 1;
+constexpr uint64_t kFlagPrefix = 2;
+constexpr uint64_t kFlagError = 3;
+
+// Device status codes (same values as sz_status in splitzip.h).
+constexpr int kStatusCapacity = 3;
+constexpr int kStatusCorrupt = 4;
+constexpr int kStatusTimeout = 5;
+
+__device__ __forceinline__ uint64_t pack_status(uint64_t flag, uint32_t aggregate, uint32_t prefix) {
+    return (flag << 62) | ((uint64_t)(aggregate & 0x3FFFFFFFu) << 32) | prefix;
+}
+__device__ __forceinline__ uint32_t status_flag(uint64_t w) { return (uint32_t)(w >> 62); }
+__device__ __forceinline__ uint32_t status_aggregate(uint64_t w) { return (uint32_t)(w >> 32) & 0x3FFFFFFFu; }
+__device__ __forceinline__ uint32_t status_prefix(uint64_t w) { return (uint32_t)w; }
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Streaming (read-once) global loads that skip L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Evict-first stores for output that is not read again by this kernel.
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream_v2(void* p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait (bounded) until tile `idx` has published its prefix; returns the word,
+// or a word with kFlagError if the wait ran out or the tile reported an error.
+__device__ __forceinline__ uint64_t wait_for_prefix(const uint64_t* status, uint32_t idx, uint64_t limit_ns) {
+    uint64_t w = ld_relaxed_u64(status + idx);
+    if (status_flag(w) == kFlagPrefix || status_flag(w) == kFlagError) return w;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(100);
+        w = ld_relaxed_u64(status + idx);
+        const uint32_t f = status_flag(w);
+        if (f == kFlagPrefix || f == kFlagError) return w;
+        if (globaltimer_ns() - t0 > limit_ns) return pack_status(kFlagError, 0, 0);
+    }
+}
+
+// Decoupled look-back, run by one full warp of the block that owns `tile`.
+// Publishes the tile's aggregate, sums predecessors' aggregates back to the
+// nearest published prefix (32 tiles per step), publishes the tile's own
+// prefix and returns it (same value in every lane).  On a timeout or a
+// predecessor error it publishes kFlagError and sets *failed.
+__device__ __forceinline__ uint32_t lookback_prefix(uint64_t* status, uint32_t tile, uint32_t aggregate,
+                                                    uint64_t limit_ns, bool* failed) {
+    const uint32_t lane = threadIdx.x & 31u;
+    *failed = false;
+    if (tile == 0) {
+        if (lane == 0) st_relaxed_u64(status, pack_status(kFlagPrefix, aggregate, 0));
+        return 0;
+    }
+    if (lane == 0) st_relaxed_u64(status + tile, pack_status(kFlagAggregate, aggregate, 0));
+
+    uint32_t prefix = 0;
+    int64_t first = (int64_t)tile - 1;  // predecessor examined by lane 0
+    uint64_t t0 = 0;
+    bool clock_started = false;
+    while (true) {
+        const int64_t idx = first - (int64_t)lane;
+        uint64_t w;
+        while (true) {
+            // Lanes past tile 0 read as "prefix 0"; tile 0 always publishes a
+            // prefix, so no window ever needs to look beyond it.
+            w = idx >= 0 ? ld_relaxed_u64(status + idx) : pack_status(kFlagPrefix, 0, 0);
+            const uint32_t f = status_flag(w);
+            if (__any_sync(0xFFFFFFFFu, f == kFlagError)) {
+                *failed = true;
+                break;
+            }
+            if (__all_sync(0xFFFFFFFFu, f != kFlagNone)) break;
+            if (!clock_started) {
+                t0 = globaltimer_ns();
+                clock_started = true;
+            } else if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > limit_ns)) {  // warp-uniform
+                *failed = true;
+                break;
+            }
+            __nanosleep(64);
+        }
+        if (*failed) break;
+        const uint32_t have_prefix = __ballot_sync(0xFFFFFFFFu, status_flag(w) == kFlagPrefix);
+        const uint32_t agg = status_aggregate(w);
+        if (have_prefix) {
+            const uint32_t nearest = __ffs(have_prefix) - 1;
+            uint32_t part = 0;
+            if (lane < nearest) part = agg;
+            if (lane == nearest) part = agg + status_prefix(w);
+            prefix += __reduce_add_sync(0xFFFFFFFFu, part);
+            break;
+        }
+        prefix += __reduce_add_sync(0xFFFFFFFFu, agg);
+        first -= 32;
+    }
+    if (*failed) {
+        if (lane == 0) st_relaxed_u64(status + tile, pack_status(kFlagError, 0, 0));
+        return 0;
+    }
+    if (lane == 0) st_relaxed_u64(status + tile, pack_status(kFlagPrefix, aggregate, prefix));
+    return prefix;
+}
+
+// Little-endian byte stores for the few unaligned header fields.
+__device__ __forceinline__ void store_u32_le(uint8_t* p, uint32_t v) {
+    p[0] = (uint8_t)v;
+    p[1] = (uint8_t)(v >> 8);
+    p[2] = (uint8_t)(v >> 16);
+    p[3] = (uint8_t)(v >> 24);
+}
+__device__ __forceinline__ uint32_t load_u32_le(const uint8_t* p) {
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+}  // namespace sz
+
+namespace sz {
+
+// Position (u16, little-endian) of escape record j; records are 3 bytes.
+__device__ __forceinline__ uint32_t rec_pos(const uint8_t* rec, uint32_t j) {
+    return (uint32_t)rec[3ull * j] | ((uint32_t)rec[3ull * j + 1] << 8);
+}
+
+// Block-wide lower bounds in one chunk's escape positions.
+//
+// For key a and key b, returns the index of the first record in [o, o + m)
+// whose position is >= key, assuming positions ascend (m in 1..65536).  Two
+// rounds: 1024 evenly spaced probes bracket each answer to at most
+// ceil(65536 / 1024) = 64 records; a second round counts inside the bracket.
+// The result depends only on the data, so two blocks asking for the same key
+// get the same index even for a corrupt stream; the decoders rely on that to
+// give every record to exactly one tile.  Must be called by all THREADS
+// threads of the block; s_cnt is 4 words of shared scratch.
+template <uint32_t THREADS>
+__device__ void block_lower_bounds(const uint8_t* rec, uint32_t o, uint32_t m, uint32_t key_a, uint32_t key_b,
+                                   uint32_t* s_cnt, uint32_t* out_a, uint32_t* out_b) {
+    constexpr uint32_t kProbes = 1024;
+    constexpr uint32_t kPer = kProbes / THREADS;
+    static_assert(kProbes % THREADS == 0 && THREADS >= 128, "two 64-record brackets need 128 threads");
+    const uint32_t tid = threadIdx.x, lane = tid & 31u;
+    auto probe = [&](uint32_t i) { return o + (uint32_t)(((uint64_t)i * m) / kProbes); };
+    if (tid < 4) s_cnt[tid] = 0;
+    __syncthreads();
+    uint32_t ca = 0, cb = 0;
+#pragma unroll
+    for (uint32_t u = 0; u < kPer; u++) {
+        const uint32_t pos = rec_pos(rec, probe(tid * kPer + u));
+        ca += pos < key_a;
+        cb += pos < key_b;
+    }
+    ca = __reduce_add_sync(0xFFFFFFFFu, ca);
+    cb = __reduce_add_sync(0xFFFFFFFFu, cb);
+    if (lane == 0) atomicAdd(&s_cnt[0], ca), atomicAdd(&s_cnt[1], cb);
+    __syncthreads();
+    uint32_t lo[2], hi[2];
+#pragma unroll
+    for (int s = 0; s < 2; s++) {
+        const uint32_t c = s_cnt[s];
+        lo[s] = c == 0 ? o : probe(c - 1) + 1;
+        hi[s] = c == kProbes ? o + m : probe(c);
+        if (lo[s] > hi[s]) lo[s] = hi[s];  // only for corrupt (unsorted) data
+    }
+    // Second round: threads [0, T/2) bracket a, [T/2, T) bracket b.
+    const uint32_t half = THREADS / 2;
+    const uint32_t s = tid / half, t = tid % half;
+    uint32_t below = 0;
+    for (uint32_t u = t; u < hi[s] - lo[s]; u += half) below += rec_pos(rec, lo[s] + u) < (s == 0 ? key_a : key_b);
+    below = __reduce_add_sync(0xFFFFFFFFu, below);
+    if (lane == 0 && below) atomicAdd(&s_cnt[2 + s], below);
+    __syncthreads();
+    *out_a = lo[0] + s_cnt[2];
+    *out_b = lo[1] + s_cnt[3];
+    __syncthreads();
+}
+
+}  // namespace sz
+
+namespace sz {
+
+// Decode side: the escape records that fall in one tile.
+//
+// Checks the tile's chunk header against the stream (count fits the chunk,
+// offset + count within the E records the stream size implies; the first
+// tile of a chunk also checks that offsets are the running sum of counts and
+// that the last chunk ends at E), finds the tile's run [r0, r1) of the chunk's
+// sorted records, and calls apply(q, exponent) for every record of the run
+// whose position lies in the tile (q = element index inside the tile) and is
+// above the previous position of its chunk.  Any failed check sets *s_bad.
+// The runs of a chunk's tiles meet exactly (same search, same keys), so every
+// record of a valid stream is applied once and every record of a corrupt one
+// is checked once.  For E5M2 an exponent must also fit in 5 bits.
+//
+// Must be called by all THREADS threads; ends with a block barrier, so what
+// apply() wrote to shared memory is visible afterwards.  *s_bad must be
+// initialised (and a barrier passed) before the call.
+template <uint32_t THREADS, uint32_t TILE, bool FP8, typename Apply>
+__device__ void for_each_tile_escape(const DecodeParams& p, uint32_t tile, uint32_t* s_scratch, int* s_bad,
+                                     Apply apply) {
+    constexpr uint32_t kTilesPerChunk = kChunk / TILE;
+    static_assert(kChunk % TILE == 0, "tiles must not straddle chunks");
+    const uint32_t tid = threadIdx.x;
+    const uint64_t n = p.L.n;
+    const uint64_t base = (uint64_t)tile * TILE;
+    const uint32_t chunk = tile / kTilesPerChunk;
+    const uint32_t p0 = (tile % kTilesPerChunk) * TILE;
+    const uint32_t tile_len = base >= n ? 0u : (n - base >= TILE ? TILE : (uint32_t)(n - base));
+    const uint8_t* rec = p.in + p.L.rec_off;
+
+    if (tid == 0) {
+        uint32_t o = 0, m = 0;
+        if (p.L.num_chunks > 0) {
+            const uint8_t* h = p.in + p.L.hdr_off + 8ull * chunk;
+            o = load_u32_le(h);
+            m = load_u32_le(h + 4);
+            const uint64_t rest = n - (uint64_t)chunk * kChunk;
+            const uint64_t chunk_len = rest < kChunk ? rest : kChunk;
+            bool bad = m > chunk_len || o > p.n_esc || m > p.n_esc - o;
+            if (tile % kTilesPerChunk == 0) {
+                if (chunk == 0) {
+                    bad |= o != 0;
+                } else {
+                    const uint64_t po = load_u32_le(h - 8), pm = load_u32_le(h - 4);
+                    bad |= (uint64_t)o != po + pm;
+                }
+                if (chunk == p.L.num_chunks - 1) bad |= (uint64_t)o + m != p.n_esc;
+            }
+            if (bad) *s_bad = 1, m = 0;
+        }
+        s_scratch[4] = o;
+        s_scratch[5] = m;
+    }
+    __syncthreads();
+    const uint32_t o = s_scratch[4], m = s_scratch[5];
+    if (m == 0) return;  // block-uniform
+
+    const bool first_in_chunk = tile % kTilesPerChunk == 0;
+    const bool last_in_chunk = tile % kTilesPerChunk == kTilesPerChunk - 1 || tile == p.num_tiles - 1;
+    uint32_t r0 = o, r1 = o + m;
+    if (!(first_in_chunk && last_in_chunk)) {
+        uint32_t a, b;
+        block_lower_bounds<THREADS>(rec, o, m, p0, p0 + TILE, s_scratch, &a, &b);
+        if (!first_in_chunk) r0 = a;
+        if (!last_in_chunk) r1 = b;
+    }
+    if (r1 < r0) {
+        if (tid == 0) *s_bad = 1;
+    } else {
+        for (uint32_t j = r0 + tid; j < r1; j += THREADS) {
+            const uint32_t pos = rec_pos(rec, j);
+            const uint32_t e = rec[3ull * j + 2];
+            const bool in_tile = pos >= p0 && pos - p0 < tile_len;
+            const bool ordered = j == o || pos > rec_pos(rec, j - 1);
+            if (!in_tile || !ordered || (FP8 && e >= 32)) {
+                *s_bad = 1;
+                continue;
+            }
+            apply(pos - p0, e);
+        }
+    }
+    __syncthreads();
+}
+
+}  // namespace sz

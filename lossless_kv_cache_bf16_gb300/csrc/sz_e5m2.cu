@@ -1,0 +1,385 @@
+// sz_e5m2.cu -- SplitZip FP8 E5M2 encode and decode kernels for sm_103a.
+//
+// Method: SplitZip technical summary (gist.science/es), "Contribuciones
+// Clave", item 4 "Extensibilidad" (the codec extends to FP8 E5M2 KV caches),
+// with the encode/decode steps of "Metodologia: SplitZip".  Each element
+// becomes a 7-bit field code | (sign << 2 | mantissa) << 4; eight fields make
+// a 56-bit little-endian word stored as 7 bytes; escapes use the same
+// (u16 position, u8 exponent) stream as BF16.
+//
+// Work layout.  A block of 128 threads owns a tile of 16,384 elements (four
+// tiles per chunk); thread t owns the 128 contiguous elements [128t, 128t+128)
+// of the tile = 16 groups = 128 input bytes and 112 packed bytes.  A warp's
+// 4 KB of elements and 3.5 KB of packed bytes move between global and
+// registers through a per-warp shared-memory transpose, so every global
+// access is a fully coalesced 16 B/lane instruction and every shared access
+// is free of bank conflicts (XOR swizzle for 8-piece rows; the 7-piece rows
+// need none because 7 is odd).
+#include "sz_device.cuh"
+#include "sz_params.h"
+
+namespace sz {
+
+namespace {
+
+constexpr uint32_t kTilesPerChunk = kChunk / kE5Tile;  // 4
+static_assert(kChunk % kE5Tile == 0, "tiles must not straddle chunks");
+constexpr uint32_t kWarps = kE5Threads / 32;
+constexpr uint32_t kWarpElems = 32 * kE5PerThread;     // 4096
+constexpr uint32_t kStageRecs = 2048;                   // records staged in shared memory per tile
+
+// 16-byte slot of piece s (0..7) of thread-row r in an 8-piece swizzled row set.
+__device__ __forceinline__ uint32_t swz8(uint32_t r, uint32_t s) { return r * 8u + (s ^ (r & 7u)); }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Encode (same single-pass escape compaction as BF16; see sz_bf16.cu).
+//
+// The warp's input bytes stay in shared memory (swizzled rows, one per
+// thread) for the whole tile: packing reads them 16 bytes at a time and the
+// escape records read the exponents of escaped elements back from there, so
+// no thread holds its 128 input bytes in registers.  Packed bytes go to a
+// second per-warp buffer (7 pieces per row) and leave with coalesced stores.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kE5Threads) encode_e5m2_kernel(const EncodeParams p) {
+    __shared__ uint8_t s_field[256];                    // byte -> field; 0x80 marks an escape
+    __shared__ __align__(16) uint4 s_in[kWarps][256];   // 8 swizzled pieces per thread
+    __shared__ __align__(16) uint4 s_out[kWarps][224];  // 7 pieces per thread
+    __shared__ uint8_t s_rec[3 * kStageRecs];
+    __shared__ uint32_t s_warp_esc[kWarps];
+    __shared__ uint32_t s_tile, s_prefix;
+    __shared__ int s_failed;
+
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    for (uint32_t x = tid; x < 256; x += kE5Threads) {
+        const uint32_t e = (x >> 2) & 31u;
+        uint32_t code = 0xFFu;
+#pragma unroll
+        for (int k = 0; k < kCodes; k++)
+            if (p.cb[k] == e) code = (uint32_t)k;
+        const uint32_t sm3 = ((x >> 7) << 2) | (x & 3u);
+        s_field[x] = (uint8_t)(code == 0xFFu ? (0x80u | (sm3 << 4)) : (code | (sm3 << 4)));
+    }
+    if (tid == 0) s_tile = atomicAdd(p.ticket, 1u);
+    __syncthreads();
+    const uint32_t tile = s_tile;
+    if (tile >= p.num_tiles) return;  // only with the stalled-predecessor test hook
+    const uint64_t n = p.L.n;
+    const uint64_t warp_base = (uint64_t)tile * kE5Tile + warp * kWarpElems;
+    const uint64_t thread_base = warp_base + lane * kE5PerThread;
+    const bool warp_full = p.vec && warp_base + kWarpElems <= n;
+    const uint32_t cnt = thread_base >= n ? 0u : (n - thread_base >= kE5PerThread ? kE5PerThread : (uint32_t)(n - thread_base));
+
+    // Input bytes into this thread's row.  Bytes past n read as exponent
+    // cb[0] with sign and mantissa 0, which packs to field 0 and is no escape.
+    if (warp_full) {
+#pragma unroll
+        for (uint32_t i = 0; i < 8; i++) {
+            const uint32_t piece = lane + 32 * i;
+            s_in[warp][swz8(piece >> 3, piece & 7u)] = ld_stream_v4(p.in + warp_base + 16 * piece);
+        }
+    } else {
+        const uint32_t pad = (uint32_t)p.cb[0] << 2;
+        for (uint32_t s = 0; s < 8; s++) {
+            uint32_t w[4];
+#pragma unroll
+            for (uint32_t q = 0; q < 4; q++) {
+                uint32_t v = 0;
+#pragma unroll
+                for (uint32_t t = 0; t < 4; t++) {
+                    const uint32_t j = 16 * s + 4 * q + t;
+                    v |= (j < cnt ? (uint32_t)p.in[thread_base + j] : pad) << (8 * t);
+                }
+                w[q] = v;
+            }
+            s_in[warp][swz8(lane, s)] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    __syncwarp();
+
+    // Pack: each group's 56 bits are appended (32 + 24 bits) to a bit
+    // accumulator; each append completes at most one 32-bit word, and every
+    // fourth word completes one 16-byte piece of the row's 7.
+    uint32_t escm[4] = {0, 0, 0, 0};
+    {
+        uint64_t acc = 0;
+        uint32_t nbits = 0, nwords = 0;
+        uint32_t words[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int s = 0; s < 8; s++) {
+            const uint4 v = s_in[warp][swz8(lane, s)];
+            const uint32_t in4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int h = 0; h < 2; h++) {  // group 2s + h
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    const int e = 16 * s + 8 * h + j;  // element inside the thread
+                    const uint32_t f = s_field[(in4[2 * h + (j >> 2)] >> (8 * (j & 3))) & 0xFFu];
+                    escm[e >> 5] |= (f >> 7) << (e & 31);
+                    const uint32_t f7 = f & 0x7Fu;
+                    const int bit = 7 * j;
+                    if (bit + 7 <= 32) {
+                        lo |= f7 << bit;
+                    } else if (bit >= 32) {
+                        hi |= f7 << (bit - 32);
+                    } else {
+                        lo |= f7 << bit;
+                        hi |= f7 >> (32 - bit);
+                    }
+                }
+#pragma unroll
+                for (int part = 0; part < 2; part++) {
+                    acc |= (uint64_t)(part == 0 ? lo : hi) << nbits;
+                    nbits += part == 0 ? 32 : 24;
+                    if (nbits >= 32) {
+                        words[nwords & 3] = (uint32_t)acc;
+                        acc >>= 32;
+                        nbits -= 32;
+                        if ((++nwords & 3) == 0)
+                            s_out[warp][lane * 7 + (nwords >> 2) - 1] = make_uint4(words[0], words[1], words[2], words[3]);
+                    }
+                }
+            }
+        }
+    }
+    __syncwarp();
+
+    const uint64_t out_base = warp_base / 8 * 7;  // packed bytes before this warp
+    if (warp_full) {
+#pragma unroll
+        for (uint32_t i = 0; i < 7; i++) {
+            const uint32_t piece = lane + 32 * i;
+            st_stream_v4(p.out + out_base + 16 * piece, s_out[warp][piece]);
+        }
+    } else if (cnt > 0) {
+        const uint32_t nbytes = 7 * ((cnt + 7) / 8);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(&s_out[warp][lane * 7]);
+        uint8_t* dst = p.out + out_base + lane * 112u;
+        for (uint32_t b = 0; b < nbytes; b++) dst[b] = src[b];
+    }
+
+    // Rank escapes: thread order, then element order inside the thread.
+    const uint32_t mine = __popc(escm[0]) + __popc(escm[1]) + __popc(escm[2]) + __popc(escm[3]);
+    uint32_t incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= (uint32_t)d) incl += a;
+    }
+    if (lane == 31) s_warp_esc[warp] = incl;
+    __syncthreads();
+    uint32_t rank = incl - mine, tile_esc = 0;
+#pragma unroll
+    for (uint32_t v = 0; v < kWarps; v++) {
+        const uint32_t c = s_warp_esc[v];
+        if (v < warp) rank += c;
+        tile_esc += c;
+    }
+    const bool staged = tile_esc <= kStageRecs;
+
+    // Writes this thread's records, in element order, from record `rank` on;
+    // exponents come back from the input row in shared memory.
+    const uint8_t* row = reinterpret_cast<const uint8_t*>(&s_in[warp][0]);
+    auto emit = [&](uint8_t* dst_base, uint64_t limit) {
+        uint64_t at = 3ull * rank;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t m = escm[q];
+            while (m) {
+                const uint32_t j = 32 * q + __ffs(m) - 1;
+                m &= m - 1;
+                const uint32_t byte = row[swz8(lane, j >> 4) * 16u + (j & 15u)];
+                const uint32_t pos = (uint32_t)(thread_base + j) & 0xFFFFu;
+                if (at + 3 <= limit) {
+                    dst_base[at] = (uint8_t)pos;
+                    dst_base[at + 1] = (uint8_t)(pos >> 8);
+                    dst_base[at + 2] = (uint8_t)((byte >> 2) & 31u);
+                }
+                at += 3;
+            }
+        }
+    };
+    if (mine && staged) emit(s_rec, sizeof(s_rec));
+
+    if (warp == 0) {
+        bool failed;
+        const uint32_t prefix = lookback_prefix(p.tile_status, tile, tile_esc, p.wait_limit_ns, &failed);
+        if (lane == 0) s_prefix = prefix, s_failed = failed;
+    }
+    __syncthreads();
+    if (s_failed) {
+        if (tid == 0 && p.status) atomicMax(p.status, kStatusTimeout);
+        return;
+    }
+    const uint32_t prefix = s_prefix;
+    const uint64_t dst = p.L.rec_off + 3ull * prefix;
+    if (staged) {
+        const uint32_t nbytes = 3u * tile_esc;
+        for (uint32_t b = tid; b < nbytes; b += kE5Threads)
+            if (dst + b < p.capacity) p.out[dst + b] = s_rec[b];
+    } else if (mine) {
+        // Too many escapes to stage: write them straight to their place.
+        emit(p.out + dst, p.capacity > dst ? p.capacity - dst : 0);
+    }
+
+    if (tid == 0) {
+        if (tile % kTilesPerChunk == 0 && tile > 0) {
+            const uint64_t wprev = wait_for_prefix(p.tile_status, tile - kTilesPerChunk, p.wait_limit_ns);
+            if (status_flag(wprev) == kFlagError) {
+                if (p.status) atomicMax(p.status, kStatusTimeout);
+            } else {
+                const uint32_t c = tile / kTilesPerChunk - 1;
+                const uint32_t first = status_prefix(wprev);
+                store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
+                store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, prefix - first);
+            }
+        }
+        if (tile == p.num_tiles - 1) {
+            const uint32_t total = prefix + tile_esc;
+            const unsigned long long size = p.L.rec_off + 3ull * total;
+            *p.out_bytes = size;
+            if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
+            if (p.L.num_chunks > 0) {
+                const uint32_t c = p.L.num_chunks - 1;
+                const uint32_t first_tile = c * kTilesPerChunk;
+                uint32_t first = prefix;
+                bool ok = true;
+                if (first_tile != tile) {
+                    const uint64_t wf = wait_for_prefix(p.tile_status, first_tile, p.wait_limit_ns);
+                    ok = status_flag(wf) != kFlagError;
+                    first = status_prefix(wf);
+                }
+                if (ok) {
+                    store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
+                    store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, total - first);
+                } else if (p.status) {
+                    atomicMax(p.status, kStatusTimeout);
+                }
+            }
+        }
+    }
+    if (tile == 0 && tid < kCodes) p.out[p.L.cb_off + tid] = p.cb[tid];
+}
+
+// ---------------------------------------------------------------------------
+// Decode: packed groups -> fields -> bytes through a 128-entry LUT, staged in
+// the warp's transpose buffer where the tile's escapes patch the exponent
+// bits, then stored with coalesced 16-byte writes.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kE5Threads) decode_e5m2_kernel(const DecodeParams p) {
+    __shared__ uint8_t s_dec[128];  // field -> E5M2 byte
+    __shared__ __align__(16) uint4 s_xpose[kWarps][256];
+    __shared__ uint32_t s_cnt[6];
+    __shared__ int s_bad;
+
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint32_t tile = blockIdx.x;
+    const uint64_t n = p.L.n;
+    const uint64_t warp_base = (uint64_t)tile * kE5Tile + warp * kWarpElems;
+    const uint64_t thread_base = warp_base + lane * kE5PerThread;
+    const bool warp_full = p.vec && warp_base + kWarpElems <= n;
+    const uint32_t cnt = thread_base >= n ? 0u : (n - thread_base >= kE5PerThread ? kE5PerThread : (uint32_t)(n - thread_base));
+    const uint8_t* cb = p.in + p.L.cb_off;
+
+    {
+        const uint32_t f = tid;  // 128 threads, one field value each
+        const uint32_t sm3 = f >> 4;
+        s_dec[f] = (uint8_t)(((sm3 >> 2) << 7) | ((uint32_t)cb[f & 15u] << 2) | (sm3 & 3u));
+    }
+    if (tid == 0) s_bad = 0;
+
+    // Packed bytes of this thread: 28 words (16 groups).
+    uint32_t pw[28];
+    const uint64_t in_base = warp_base / 8 * 7;
+    if (warp_full) {
+#pragma unroll
+        for (uint32_t i = 0; i < 7; i++) {
+            const uint32_t piece = lane + 32 * i;
+            s_xpose[warp][piece] = ld_stream_v4(p.in + in_base + 16 * piece);
+        }
+        __syncwarp();
+#pragma unroll
+        for (uint32_t i = 0; i < 7; i++) {
+            const uint4 v = s_xpose[warp][lane * 7 + i];
+            pw[4 * i] = v.x, pw[4 * i + 1] = v.y, pw[4 * i + 2] = v.z, pw[4 * i + 3] = v.w;
+        }
+    } else {
+        const uint32_t nbytes = 7 * ((cnt + 7) / 8);
+        const uint8_t* src = p.in + in_base + lane * 112u;
+#pragma unroll
+        for (int k = 0; k < 28; k++) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int t = 0; t < 4; t++)
+                if ((uint32_t)(4 * k + t) < nbytes) v |= (uint32_t)src[4 * k + t] << (8 * t);
+            pw[k] = v;
+        }
+    }
+    __syncthreads();  // s_dec, s_bad ready; transpose buffer free again
+
+    if (tid < kCodes) {  // 16 distinct exponents that fit in 5 bits
+        bool bad = cb[tid] >= 32;
+        for (int k = 0; k < kCodes; k++) bad |= (k != (int)tid) && cb[k] == cb[tid];
+        if (bad) s_bad = 1;
+    }
+
+    // Dense pass into the transpose buffer (this thread's row, swizzled).
+#pragma unroll
+    for (int s = 0; s < 8; s++) {
+        uint32_t y[4];
+#pragma unroll
+        for (int w = 0; w < 4; w++) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                const int j = 16 * s + 4 * w + t;  // element inside the thread
+                const int g = j / 8, bit = 7 * (j % 8);
+                // 56-bit group value starts at byte 7g of the thread's packed bytes.
+                const int byte0 = 7 * g + bit / 8, sh = bit % 8;
+                const uint32_t lo = (pw[byte0 / 4] >> (8 * (byte0 % 4))) & 0xFFu;
+                const int byte1 = byte0 + 1;
+                const uint32_t hi = byte1 < 7 * (g + 1) ? (pw[byte1 / 4] >> (8 * (byte1 % 4))) & 0xFFu : 0u;
+                const uint32_t f = ((lo | (hi << 8)) >> sh) & 0x7Fu;
+                v |= (uint32_t)s_dec[f] << (8 * t);
+            }
+            y[w] = v;
+        }
+        s_xpose[warp][swz8(lane, s)] = make_uint4(y[0], y[1], y[2], y[3]);
+    }
+
+    // Escapes: patch the exponent bits of the staged bytes.
+    uint8_t* staged = reinterpret_cast<uint8_t*>(&s_xpose[0][0]);
+    for_each_tile_escape<kE5Threads, kE5Tile, true>(p, tile, s_cnt, &s_bad, [&](uint32_t q, uint32_t e) {
+        const uint32_t t = q >> 7, b = q & 127u;  // owning thread of the tile, byte inside its row
+        const uint32_t w = t >> 5, l = t & 31u;
+        uint8_t* at = staged + (w * 256u + swz8(l, b >> 4)) * 16u + (b & 15u);
+        *at = (uint8_t)((*at & 0x83u) | (e << 2));
+    });
+    __syncthreads();
+
+    if (warp_full) {
+#pragma unroll
+        for (uint32_t i = 0; i < 8; i++) {
+            const uint32_t piece = lane + 32 * i;
+            st_stream_v4(p.out + warp_base + 16 * piece, s_xpose[warp][swz8(piece >> 3, piece & 7u)]);
+        }
+    } else {
+        for (uint32_t b = 0; b < cnt; b++)
+            p.out[thread_base + b] = staged[(warp * 256u + swz8(lane, b >> 4)) * 16u + (b & 15u)];
+    }
+    if (tid == 0 && s_bad && p.status) atomicMax(p.status, kStatusCorrupt);
+}
+
+cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
+    encode_e5m2_kernel<<<p.num_tiles, kE5Threads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {
+    decode_e5m2_kernel<<<p.num_tiles, kE5Threads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace sz

@@ -1,0 +1,68 @@
+// sz_params.h -- host/device launch parameters shared by the SplitZip kernels
+// and the C ABI layer (not part of the public interface).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace sz {
+
+// Byte offsets of the stream sections for n elements (see splitzip.h).
+struct StreamLayout {
+    uint64_t n;
+    uint64_t dense;     // BF16: sm + nibbles; E5M2: packed groups
+    uint64_t nib_off;   // BF16 only: start of the nibble stream (= n)
+    uint64_t cb_off;    // codebook (16 bytes)
+    uint64_t hdr_off;   // chunk headers (8 bytes each)
+    uint64_t rec_off;   // escape records (3 bytes each)
+    uint32_t num_chunks;
+};
+
+struct EncodeParams {
+    StreamLayout L;
+    const uint8_t* in;
+    uint8_t* out;
+    uint64_t capacity;
+    uint32_t num_tiles;
+    uint32_t* ticket;        // workspace: tile counter
+    uint64_t* tile_status;   // workspace: one look-back word per tile
+    unsigned long long* out_bytes;
+    int* status;             // nullable
+    uint64_t wait_limit_ns;
+    int vec;                 // 1 when the aligned vector path may be used
+    uint8_t cb[16];          // ascending
+};
+
+struct DecodeParams {
+    StreamLayout L;
+    const uint8_t* in;
+    uint8_t* out;
+    uint32_t num_tiles;
+    uint32_t n_esc;          // escape count implied by the stream size
+    int* status;             // nullable
+    int vec;
+};
+
+struct HistogramParams {
+    const uint8_t* in;
+    uint64_t n;
+    unsigned long long* hist;
+    int bf16;
+};
+
+// Tile sizes (elements).  Both divide the 65,536-element chunk.
+constexpr uint32_t kBf16Threads = 256;
+constexpr uint32_t kBf16PerThread = 32;
+constexpr uint32_t kBf16Tile = kBf16Threads * kBf16PerThread;   // 8192
+constexpr uint32_t kE5Threads = 128;
+constexpr uint32_t kE5PerThread = 128;                          // 16 groups of 8
+constexpr uint32_t kE5Tile = kE5Threads * kE5PerThread;         // 16384
+
+cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_histogram(const HistogramParams& p, cudaStream_t s);
+
+}  // namespace sz

@@ -1,0 +1,183 @@
+"""Python binding of the SplitZip C ABI (``include/splitzip.h``).
+
+Argument marshalling only: every function forwards to ``libsplitzip.so`` with
+the same name, passing device pointers of torch CUDA tensors and the current
+CUDA stream.  All work runs in the library's CUDA kernels; there is no CPU
+path, and importing this module fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+SZ_OK = 0
+SZ_ERR_INVALID_ARG = 1
+SZ_ERR_UNSUPPORTED = 2
+SZ_ERR_CAPACITY = 3
+SZ_ERR_CORRUPT = 4
+SZ_ERR_TIMEOUT = 5
+SZ_ERR_CUDA = 6
+
+SZ_BF16 = 0
+SZ_FP8_E5M2 = 1
+SZ_CHUNK_ELEMS = 65536
+SZ_CODEBOOK_SIZE = 16
+
+ELEMENT_BYTES = {SZ_BF16: 2, SZ_FP8_E5M2: 1}
+
+
+class SplitZipError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {sz_status_string(status)} ({status})")
+        self.status = status
+
+
+class sz_codebook(ctypes.Structure):
+    _fields_ = [("exp", ctypes.c_uint8 * SZ_CODEBOOK_SIZE)]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIBRARY
+    if not os.path.exists(path):
+        raise RuntimeError(f"SplitZip CUDA library not found at {path}; build it with "
+                           "`python -m lossless_kv_cache_bf16_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, sz, i32, u64p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_ulonglong)
+    cbp = ctypes.POINTER(sz_codebook)
+    sigs = {
+        "sz_encoded_size": (sz, [i32, sz, sz]),
+        "sz_workspace_size": (sz, [i32, sz]),
+        "sz_histogram_bins": (sz, [i32]),
+        "sz_histogram": (i32, [i32, vp, sz, vp, vp]),
+        "sz_codebook_from_histogram": (i32, [i32, u64p, cbp]),
+        "sz_calibrate": (i32, [i32, vp, sz, vp, cbp, vp]),
+        "sz_encode": (i32, [i32, cbp, vp, sz, vp, sz, vp, vp, vp, sz, vp]),
+        "sz_decode": (i32, [i32, vp, sz, sz, vp, vp, vp]),
+        "sz_status_string": (ctypes.c_char_p, [i32]),
+        "sz_debug_encode_stalled": (i32, [i32, cbp, vp, sz, vp, sz, vp, vp, vp, sz, ctypes.c_ulonglong, vp]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+# ---- marshalling helpers -----------------------------------------------------
+
+def _dev_ptr(t: torch.Tensor | None, what: str):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _elements(dt: int, t: torch.Tensor) -> int:
+    nbytes = t.numel() * t.element_size()
+    if nbytes % ELEMENT_BYTES[dt]:
+        raise ValueError("tensor size is not a whole number of elements")
+    return nbytes // ELEMENT_BYTES[dt]
+
+
+def _codebook(cb) -> sz_codebook:
+    vals = [int(v) for v in (cb.tolist() if hasattr(cb, "tolist") else cb)]
+    if len(vals) != SZ_CODEBOOK_SIZE:
+        raise ValueError("a codebook has 16 exponents")
+    c = sz_codebook()
+    for k, v in enumerate(vals):
+        c.exp[k] = v
+    return c
+
+
+def _check(fn: str, status: int):
+    if status != SZ_OK:
+        raise SplitZipError(fn, status)
+
+
+# ---- the C ABI, same names ---------------------------------------------------
+
+def sz_status_string(status: int) -> str:
+    return LIB.sz_status_string(status).decode()
+
+
+def sz_encoded_size(dt: int, n: int, n_escapes: int) -> int:
+    return int(LIB.sz_encoded_size(dt, n, n_escapes))
+
+
+def sz_workspace_size(dt: int, n: int) -> int:
+    return int(LIB.sz_workspace_size(dt, n))
+
+
+def sz_histogram_bins(dt: int) -> int:
+    return int(LIB.sz_histogram_bins(dt))
+
+
+def sz_histogram(dt: int, sample: torch.Tensor, hist: torch.Tensor, stream=None) -> None:
+    """hist: int64/uint64 CUDA tensor of sz_histogram_bins(dt) counts (overwritten)."""
+    assert hist.numel() == sz_histogram_bins(dt) and hist.element_size() == 8
+    _check("sz_histogram", LIB.sz_histogram(dt, _dev_ptr(sample, "sample"), _elements(dt, sample),
+                                            _dev_ptr(hist, "hist"), _stream(stream)))
+
+
+def sz_codebook_from_histogram(dt: int, hist) -> list[int]:
+    vals = [int(v) for v in (hist.tolist() if hasattr(hist, "tolist") else hist)]
+    arr = (ctypes.c_ulonglong * len(vals))(*vals)
+    cb = sz_codebook()
+    _check("sz_codebook_from_histogram", LIB.sz_codebook_from_histogram(dt, arr, ctypes.byref(cb)))
+    return list(cb.exp)
+
+
+def sz_calibrate(dt: int, sample: torch.Tensor, hist: torch.Tensor, stream=None) -> list[int]:
+    """Offline calibration; synchronises the stream; returns the 16 exponents."""
+    cb = sz_codebook()
+    _check("sz_calibrate", LIB.sz_calibrate(dt, _dev_ptr(sample, "sample"), _elements(dt, sample),
+                                            _dev_ptr(hist, "hist"), ctypes.byref(cb), _stream(stream)))
+    return list(cb.exp)
+
+
+def sz_encode(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
+              status: torch.Tensor | None, ws: torch.Tensor, stream=None, n: int | None = None) -> None:
+    """Asynchronous encode of x (n elements, default all of x) into out."""
+    c = _codebook(cb)
+    n = _elements(dt, x) if n is None else n
+    _check("sz_encode", LIB.sz_encode(dt, ctypes.byref(c), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
+                                      out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                      _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
+                                      ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sz_decode(dt: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, y: torch.Tensor,
+              status: torch.Tensor | None, stream=None) -> None:
+    """Asynchronous decode of the first in_bytes bytes of stream_bytes into y."""
+    if in_bytes > stream_bytes.numel() * stream_bytes.element_size():
+        raise ValueError("in_bytes exceeds the stream buffer")
+    if n * ELEMENT_BYTES[dt] > y.numel() * y.element_size():
+        raise ValueError("output buffer too small")
+    _check("sz_decode", LIB.sz_decode(dt, _dev_ptr(stream_bytes, "stream"), in_bytes, n, _dev_ptr(y, "y"),
+                                      _dev_ptr(status, "status"), _stream(stream)))
+
+
+def sz_debug_encode_stalled(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
+                            status: torch.Tensor, ws: torch.Tensor, wait_limit_ns: int, stream=None) -> None:
+    c = _codebook(cb)
+    _check("sz_debug_encode_stalled",
+           LIB.sz_debug_encode_stalled(dt, ctypes.byref(c), _dev_ptr(x, "x"), _elements(dt, x), _dev_ptr(out, "out"),
+                                       out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                       _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
+                                       ws.numel() * ws.element_size(), wait_limit_ns, _stream(stream)))

@@ -10,7 +10,13 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
-    config.addinivalue_line("markers", "slow: full-size workloads (minutes)")
+    # The CUDA library (cross-compiled for sm_103a; loads without a GPU) and the
+    # C oracle are built in-tree on first use; both builds are no-ops when current.
+    from lossless_kv_cache_bf16_gb300 import build
+    from oracle import oracle
+
+    build.build()
+    oracle.build()
 
 
 @pytest.fixture(scope="session")

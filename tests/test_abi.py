@@ -1,0 +1,95 @@
+"""The C ABI library on a host without a GPU: it loads, exports every symbol
+that include/splitzip.h declares, and its host-only logic (closed-form sizes,
+top-16 selection, argument checks that return before any CUDA call) agrees
+with the oracle and the header's contract.  No compute runs here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "splitzip.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sz_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def S():
+    from lossless_kv_cache_bf16_gb300 import splitzip
+
+    return splitzip
+
+
+def test_exports_every_declared_symbol(S):
+    names = declared_functions()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(S.LIB, name), f"{name} declared but not exported"
+        assert callable(getattr(S, name)), f"binding lacks {name}"
+
+
+def test_encoded_size_matches_oracle(S, orc):
+    for dt in (O.BF16, O.E5M2):
+        for n in (0, 1, 2, 7, 8, 9, 65535, 65536, 65537, 536870912, 4294967295):
+            for e in (0, 1, n // 3, n):
+                assert S.sz_encoded_size(dt, n, e) == orc.encoded_size(dt, n, e)
+    assert S.sz_encoded_size(7, 10, 0) == 0
+
+
+def test_workspace_size(S):
+    for dt, tile in ((S.SZ_BF16, 8192), (S.SZ_FP8_E5M2, 16384)):
+        assert S.sz_workspace_size(dt, 0) == 16 + 8
+        assert S.sz_workspace_size(dt, tile) == 16 + 8
+        assert S.sz_workspace_size(dt, tile + 1) == 16 + 16
+        assert S.sz_workspace_size(dt, 939524096) == 16 + 8 * (939524096 // tile)
+
+
+def test_codebook_selection_matches_oracle(S, orc):
+    rng = np.random.default_rng(1)
+    for dt, bins in ((O.BF16, 256), (O.E5M2, 32)):
+        for trial in range(200):
+            hist = rng.integers(0, 4, bins).astype(np.uint64) * rng.integers(0, 3, bins).astype(np.uint64)
+            if trial % 3 == 0:
+                hist[:] = 0
+                hist[rng.integers(0, bins, 5)] = 7  # ties and fewer than 16 seen
+            assert S.sz_codebook_from_histogram(dt, hist) == orc.codebook_from_histogram(dt, hist).tolist()
+
+
+def test_host_argument_checks_return_before_launching(S):
+    """Invalid arguments return at once; the fake device pointers are never used."""
+    lib = S.LIB
+    fake = ctypes.c_void_p(0x10000)
+    cb = S._codebook(list(range(120, 136)))
+    dup = S._codebook([120] * 16)
+    n = 1000
+    cap = S.sz_encoded_size(0, n, n)
+    ws = S.sz_workspace_size(0, n)
+    enc = lambda dt, c, cap_, ws_, n_=n, out=fake: lib.sz_encode(dt, ctypes.byref(c), fake, n_, out, cap_, fake, None, fake, ws_, None)
+    assert enc(0, dup, cap, ws) == S.SZ_ERR_INVALID_ARG
+    assert enc(1, cb, cap, ws) == S.SZ_ERR_INVALID_ARG            # exponents >= 32 for E5M2
+    assert enc(5, cb, cap, ws) == S.SZ_ERR_INVALID_ARG
+    assert enc(0, cb, 10, ws) == S.SZ_ERR_CAPACITY
+    assert enc(0, cb, cap, 8) == S.SZ_ERR_CAPACITY
+    assert enc(0, cb, cap, ws, n_=1 << 32) == S.SZ_ERR_INVALID_ARG
+    assert enc(0, cb, cap, ws, out=None) == S.SZ_ERR_INVALID_ARG
+    fixed = S.sz_encoded_size(0, n, 0)
+    dec = lambda size, n_=n: lib.sz_decode(0, fake, size, n_, fake, None, None)
+    assert dec(fixed - 1) == S.SZ_ERR_CORRUPT
+    assert dec(fixed + 1) == S.SZ_ERR_CORRUPT
+    assert dec(fixed + 3 * (n + 1)) == S.SZ_ERR_CORRUPT         # more escapes than elements
+    assert lib.sz_decode(0, None, fixed, n, fake, None, None) == S.SZ_ERR_INVALID_ARG
+    assert lib.sz_debug_encode_stalled(0, ctypes.byref(cb), fake, n, fake, cap, fake, None, fake, ws, 1000, None) == S.SZ_ERR_INVALID_ARG
+
+
+def test_status_strings(S):
+    assert S.sz_status_string(0) == "SZ_OK"
+    assert S.sz_status_string(5) == "SZ_ERR_TIMEOUT"
+    assert S.sz_status_string(99) == "SZ_ERR_UNKNOWN"

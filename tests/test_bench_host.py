@@ -1,0 +1,74 @@
+"""bench.py host logic (CPU): throughput aggregation, the link model, the
+profile-traffic lookup, and the N>1 path's max-over-ranks timing run as two
+gloo ranks on 127.0.0.1."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_aggregate_uses_slowest_rank():
+    value, t = bench.aggregate(10 ** 9, [0.5, 0.25])
+    assert t == 0.5 and value == pytest.approx(2 * 10 ** 9 / 0.5 / 1e9)
+
+
+def test_link_model():
+    m = bench.link_model(10 ** 9, 750_000_000, 0.001, 0.0005)
+    raw = 10 ** 9 / 50e9
+    coded = 0.001 + 750_000_000 / 50e9 + 0.0005
+    assert m["50GBps"]["speedup"] == pytest.approx(raw / coded)
+    assert m["100GBps"]["raw_ms"] == pytest.approx(10.0)
+
+
+def test_traffic_is_null_without_matching_profile(tmp_path, monkeypatch):
+    assert bench.profiled_traffic("encode_bf16_kernel", "no_such_workload") is None
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    os.makedirs(tmp_path / "profiles")
+    csrc = tmp_path / "lossless_kv_cache_bf16_gb300" / "csrc"
+    os.makedirs(csrc)
+    for name in bench.KERNEL_SOURCES["encode_bf16_kernel"]:
+        (csrc / name).write_text("v1")
+    h = bench.kernel_source_hash("encode_bf16_kernel")
+    (tmp_path / "profiles" / "encode_bf16_kernel_w.txt").write_text(
+        f"kernel_source_sha256_16: {h}\ndram_bytes_per_launch: 1234\n")
+    assert bench.profiled_traffic("encode_bf16_kernel", "w") == 1234
+    (csrc / "sz_bf16.cu").write_text("v2")   # kernel changed since the capture
+    assert bench.profiled_traffic("encode_bf16_kernel", "w") is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    elapsed = [0.75, 0.5][rank]
+    per_rank = bench.gather_elapsed(dist, elapsed, torch.device("cpu"))
+    value, t = bench.aggregate(3 * 10 ** 9, per_rank)
+    q.put((rank, per_rank, value, t))
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, per_rank, value, t in out:
+        assert per_rank == [0.75, 0.5]
+        assert t == 0.75
+        assert value == pytest.approx(2 * 3 * 10 ** 9 / 0.75 / 1e9)

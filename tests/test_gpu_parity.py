@@ -1,0 +1,154 @@
+"""CUDA codec vs the CPU oracle, element by element (GPU).
+
+Encoded streams must be byte-identical to the oracle's and decoding must give
+the input back bit for bit: the codec is integer bit manipulation, so the
+tolerance is zero (SplitZip abstract, arXiv 2605.01708v2: the KV tensors are
+preserved bitwise).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from tests import gpu_codec as G
+from tests.oracle_pins import CB_EDGES, CB_E5_EDGES, CB_E5_MID, CB_MID
+
+pytestmark = pytest.mark.gpu
+
+ODT = {"bf16": O.BF16, "e5m2": O.E5M2}
+
+
+def roundtrip_vs_oracle(orc, kind, cb, x: torch.Tensor, **kw):
+    """Encode on the GPU, compare with the oracle byte for byte, decode on the
+    GPU, compare with the input bit for bit."""
+    dt, odt = G.DT[kind], ODT[kind]
+    xh = G.as_bytes(x)
+    n = G.elements(dt, x)
+    want = orc.encode(odt, cb, xh)
+    got, status, size = G.encode(dt, cb, x, out_offset=kw.get("out_offset", 0))
+    assert status == 0, f"encode status {status}"
+    assert size == want.size
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero(got != want)
+        pytest.fail(f"stream differs from the oracle at {bad.size} bytes, first at {bad[:8]} (size {size})")
+    st, y, guard_ok = G.decode(dt, got, n, out_offset=kw.get("dec_out_offset", 0), in_offset=kw.get("dec_in_offset", 0))
+    assert st == 0 and guard_ok
+    assert np.array_equal(y, xh), "decode is not bit-exact"
+    return got
+
+
+def _gauss(n, scale_sigma=2.0, seed=0, device="cuda"):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    s = torch.exp(scale_sigma * torch.randn(n, generator=g, device=device))
+    return (torch.randn(n, generator=g, device=device) * s).to(torch.bfloat16)
+
+
+def _bytes(n, seed=0):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randint(0, 256, (n,), generator=g, device="cuda", dtype=torch.uint8)
+
+
+EDGE_N = [0, 1, 2, 3, 7, 8, 9, 31, 32, 33, 255, 256, 257, 1023, 1024, 1025, 4095, 4097, 8191, 8192, 8193,
+          16383, 16384, 16385, 65535, 65536, 65537, 131073, 200003, 3 * 65536 + 12345]
+
+
+@pytest.mark.parametrize("n", EDGE_N)
+def test_bf16_edge_sizes(orc, n):
+    roundtrip_vs_oracle(orc, "bf16", CB_MID, _gauss(n, seed=n))
+
+
+@pytest.mark.parametrize("n", EDGE_N)
+def test_e5m2_edge_sizes(orc, n):
+    roundtrip_vs_oracle(orc, "e5m2", CB_E5_MID, _bytes(n, seed=n))
+
+
+def test_bf16_bruteforce_all_patterns(orc):
+    x = torch.arange(65536, dtype=torch.int32, device="cuda").to(torch.int16).view(torch.bfloat16)
+    for cb in (CB_MID, CB_EDGES):
+        s = roundtrip_vs_oracle(orc, "bf16", cb, x)
+        assert s.size == 282648
+    # Every pattern in a shuffled order across several tiles and chunks.
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    perm = torch.cat([torch.randperm(65536, generator=g, device="cuda") for _ in range(5)])
+    roundtrip_vs_oracle(orc, "bf16", CB_EDGES, x[perm].contiguous())
+
+
+def test_e5m2_bruteforce_all_patterns(orc):
+    x = torch.arange(256, dtype=torch.int32, device="cuda").to(torch.uint8)
+    for cb in (CB_E5_MID, CB_E5_EDGES):
+        s = roundtrip_vs_oracle(orc, "e5m2", cb, x)
+        assert s.size == 632
+    g = torch.Generator(device="cuda")
+    g.manual_seed(6)
+    perm = torch.randint(0, 256, (5 * 65536 + 77,), generator=g, device="cuda")
+    roundtrip_vs_oracle(orc, "e5m2", CB_E5_EDGES, x[perm].contiguous())
+
+
+def test_unaligned_buffers(orc):
+    base = _gauss(3 * 65536 + 40, seed=11)
+    roundtrip_vs_oracle(orc, "bf16", CB_MID, base[1:], out_offset=1, dec_out_offset=2, dec_in_offset=3)
+    b8 = _bytes(2 * 65536 + 41, seed=12)
+    roundtrip_vs_oracle(orc, "e5m2", CB_E5_MID, b8[3:], out_offset=5, dec_out_offset=1, dec_in_offset=7)
+
+
+def test_all_escape_and_no_escape(orc):
+    n = 3 * 65536 + 999
+    x = _gauss(n, seed=13).view(torch.int16).to(torch.int32) & 0xFFFF
+    g = torch.Generator(device="cuda")
+    g.manual_seed(14)
+    outside = torch.randint(10, 110, (n,), generator=g, device="cuda", dtype=torch.int32)
+    inside = torch.randint(120, 136, (n,), generator=g, device="cuda", dtype=torch.int32)
+    x_all = ((x & 0x807F) | (outside << 7)).to(torch.int16).view(torch.bfloat16)
+    x_none = ((x & 0x807F) | (inside << 7)).to(torch.int16).view(torch.bfloat16)
+    s = roundtrip_vs_oracle(orc, "bf16", CB_MID, x_all)
+    assert s.size == n + (n + 1) // 2 + 3 * n + 16 + 8 * 4
+    s = roundtrip_vs_oracle(orc, "bf16", CB_MID, x_none)
+    assert s.size == n + (n + 1) // 2 + 16 + 8 * 4
+    b = _bytes(n, seed=15).to(torch.int32)
+    e_out = torch.randint(0, 14, (n,), generator=g, device="cuda", dtype=torch.int32)
+    b_all = ((b & 0x83) | (e_out << 2)).to(torch.uint8)
+    s = roundtrip_vs_oracle(orc, "e5m2", CB_E5_MID, b_all)
+    assert s.size == 7 * ((n + 7) // 8) + 3 * n + 16 + 8 * 4
+
+
+def test_calibration_matches_oracle(orc):
+    from lossless_kv_cache_bf16_gb300 import workloads as W
+
+    for kind, sample in (("bf16", W.kv_tiny("cuda", 1)), ("e5m2", W.fp8_e5m2_kv("cuda", 1, layers=1, tokens=256)),
+                         ("bf16", _gauss(100003, seed=3))):
+        cb, hist = G.calibrate(G.DT[kind], sample)
+        xh = G.as_bytes(sample)
+        assert np.array_equal(hist, orc.histogram(ODT[kind], xh))
+        assert np.array_equal(cb, orc.calibrate(ODT[kind], xh))
+
+
+def test_tiny_config(orc):
+    from lossless_kv_cache_bf16_gb300 import workloads as W
+
+    x = W.kv_tiny("cuda", 0)
+    cb, _ = G.calibrate(G.DT["bf16"], W.kv_tiny("cuda", 1))
+    roundtrip_vs_oracle(orc, "bf16", cb, x)
+
+
+def test_encode_on_side_stream(orc):
+    x = _gauss(5 * 65536 + 3, seed=21)
+    s = torch.cuda.Stream()
+    want = orc.encode(O.BF16, CB_MID, G.as_bytes(x))
+    with torch.cuda.stream(s):
+        got, st, size = G.encode(G.DT["bf16"], CB_MID, x, stream=s)
+    assert st == 0 and np.array_equal(got, want)
+
+
+def test_capacity_overflow_reported(orc):
+    from lossless_kv_cache_bf16_gb300 import splitzip as S
+
+    x = _gauss(2 * 65536 + 5, seed=22)
+    n = x.numel()
+    want = orc.encode(O.BF16, CB_MID, G.as_bytes(x))
+    cap = S.sz_encoded_size(S.SZ_BF16, n, 0) + 30  # room for 10 escapes only
+    got, st, size = G.encode(S.SZ_BF16, CB_MID, x, capacity=cap)
+    assert st == S.SZ_ERR_CAPACITY and size == want.size
+    assert np.array_equal(got[:cap], want[:cap])  # everything that fits is right
