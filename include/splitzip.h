@@ -158,6 +158,30 @@ sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n,
 /* Human-readable name of a status code (static string). */
 const char* sz_status_string(int status);
 
+/* sz_encode for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this entry point exists for integration only.  Some callers
+ * cannot call cudaMalloc -- for instance a serving engine that has handed
+ * almost all device memory to its KV-cache pool and forbids further
+ * allocations, or a latency-critical path that must not take cudaMalloc's
+ * implicit device synchronisation -- and so cannot provide the workspace
+ * that sz_encode takes.  This call uses a workspace of 1 MiB + 16 bytes held
+ * in a static device array inside the library instead, and otherwise behaves
+ * exactly like sz_encode (same arguments, stream bytes, d_out_bytes and
+ * d_status semantics).  It allocates nothing and calls no allocating routine.
+ *  - Limit: n up to 2^30 BF16 or 2^31 E5M2 elements (131,072 tiles); larger n
+ *    returns SZ_ERR_CAPACITY at once and launches nothing.
+ *  - Every GPU that loads the library holds the 1 MiB array until the
+ *    process exits.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls on a device share the one array (each call clears what it
+ *    uses first), so calls that can overlap on the GPU -- on different
+ *    streams without ordering between them -- race and corrupt each other's
+ *    output.  Serialise them, e.g. by issuing them on one stream. */
+sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n,
+                            void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
+                            int* d_status, cudaStream_t stream);
+
 /* Testing hook, not for production use: sz_encode, except that the tile
  * counter starts at 1, so tile 0 is never processed and its successors'
  * bounded wait for its escape count runs out after wait_limit_ns.  Lets a

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "splitzip.h"
 #include "sz_params.h"
@@ -96,6 +97,38 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     return from_cuda(err);
 }
 
+// ---- encode without allocation ---------------------------------------------
+// sz_encode_noalloc keeps its workspace in this file-scope device array
+// instead of taking one from the caller.  Every GPU that loads the library
+// holds the array until the process exits.  Sized for 131,072 tiles: 2^30
+// BF16 or 2^31 E5M2 elements (2 GiB of input either way).
+constexpr uint64_t kNoAllocMaxTiles = 131072;
+constexpr uint64_t kNoAllocScratchBytes = 16 + 8 * kNoAllocMaxTiles;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Host code cannot use g_noalloc_scratch as a device address (in host code the
+// name is a host-side stand-in), so its device address is looked up once per
+// device, with that device current, and cached.
+constexpr int kMaxDevices = 128;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+sz_status noalloc_scratch_for_current_device(void** out) {
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return from_cuda(err);
+    if (dev < 0 || dev >= kMaxDevices) return SZ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (err != cudaSuccess) return from_cuda(err);
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SZ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -158,6 +191,18 @@ sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size
                     size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws, size_t ws_bytes,
                     cudaStream_t stream) {
     return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
+                       kWaitLimitNs, stream);
+}
+
+sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
+                            size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, cudaStream_t stream) {
+    if (!dtype_ok(dt)) return SZ_ERR_INVALID_ARG;
+    if (workspace_bytes(dt, n) > kNoAllocScratchBytes) return SZ_ERR_CAPACITY;  // beyond the static scratch
+    void* ws = nullptr;
+    const sz_status st = noalloc_scratch_for_current_device(&ws);
+    if (st != SZ_OK) return st;
+    // encode_impl clears the part of the scratch the kernel uses before launching.
+    return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, ws, kNoAllocScratchBytes, 0,
                        kWaitLimitNs, stream);
 }
 

@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "sz_decode": (i32, [i32, vp, sz, sz, vp, vp, vp]),
         "sz_status_string": (ctypes.c_char_p, [i32]),
         "sz_debug_encode_stalled": (i32, [i32, cbp, vp, sz, vp, sz, vp, vp, vp, sz, ctypes.c_ulonglong, vp]),
+        "sz_encode_noalloc": (i32, [i32, cbp, vp, sz, vp, sz, vp, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -171,6 +172,18 @@ def sz_decode(dt: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, y: tor
         raise ValueError("output buffer too small")
     _check("sz_decode", LIB.sz_decode(dt, _dev_ptr(stream_bytes, "stream"), in_bytes, n, _dev_ptr(y, "y"),
                                       _dev_ptr(status, "status"), _stream(stream)))
+
+
+def sz_encode_noalloc(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
+                      status: torch.Tensor | None, stream=None, n: int | None = None) -> None:
+    """sz_encode without a caller workspace (the library's static scratch is
+    used instead), for callers that cannot allocate device memory."""
+    c = _codebook(cb)
+    n = _elements(dt, x) if n is None else n
+    _check("sz_encode_noalloc", LIB.sz_encode_noalloc(dt, ctypes.byref(c), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
+                                                      out.numel() * out.element_size(),
+                                                      _dev_ptr(out_bytes, "out_bytes"), _dev_ptr(status, "status"),
+                                                      _stream(stream)))
 
 
 def sz_debug_encode_stalled(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
