@@ -120,9 +120,11 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.proc = None
+        self.started = False
         self.gpu = gpu_index
 
     def start(self):
+        self.started = True
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
@@ -132,7 +134,8 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            why = "nvidia-smi unavailable" if self.started else "not sampled (--profile)"
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [why], "samples": 0}
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
@@ -180,7 +183,14 @@ def main():
                     choices=["llama8b_prefill", "long_ctx_gqa", "fp8_e5m2", "escape_sweep", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="use only the first L layers of a layered workload (smaller captures for ncu)")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the timed encode/decode steps: no clock warm-up, e2e, memcpy or CPU baseline")
     args = ap.parse_args()
+    if args.profile:
+        args.no_cpu_baseline = True
+        args.e2e_steps = 0
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
@@ -250,6 +260,9 @@ def main():
 
     x = W.workload(args.config, dev)
     sample = W.calibration_sample(args.config, dev, full=x)
+    if args.layers is not None:
+        assert x.dim() == 5 and 0 < args.layers <= x.shape[0], "--layers needs a layered workload"
+        x = x[: args.layers].contiguous()
     hist = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device=dev)
     cb = S.sz_calibrate(dt, sample, hist)
     del sample
@@ -284,12 +297,13 @@ def main():
         decode(size)
     # Keep the GPU busy for a moment so the clock sampler sees it under load.
     sampler = ClockSampler(local_rank)
-    sampler.start()
-    t_end = time.time() + 0.6
-    while time.time() < t_end:
-        encode()
-        decode(size)
-        torch.cuda.synchronize()
+    if not args.profile:
+        sampler.start()
+        t_end = time.time() + 0.6
+        while time.time() < t_end:
+            encode()
+            decode(size)
+            torch.cuda.synchronize()
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -318,48 +332,53 @@ def main():
 
     value, t_max = aggregate(K * n_bytes, gather_elapsed(dist, elapsed, dev))
 
-    # End to end through the C ABI with host buffers: pinned H2D of the input,
-    # encode, decode, D2H of the decoded tensor, every step.
-    xh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
-    xh.copy_(x.view(torch.uint8).reshape(-1))
-    yh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
-    xv = x.view(torch.uint8).reshape(-1)
-    yv = y.view(torch.uint8).reshape(-1)
-    for _ in range(2):
-        xv.copy_(xh, non_blocking=True)
-        encode()
-        decode(size)
-        yh.copy_(yv, non_blocking=True)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_a.record(stream)
-    for _ in range(args.e2e_steps):
-        xv.copy_(xh, non_blocking=True)
-        encode()
-        decode(size)
-        yh.copy_(yv, non_blocking=True)
-    e_b.record(stream)
-    torch.cuda.synchronize()
-    e2e_t = e_a.elapsed_time(e_b) / 1e3
-    e2e_value, _ = aggregate(args.e2e_steps * n_bytes, gather_elapsed(dist, e2e_t, dev))
-    assert torch.equal(yh, xh), "end-to-end round trip is not bit-exact"
+    e2e = None
+    memcpy_gbs = None
+    if not args.profile and args.e2e_steps > 0:
+        # End to end through the C ABI with host buffers: pinned H2D of the input,
+        # encode, decode, D2H of the decoded tensor, every step.
+        xh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
+        xh.copy_(x.view(torch.uint8).reshape(-1))
+        yh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
+        xv = x.view(torch.uint8).reshape(-1)
+        yv = y.view(torch.uint8).reshape(-1)
+        for _ in range(2):
+            xv.copy_(xh, non_blocking=True)
+            encode()
+            decode(size)
+            yh.copy_(yv, non_blocking=True)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        for _ in range(args.e2e_steps):
+            xv.copy_(xh, non_blocking=True)
+            encode()
+            decode(size)
+            yh.copy_(yv, non_blocking=True)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        e2e_t = e_a.elapsed_time(e_b) / 1e3
+        e2e_value, _ = aggregate(args.e2e_steps * n_bytes, gather_elapsed(dist, e2e_t, dev))
+        assert torch.equal(yh, xh), "end-to-end round trip is not bit-exact"
 
-    # Device-to-device copy bandwidth in the same run (bytes = read + write).
-    a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    b = torch.empty_like(a)
-    for _ in range(3):
-        b.copy_(a)
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c0.record(stream)
-    for _ in range(10):
-        b.copy_(a)
-    c1.record(stream)
-    torch.cuda.synchronize()
-    memcpy_gbs = 2 * a.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
-    del a, b
+        # Device-to-device copy bandwidth in the same run (bytes = read + write).
+        a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        b = torch.empty_like(a)
+        for _ in range(3):
+            b.copy_(a)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(10):
+            b.copy_(a)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        memcpy_gbs = 2 * a.numel() * 10 / (c0.elapsed_time(c1) / 1e3) / 1e9
+        del a, b
 
+        e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": n_bytes, "d2h_bytes_per_step": n_bytes,
+               "steps": args.e2e_steps}
     te, td = statistics.mean(t_enc), statistics.mean(t_dec)
     enc_gbs, dec_gbs = n_bytes / te / 1e9, n_bytes / td / 1e9
     peak, peak_src = measured_peaks()
@@ -394,7 +413,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u8" if not is_bf16 else "u16", "data": "synthetic",
-        "config": {"workload": args.config, "elements": n, "input_bytes": n_bytes,
+        "config": {"workload": args.config + (f"[:{args.layers} layers]" if args.layers else ""), "elements": n, "input_bytes": n_bytes,
                    "step": "one sz_encode + one sz_decode of the whole tensor",
                    "l2": "inputs larger than L2 (129 MB); no flush", "parallelism": f"{world} independent shards"},
         "encode_gbs": enc_gbs, "decode_gbs": dec_gbs,
@@ -407,8 +426,7 @@ def main():
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
                           "hardware": "not named on the pages"},
         "roofline": roofline, "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": n_bytes, "d2h_bytes_per_step": n_bytes,
-                "steps": args.e2e_steps},
+        "e2e": e2e,
         "gpu_launches": 2 * K, "clocks": clocks,
     }
     print(json.dumps(line))

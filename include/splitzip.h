@@ -164,13 +164,13 @@ const char* sz_status_string(int status);
  * almost all device memory to its KV-cache pool and forbids further
  * allocations, or a latency-critical path that must not take cudaMalloc's
  * implicit device synchronisation -- and so cannot provide the workspace
- * that sz_encode takes.  This call uses a workspace of 1 MiB + 16 bytes held
- * in a static device array inside the library instead, and otherwise behaves
+ * that sz_encode takes.  This call uses a workspace of 512 KiB + 16 bytes
+ * held in a static device array inside the library instead, and otherwise behaves
  * exactly like sz_encode (same arguments, stream bytes, d_out_bytes and
  * d_status semantics).  It allocates nothing and calls no allocating routine.
- *  - Limit: n up to 2^30 BF16 or 2^31 E5M2 elements (131,072 tiles); larger n
- *    returns SZ_ERR_CAPACITY at once and launches nothing.
- *  - Every GPU that loads the library holds the 1 MiB array until the
+ *  - Limit: n up to 2^30 elements of either dtype; larger n returns
+ *    SZ_ERR_CAPACITY at once and launches nothing.
+ *  - Every GPU that loads the library holds the 512 KiB array until the
  *    process exits.
  *  - The first call on each device looks up the array's device address with
  *    that device current; make that first call before any stream capture.

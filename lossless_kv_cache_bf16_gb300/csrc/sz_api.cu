@@ -18,9 +18,14 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded inter-block waits: 
 bool dtype_ok(int dt) { return dt == SZ_BF16 || dt == SZ_FP8_E5M2; }
 uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 uint64_t dense_bytes(sz_dtype dt, uint64_t n) { return dt == SZ_BF16 ? n + cdiv(n, 2) : 7 * cdiv(n, 8); }
-uint64_t tile_elems(sz_dtype dt) { return dt == SZ_BF16 ? kBf16Tile : kE5Tile; }
+// Elements per look-back tile of the encoder (one workspace word each).
+uint64_t tile_elems(sz_dtype dt) { return dt == SZ_BF16 ? kBf16ScanTile : kE5Tile; }
 uint64_t tiles_for(sz_dtype dt, uint64_t n) { return std::max<uint64_t>(1, cdiv(n, tile_elems(dt))); }
 uint64_t workspace_bytes(sz_dtype dt, uint64_t n) { return 16 + 8 * tiles_for(dt, n); }
+// Tiles of the decoder (independent of the encoder's look-back tiles).
+uint64_t decode_tiles_for(sz_dtype dt, uint64_t n) {
+    return std::max<uint64_t>(1, cdiv(n, dt == SZ_BF16 ? kBf16Tile : kE5Tile));
+}
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 StreamLayout layout_for(sz_dtype dt, uint64_t n) {
@@ -84,6 +89,8 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     p.wait_limit_ns = wait_ns;
     std::memcpy(p.cb, h_cb->exp, SZ_CODEBOOK_SIZE);
     std::sort(p.cb, p.cb + SZ_CODEBOOK_SIZE);  // code k = k-th smallest exponent
+    p.contig = p.cb[SZ_CODEBOOK_SIZE - 1] - p.cb[0] == SZ_CODEBOOK_SIZE - 1;
+    p.skip_first = first_ticket;
     if (dt == SZ_BF16)
         p.vec = aligned(d_in, 16) && aligned(d_out, 8) && aligned(static_cast<uint8_t*>(d_out) + n, 4);
     else
@@ -100,10 +107,12 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
 // ---- encode without allocation ---------------------------------------------
 // sz_encode_noalloc keeps its workspace in this file-scope device array
 // instead of taking one from the caller.  Every GPU that loads the library
-// holds the array until the process exits.  Sized for 131,072 tiles: 2^30
-// BF16 or 2^31 E5M2 elements (2 GiB of input either way).
-constexpr uint64_t kNoAllocMaxTiles = 131072;
-constexpr uint64_t kNoAllocScratchBytes = 16 + 8 * kNoAllocMaxTiles;
+// holds the array until the process exits.  Sized for n up to 2^30 elements
+// of either dtype: 512 KiB + 16 bytes.
+constexpr uint64_t kNoAllocMaxElems = 1ull << 30;
+constexpr uint64_t kNoAllocScratchBytes =
+    16 + 8 * ((kNoAllocMaxElems + std::min<uint64_t>(kBf16ScanTile, kE5Tile) - 1) /
+              std::min<uint64_t>(kBf16ScanTile, kE5Tile));
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Host code cannot use g_noalloc_scratch as a device address (in host code the
@@ -197,7 +206,8 @@ sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size
 sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                             size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, cudaStream_t stream) {
     if (!dtype_ok(dt)) return SZ_ERR_INVALID_ARG;
-    if (workspace_bytes(dt, n) > kNoAllocScratchBytes) return SZ_ERR_CAPACITY;  // beyond the static scratch
+    if ((uint64_t)n > kNoAllocMaxElems || workspace_bytes(dt, n) > kNoAllocScratchBytes)
+        return SZ_ERR_CAPACITY;  // beyond the static scratch
     void* ws = nullptr;
     const sz_status st = noalloc_scratch_for_current_device(&ws);
     if (st != SZ_OK) return st;
@@ -228,9 +238,10 @@ sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, vo
     p.L = layout_for(dt, n);
     p.in = static_cast<const uint8_t*>(d_in);
     p.out = static_cast<uint8_t*>(d_out);
-    p.num_tiles = (uint32_t)tiles_for(dt, n);
+    p.num_tiles = (uint32_t)decode_tiles_for(dt, n);
     p.n_esc = (uint32_t)n_esc;
     p.status = d_status;
+    p.wait_limit_ns = kWaitLimitNs;
     if (dt == SZ_BF16)
         p.vec = aligned(d_in, 8) && aligned(static_cast<const uint8_t*>(d_in) + n, 4) && aligned(d_out, 16);
     else

@@ -14,6 +14,9 @@
 // (k, lane, j) inside each warp, which is the order escapes are ranked in.
 #include "sz_device.cuh"
 #include "sz_params.h"
+#include "sz_pipeline.cuh"
+
+#include <algorithm>
 
 namespace sz {
 
@@ -23,10 +26,6 @@ constexpr uint32_t kTilesPerChunk = kChunk / kBf16Tile;  // 8
 static_assert(kChunk % kBf16Tile == 0, "tiles must not straddle chunks");
 constexpr uint32_t kWarps = kBf16Threads / 32;
 
-__device__ __forceinline__ uint64_t group_start(uint64_t base, uint32_t warp, uint32_t k, uint32_t lane) {
-    return base + warp * 1024u + k * 256u + lane * 8u;
-}
-
 // sign|mantissa bytes of the two BF16 values in a 32-bit word, at bytes 0 and 2.
 __device__ __forceinline__ uint32_t sm_pair(uint32_t w) {
     return (w & 0x007F007Fu) | ((w >> 8) & 0x00800080u);
@@ -35,306 +34,692 @@ __device__ __forceinline__ uint32_t sm_pair(uint32_t w) {
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Encode.  One pass: dense streams are stored as soon as they are computed;
-// the tile's escapes are ranked (warp ballot/popc scans, then a block scan),
-// staged in shared memory, and copied out once the decoupled look-back has
-// given the number of escapes in all earlier tiles.
+// Encode: a persistent, warp-specialised kernel (cooperative launch).
+//
+// The escape offset is resolved per "scan tile" of 32,768 elements (four
+// 8,192-element sub-tiles; two scan tiles per chunk).  Block b owns scan
+// tiles b, b + G, b + 2G, ... (G co-resident blocks), so every predecessor of
+// a scan tile is in flight or done and no tile ticket is needed.  Nine warps:
+//  * eight compute warps take sub-tiles from a 4-stage ring of shared-memory
+//    buffers filled by TMA bulk copies (thread 0 issues them).  Per sub-tile
+//    they split, code and pack, store the dense streams, and rank the
+//    escapes (ballot/popc warp scans, then a block scan), staging them as
+//    3-byte records in the scan tile's record slot.  After a scan tile's
+//    last sub-tile they publish its escape count for the look-back at once;
+//  * one scanner warp takes finished scan tiles in order, runs the look-back
+//    (256 predecessors per memory round trip), copies the staged records to
+//    their place, and writes the chunk headers, the codebook and the stream
+//    size.  A chunk's last scan tile writes the chunk's header from its own
+//    prefix and its predecessor's count, both at hand after its look-back.
+// A scan tile with more escapes than a slot holds ("overflow") is re-read
+// from global memory by the compute warps once the scanner has published its
+// offset, and its records are written directly.  Every wait is bounded.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBf16Threads) encode_bf16_kernel(const EncodeParams p) {
-    __shared__ uint8_t s_code[256];              // exponent -> code; 0x10 marks an escape
-    __shared__ uint8_t s_rec[3 * kBf16Tile];     // this tile's escape records, in order
-    __shared__ uint32_t s_warp_esc[kWarps];
-    __shared__ uint32_t s_tile, s_prefix;
-    __shared__ int s_failed;
+namespace {
 
+constexpr uint32_t kEncStages = 4;
+constexpr uint32_t kRecSlots = 2;
+constexpr uint32_t kSubsPerScan = 4;
+constexpr uint32_t kScanTile = kBf16Tile * kSubsPerScan;      // 32768 elements
+constexpr uint32_t kScansPerChunk = kChunk / kScanTile;       // 2
+constexpr uint32_t kSlotRecs = 4096;                          // records staged per scan tile
+constexpr uint32_t kComputeThreads = kBf16Threads;           // 256
+constexpr uint32_t kEncThreads = kComputeThreads + 32;       // + scanner warp
+constexpr uint32_t kTileBytes = kBf16Tile * 2;               // 16 KB of BF16 per sub-tile
+static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
+
+struct EncodeSmem {
+    alignas(128) uint8_t in[kEncStages][kTileBytes];
+    uint8_t rec[kRecSlots][3 * kSlotRecs];
+    uint64_t full[kEncStages];        // TMA -> compute: sub-tile landed
+    uint64_t staged[kRecSlots];       // compute -> scanner: scan tile finished
+    uint64_t prefix_ready[kRecSlots]; // scanner -> compute: offset published
+    uint64_t recfree[kRecSlots];      // scanner -> compute: slot reusable
+    uint32_t tile_esc[kRecSlots];
+    uint32_t prefix[kRecSlots];
+    int overflow[kRecSlots];
+    int failed[kRecSlots];
+    uint32_t warp_esc[2][kWarps];
+    uint8_t code[256];                // exponent -> code; 0x10 marks an escape
+};
+
+struct GroupOut {
+    uint32_t sm_lo, sm_hi, nib, esc;
+};
+
+// Split and code one group of 8 elements (four BF16 pairs).  CONTIG: the
+// codebook is cb0..cb0+15, so code = exponent - cb0 with one range test per
+// element, computed two elements per 32-bit word (16-bit lanes).
+template <bool CONTIG>
+__device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t cnt, uint32_t lane_add,
+                                               const uint8_t* s_code) {
+    GroupOut o;
+    o.sm_lo = __byte_perm(sm_pair(w[0]), sm_pair(w[1]), 0x6420);
+    o.sm_hi = __byte_perm(sm_pair(w[2]), sm_pair(w[3]), 0x6420);
+    uint32_t m = 0;
+    if (CONTIG) {
+        // Per 16-bit lane: u = exponent + 256 - cb0; in the codebook iff
+        // u is in [256, 272), and then the code is u & 0xF.
+        uint32_t u[4], bad = 0;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            u[q] = ((w[q] >> 7) & 0x00FF00FFu) + lane_add;
+            bad |= (u[q] & 0x01F001F0u) ^ 0x01000100u;
+        }
+        uint32_t a = (u[0] & 0x000F000Fu) | ((u[1] & 0x000F000Fu) << 8);  // codes 0,2,1,3 at bytes 0..3
+        uint32_t b = (u[2] & 0x000F000Fu) | ((u[3] & 0x000F000Fu) << 8);
+        a |= a >> 12;  // low half: code0 | code1 << 4 | code2 << 8 | code3 << 12
+        b |= b >> 12;
+        uint32_t nib = __byte_perm(a, b, 0x5410);
+        if (bad) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const uint32_t f = (u[j >> 1] >> (16 * (j & 1))) & 0x1F0u;
+                if (f != 0x100u) {
+                    m |= 1u << j;
+                    nib &= ~(0xFu << (4 * j));
+                }
+            }
+        }
+        o.nib = nib;
+    } else {
+        uint32_t nib = 0, flags = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t c = s_code[(w[j >> 1] >> (7 + 16 * (j & 1))) & 0xFFu];
+            nib |= (c & 0xFu) << (4 * j);
+            flags |= (c & 0x10u) << j;  // bit 4 + j set for an escape
+        }
+        m = (flags >> 4) & 0xFFu;
+        o.nib = nib;
+    }
+    if (cnt < 8) {
+        m &= (1u << cnt) - 1u;
+        o.nib &= (uint32_t)((1ull << (4 * cnt)) - 1ull);
+    }
+    o.esc = m;
+    return o;
+}
+
+// Escape ranks inside one warp's 1024 elements, in (k, lane, j) order:
+// off[k] = escapes of this warp before lane's group k; returns the warp total.
+__device__ __forceinline__ uint32_t warp_escape_ranks(const uint32_t (&esc)[4], uint32_t lane, uint32_t (&off)[4]) {
+    off[0] = off[1] = off[2] = off[3] = 0;
+    if (!__any_sync(0xFFFFFFFFu, (esc[0] | esc[1] | esc[2] | esc[3]) != 0)) return 0;
+    const uint32_t c01 = __popc(esc[0]) | ((uint32_t)__popc(esc[1]) << 16);
+    const uint32_t c23 = __popc(esc[2]) | ((uint32_t)__popc(esc[3]) << 16);
+    uint32_t s01 = c01, s23 = c23;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, s01, d);
+        const uint32_t b = __shfl_up_sync(0xFFFFFFFFu, s23, d);
+        if (lane >= (uint32_t)d) s01 += a, s23 += b;
+    }
+    const uint32_t t01 = __shfl_sync(0xFFFFFFFFu, s01, 31);
+    const uint32_t t23 = __shfl_sync(0xFFFFFFFFu, s23, 31);
+    const uint32_t x01 = s01 - c01, x23 = s23 - c23;
+    const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
+    off[0] = x01 & 0xFFFFu;
+    off[1] = tot0 + (x01 >> 16);
+    off[2] = tot0 + tot1 + (x23 & 0xFFFFu);
+    off[3] = tot0 + tot1 + tot2 + (x23 >> 16);
+    return tot0 + tot1 + tot2 + tot3;
+}
+
+}  // namespace
+
+template <bool CONTIG>
+__global__ void __launch_bounds__(kEncThreads, 1) encode_bf16_kernel(const EncodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    {
+    const uint64_t n = p.L.n;
+    const uint32_t G = p.grid;
+    const uint32_t num_scan = p.num_tiles;                          // scan tiles
+    const uint32_t num_subs = n == 0 ? 1u : (uint32_t)((n + kBf16Tile - 1) / kBf16Tile);
+    const uint32_t k0 = (p.skip_first && blockIdx.x == 0) ? 1u : 0u;  // test hook: skip scan tile 0
+    const uint32_t my_scans = blockIdx.x >= num_scan ? 0u : (num_scan - 1 - blockIdx.x) / G + 1;
+    auto scan_of = [&](uint32_t k) { return blockIdx.x + k * G; };
+    // Sub-tiles of this block, in order: index i -> scan tile k0 + i/4, part i%4.
+    const uint32_t my_subs =
+        my_scans <= k0 ? 0u
+                       : (my_scans - k0 - 1) * kSubsPerScan +
+                             min(kSubsPerScan, num_subs - scan_of(my_scans - 1) * kSubsPerScan);
+    auto sub_of = [&](uint32_t i) { return scan_of(k0 + i / kSubsPerScan) * kSubsPerScan + i % kSubsPerScan; };
+
+    if (tid == 0) {
+        for (uint32_t s = 0; s < kEncStages; s++) mbar_init(&S.full[s], 1);
+        for (uint32_t r = 0; r < kRecSlots; r++) {
+            mbar_init(&S.staged[r], kComputeThreads);
+            mbar_init(&S.prefix_ready[r], 1);
+            mbar_init(&S.recfree[r], 1);
+        }
+        fence_mbar_init();
+    }
+    if (tid < 256) {
         uint32_t code = 0x10u;
 #pragma unroll
         for (int k = 0; k < kCodes; k++)
             if (p.cb[k] == tid) code = (uint32_t)k;
-        s_code[tid] = (uint8_t)code;
-    }
-    if (tid == 0) s_tile = atomicAdd(p.ticket, 1u);
-    __syncthreads();
-    const uint32_t tile = s_tile;
-    if (tile >= p.num_tiles) return;  // only with the stalled-predecessor test hook
-    const uint64_t n = p.L.n;
-    const uint64_t base = (uint64_t)tile * kBf16Tile;
-
-    // Load the four groups of 8 elements.
-    uint32_t w[4][4];
-    uint32_t cnt[4];
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const uint64_t i0 = group_start(base, warp, k, lane);
-        cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
-        if (p.vec && cnt[k] == 8) {
-            const uint4 v = ld_stream_v4(p.in + 2 * i0);
-            w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 4; q++) w[k][q] = 0;
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if ((uint32_t)j < cnt[k]) {
-                    const uint8_t* e = p.in + 2 * (i0 + j);
-                    w[k][j >> 1] |= ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) << (16 * (j & 1));
-                }
-            }
-        }
-    }
-
-    // Split, code, pack, store; collect the escape mask of each group.
-    uint32_t esc[4];
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const uint64_t i0 = group_start(base, warp, k, lane);
-        const uint32_t sm_lo = __byte_perm(sm_pair(w[k][0]), sm_pair(w[k][1]), 0x6420);
-        const uint32_t sm_hi = __byte_perm(sm_pair(w[k][2]), sm_pair(w[k][3]), 0x6420);
-        uint32_t nib = 0, m = 0;
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const uint32_t e = (w[k][j >> 1] >> (7 + 16 * (j & 1))) & 0xFFu;
-            const uint32_t c = s_code[e];
-            nib |= (c & 0xFu) << (4 * j);
-            m |= (c >> 4) << j;
-        }
-        const uint32_t valid = (1u << cnt[k]) - 1u;  // cnt <= 8
-        m &= valid;
-        if (cnt[k] < 8) nib &= (uint32_t)((1ull << (4 * cnt[k])) - 1ull);
-        esc[k] = m;
-        if (p.vec && cnt[k] == 8) {
-            st_stream_v2(p.out + i0, make_uint2(sm_lo, sm_hi));
-            st_stream_u32(p.out + p.L.nib_off + i0 / 2, nib);
-        } else if (cnt[k] > 0) {
-            const uint64_t smv = (uint64_t)sm_lo | ((uint64_t)sm_hi << 32);
-            for (uint32_t j = 0; j < cnt[k]; j++) p.out[i0 + j] = (uint8_t)(smv >> (8 * j));
-            for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++) p.out[p.L.nib_off + i0 / 2 + b] = (uint8_t)(nib >> (8 * b));
-        }
-    }
-
-    // Rank escapes inside the warp in (k, lane, j) order: per-lane counts of
-    // the four groups packed two per word, inclusive warp scans.
-    uint32_t off[4] = {0, 0, 0, 0};
-    uint32_t warp_total = 0;
-    if (__any_sync(0xFFFFFFFFu, (esc[0] | esc[1] | esc[2] | esc[3]) != 0)) {
-        const uint32_t c01 = __popc(esc[0]) | ((uint32_t)__popc(esc[1]) << 16);
-        const uint32_t c23 = __popc(esc[2]) | ((uint32_t)__popc(esc[3]) << 16);
-        uint32_t s01 = c01, s23 = c23;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, s01, d);
-            const uint32_t b = __shfl_up_sync(0xFFFFFFFFu, s23, d);
-            if (lane >= (uint32_t)d) s01 += a, s23 += b;
-        }
-        const uint32_t t01 = __shfl_sync(0xFFFFFFFFu, s01, 31);
-        const uint32_t t23 = __shfl_sync(0xFFFFFFFFu, s23, 31);
-        const uint32_t x01 = s01 - c01, x23 = s23 - c23;
-        const uint32_t tot0 = t01 & 0xFFFFu, tot1 = t01 >> 16, tot2 = t23 & 0xFFFFu, tot3 = t23 >> 16;
-        off[0] = x01 & 0xFFFFu;
-        off[1] = tot0 + (x01 >> 16);
-        off[2] = tot0 + tot1 + (x23 & 0xFFFFu);
-        off[3] = tot0 + tot1 + tot2 + (x23 >> 16);
-        warp_total = tot0 + tot1 + tot2 + tot3;
-    }
-    if (lane == 0) s_warp_esc[warp] = warp_total;
-    __syncthreads();
-    uint32_t warp_off = 0, tile_esc = 0;
-#pragma unroll
-    for (uint32_t v = 0; v < kWarps; v++) {
-        const uint32_t c = s_warp_esc[v];
-        if (v < warp) warp_off += c;
-        tile_esc += c;
-    }
-
-    // Stage this tile's records (position inside the chunk, raw exponent).
-    if (tile_esc != 0) {
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            if (esc[k] == 0) continue;
-            const uint64_t i0 = group_start(base, warp, k, lane);
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if ((esc[k] >> j) & 1u) {
-                    const uint32_t r = warp_off + off[k] + __popc(esc[k] & ((1u << j) - 1u));
-                    const uint32_t pos = (uint32_t)(i0 + j) & 0xFFFFu;
-                    const uint32_t e = (w[k][j >> 1] >> (7 + 16 * (j & 1))) & 0xFFu;
-                    s_rec[3 * r + 0] = (uint8_t)pos;
-                    s_rec[3 * r + 1] = (uint8_t)(pos >> 8);
-                    s_rec[3 * r + 2] = (uint8_t)e;
-                }
-            }
-        }
-    }
-
-    // Escapes in all earlier tiles (decoupled look-back by warp 0).
-    if (warp == 0) {
-        bool failed;
-        const uint32_t prefix = lookback_prefix(p.tile_status, tile, tile_esc, p.wait_limit_ns, &failed);
-        if (lane == 0) s_prefix = prefix, s_failed = failed;
+        S.code[tid] = (uint8_t)code;
     }
     __syncthreads();
-    if (s_failed) {
-        if (tid == 0 && p.status) atomicMax(p.status, kStatusTimeout);
-        return;
-    }
-    const uint32_t prefix = s_prefix;
 
-    // Copy the staged records to their final place (bytes, coalesced).
-    if (tile_esc != 0) {
-        const uint64_t dst = p.L.rec_off + 3ull * prefix;
-        const uint32_t nbytes = 3u * tile_esc;
-        for (uint32_t b = tid; b < nbytes; b += kBf16Threads)
-            if (dst + b < p.capacity) p.out[dst + b] = s_rec[b];
-    }
-
-    if (tid == 0) {
-        // The first tile of chunk c closes the header of chunk c - 1.
-        if (tile % kTilesPerChunk == 0 && tile > 0) {
-            const uint64_t wprev = wait_for_prefix(p.tile_status, tile - kTilesPerChunk, p.wait_limit_ns);
-            if (status_flag(wprev) == kFlagError) {
-                if (p.status) atomicMax(p.status, kStatusTimeout);
+    if (warp < kWarps) {
+        // ===================== compute warps =====================
+        const uint32_t lane_add = (0x100u - p.cb[0]) * 0x00010001u;
+        auto full_sub = [&](uint32_t u) { return p.vec && (uint64_t)(u + 1) * kBf16Tile <= n; };
+        auto issue = [&](uint32_t i) {  // thread 0 only: sub-tile i of this block into ring slot i % 4
+            const uint32_t u = sub_of(i), slot = i % kEncStages;
+            if (full_sub(u)) {
+                mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
+                bulk_g2s(S.in[slot], p.in + (uint64_t)u * kTileBytes, kTileBytes, &S.full[slot]);
             } else {
-                const uint32_t c = tile / kTilesPerChunk - 1;
-                const uint32_t first = status_prefix(wprev);
-                store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
-                store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, prefix - first);
+                mbar_arrive(&S.full[slot]);  // read straight from global instead
+            }
+        };
+        uint32_t issued = 0, waited = 0;
+        if (tid == 0)
+            for (; issued < my_subs && issued < kEncStages; issued++) issue(issued);
+
+        // Loads the 4 groups of sub-tile u from shared memory or global memory.
+        auto load_groups = [&](uint32_t u, const uint8_t* buf, uint32_t (&w)[4][4], uint32_t (&cnt)[4]) {
+            const uint64_t base = (uint64_t)u * kBf16Tile;
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
+                const uint64_t i0 = base + q0;
+                cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
+                if (buf) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(buf + 2 * q0);
+                    w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
+                } else if (p.vec && cnt[k] == 8) {
+                    const uint4 v = ld_stream_v4(p.in + 2 * i0);
+                    w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) w[k][q] = 0;
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) {
+                        if ((uint32_t)jj < cnt[k]) {
+                            const uint8_t* e = p.in + 2 * (i0 + jj);
+                            w[k][jj >> 1] |= ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) << (16 * (jj & 1));
+                        }
+                    }
+                }
+            }
+        };
+        // Writes the records of this thread's escapes, ranks from `first` on.
+        auto emit = [&](uint64_t u, const uint32_t (&w)[4][4], const uint32_t (&esc)[4], const uint32_t (&off)[4],
+                        uint64_t first, uint8_t* dst, uint64_t limit) {
+            const uint64_t base = u * kBf16Tile;
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                if (esc[k] == 0) continue;
+                const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) {
+                    if ((esc[k] >> jj) & 1u) {
+                        const uint64_t at = 3ull * (first + off[k] + __popc(esc[k] & ((1u << jj) - 1u)));
+                        const uint32_t pos = (uint32_t)(i0 + jj) & 0xFFFFu;
+                        const uint32_t e = (w[k][jj >> 1] >> (7 + 16 * (jj & 1))) & 0xFFu;
+                        if (at + 3 <= limit) {
+                            dst[at] = (uint8_t)pos;
+                            dst[at + 1] = (uint8_t)(pos >> 8);
+                            dst[at + 2] = (uint8_t)e;
+                        }
+                    }
+                }
+            }
+        };
+
+        bool aborted = false;
+        uint32_t i = 0;                     // sub-tiles processed by this block
+        uint32_t run = 0;                   // escapes so far in the current scan tile
+        for (uint32_t ks = 0; ks + k0 < my_scans && !aborted; ks++) {
+            const uint32_t st = scan_of(k0 + ks), r = ks % kRecSlots;
+            const uint32_t subs = min(kSubsPerScan, num_subs - st * kSubsPerScan);
+            bool failed_wait = false;
+            // Record slot r was last used two scan tiles ago; wait until it is free.
+            if (ks >= kRecSlots) failed_wait = !mbar_wait(&S.recfree[r], ((ks / kRecSlots) - 1) & 1u, p.wait_limit_ns);
+            run = 0;
+            for (uint32_t part = 0; part < subs; part++, i++) {
+                const uint32_t slot = i % kEncStages;
+                const uint32_t u = st * kSubsPerScan + part;
+                const uint64_t base = (uint64_t)u * kBf16Tile;
+                failed_wait |= !mbar_wait(&S.full[slot], (i / kEncStages) & 1u, p.wait_limit_ns);
+                if (!failed_wait) waited = i + 1;
+                uint32_t w[4][4], cnt[4];
+                load_groups(u, full_sub(u) ? S.in[slot] : nullptr, w, cnt);
+
+                uint32_t esc[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
+                    const GroupOut o = code_group<CONTIG>(w[k], cnt[k], lane_add, S.code);
+                    esc[k] = o.esc;
+                    if (p.vec && cnt[k] == 8) {
+                        st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
+                        st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
+                    } else if (cnt[k] > 0) {
+                        const uint64_t smv = (uint64_t)o.sm_lo | ((uint64_t)o.sm_hi << 32);
+                        for (uint32_t jj = 0; jj < cnt[k]; jj++) p.out[i0 + jj] = (uint8_t)(smv >> (8 * jj));
+                        for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++)
+                            p.out[p.L.nib_off + i0 / 2 + b] = (uint8_t)(o.nib >> (8 * b));
+                    }
+                }
+                uint32_t off[4];
+                const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
+                if (lane == 0) S.warp_esc[i & 1][warp] = warp_total;
+                // Block barrier: warp totals visible, and the ring slot consumed
+                // by every compute thread.  It also votes on failed waits.
+                if (named_sync_or(1, kComputeThreads, failed_wait)) {
+                    aborted = true;
+                    break;
+                }
+                if (tid == 0 && issued < my_subs) issue(issued++);
+                uint32_t warp_off = 0, sub_esc = 0;
+#pragma unroll
+                for (uint32_t v = 0; v < kWarps; v++) {
+                    const uint32_t c = S.warp_esc[i & 1][v];
+                    if (v < warp) warp_off += c;
+                    sub_esc += c;
+                }
+                if (run + sub_esc <= kSlotRecs && sub_esc) {
+                    uint32_t o4[4] = {off[0], off[1], off[2], off[3]};
+                    emit(u, w, esc, o4, run + warp_off, S.rec[r], sizeof(S.rec[r]));
+                }
+                run += sub_esc;
+            }
+            if (aborted) break;
+            const bool overflow = run > kSlotRecs;
+            if (tid == 0) {
+                // Publish the scan tile's escape count at once: successors'
+                // look-backs need it and must not wait for this block's scanner.
+                st_relaxed_u64(p.tile_status + st,
+                               st == 0 ? pack_status(kFlagPrefix, run, 0) : pack_status(kFlagAggregate, run, 0));
+                S.tile_esc[r] = run;
+                S.overflow[r] = overflow;
+            }
+            mbar_arrive(&S.staged[r]);
+            if (overflow) {
+                // Second pass over the scan tile: re-read it, rank again, and
+                // write the records straight to their place.
+                failed_wait = !mbar_wait(&S.prefix_ready[r], (ks / kRecSlots) & 1u, p.wait_limit_ns);
+                if (named_sync_or(1, kComputeThreads, failed_wait)) {
+                    aborted = true;
+                    break;
+                }
+                const bool ok = !S.failed[r];
+                const uint64_t dst = p.L.rec_off + 3ull * S.prefix[r];
+                uint32_t run2 = 0;
+                for (uint32_t part = 0; part < subs; part++) {
+                    const uint32_t u = st * kSubsPerScan + part;
+                    uint32_t w[4][4], cnt[4], esc[4], off[4];
+                    load_groups(u, nullptr, w, cnt);
+#pragma unroll
+                    for (int k = 0; k < 4; k++) esc[k] = code_group<CONTIG>(w[k], cnt[k], lane_add, S.code).esc;
+                    const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
+                    if (lane == 0) S.warp_esc[part & 1][warp] = warp_total;
+                    named_sync(1, kComputeThreads);
+                    uint32_t warp_off = 0, sub_esc = 0;
+#pragma unroll
+                    for (uint32_t v = 0; v < kWarps; v++) {
+                        const uint32_t c = S.warp_esc[part & 1][v];
+                        if (v < warp) warp_off += c;
+                        sub_esc += c;
+                    }
+                    if (ok) emit(u, w, esc, off, run2 + warp_off, p.out + dst, p.capacity > dst ? p.capacity - dst : 0);
+                    run2 += sub_esc;
+                }
+                named_sync(1, kComputeThreads);  // warp_esc reads done before the next reuse
             }
         }
-        // The last tile knows the total: stream size and the last header.
-        if (tile == p.num_tiles - 1) {
-            const uint32_t total = prefix + tile_esc;
-            const unsigned long long size = p.L.rec_off + 3ull * total;
-            *p.out_bytes = size;
-            if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
-            if (p.L.num_chunks > 0) {
-                const uint32_t c = p.L.num_chunks - 1;
-                const uint32_t first_tile = c * kTilesPerChunk;
-                uint32_t first = prefix;
-                bool ok = true;
-                if (first_tile != tile) {
-                    const uint64_t wf = wait_for_prefix(p.tile_status, first_tile, p.wait_limit_ns);
-                    ok = status_flag(wf) != kFlagError;
-                    first = status_prefix(wf);
+        if (aborted && p.status) atomicMax(p.status, kStatusTimeout);
+        // Copies in flight must land before the block exits (bounded).
+        if (tid == 0 && aborted)
+            for (uint32_t k = waited; k < issued; k++)
+                mbar_wait(&S.full[k % kEncStages], (k / kEncStages) & 1u, p.wait_limit_ns);
+    } else {
+        // ===================== scanner warp =====================
+        for (uint32_t ks = 0; ks + k0 < my_scans; ks++) {
+            const uint32_t r = ks % kRecSlots;
+            const uint32_t st = scan_of(k0 + ks);
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.staged[r], (ks / kRecSlots) & 1u, p.wait_limit_ns))) {
+                if (lane == 0 && p.status) atomicMax(p.status, kStatusTimeout);
+                // Publish an error so successors stop waiting for this tile.
+                if (lane == 0) st_relaxed_u64(p.tile_status + st, pack_status(kFlagError, 0, 0));
+                break;
+            }
+            const uint32_t tile_esc = S.tile_esc[r];
+            const bool overflow = S.overflow[r];
+            bool failed;
+            uint32_t agg_prev;
+            const uint32_t prefix = lookback_prefix_wide(p.tile_status, st, tile_esc, p.wait_limit_ns, &failed, &agg_prev);
+            if (lane == 0) {
+                S.prefix[r] = prefix;
+                S.failed[r] = failed;
+                mbar_arrive(&S.prefix_ready[r]);
+                if (failed && p.status) atomicMax(p.status, kStatusTimeout);
+            }
+            if (!failed && !overflow && tile_esc) {
+                const uint64_t dst = p.L.rec_off + 3ull * prefix;
+                const uint32_t nbytes = 3u * tile_esc;
+                for (uint32_t b = lane; b < nbytes; b += 32)
+                    if (dst + b < p.capacity) p.out[dst + b] = S.rec[r][b];
+            }
+            if (lane == 0 && !failed) {
+                const bool last = st == num_scan - 1;
+                // A chunk's last scan tile writes the chunk's header.
+                if (st % kScansPerChunk == kScansPerChunk - 1 || last) {
+                    const uint32_t c = st / kScansPerChunk;
+                    const bool has_prev = st % kScansPerChunk != 0;  // the chunk's first scan tile is st - 1
+                    const uint32_t first = has_prev ? prefix - agg_prev : prefix;
+                    const uint32_t count = has_prev ? agg_prev + tile_esc : tile_esc;
+                    if (p.L.num_chunks > 0) {
+                        store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
+                        store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, count);
+                    }
                 }
-                if (ok) {
-                    store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
-                    store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, total - first);
-                } else if (p.status) {
-                    atomicMax(p.status, kStatusTimeout);
+                if (last) {
+                    const unsigned long long size = p.L.rec_off + 3ull * (prefix + tile_esc);
+                    *p.out_bytes = size;
+                    if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
                 }
             }
+            if (st == 0 && lane < kCodes) p.out[p.L.cb_off + lane] = p.cb[lane];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.recfree[r]);
         }
     }
-    if (tile == 0 && tid < kCodes) p.out[p.L.cb_off + tid] = p.cb[tid];
 }
 
 // ---------------------------------------------------------------------------
-// Decode.  Dense pass: nibble byte -> two exponents through a 256-entry
-// shared LUT, joined with the sign|mantissa bytes.  Escapes of the tile (a
-// contiguous run of the chunk's sorted records) are checked and spread into
-// a shared bitmap + exponent table before the dense pass, so they are
-// applied in registers and every output byte is stored once.
+// Decode: a persistent kernel; block b owns the contiguous tile range
+// [bT/G, (b+1)T/G).  Because escape records are stored in element order, a
+// block's records also form one contiguous run of the stream: one block
+// search finds where the run starts (only when the range starts inside a
+// chunk), then a cursor walks the records through a shared-memory window.
+// Dense input (sign|mantissa bytes and nibbles) arrives through a 4-stage ring
+// of TMA bulk copies.  Per tile: nibble byte -> two exponents via a 256-entry
+// LUT, joined with the sm bytes; the tile's escapes are spread into a bitmap
+// and an exponent table and applied in registers, so every output byte is
+// stored once.
+//
+// Validation: every record is consumed by exactly one tile and checked there
+// (position inside the tile, above the previous one); a chunk's last tile
+// checks that all of the chunk's records were consumed, and a block whose
+// range ends inside a chunk checks that its cursor stops where the next
+// block's search starts.  Headers are checked as running sums.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBf16Threads) decode_bf16_kernel(const DecodeParams p) {
-    __shared__ uint32_t s_lut[256];
-    __shared__ uint32_t s_bits[kBf16Threads];
-    __shared__ uint8_t s_patch[kBf16Tile];
-    __shared__ uint32_t s_cnt[6];
-    __shared__ int s_bad;
+namespace {
 
+constexpr uint32_t kDecStages = 4;
+constexpr uint32_t kDecThreads = kBf16Threads;  // 256
+constexpr uint32_t kWindowRecs = 1024;
+
+struct DecodeSmem {
+    alignas(128) uint8_t sm[kDecStages][kBf16Tile];
+    alignas(128) uint8_t nib[kDecStages][kBf16Tile / 2];
+    uint64_t full[kDecStages];
+    uint32_t lut[256];
+    uint32_t bits[kDecThreads];
+    uint8_t patch[kBf16Tile];
+    uint8_t win[3 * kWindowRecs];
+    uint32_t scratch[8];
+    int bad;
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(kDecThreads, 1) decode_bf16_kernel(const DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint32_t tile = blockIdx.x;
     const uint64_t n = p.L.n;
-    const uint64_t base = (uint64_t)tile * kBf16Tile;
+    const uint32_t T = p.num_tiles, G = gridDim.x;
+    const uint32_t t_begin = (uint32_t)((uint64_t)blockIdx.x * T / G);
+    const uint32_t t_end = (uint32_t)((uint64_t)(blockIdx.x + 1) * T / G);
     const uint8_t* cb = p.in + p.L.cb_off;
+    const uint8_t* rec = p.in + p.L.rec_off;
+    // Bulk copies need both dense streams 16-byte aligned.
+    const bool tma = p.vec && (reinterpret_cast<uintptr_t>(p.in) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(p.in + p.L.nib_off) % 16 == 0);
 
-    s_lut[tid] = ((uint32_t)cb[tid & 15u] << 7) | ((uint32_t)cb[tid >> 4] << 23);
-    s_bits[tid] = 0;
-    if (tid == 0) s_bad = 0;
-
-    // Dense loads first, so they are in flight during the escape search.
-    uint2 smv[4];
-    uint32_t nibv[4], cnt[4];
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const uint64_t i0 = group_start(base, warp, k, lane);
-        cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
-        if (p.vec && cnt[k] == 8) {
-            smv[k] = ld_stream_v2(p.in + i0);
-            nibv[k] = ld_stream_u32(p.in + p.L.nib_off + i0 / 2);
-        } else {
-            uint64_t s = 0;
-            uint32_t nb = 0;
-            for (uint32_t j = 0; j < cnt[k]; j++) s |= (uint64_t)p.in[i0 + j] << (8 * j);
-            for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++) nb |= (uint32_t)p.in[p.L.nib_off + i0 / 2 + b] << (8 * b);
-            smv[k] = make_uint2((uint32_t)s, (uint32_t)(s >> 32));
-            nibv[k] = nb;
-        }
+    if (tid == 0) {
+        for (uint32_t s = 0; s < kDecStages; s++) mbar_init(&S.full[s], 1);
+        S.bad = 0;
+        fence_mbar_init();
     }
-    __syncthreads();  // s_bad initialised
-
+    S.lut[tid] = ((uint32_t)cb[tid & 15u] << 7) | ((uint32_t)cb[tid >> 4] << 23);
     if (tid < kCodes) {  // a codebook is 16 distinct exponents
         bool dup = false;
         for (int k = 0; k < kCodes; k++) dup |= (k != (int)tid) && cb[k] == cb[tid];
-        if (dup) s_bad = 1;
+        if (dup) S.bad = 1;  // ordered before the reads by the barriers below
     }
+    __syncthreads();
 
-    // Spread this tile's escapes into a bitmap (bit k*8+j of thread
-    // warp*32+lane) and a per-element exponent table.
-    for_each_tile_escape<kBf16Threads, kBf16Tile, false>(p, tile, s_cnt, &s_bad, [&](uint32_t q, uint32_t e) {
-        s_patch[q] = (uint8_t)e;
-        const uint32_t owner = (q >> 10) * 32u + ((q >> 3) & 31u);
-        const uint32_t bit = ((q >> 8) & 3u) * 8u + (q & 7u);
-        atomicOr(&s_bits[owner], 1u << bit);
-    });
-
-    const uint32_t bits = s_bits[tid];
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const uint64_t i0 = group_start(base, warp, k, lane);
-        uint32_t y[4];
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const uint32_t smw = q < 2 ? smv[k].x : smv[k].y;
-            const uint32_t t = __byte_perm(smw, 0, (q & 1) ? 0x4342 : 0x4140);
-            y[q] = (t & 0x007F007Fu) | ((t & 0x00800080u) << 8) | s_lut[(nibv[k] >> (8 * q)) & 0xFFu];
-        }
-        const uint32_t gb = (bits >> (8 * k)) & 0xFFu;
-        if (gb) {
-            const uint32_t qbase = warp * 1024u + k * 256u + lane * 8u;
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if ((gb >> j) & 1u) {
-                    const uint32_t sh = 7 + 16 * (j & 1);
-                    y[j >> 1] = (y[j >> 1] & ~(0xFFu << sh)) | ((uint32_t)s_patch[qbase + j] << sh);
-                }
-            }
-        }
-        if (p.vec && cnt[k] == 8) {
-            st_stream_v4(p.out + 2 * i0, make_uint4(y[0], y[1], y[2], y[3]));
+    auto full_tile = [&](uint32_t t) { return tma && (uint64_t)(t + 1) * kBf16Tile <= n; };
+    auto issue = [&](uint32_t slot, uint32_t t) {  // thread 0 only
+        if (full_tile(t)) {
+            mbar_arrive_expect_tx(&S.full[slot], kBf16Tile + kBf16Tile / 2);
+            bulk_g2s(S.sm[slot], p.in + (uint64_t)t * kBf16Tile, kBf16Tile, &S.full[slot]);
+            bulk_g2s(S.nib[slot], p.in + p.L.nib_off + (uint64_t)t * (kBf16Tile / 2), kBf16Tile / 2, &S.full[slot]);
         } else {
+            mbar_arrive(&S.full[slot]);
+        }
+    };
+    uint32_t issued = 0, waited = 0;
+    if (tid == 0)
+        for (uint32_t t = t_begin; t < t_end && t < t_begin + kDecStages; t++, issued++) issue((t - t_begin) % kDecStages, t);
+
+    // Record window [win_lo, win_lo + win_len) and the walk state.
+    uint32_t win_lo = 0, win_len = 0;
+    uint32_t chunk_o = 0, chunk_end = 0, cursor = 0;
+    auto win_pos = [&](uint32_t j) {
+        const uint8_t* r = S.win + 3 * (j - win_lo);
+        return (uint32_t)r[0] | ((uint32_t)r[1] << 8);
+    };
+    auto refill = [&](uint32_t from) {  // block-wide; ends with a barrier
+        __syncthreads();
+        win_lo = from;
+        win_len = min(kWindowRecs, p.n_esc - from);
+        for (uint32_t b = tid; b < 3 * win_len; b += kDecThreads) S.win[b] = rec[3ull * from + b];
+        __syncthreads();
+    };
+
+    bool aborted = false;
+    uint32_t i = 0;
+    for (uint32_t t = t_begin; t < t_end; t++, i++) {
+        const uint32_t slot = i % kDecStages;
+        const uint64_t base = (uint64_t)t * kBf16Tile;
+        const uint32_t chunk = t / kTilesPerChunk;
+        const uint32_t p0 = (t % kTilesPerChunk) * kBf16Tile;
+        const uint32_t tile_len = n - base >= kBf16Tile ? kBf16Tile : (uint32_t)(n - base);
+        const bool first_of_chunk = t % kTilesPerChunk == 0;
+        const bool last_of_chunk = t % kTilesPerChunk == kTilesPerChunk - 1 || t == T - 1;
+
+        // Chunk header: at each chunk start and at the start of the range
+        // (n = 0 has no chunk and no header).
+        if (p.L.num_chunks > 0 && (first_of_chunk || t == t_begin)) {
+            if (tid == 0) {
+                const uint8_t* h = p.in + p.L.hdr_off + 8ull * chunk;
+                const uint32_t o = load_u32_le(h), m = load_u32_le(h + 4);
+                const uint64_t rest = n - (uint64_t)chunk * kChunk;
+                const uint64_t chunk_len = rest < kChunk ? rest : kChunk;
+                bool bad = m > chunk_len || o > p.n_esc || m > p.n_esc - o;
+                if (first_of_chunk) {
+                    if (chunk == 0) {
+                        bad |= o != 0;
+                    } else {
+                        const uint64_t po = load_u32_le(h - 8), pm = load_u32_le(h - 4);
+                        bad |= (uint64_t)o != po + pm;
+                    }
+                    if (chunk == p.L.num_chunks - 1) bad |= (uint64_t)o + m != p.n_esc;
+                }
+                if (bad) S.bad = 1;
+                S.scratch[6] = o;
+                S.scratch[7] = bad ? 0u : m;
+            }
+            __syncthreads();
+            const uint32_t o = S.scratch[6], m = S.scratch[7];
+            chunk_o = o;
+            chunk_end = o + m;
+            cursor = o;
+            if (!first_of_chunk && m > 0) {  // range starts inside the chunk
+                uint32_t a, b;
+                block_lower_bounds<kDecThreads>(rec, o, m, p0, p0, S.scratch, &a, &b);
+                cursor = a;
+            }
+            __syncthreads();
+        }
+
+        S.bits[tid] = 0;
+        // Dense input of this tile.
+        const bool failed_wait = !mbar_wait(&S.full[slot], (i / kDecStages) & 1u, p.wait_limit_ns);
+        if (!failed_wait) waited = i + 1;
+        if (__syncthreads_or(failed_wait)) {
+            aborted = true;
+            break;
+        }
+        const bool from_smem = full_tile(t);
+        uint2 smv[4];
+        uint32_t nibv[4], cnt[4];
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                if ((uint32_t)j < cnt[k]) {
-                    const uint32_t v = y[j >> 1] >> (16 * (j & 1));
-                    p.out[2 * (i0 + j)] = (uint8_t)v;
-                    p.out[2 * (i0 + j) + 1] = (uint8_t)(v >> 8);
+        for (int k = 0; k < 4; k++) {
+            const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
+            const uint64_t i0 = base + q0;
+            cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
+            if (from_smem) {
+                smv[k] = *reinterpret_cast<const uint2*>(&S.sm[slot][q0]);
+                nibv[k] = *reinterpret_cast<const uint32_t*>(&S.nib[slot][q0 / 2]);
+            } else if (p.vec && cnt[k] == 8) {
+                smv[k] = ld_stream_v2(p.in + i0);
+                nibv[k] = ld_stream_u32(p.in + p.L.nib_off + i0 / 2);
+            } else {
+                uint64_t sv = 0;
+                uint32_t nb = 0;
+                for (uint32_t jj = 0; jj < cnt[k]; jj++) sv |= (uint64_t)p.in[i0 + jj] << (8 * jj);
+                for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++) nb |= (uint32_t)p.in[p.L.nib_off + i0 / 2 + b] << (8 * b);
+                smv[k] = make_uint2((uint32_t)sv, (uint32_t)(sv >> 32));
+                nibv[k] = nb;
+            }
+        }
+
+        // This tile's records: the prefix of the run with position < tile end.
+        uint32_t prev = 0xFFFFFFFFu;  // position of the tile's previous record
+        while (cursor < chunk_end) {
+            const uint32_t nb = min(kDecThreads, chunk_end - cursor);
+            if (cursor < win_lo || cursor + nb > win_lo + win_len) refill(cursor);
+            uint32_t pos = 0xFFFFFFFFu, e = 0;
+            if (tid < nb) {
+                pos = win_pos(cursor + tid);
+                e = S.win[3 * (cursor + tid - win_lo) + 2];
+            }
+            const bool mine = tid < nb && pos < p0 + kBf16Tile;
+            const uint32_t k = (uint32_t)__syncthreads_count(mine);
+            if (tid < k) {
+                const uint32_t before = tid == 0 ? prev : win_pos(cursor + tid - 1);
+                const bool ok = pos >= p0 && pos - p0 < tile_len && (before == 0xFFFFFFFFu || pos > before);
+                if (!ok) {
+                    S.bad = 1;
+                } else {
+                    const uint32_t q = pos - p0;
+                    S.patch[q] = (uint8_t)e;
+                    atomicOr(&S.bits[(q >> 10) * 32u + ((q >> 3) & 31u)], 1u << (((q >> 8) & 3u) * 8u + (q & 7u)));
+                }
+            }
+            if (k > 0) prev = win_pos(cursor + k - 1);
+            cursor += k;
+            __syncthreads();
+            if (k < nb) break;
+        }
+        if (last_of_chunk && cursor != chunk_end && tid == 0) S.bad = 1;
+        if (t == t_end - 1 && !last_of_chunk && chunk_end > chunk_o) {
+            // Hand-off: the next block starts its walk where its search says.
+            uint32_t a, b;
+            block_lower_bounds<kDecThreads>(rec, chunk_o, chunk_end - chunk_o, p0 + kBf16Tile, p0 + kBf16Tile,
+                                            S.scratch, &a, &b);
+            if (tid == 0 && a != cursor) S.bad = 1;
+        }
+
+        const uint32_t bits = S.bits[tid];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
+            uint32_t y[4];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t smw = q < 2 ? smv[k].x : smv[k].y;
+                const uint32_t tt = __byte_perm(smw, 0, (q & 1) ? 0x4342 : 0x4140);
+                y[q] = (tt & 0x007F007Fu) | ((tt & 0x00800080u) << 8) | S.lut[(nibv[k] >> (8 * q)) & 0xFFu];
+            }
+            const uint32_t gb = (bits >> (8 * k)) & 0xFFu;
+            if (gb) {
+                const uint32_t qbase = warp * 1024u + k * 256u + lane * 8u;
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) {
+                    if ((gb >> jj) & 1u) {
+                        const uint32_t sh = 7 + 16 * (jj & 1);
+                        y[jj >> 1] = (y[jj >> 1] & ~(0xFFu << sh)) | ((uint32_t)S.patch[qbase + jj] << sh);
+                    }
+                }
+            }
+            if (p.vec && cnt[k] == 8) {
+                st_stream_v4(p.out + 2 * i0, make_uint4(y[0], y[1], y[2], y[3]));
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) {
+                    if ((uint32_t)jj < cnt[k]) {
+                        const uint32_t v = y[jj >> 1] >> (16 * (jj & 1));
+                        p.out[2 * (i0 + jj)] = (uint8_t)v;
+                        p.out[2 * (i0 + jj) + 1] = (uint8_t)(v >> 8);
+                    }
                 }
             }
         }
+        __syncthreads();  // stage slot, bitmap and patch table free again
+        if (tid == 0 && t + kDecStages < t_end) issue(slot, t + kDecStages), issued++;
     }
-    if (tid == 0 && s_bad && p.status) atomicMax(p.status, kStatusCorrupt);
+    if (tid == 0 && aborted) {
+        for (uint32_t k = waited; k < issued; k++)
+            mbar_wait(&S.full[k % kDecStages], (k / kDecStages) & 1u, p.wait_limit_ns);
+        if (p.status) atomicMax(p.status, kStatusTimeout);
+    }
+    __syncthreads();
+    if (tid == 0 && S.bad && p.status) atomicMax(p.status, kStatusCorrupt);
 }
 
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
-    encode_bf16_kernel<<<p.num_tiles, kBf16Threads, 0, s>>>(p);
-    return cudaGetLastError();
+    const size_t smem = sizeof(EncodeSmem);
+    const void* kern = p.contig ? (const void*)encode_bf16_kernel<true> : (const void*)encode_bf16_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (err == cudaSuccess) err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kEncThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    // All blocks must be co-resident: a tile waits for its predecessors,
+    // which belong to other blocks.  The cooperative launch guarantees it.
+    EncodeParams q = p;
+    q.grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)per_sm * sms);
+    void* args[] = {&q};
+    err = cudaLaunchCooperativeKernel(kern, q.grid, kEncThreads, args, smem, s);
+    return err == cudaSuccess ? cudaGetLastError() : err;
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
-    decode_bf16_kernel<<<p.num_tiles, kBf16Threads, 0, s>>>(p);
+    const size_t smem = sizeof(DecodeSmem);
+    cudaError_t err = cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (err == cudaSuccess) err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_bf16_kernel, kDecThreads, smem);
+    if (err != cudaSuccess) return err;
+    const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
+    decode_bf16_kernel<<<grid, kDecThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

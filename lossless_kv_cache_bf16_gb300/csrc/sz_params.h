@@ -31,6 +31,9 @@ struct EncodeParams {
     int* status;             // nullable
     uint64_t wait_limit_ns;
     int vec;                 // 1 when the aligned vector path may be used
+    uint32_t grid;           // persistent kernels: blocks in the (cooperative) launch
+    uint32_t skip_first;     // test hook: tile 0 is never processed
+    int contig;              // codebook is 16 consecutive exponents cb[0]..cb[0]+15
     uint8_t cb[16];          // ascending
 };
 
@@ -42,6 +45,7 @@ struct DecodeParams {
     uint32_t n_esc;          // escape count implied by the stream size
     int* status;             // nullable
     int vec;
+    uint64_t wait_limit_ns;  // bounded waits for in-kernel copies
 };
 
 struct HistogramParams {
@@ -55,6 +59,7 @@ struct HistogramParams {
 constexpr uint32_t kBf16Threads = 256;
 constexpr uint32_t kBf16PerThread = 32;
 constexpr uint32_t kBf16Tile = kBf16Threads * kBf16PerThread;   // 8192
+constexpr uint32_t kBf16ScanTile = 4 * kBf16Tile;                // encode look-back unit: 32768
 constexpr uint32_t kE5Threads = 128;
 constexpr uint32_t kE5PerThread = 128;                          // 16 groups of 8
 constexpr uint32_t kE5Tile = kE5Threads * kE5PerThread;         // 16384

@@ -45,7 +45,8 @@ def test_encoded_size_matches_oracle(S, orc):
 
 
 def test_workspace_size(S):
-    for dt, tile in ((S.SZ_BF16, 8192), (S.SZ_FP8_E5M2, 16384)):
+    # One look-back word per encoder tile: 32,768 BF16 or 16,384 E5M2 elements.
+    for dt, tile in ((S.SZ_BF16, 32768), (S.SZ_FP8_E5M2, 16384)):
         assert S.sz_workspace_size(dt, 0) == 16 + 8
         assert S.sz_workspace_size(dt, tile) == 16 + 8
         assert S.sz_workspace_size(dt, tile + 1) == 16 + 16
