@@ -26,11 +26,6 @@ constexpr uint32_t kTilesPerChunk = kChunk / kBf16Tile;  // 8
 static_assert(kChunk % kBf16Tile == 0, "tiles must not straddle chunks");
 constexpr uint32_t kWarps = kBf16Threads / 32;
 
-// sign|mantissa bytes of the two BF16 values in a 32-bit word, at bytes 0 and 2.
-__device__ __forceinline__ uint32_t sm_pair(uint32_t w) {
-    return (w & 0x007F007Fu) | ((w >> 8) & 0x00800080u);
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -57,12 +52,12 @@ __device__ __forceinline__ uint32_t sm_pair(uint32_t w) {
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr uint32_t kEncStages = 4;
+constexpr uint32_t kEncStages = 3;
 constexpr uint32_t kRecSlots = 2;
 constexpr uint32_t kSubsPerScan = 4;
 constexpr uint32_t kScanTile = kBf16Tile * kSubsPerScan;      // 32768 elements
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;       // 2
-constexpr uint32_t kSlotRecs = 4096;                          // records staged per scan tile
+constexpr uint32_t kSlotRecs = 2048;                          // records staged per scan tile
 constexpr uint32_t kComputeThreads = kBf16Threads;           // 256
 constexpr uint32_t kEncThreads = kComputeThreads + 32;       // + scanner warp
 constexpr uint32_t kTileBytes = kBf16Tile * 2;               // 16 KB of BF16 per sub-tile
@@ -79,7 +74,7 @@ struct EncodeSmem {
     uint32_t prefix[kRecSlots];
     int overflow[kRecSlots];
     int failed[kRecSlots];
-    uint32_t warp_esc[2][kWarps];
+    alignas(16) uint32_t warp_esc[2][kWarps];
     uint8_t code[256];                // exponent -> code; 0x10 marks an escape
 };
 
@@ -90,12 +85,20 @@ struct GroupOut {
 // Split and code one group of 8 elements (four BF16 pairs).  CONTIG: the
 // codebook is cb0..cb0+15, so code = exponent - cb0 with one range test per
 // element, computed two elements per 32-bit word (16-bit lanes).
-template <bool CONTIG>
+// sign|mantissa bytes of the four BF16 values in two words: the low bytes
+// (exponent bit 0 | mantissa) and high bytes (sign | exponent bits 7..1) are
+// gathered with byte permutes, then one 3-input op keeps mantissa and sign.
+__device__ __forceinline__ uint32_t sm_quad(uint32_t w0, uint32_t w1) {
+    const uint32_t lo = __byte_perm(w0, w1, 0x6420), hi = __byte_perm(w0, w1, 0x7531);
+    return (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
+}
+
+template <bool CONTIG, bool FULL>
 __device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t cnt, uint32_t lane_add,
                                                const uint8_t* s_code) {
     GroupOut o;
-    o.sm_lo = __byte_perm(sm_pair(w[0]), sm_pair(w[1]), 0x6420);
-    o.sm_hi = __byte_perm(sm_pair(w[2]), sm_pair(w[3]), 0x6420);
+    o.sm_lo = sm_quad(w[0], w[1]);
+    o.sm_hi = sm_quad(w[2], w[3]);
     uint32_t m = 0;
     if (CONTIG) {
         // Per 16-bit lane: u = exponent + 256 - cb0; in the codebook iff
@@ -133,7 +136,7 @@ __device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t 
         m = (flags >> 4) & 0xFFu;
         o.nib = nib;
     }
-    if (cnt < 8) {
+    if (!FULL && cnt < 8) {
         m &= (1u << cnt) - 1u;
         o.nib &= (uint32_t)((1ull << (4 * cnt)) - 1ull);
     }
@@ -169,7 +172,7 @@ __device__ __forceinline__ uint32_t warp_escape_ranks(const uint32_t (&esc)[4], 
 }  // namespace
 
 template <bool CONTIG>
-__global__ void __launch_bounds__(kEncThreads, 1) encode_bf16_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kEncThreads, 3) encode_bf16_kernel(const EncodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -289,23 +292,35 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_bf16_kernel(const Encod
                 const uint64_t base = (uint64_t)u * kBf16Tile;
                 failed_wait |= !mbar_wait(&S.full[slot], (i / kEncStages) & 1u, p.wait_limit_ns);
                 if (!failed_wait) waited = i + 1;
-                uint32_t w[4][4], cnt[4];
-                load_groups(u, full_sub(u) ? S.in[slot] : nullptr, w, cnt);
-
-                uint32_t esc[4];
+                uint32_t w[4][4], cnt[4], esc[4];
+                if (full_sub(u)) {
+                    // Whole sub-tile in range, buffers aligned: no bounds logic.
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
-                    const GroupOut o = code_group<CONTIG>(w[k], cnt[k], lane_add, S.code);
-                    esc[k] = o.esc;
-                    if (p.vec && cnt[k] == 8) {
-                        st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
-                        st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
-                    } else if (cnt[k] > 0) {
-                        const uint64_t smv = (uint64_t)o.sm_lo | ((uint64_t)o.sm_hi << 32);
-                        for (uint32_t jj = 0; jj < cnt[k]; jj++) p.out[i0 + jj] = (uint8_t)(smv >> (8 * jj));
-                        for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++)
-                            p.out[p.L.nib_off + i0 / 2 + b] = (uint8_t)(o.nib >> (8 * b));
+                    for (int k = 0; k < 4; k++) {
+                        const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
+                        const uint4 v = *reinterpret_cast<const uint4*>(S.in[slot] + 2 * q0);
+                        w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
+                        const GroupOut o = code_group<CONTIG, true>(w[k], 8, lane_add, S.code);
+                        esc[k] = o.esc;
+                        st_stream_v2(p.out + base + q0, make_uint2(o.sm_lo, o.sm_hi));
+                        st_stream_u32(p.out + p.L.nib_off + (base + q0) / 2, o.nib);
+                    }
+                } else {
+                    load_groups(u, nullptr, w, cnt);
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
+                        const GroupOut o = code_group<CONTIG, false>(w[k], cnt[k], lane_add, S.code);
+                        esc[k] = o.esc;
+                        if (p.vec && cnt[k] == 8) {
+                            st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
+                            st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
+                        } else if (cnt[k] > 0) {
+                            const uint64_t smv = (uint64_t)o.sm_lo | ((uint64_t)o.sm_hi << 32);
+                            for (uint32_t jj = 0; jj < cnt[k]; jj++) p.out[i0 + jj] = (uint8_t)(smv >> (8 * jj));
+                            for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++)
+                                p.out[p.L.nib_off + i0 / 2 + b] = (uint8_t)(o.nib >> (8 * b));
+                        }
                     }
                 }
                 uint32_t off[4];
@@ -319,11 +334,15 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_bf16_kernel(const Encod
                 }
                 if (tid == 0 && issued < my_subs) issue(issued++);
                 uint32_t warp_off = 0, sub_esc = 0;
+                {
+                    const uint4 a = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][0]);
+                    const uint4 b = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][4]);
+                    const uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-                for (uint32_t v = 0; v < kWarps; v++) {
-                    const uint32_t c = S.warp_esc[i & 1][v];
-                    if (v < warp) warp_off += c;
-                    sub_esc += c;
+                    for (uint32_t v = 0; v < kWarps; v++) {
+                        warp_off += v < warp ? c[v] : 0u;
+                        sub_esc += c[v];
+                    }
                 }
                 if (run + sub_esc <= kSlotRecs && sub_esc) {
                     uint32_t o4[4] = {off[0], off[1], off[2], off[3]};
@@ -358,7 +377,7 @@ __global__ void __launch_bounds__(kEncThreads, 1) encode_bf16_kernel(const Encod
                     uint32_t w[4][4], cnt[4], esc[4], off[4];
                     load_groups(u, nullptr, w, cnt);
 #pragma unroll
-                    for (int k = 0; k < 4; k++) esc[k] = code_group<CONTIG>(w[k], cnt[k], lane_add, S.code).esc;
+                    for (int k = 0; k < 4; k++) esc[k] = code_group<CONTIG, false>(w[k], cnt[k], lane_add, S.code).esc;
                     const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
                     if (lane == 0) S.warp_esc[part & 1][warp] = warp_total;
                     named_sync(1, kComputeThreads);
@@ -472,7 +491,7 @@ struct DecodeSmem {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kDecThreads, 1) decode_bf16_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, 3) decode_bf16_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -574,7 +593,44 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_bf16_kernel(const Decod
             __syncthreads();
         }
 
-        S.bits[tid] = 0;
+        S.bits[tid] = 0;  // the previous tile's reads ended at its final barrier
+        // This tile's records: the prefix of the run with position < tile end.
+        uint32_t prev = 0xFFFFFFFFu;  // position of the tile's previous record
+        while (cursor < chunk_end) {
+            const uint32_t nb = min(kDecThreads, chunk_end - cursor);
+            if (cursor < win_lo || cursor + nb > win_lo + win_len) refill(cursor);
+            uint32_t pos = 0xFFFFFFFFu, e = 0;
+            if (tid < nb) {
+                pos = win_pos(cursor + tid);
+                e = S.win[3 * (cursor + tid - win_lo) + 2];
+            }
+            const bool mine = tid < nb && pos < p0 + kBf16Tile;
+            const uint32_t k = (uint32_t)__syncthreads_count(mine);
+            if (tid < k) {
+                const uint32_t before = tid == 0 ? prev : win_pos(cursor + tid - 1);
+                const bool ok = pos >= p0 && pos - p0 < tile_len && (before == 0xFFFFFFFFu || pos > before);
+                if (!ok) {
+                    S.bad = 1;
+                } else {
+                    const uint32_t q = pos - p0;
+                    S.patch[q] = (uint8_t)e;
+                    atomicOr(&S.bits[(q >> 10) * 32u + ((q >> 3) & 31u)], 1u << (((q >> 8) & 3u) * 8u + (q & 7u)));
+                }
+            }
+            if (k > 0) prev = win_pos(cursor + k - 1);
+            cursor += k;
+            if (k < nb) break;  // the barrier after the input wait orders the applies
+            __syncthreads();    // window reads done before the next batch may refill it
+        }
+        if (last_of_chunk && cursor != chunk_end && tid == 0) S.bad = 1;
+        if (t == t_end - 1 && !last_of_chunk && chunk_end > chunk_o) {
+            // Hand-off: the next block starts its walk where its search says.
+            uint32_t a, b;
+            block_lower_bounds<kDecThreads>(rec, chunk_o, chunk_end - chunk_o, p0 + kBf16Tile, p0 + kBf16Tile,
+                                            S.scratch, &a, &b);
+            if (tid == 0 && a != cursor) S.bad = 1;
+        }
+
         // Dense input of this tile.
         const bool failed_wait = !mbar_wait(&S.full[slot], (i / kDecStages) & 1u, p.wait_limit_ns);
         if (!failed_wait) waited = i + 1;
@@ -606,43 +662,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_bf16_kernel(const Decod
             }
         }
 
-        // This tile's records: the prefix of the run with position < tile end.
-        uint32_t prev = 0xFFFFFFFFu;  // position of the tile's previous record
-        while (cursor < chunk_end) {
-            const uint32_t nb = min(kDecThreads, chunk_end - cursor);
-            if (cursor < win_lo || cursor + nb > win_lo + win_len) refill(cursor);
-            uint32_t pos = 0xFFFFFFFFu, e = 0;
-            if (tid < nb) {
-                pos = win_pos(cursor + tid);
-                e = S.win[3 * (cursor + tid - win_lo) + 2];
-            }
-            const bool mine = tid < nb && pos < p0 + kBf16Tile;
-            const uint32_t k = (uint32_t)__syncthreads_count(mine);
-            if (tid < k) {
-                const uint32_t before = tid == 0 ? prev : win_pos(cursor + tid - 1);
-                const bool ok = pos >= p0 && pos - p0 < tile_len && (before == 0xFFFFFFFFu || pos > before);
-                if (!ok) {
-                    S.bad = 1;
-                } else {
-                    const uint32_t q = pos - p0;
-                    S.patch[q] = (uint8_t)e;
-                    atomicOr(&S.bits[(q >> 10) * 32u + ((q >> 3) & 31u)], 1u << (((q >> 8) & 3u) * 8u + (q & 7u)));
-                }
-            }
-            if (k > 0) prev = win_pos(cursor + k - 1);
-            cursor += k;
-            __syncthreads();
-            if (k < nb) break;
-        }
-        if (last_of_chunk && cursor != chunk_end && tid == 0) S.bad = 1;
-        if (t == t_end - 1 && !last_of_chunk && chunk_end > chunk_o) {
-            // Hand-off: the next block starts its walk where its search says.
-            uint32_t a, b;
-            block_lower_bounds<kDecThreads>(rec, chunk_o, chunk_end - chunk_o, p0 + kBf16Tile, p0 + kBf16Tile,
-                                            S.scratch, &a, &b);
-            if (tid == 0 && a != cursor) S.bad = 1;
-        }
-
         const uint32_t bits = S.bits[tid];
 #pragma unroll
         for (int k = 0; k < 4; k++) {
@@ -650,9 +669,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_bf16_kernel(const Decod
             uint32_t y[4];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
+                // Each sm byte twice per 16-bit half: the high copy keeps the
+                // sign (bit 15), the low copy the mantissa (bits 0..6).
                 const uint32_t smw = q < 2 ? smv[k].x : smv[k].y;
-                const uint32_t tt = __byte_perm(smw, 0, (q & 1) ? 0x4342 : 0x4140);
-                y[q] = (tt & 0x007F007Fu) | ((tt & 0x00800080u) << 8) | S.lut[(nibv[k] >> (8 * q)) & 0xFFu];
+                const uint32_t tt = __byte_perm(smw, 0, (q & 1) ? 0x3322 : 0x1100);
+                y[q] = (tt & 0x807F807Fu) | S.lut[(nibv[k] >> (8 * q)) & 0xFFu];
             }
             const uint32_t gb = (bits >> (8 * k)) & 0xFFu;
             if (gb) {
