@@ -52,12 +52,24 @@ constexpr uint32_t kWarps = kBf16Threads / 32;
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr uint32_t kEncStages = 3;
-constexpr uint32_t kRecSlots = 2;
+#ifndef SZ_ENC_STAGES
+#define SZ_ENC_STAGES 3
+#endif
+#ifndef SZ_ENC_SLOTS
+#define SZ_ENC_SLOTS 2
+#endif
+#ifndef SZ_ENC_SLOT_RECS
+#define SZ_ENC_SLOT_RECS 2048
+#endif
+#ifndef SZ_ENC_MIN_BLOCKS
+#define SZ_ENC_MIN_BLOCKS 3
+#endif
+constexpr uint32_t kEncStages = SZ_ENC_STAGES;   // input ring depth (16 KB sub-tiles)
+constexpr uint32_t kRecSlots = SZ_ENC_SLOTS;     // scan tiles the compute warps may run ahead
 constexpr uint32_t kSubsPerScan = 4;
 constexpr uint32_t kScanTile = kBf16Tile * kSubsPerScan;      // 32768 elements
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;       // 2
-constexpr uint32_t kSlotRecs = 2048;                          // records staged per scan tile
+constexpr uint32_t kSlotRecs = SZ_ENC_SLOT_RECS;              // records staged per scan tile
 constexpr uint32_t kComputeThreads = kBf16Threads;           // 256
 constexpr uint32_t kEncThreads = kComputeThreads + 32;       // + scanner warp
 constexpr uint32_t kTileBytes = kBf16Tile * 2;               // 16 KB of BF16 per sub-tile
@@ -82,54 +94,56 @@ struct GroupOut {
     uint32_t sm_lo, sm_hi, nib, esc;
 };
 
-// Split and code one group of 8 elements (four BF16 pairs).  CONTIG: the
-// codebook is cb0..cb0+15, so code = exponent - cb0 with one range test per
-// element, computed two elements per 32-bit word (16-bit lanes).
-// sign|mantissa bytes of the four BF16 values in two words: the low bytes
-// (exponent bit 0 | mantissa) and high bytes (sign | exponent bits 7..1) are
-// gathered with byte permutes, then one 3-input op keeps mantissa and sign.
-__device__ __forceinline__ uint32_t sm_quad(uint32_t w0, uint32_t w1) {
-    const uint32_t lo = __byte_perm(w0, w1, 0x6420), hi = __byte_perm(w0, w1, 0x7531);
-    return (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
+// Exponent of element j (0..7) of a group from its four BF16-pair words.
+__device__ __forceinline__ uint32_t group_exponent(const uint32_t (&w)[4], uint32_t j) {
+    const uint32_t lo = (j & 2) ? w[1] : w[0], hi = (j & 2) ? w[3] : w[2];
+    const uint32_t word = (j & 4) ? hi : lo;
+    return (word >> (7 + 16 * (j & 1))) & 0xFFu;
 }
 
+// Split and code one group of 8 elements (four 32-bit words of BF16 pairs).
+// The low bytes (exponent bit 0 | mantissa) and high bytes (sign | exponent
+// bits 7..1) of four elements are gathered with byte permutes; the
+// sign|mantissa bytes then take one 3-input op, and the four exponents two
+// shifts and one 3-input op.
+// CONTIG (codebook cb0..cb0+15): d = exponent - cb0 mod 256 per byte, with a
+// carry-free byte-wise add; the element is in the codebook iff d < 16, and d
+// is then its code.  Escaped elements are rare, so their nibbles are fixed in
+// a separate branch.
 template <bool CONTIG, bool FULL>
-__device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t cnt, uint32_t lane_add,
+__device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t cnt, uint32_t sub_lo,
                                                const uint8_t* s_code) {
     GroupOut o;
-    o.sm_lo = sm_quad(w[0], w[1]);
-    o.sm_hi = sm_quad(w[2], w[3]);
+    const uint32_t L0 = __byte_perm(w[0], w[1], 0x6420), H0 = __byte_perm(w[0], w[1], 0x7531);
+    const uint32_t L1 = __byte_perm(w[2], w[3], 0x6420), H1 = __byte_perm(w[2], w[3], 0x7531);
+    o.sm_lo = (H0 & 0x80808080u) | (L0 & 0x7F7F7F7Fu);
+    o.sm_hi = (H1 & 0x80808080u) | (L1 & 0x7F7F7F7Fu);
+    const uint32_t e0 = ((H0 << 1) & 0xFEFEFEFEu) | ((L0 >> 7) & 0x01010101u);  // exponents 0..3
+    const uint32_t e1 = ((H1 << 1) & 0xFEFEFEFEu) | ((L1 >> 7) & 0x01010101u);  // exponents 4..7
     uint32_t m = 0;
     if (CONTIG) {
-        // Per 16-bit lane: u = exponent + 256 - cb0; in the codebook iff
-        // u is in [256, 272), and then the code is u & 0xF.
-        uint32_t u[4], bad = 0;
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            u[q] = ((w[q] >> 7) & 0x00FF00FFu) + lane_add;
-            bad |= (u[q] & 0x01F001F0u) ^ 0x01000100u;
+        // sub_lo = (256 - cb0) mod 256 in every byte.
+        const uint32_t b7 = sub_lo & 0x7F7F7F7Fu, b8 = sub_lo & 0x80808080u;
+        const uint32_t d0 = ((e0 & 0x7F7F7F7Fu) + b7) ^ (e0 & 0x80808080u) ^ b8;
+        const uint32_t d1 = ((e1 & 0x7F7F7F7Fu) + b7) ^ (e1 & 0x80808080u) ^ b8;
+        uint32_t c0 = d0, c1 = d1;
+        if ((d0 | d1) & 0xF0F0F0F0u) {
+            // Escapes: bytes with d >= 16.  One flag bit per byte (bit 0),
+            // codes of escaped bytes zeroed, flags gathered into a mask.
+            uint32_t f0 = d0 & 0xF0F0F0F0u, f1 = d1 & 0xF0F0F0F0u;
+            f0 |= f0 >> 2, f1 |= f1 >> 2;
+            f0 |= f0 >> 1, f1 |= f1 >> 1;
+            f0 = (f0 >> 4) & 0x01010101u, f1 = (f1 >> 4) & 0x01010101u;
+            c0 &= ~(f0 * 0xFFu), c1 &= ~(f1 * 0xFFu);
+            m = ((f0 * 0x01020408u) >> 24) | (((f1 * 0x01020408u) >> 20) & 0xF0u);
         }
-        uint32_t a = (u[0] & 0x000F000Fu) | ((u[1] & 0x000F000Fu) << 8);  // codes 0,2,1,3 at bytes 0..3
-        uint32_t b = (u[2] & 0x000F000Fu) | ((u[3] & 0x000F000Fu) << 8);
-        a |= a >> 12;  // low half: code0 | code1 << 4 | code2 << 8 | code3 << 12
-        b |= b >> 12;
-        uint32_t nib = __byte_perm(a, b, 0x5410);
-        if (bad) {
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const uint32_t f = (u[j >> 1] >> (16 * (j & 1))) & 0x1F0u;
-                if (f != 0x100u) {
-                    m |= 1u << j;
-                    nib &= ~(0xFu << (4 * j));
-                }
-            }
-        }
-        o.nib = nib;
+        const uint32_t p0 = c0 | (c0 >> 4), p1 = c1 | (c1 >> 4);  // bytes 0, 2: code pairs
+        o.nib = __byte_perm(p0, p1, 0x6420);
     } else {
         uint32_t nib = 0, flags = 0;
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-            const uint32_t c = s_code[(w[j >> 1] >> (7 + 16 * (j & 1))) & 0xFFu];
+            const uint32_t c = s_code[((j < 4 ? e0 : e1) >> (8 * (j & 3))) & 0xFFu];
             nib |= (c & 0xFu) << (4 * j);
             flags |= (c & 0x10u) << j;  // bit 4 + j set for an escape
         }
@@ -172,7 +186,7 @@ __device__ __forceinline__ uint32_t warp_escape_ranks(const uint32_t (&esc)[4], 
 }  // namespace
 
 template <bool CONTIG>
-__global__ void __launch_bounds__(kEncThreads, 3) encode_bf16_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kEncThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_kernel(const EncodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -210,7 +224,7 @@ __global__ void __launch_bounds__(kEncThreads, 3) encode_bf16_kernel(const Encod
 
     if (warp < kWarps) {
         // ===================== compute warps =====================
-        const uint32_t lane_add = (0x100u - p.cb[0]) * 0x00010001u;
+        const uint32_t lane_add = ((0x100u - p.cb[0]) & 0xFFu) * 0x01010101u;  // (256 - cb0) per byte
         auto full_sub = [&](uint32_t u) { return p.vec && (uint64_t)(u + 1) * kBf16Tile <= n; };
         auto issue = [&](uint32_t i) {  // thread 0 only: sub-tile i of this block into ring slot i % 4
             const uint32_t u = sub_of(i), slot = i % kEncStages;
@@ -258,20 +272,19 @@ __global__ void __launch_bounds__(kEncThreads, 3) encode_bf16_kernel(const Encod
             const uint64_t base = u * kBf16Tile;
 #pragma unroll
             for (int k = 0; k < 4; k++) {
-                if (esc[k] == 0) continue;
-                const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
-#pragma unroll
-                for (int jj = 0; jj < 8; jj++) {
-                    if ((esc[k] >> jj) & 1u) {
-                        const uint64_t at = 3ull * (first + off[k] + __popc(esc[k] & ((1u << jj) - 1u)));
-                        const uint32_t pos = (uint32_t)(i0 + jj) & 0xFFFFu;
-                        const uint32_t e = (w[k][jj >> 1] >> (7 + 16 * (jj & 1))) & 0xFFu;
-                        if (at + 3 <= limit) {
-                            dst[at] = (uint8_t)pos;
-                            dst[at + 1] = (uint8_t)(pos >> 8);
-                            dst[at + 2] = (uint8_t)e;
-                        }
+                uint32_t msk = esc[k];
+                const uint32_t pos0 = (uint32_t)(base + warp * 1024u + k * 256u + lane * 8u) & 0xFFFFu;
+                uint64_t at = 3ull * (first + off[k]);
+                while (msk) {  // only the set bits; usually one iteration
+                    const uint32_t jj = __ffs(msk) - 1;
+                    msk &= msk - 1;
+                    const uint32_t pos = pos0 + jj;  // a group never straddles a chunk
+                    if (at + 3 <= limit) {
+                        dst[at] = (uint8_t)pos;
+                        dst[at + 1] = (uint8_t)(pos >> 8);
+                        dst[at + 2] = (uint8_t)group_exponent(w[k], jj);
                     }
+                    at += 3;
                 }
             }
         };

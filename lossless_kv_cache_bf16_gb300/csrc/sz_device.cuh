@@ -217,7 +217,9 @@ __device__ __forceinline__ uint32_t lookback_prefix_wide(uint64_t* status, uint3
                     *failed = true;
                     break;
                 }
-                __nanosleep(32);
+                // Predecessors are other blocks' tiles in flight: poll every
+                // few hundred ns rather than spin (spinning costs issue slots).
+                __nanosleep(256);
 #pragma unroll
                 for (int u = 0; u < kPer; u++)
                     if ((invalid >> u) & 1u) w[u] = ld_relaxed_u64(status + (first - (int64_t)(kPer * lane + u)));

@@ -41,11 +41,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed; false on timeout.
+// Polls back off with a short sleep so that waiting warps do not take issue
+// slots from the warps doing the work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
+    uint32_t sleep_ns = 32;
+    while (!mbar_try_wait(bar, parity)) {
         if (globaltimer_ns() - t0 > limit_ns) return false;
+        __nanosleep(sleep_ns);
+        sleep_ns = sleep_ns < 256 ? 2 * sleep_ns : 256;
+    }
     return true;
 }
 
