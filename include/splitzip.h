@@ -92,11 +92,13 @@ typedef struct sz_codebook {
  * Host only; returns 0 for an unknown dtype. */
 size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes);
 
-/* Bytes of device workspace that sz_encode needs for n elements: one status
- * word per tile for the ordered escape compaction plus a tile counter.  The
- * workspace is scratch: its contents on entry do not matter (sz_encode
- * clears what it uses), and it must not be shared by encodes that can run at
- * the same time.  Host only; returns 0 for an unknown dtype. */
+/* Bytes of device workspace that sz_encode needs for n elements.  BF16: the
+ * escape count of every 32,768-element scan tile and up to 1,024 staged
+ * escape records per scan tile (about 4.7% of the input size); E5M2: one
+ * look-back word per 16,384-element tile plus a tile counter.  The workspace
+ * is scratch: its contents on entry do not matter, and it must not be shared
+ * by encodes that can run at the same time.  Host only; returns 0 for an
+ * unknown dtype. */
 size_t sz_workspace_size(sz_dtype dt, size_t n);
 
 /* Number of exponent bins: 256 (BF16) or 32 (E5M2); 0 for an unknown dtype. */
@@ -164,13 +166,15 @@ const char* sz_status_string(int status);
  * almost all device memory to its KV-cache pool and forbids further
  * allocations, or a latency-critical path that must not take cudaMalloc's
  * implicit device synchronisation -- and so cannot provide the workspace
- * that sz_encode takes.  This call uses a workspace of 512 KiB + 16 bytes
- * held in a static device array inside the library instead, and otherwise behaves
+ * that sz_encode takes.  This call uses a workspace of about 6.1 MiB held
+ * in a static device array inside the library instead, and otherwise behaves
  * exactly like sz_encode (same arguments, stream bytes, d_out_bytes and
  * d_status semantics).  It allocates nothing and calls no allocating routine.
- *  - Limit: n up to 2^30 elements of either dtype; larger n returns
- *    SZ_ERR_CAPACITY at once and launches nothing.
- *  - Every GPU that loads the library holds the 512 KiB array until the
+ *  - Limit: n up to 2^28 elements of either dtype; larger n returns
+ *    SZ_ERR_CAPACITY at once and launches nothing.  Its smaller staging area
+ *    (256 escape records per BF16 scan tile) makes scan tiles with more
+ *    escapes take a slower re-derivation path; the output is the same.
+ *  - Every GPU that loads the library holds the 6.1 MiB array until the
  *    process exits.
  *  - The first call on each device looks up the array's device address with
  *    that device current; make that first call before any stream capture.
@@ -182,11 +186,12 @@ sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_
                             void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
                             int* d_status, cudaStream_t stream);
 
-/* Testing hook, not for production use: sz_encode, except that the tile
- * counter starts at 1, so tile 0 is never processed and its successors'
- * bounded wait for its escape count runs out after wait_limit_ns.  Lets a
- * test check that the wait ends with SZ_ERR_TIMEOUT in *d_status instead of
- * hanging.  d_status must not be NULL. */
+/* Testing hook, not for production use: sz_encode, except that one wait
+ * inside the encode never completes -- BF16: the first input copy of block 0
+ * is never issued, so that block's wait for it runs out; E5M2: tile 0 is never
+ * processed, so its successors' wait for its escape count runs out.  The wait
+ * gives up after wait_limit_ns.  Lets a test check that the wait ends with
+ * SZ_ERR_TIMEOUT in *d_status instead of hanging.  d_status must not be NULL. */
 sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const void* d_in,
                                   size_t n, void* d_out, size_t out_capacity,
                                   unsigned long long* d_out_bytes, int* d_status,

@@ -21,7 +21,18 @@ uint64_t dense_bytes(sz_dtype dt, uint64_t n) { return dt == SZ_BF16 ? n + cdiv(
 // Elements per look-back tile of the encoder (one workspace word each).
 uint64_t tile_elems(sz_dtype dt) { return dt == SZ_BF16 ? kBf16ScanTile : kE5Tile; }
 uint64_t tiles_for(sz_dtype dt, uint64_t n) { return std::max<uint64_t>(1, cdiv(n, tile_elems(dt))); }
-uint64_t workspace_bytes(sz_dtype dt, uint64_t n) { return 16 + 8 * tiles_for(dt, n); }
+
+// BF16 encode stages up to this many escape records per scan tile in the
+// workspace; scan tiles with more are re-derived by the finish kernel.
+constexpr uint32_t kStageRecs = 1024;
+uint64_t align16(uint64_t x) { return (x + 15) & ~15ull; }
+// BF16: [u32 count per scan tile][3 * cap bytes of records per scan tile].
+// E5M2: [tile counter, 16 bytes][u64 look-back word per tile].
+uint64_t workspace_bytes(sz_dtype dt, uint64_t n, uint32_t cap = kStageRecs) {
+    const uint64_t tiles = tiles_for(dt, n);
+    if (dt == SZ_BF16) return align16(4 * tiles) + 3ull * cap * tiles;
+    return 16 + 8 * tiles;
+}
 // Tiles of the decoder (independent of the encoder's look-back tiles).
 uint64_t decode_tiles_for(sz_dtype dt, uint64_t n) {
     return std::max<uint64_t>(1, cdiv(n, dt == SZ_BF16 ? kBf16Tile : kE5Tile));
@@ -66,14 +77,15 @@ bool codebook_ok(sz_dtype dt, const uint8_t* cb) {
 
 sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                       size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
-                      size_t ws_bytes, uint32_t first_ticket, uint64_t wait_ns, cudaStream_t stream) {
+                      size_t ws_bytes, uint32_t first_ticket, uint64_t wait_ns, cudaStream_t stream,
+                      uint32_t stage_recs = kStageRecs) {
     if (!dtype_ok(dt) || !h_cb || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
     if ((n > 0 && !d_in) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
     if (dt == SZ_BF16 && !aligned(d_in, 2)) return SZ_ERR_INVALID_ARG;
     if (!aligned(d_ws, 16) || !aligned(d_out_bytes, 8) || (d_status && !aligned(d_status, 4))) return SZ_ERR_INVALID_ARG;
     if (!codebook_ok(dt, h_cb->exp)) return SZ_ERR_INVALID_ARG;
     if (out_capacity < sz_encoded_size(dt, n, 0)) return SZ_ERR_CAPACITY;
-    const uint64_t ws_need = workspace_bytes(dt, n);
+    const uint64_t ws_need = workspace_bytes(dt, n, stage_recs);
     if (ws_bytes < ws_need) return SZ_ERR_CAPACITY;
 
     EncodeParams p{};
@@ -84,6 +96,9 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     p.num_tiles = (uint32_t)tiles_for(dt, n);
     p.ticket = static_cast<uint32_t*>(d_ws);
     p.tile_status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(d_ws) + 16);
+    p.ws_count = static_cast<uint32_t*>(d_ws);
+    p.ws_rec = static_cast<uint8_t*>(d_ws) + align16(4 * (uint64_t)p.num_tiles);
+    p.ws_cap = stage_recs;
     p.out_bytes = d_out_bytes;
     p.status = d_status;
     p.wait_limit_ns = wait_ns;
@@ -96,8 +111,9 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     else
         p.vec = aligned(d_in, 16) && aligned(d_out, 16);
 
-    cudaError_t err = cudaMemsetAsync(d_ws, 0, ws_need, stream);
-    if (err == cudaSuccess && first_ticket) err = cudaMemsetAsync(d_ws, (int)first_ticket, 1, stream);
+    // BF16 writes every count it reads, so only the E5M2 look-back words need clearing.
+    cudaError_t err = dt == SZ_BF16 ? cudaSuccess : cudaMemsetAsync(d_ws, 0, ws_need, stream);
+    if (err == cudaSuccess && first_ticket && dt != SZ_BF16) err = cudaMemsetAsync(d_ws, (int)first_ticket, 1, stream);
     if (err == cudaSuccess && d_status) err = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
     if (err != cudaSuccess) return from_cuda(err);
     err = dt == SZ_BF16 ? launch_encode_bf16(p, stream) : launch_encode_e5m2(p, stream);
@@ -107,12 +123,15 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
 // ---- encode without allocation ---------------------------------------------
 // sz_encode_noalloc keeps its workspace in this file-scope device array
 // instead of taking one from the caller.  Every GPU that loads the library
-// holds the array until the process exits.  Sized for n up to 2^30 elements
-// of either dtype: 512 KiB + 16 bytes.
-constexpr uint64_t kNoAllocMaxElems = 1ull << 30;
+// holds the array until the process exits.  Sized for n up to 2^28 elements
+// of either dtype, staging up to 256 escape records per BF16 scan tile (the
+// rest are re-derived): 6.1 MiB.
+constexpr uint64_t kNoAllocMaxElems = 1ull << 28;
+constexpr uint32_t kNoAllocStageRecs = 256;
 constexpr uint64_t kNoAllocScratchBytes =
-    16 + 8 * ((kNoAllocMaxElems + std::min<uint64_t>(kBf16ScanTile, kE5Tile) - 1) /
-              std::min<uint64_t>(kBf16ScanTile, kE5Tile));
+    ((kNoAllocMaxElems / kBf16ScanTile) * (4 + 3ull * kNoAllocStageRecs)) > (16 + 8 * (kNoAllocMaxElems / kE5Tile))
+        ? (kNoAllocMaxElems / kBf16ScanTile) * (4 + 3ull * kNoAllocStageRecs)
+        : (16 + 8 * (kNoAllocMaxElems / kE5Tile));
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Host code cannot use g_noalloc_scratch as a device address (in host code the
@@ -206,14 +225,14 @@ sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size
 sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                             size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, cudaStream_t stream) {
     if (!dtype_ok(dt)) return SZ_ERR_INVALID_ARG;
-    if ((uint64_t)n > kNoAllocMaxElems || workspace_bytes(dt, n) > kNoAllocScratchBytes)
+    if ((uint64_t)n > kNoAllocMaxElems || workspace_bytes(dt, n, kNoAllocStageRecs) > kNoAllocScratchBytes)
         return SZ_ERR_CAPACITY;  // beyond the static scratch
     void* ws = nullptr;
     const sz_status st = noalloc_scratch_for_current_device(&ws);
     if (st != SZ_OK) return st;
     // encode_impl clears the part of the scratch the kernel uses before launching.
     return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, ws, kNoAllocScratchBytes, 0,
-                       kWaitLimitNs, stream);
+                       kWaitLimitNs, stream, kNoAllocStageRecs);
 }
 
 sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,

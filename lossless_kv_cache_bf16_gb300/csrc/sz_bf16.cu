@@ -29,63 +29,43 @@ constexpr uint32_t kWarps = kBf16Threads / 32;
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Encode: a persistent, warp-specialised kernel (cooperative launch).
+// Encode, in two kernels.
 //
-// The escape offset is resolved per "scan tile" of 32,768 elements (four
-// 8,192-element sub-tiles; two scan tiles per chunk).  Block b owns scan
-// tiles b, b + G, b + 2G, ... (G co-resident blocks), so every predecessor of
-// a scan tile is in flight or done and no tile ticket is needed.  Nine warps:
-//  * eight compute warps take sub-tiles from a 4-stage ring of shared-memory
-//    buffers filled by TMA bulk copies (thread 0 issues them).  Per sub-tile
-//    they split, code and pack, store the dense streams, and rank the
-//    escapes (ballot/popc warp scans, then a block scan), staging them as
-//    3-byte records in the scan tile's record slot.  After a scan tile's
-//    last sub-tile they publish its escape count for the look-back at once;
-//  * one scanner warp takes finished scan tiles in order, runs the look-back
-//    (256 predecessors per memory round trip), copies the staged records to
-//    their place, and writes the chunk headers, the codebook and the stream
-//    size.  A chunk's last scan tile writes the chunk's header from its own
-//    prefix and its predecessor's count, both at hand after its look-back.
-// A scan tile with more escapes than a slot holds ("overflow") is re-read
-// from global memory by the compute warps once the scanner has published its
-// offset, and its records are written directly.  Every wait is bounded.
+// 1. encode_bf16_kernel streams the tensor: a persistent kernel whose blocks
+//    take 32,768-element "scan tiles" (four 8,192-element sub-tiles) in
+//    round-robin order.  Sub-tiles arrive through a 4-stage ring of TMA bulk
+//    copies; per sub-tile the block splits, codes and packs, stores the dense
+//    streams, and ranks the escapes (ballot/popc warp scans, then a block
+//    scan).  Each scan tile's escape count and its first ws_cap records, in
+//    element order, go to the workspace.  Blocks never wait for each other.
+// 2. finish_bf16_kernel turns the counts into escape offsets (a block-wide
+//    scan over each block's range of scan tiles, on top of the sum of all
+//    earlier counts), copies the staged records into the stream, writes the
+//    chunk headers and the stream size, and re-derives the records of any
+//    scan tile with more than ws_cap escapes from the input.
+// The records cost 6 extra bytes of traffic per escape (staged, read back),
+// a small price for a streaming pass without inter-block waits.
 // ---------------------------------------------------------------------------
 namespace {
 
 #ifndef SZ_ENC_STAGES
 #define SZ_ENC_STAGES 3
 #endif
-#ifndef SZ_ENC_SLOTS
-#define SZ_ENC_SLOTS 2
-#endif
-#ifndef SZ_ENC_SLOT_RECS
-#define SZ_ENC_SLOT_RECS 2048
-#endif
 #ifndef SZ_ENC_MIN_BLOCKS
 #define SZ_ENC_MIN_BLOCKS 3
 #endif
 constexpr uint32_t kEncStages = SZ_ENC_STAGES;   // input ring depth (16 KB sub-tiles)
-constexpr uint32_t kRecSlots = SZ_ENC_SLOTS;     // scan tiles the compute warps may run ahead
 constexpr uint32_t kSubsPerScan = 4;
 constexpr uint32_t kScanTile = kBf16Tile * kSubsPerScan;      // 32768 elements
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;       // 2
-constexpr uint32_t kSlotRecs = SZ_ENC_SLOT_RECS;              // records staged per scan tile
 constexpr uint32_t kComputeThreads = kBf16Threads;           // 256
-constexpr uint32_t kEncThreads = kComputeThreads + 32;       // + scanner warp
 constexpr uint32_t kTileBytes = kBf16Tile * 2;               // 16 KB of BF16 per sub-tile
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
+static_assert(kScanTile == kBf16ScanTile, "scan tile size shared with the host");
 
 struct EncodeSmem {
     alignas(128) uint8_t in[kEncStages][kTileBytes];
-    uint8_t rec[kRecSlots][3 * kSlotRecs];
     uint64_t full[kEncStages];        // TMA -> compute: sub-tile landed
-    uint64_t staged[kRecSlots];       // compute -> scanner: scan tile finished
-    uint64_t prefix_ready[kRecSlots]; // scanner -> compute: offset published
-    uint64_t recfree[kRecSlots];      // scanner -> compute: slot reusable
-    uint32_t tile_esc[kRecSlots];
-    uint32_t prefix[kRecSlots];
-    int overflow[kRecSlots];
-    int failed[kRecSlots];
     alignas(16) uint32_t warp_esc[2][kWarps];
     uint8_t code[256];                // exponent -> code; 0x10 marks an escape
 };
@@ -185,8 +165,58 @@ __device__ __forceinline__ uint32_t warp_escape_ranks(const uint32_t (&esc)[4], 
 
 }  // namespace
 
+// Loads lane's 4 groups of 8 elements of one warp's 1,024 elements starting
+// at element `base` (= sub-tile start + 1024 warp), from global memory.
+__device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64_t base, uint32_t lane,
+                                                   uint32_t (&w)[4][4], uint32_t (&cnt)[4]) {
+    const uint64_t n = p.L.n;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        const uint64_t i0 = base + k * 256u + lane * 8u;
+        cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
+        if (p.vec && cnt[k] == 8) {
+            const uint4 v = ld_stream_v4(p.in + 2 * i0);
+            w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; q++) w[k][q] = 0;
+#pragma unroll
+            for (int jj = 0; jj < 8; jj++) {
+                if ((uint32_t)jj < cnt[k]) {
+                    const uint8_t* e = p.in + 2 * (i0 + jj);
+                    w[k][jj >> 1] |= ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) << (16 * (jj & 1));
+                }
+            }
+        }
+    }
+}
+
+// Writes the records of lane's escapes among one warp's 1,024 elements
+// starting at element `base`: record index first + off[k] + rank in group.
+__device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const uint32_t (&w)[4][4],
+                                             const uint32_t (&esc)[4], const uint32_t (&off)[4], uint64_t first,
+                                             uint8_t* dst, uint64_t limit) {
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        uint32_t msk = esc[k];
+        const uint32_t pos0 = (uint32_t)(base + k * 256u + lane * 8u) & 0xFFFFu;
+        uint64_t at = 3ull * (first + off[k]);
+        while (msk) {  // only the set bits; usually one iteration
+            const uint32_t jj = __ffs(msk) - 1;
+            msk &= msk - 1;
+            const uint32_t pos = pos0 + jj;  // a group never straddles a chunk
+            if (at + 3 <= limit) {
+                dst[at] = (uint8_t)pos;
+                dst[at + 1] = (uint8_t)(pos >> 8);
+                dst[at + 2] = (uint8_t)group_exponent(w[k], jj);
+            }
+            at += 3;
+        }
+    }
+}
+
 template <bool CONTIG>
-__global__ void __launch_bounds__(kEncThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_kernel(const EncodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -194,275 +224,226 @@ __global__ void __launch_bounds__(kEncThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_ke
     const uint32_t G = p.grid;
     const uint32_t num_scan = p.num_tiles;                          // scan tiles
     const uint32_t num_subs = n == 0 ? 1u : (uint32_t)((n + kBf16Tile - 1) / kBf16Tile);
-    const uint32_t k0 = (p.skip_first && blockIdx.x == 0) ? 1u : 0u;  // test hook: skip scan tile 0
     const uint32_t my_scans = blockIdx.x >= num_scan ? 0u : (num_scan - 1 - blockIdx.x) / G + 1;
     auto scan_of = [&](uint32_t k) { return blockIdx.x + k * G; };
-    // Sub-tiles of this block, in order: index i -> scan tile k0 + i/4, part i%4.
-    const uint32_t my_subs =
-        my_scans <= k0 ? 0u
-                       : (my_scans - k0 - 1) * kSubsPerScan +
-                             min(kSubsPerScan, num_subs - scan_of(my_scans - 1) * kSubsPerScan);
-    auto sub_of = [&](uint32_t i) { return scan_of(k0 + i / kSubsPerScan) * kSubsPerScan + i % kSubsPerScan; };
+    auto subs_in = [&](uint32_t st) { return min(kSubsPerScan, num_subs - st * kSubsPerScan); };
+    // Sub-tiles of this block, in order: index i -> scan tile i/4, part i%4.
+    const uint32_t my_subs = my_scans == 0 ? 0u : (my_scans - 1) * kSubsPerScan + subs_in(scan_of(my_scans - 1));
+    auto sub_of = [&](uint32_t i) { return scan_of(i / kSubsPerScan) * kSubsPerScan + i % kSubsPerScan; };
+    auto full_sub = [&](uint32_t u) { return p.vec && (uint64_t)(u + 1) * kBf16Tile <= n; };
 
     if (tid == 0) {
         for (uint32_t s = 0; s < kEncStages; s++) mbar_init(&S.full[s], 1);
-        for (uint32_t r = 0; r < kRecSlots; r++) {
-            mbar_init(&S.staged[r], kComputeThreads);
-            mbar_init(&S.prefix_ready[r], 1);
-            mbar_init(&S.recfree[r], 1);
-        }
         fence_mbar_init();
     }
-    if (tid < 256) {
+    {
         uint32_t code = 0x10u;
 #pragma unroll
         for (int k = 0; k < kCodes; k++)
             if (p.cb[k] == tid) code = (uint32_t)k;
         S.code[tid] = (uint8_t)code;
     }
+    if (blockIdx.x == 0 && tid < kCodes) p.out[p.L.cb_off + tid] = p.cb[tid];
     __syncthreads();
 
-    if (warp < kWarps) {
-        // ===================== compute warps =====================
-        const uint32_t lane_add = ((0x100u - p.cb[0]) & 0xFFu) * 0x01010101u;  // (256 - cb0) per byte
-        auto full_sub = [&](uint32_t u) { return p.vec && (uint64_t)(u + 1) * kBf16Tile <= n; };
-        auto issue = [&](uint32_t i) {  // thread 0 only: sub-tile i of this block into ring slot i % 4
-            const uint32_t u = sub_of(i), slot = i % kEncStages;
-            if (full_sub(u)) {
-                mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
-                bulk_g2s(S.in[slot], p.in + (uint64_t)u * kTileBytes, kTileBytes, &S.full[slot]);
-            } else {
-                mbar_arrive(&S.full[slot]);  // read straight from global instead
-            }
-        };
-        uint32_t issued = 0, waited = 0;
-        if (tid == 0)
-            for (; issued < my_subs && issued < kEncStages; issued++) issue(issued);
-
-        // Loads the 4 groups of sub-tile u from shared memory or global memory.
-        auto load_groups = [&](uint32_t u, const uint8_t* buf, uint32_t (&w)[4][4], uint32_t (&cnt)[4]) {
-            const uint64_t base = (uint64_t)u * kBf16Tile;
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
-                const uint64_t i0 = base + q0;
-                cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
-                if (buf) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(buf + 2 * q0);
-                    w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
-                } else if (p.vec && cnt[k] == 8) {
-                    const uint4 v = ld_stream_v4(p.in + 2 * i0);
-                    w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; q++) w[k][q] = 0;
-#pragma unroll
-                    for (int jj = 0; jj < 8; jj++) {
-                        if ((uint32_t)jj < cnt[k]) {
-                            const uint8_t* e = p.in + 2 * (i0 + jj);
-                            w[k][jj >> 1] |= ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) << (16 * (jj & 1));
-                        }
-                    }
-                }
-            }
-        };
-        // Writes the records of this thread's escapes, ranks from `first` on.
-        auto emit = [&](uint64_t u, const uint32_t (&w)[4][4], const uint32_t (&esc)[4], const uint32_t (&off)[4],
-                        uint64_t first, uint8_t* dst, uint64_t limit) {
-            const uint64_t base = u * kBf16Tile;
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                uint32_t msk = esc[k];
-                const uint32_t pos0 = (uint32_t)(base + warp * 1024u + k * 256u + lane * 8u) & 0xFFFFu;
-                uint64_t at = 3ull * (first + off[k]);
-                while (msk) {  // only the set bits; usually one iteration
-                    const uint32_t jj = __ffs(msk) - 1;
-                    msk &= msk - 1;
-                    const uint32_t pos = pos0 + jj;  // a group never straddles a chunk
-                    if (at + 3 <= limit) {
-                        dst[at] = (uint8_t)pos;
-                        dst[at + 1] = (uint8_t)(pos >> 8);
-                        dst[at + 2] = (uint8_t)group_exponent(w[k], jj);
-                    }
-                    at += 3;
-                }
-            }
-        };
-
-        bool aborted = false;
-        uint32_t i = 0;                     // sub-tiles processed by this block
-        uint32_t run = 0;                   // escapes so far in the current scan tile
-        for (uint32_t ks = 0; ks + k0 < my_scans && !aborted; ks++) {
-            const uint32_t st = scan_of(k0 + ks), r = ks % kRecSlots;
-            const uint32_t subs = min(kSubsPerScan, num_subs - st * kSubsPerScan);
-            bool failed_wait = false;
-            // Record slot r was last used two scan tiles ago; wait until it is free.
-            if (ks >= kRecSlots) failed_wait = !mbar_wait(&S.recfree[r], ((ks / kRecSlots) - 1) & 1u, p.wait_limit_ns);
-            run = 0;
-            for (uint32_t part = 0; part < subs; part++, i++) {
-                const uint32_t slot = i % kEncStages;
-                const uint32_t u = st * kSubsPerScan + part;
-                const uint64_t base = (uint64_t)u * kBf16Tile;
-                failed_wait |= !mbar_wait(&S.full[slot], (i / kEncStages) & 1u, p.wait_limit_ns);
-                if (!failed_wait) waited = i + 1;
-                uint32_t w[4][4], cnt[4], esc[4];
-                if (full_sub(u)) {
-                    // Whole sub-tile in range, buffers aligned: no bounds logic.
-#pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
-                        const uint4 v = *reinterpret_cast<const uint4*>(S.in[slot] + 2 * q0);
-                        w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
-                        const GroupOut o = code_group<CONTIG, true>(w[k], 8, lane_add, S.code);
-                        esc[k] = o.esc;
-                        st_stream_v2(p.out + base + q0, make_uint2(o.sm_lo, o.sm_hi));
-                        st_stream_u32(p.out + p.L.nib_off + (base + q0) / 2, o.nib);
-                    }
-                } else {
-                    load_groups(u, nullptr, w, cnt);
-#pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
-                        const GroupOut o = code_group<CONTIG, false>(w[k], cnt[k], lane_add, S.code);
-                        esc[k] = o.esc;
-                        if (p.vec && cnt[k] == 8) {
-                            st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
-                            st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
-                        } else if (cnt[k] > 0) {
-                            const uint64_t smv = (uint64_t)o.sm_lo | ((uint64_t)o.sm_hi << 32);
-                            for (uint32_t jj = 0; jj < cnt[k]; jj++) p.out[i0 + jj] = (uint8_t)(smv >> (8 * jj));
-                            for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++)
-                                p.out[p.L.nib_off + i0 / 2 + b] = (uint8_t)(o.nib >> (8 * b));
-                        }
-                    }
-                }
-                uint32_t off[4];
-                const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
-                if (lane == 0) S.warp_esc[i & 1][warp] = warp_total;
-                // Block barrier: warp totals visible, and the ring slot consumed
-                // by every compute thread.  It also votes on failed waits.
-                if (named_sync_or(1, kComputeThreads, failed_wait)) {
-                    aborted = true;
-                    break;
-                }
-                if (tid == 0 && issued < my_subs) issue(issued++);
-                uint32_t warp_off = 0, sub_esc = 0;
-                {
-                    const uint4 a = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][0]);
-                    const uint4 b = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][4]);
-                    const uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-                    for (uint32_t v = 0; v < kWarps; v++) {
-                        warp_off += v < warp ? c[v] : 0u;
-                        sub_esc += c[v];
-                    }
-                }
-                if (run + sub_esc <= kSlotRecs && sub_esc) {
-                    uint32_t o4[4] = {off[0], off[1], off[2], off[3]};
-                    emit(u, w, esc, o4, run + warp_off, S.rec[r], sizeof(S.rec[r]));
-                }
-                run += sub_esc;
-            }
-            if (aborted) break;
-            const bool overflow = run > kSlotRecs;
-            if (tid == 0) {
-                // Publish the scan tile's escape count at once: successors'
-                // look-backs need it and must not wait for this block's scanner.
-                st_relaxed_u64(p.tile_status + st,
-                               st == 0 ? pack_status(kFlagPrefix, run, 0) : pack_status(kFlagAggregate, run, 0));
-                S.tile_esc[r] = run;
-                S.overflow[r] = overflow;
-            }
-            mbar_arrive(&S.staged[r]);
-            if (overflow) {
-                // Second pass over the scan tile: re-read it, rank again, and
-                // write the records straight to their place.
-                failed_wait = !mbar_wait(&S.prefix_ready[r], (ks / kRecSlots) & 1u, p.wait_limit_ns);
-                if (named_sync_or(1, kComputeThreads, failed_wait)) {
-                    aborted = true;
-                    break;
-                }
-                const bool ok = !S.failed[r];
-                const uint64_t dst = p.L.rec_off + 3ull * S.prefix[r];
-                uint32_t run2 = 0;
-                for (uint32_t part = 0; part < subs; part++) {
-                    const uint32_t u = st * kSubsPerScan + part;
-                    uint32_t w[4][4], cnt[4], esc[4], off[4];
-                    load_groups(u, nullptr, w, cnt);
-#pragma unroll
-                    for (int k = 0; k < 4; k++) esc[k] = code_group<CONTIG, false>(w[k], cnt[k], lane_add, S.code).esc;
-                    const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
-                    if (lane == 0) S.warp_esc[part & 1][warp] = warp_total;
-                    named_sync(1, kComputeThreads);
-                    uint32_t warp_off = 0, sub_esc = 0;
-#pragma unroll
-                    for (uint32_t v = 0; v < kWarps; v++) {
-                        const uint32_t c = S.warp_esc[part & 1][v];
-                        if (v < warp) warp_off += c;
-                        sub_esc += c;
-                    }
-                    if (ok) emit(u, w, esc, off, run2 + warp_off, p.out + dst, p.capacity > dst ? p.capacity - dst : 0);
-                    run2 += sub_esc;
-                }
-                named_sync(1, kComputeThreads);  // warp_esc reads done before the next reuse
-            }
+    const uint32_t lane_add = ((0x100u - p.cb[0]) & 0xFFu) * 0x01010101u;  // (256 - cb0) per byte
+    auto issue = [&](uint32_t i) {  // thread 0 only: sub-tile i of this block into ring slot i % S
+        const uint32_t u = sub_of(i), slot = i % kEncStages;
+        if (p.skip_first && blockIdx.x == 0 && i == 0) return;  // test hook: this slot never fills
+        if (full_sub(u)) {
+            mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
+            bulk_g2s(S.in[slot], p.in + (uint64_t)u * kTileBytes, kTileBytes, &S.full[slot]);
+        } else {
+            mbar_arrive(&S.full[slot]);  // read straight from global instead
         }
-        if (aborted && p.status) atomicMax(p.status, kStatusTimeout);
-        // Copies in flight must land before the block exits (bounded).
-        if (tid == 0 && aborted)
-            for (uint32_t k = waited; k < issued; k++)
-                mbar_wait(&S.full[k % kEncStages], (k / kEncStages) & 1u, p.wait_limit_ns);
-    } else {
-        // ===================== scanner warp =====================
-        for (uint32_t ks = 0; ks + k0 < my_scans; ks++) {
-            const uint32_t r = ks % kRecSlots;
-            const uint32_t st = scan_of(k0 + ks);
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&S.staged[r], (ks / kRecSlots) & 1u, p.wait_limit_ns))) {
-                if (lane == 0 && p.status) atomicMax(p.status, kStatusTimeout);
-                // Publish an error so successors stop waiting for this tile.
-                if (lane == 0) st_relaxed_u64(p.tile_status + st, pack_status(kFlagError, 0, 0));
+    };
+    uint32_t issued = 0, waited = 0;
+    if (tid == 0)
+        for (; issued < my_subs && issued < kEncStages; issued++) issue(issued);
+
+    bool aborted = false;
+    uint32_t i = 0;  // sub-tiles processed by this block
+    for (uint32_t ks = 0; ks < my_scans && !aborted; ks++) {
+        const uint32_t st = scan_of(ks);
+        const uint32_t subs = subs_in(st);
+        uint8_t* rec = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
+        uint32_t run = 0;  // escapes so far in this scan tile
+        for (uint32_t part = 0; part < subs; part++, i++) {
+            const uint32_t slot = i % kEncStages;
+            const uint32_t u = st * kSubsPerScan + part;
+            const uint64_t wbase = (uint64_t)u * kBf16Tile + warp * 1024u;
+            // A failed wait is voted on at the block barrier below, so that all
+            // threads leave the loop together.
+            const bool failed_wait = !mbar_wait(&S.full[slot], (i / kEncStages) & 1u, p.wait_limit_ns);
+            if (!failed_wait) waited = i + 1;
+            uint32_t w[4][4], cnt[4], esc[4];
+            if (full_sub(u)) {
+                // Whole sub-tile in range, buffers aligned: no bounds logic.
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
+                    const uint4 v = *reinterpret_cast<const uint4*>(S.in[slot] + 2 * q0);
+                    w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
+                    const GroupOut o = code_group<CONTIG, true>(w[k], 8, lane_add, S.code);
+                    esc[k] = o.esc;
+                    const uint64_t i0 = wbase + k * 256u + lane * 8u;
+                    st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
+                    st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
+                }
+            } else {
+                load_groups_global(p, wbase, lane, w, cnt);
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint64_t i0 = wbase + k * 256u + lane * 8u;
+                    const GroupOut o = code_group<CONTIG, false>(w[k], cnt[k], lane_add, S.code);
+                    esc[k] = o.esc;
+                    if (p.vec && cnt[k] == 8) {
+                        st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
+                        st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
+                    } else if (cnt[k] > 0) {
+                        const uint64_t smv = (uint64_t)o.sm_lo | ((uint64_t)o.sm_hi << 32);
+                        for (uint32_t jj = 0; jj < cnt[k]; jj++) p.out[i0 + jj] = (uint8_t)(smv >> (8 * jj));
+                        for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++)
+                            p.out[p.L.nib_off + i0 / 2 + b] = (uint8_t)(o.nib >> (8 * b));
+                    }
+                }
+            }
+            uint32_t off[4];
+            const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
+            if (lane == 0) S.warp_esc[i & 1][warp] = warp_total;
+            // Block barrier: warp totals visible, the ring slot consumed by
+            // every thread (its words were used by the stores above).
+            if (__syncthreads_or(failed_wait)) {
+                aborted = true;
                 break;
             }
-            const uint32_t tile_esc = S.tile_esc[r];
-            const bool overflow = S.overflow[r];
-            bool failed;
-            uint32_t agg_prev;
-            const uint32_t prefix = lookback_prefix_wide(p.tile_status, st, tile_esc, p.wait_limit_ns, &failed, &agg_prev);
-            if (lane == 0) {
-                S.prefix[r] = prefix;
-                S.failed[r] = failed;
-                mbar_arrive(&S.prefix_ready[r]);
-                if (failed && p.status) atomicMax(p.status, kStatusTimeout);
-            }
-            if (!failed && !overflow && tile_esc) {
-                const uint64_t dst = p.L.rec_off + 3ull * prefix;
-                const uint32_t nbytes = 3u * tile_esc;
-                for (uint32_t b = lane; b < nbytes; b += 32)
-                    if (dst + b < p.capacity) p.out[dst + b] = S.rec[r][b];
-            }
-            if (lane == 0 && !failed) {
-                const bool last = st == num_scan - 1;
-                // A chunk's last scan tile writes the chunk's header.
-                if (st % kScansPerChunk == kScansPerChunk - 1 || last) {
-                    const uint32_t c = st / kScansPerChunk;
-                    const bool has_prev = st % kScansPerChunk != 0;  // the chunk's first scan tile is st - 1
-                    const uint32_t first = has_prev ? prefix - agg_prev : prefix;
-                    const uint32_t count = has_prev ? agg_prev + tile_esc : tile_esc;
-                    if (p.L.num_chunks > 0) {
-                        store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
-                        store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, count);
-                    }
-                }
-                if (last) {
-                    const unsigned long long size = p.L.rec_off + 3ull * (prefix + tile_esc);
-                    *p.out_bytes = size;
-                    if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
+            if (tid == 0 && issued < my_subs) issue(issued++);
+            uint32_t warp_off = 0, sub_esc = 0;
+            {
+                const uint4 a = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][0]);
+                const uint4 b = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][4]);
+                const uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (uint32_t v = 0; v < kWarps; v++) {
+                    warp_off += v < warp ? c[v] : 0u;
+                    sub_esc += c[v];
                 }
             }
-            if (st == 0 && lane < kCodes) p.out[p.L.cb_off + lane] = p.cb[lane];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.recfree[r]);
+            // Records beyond ws_cap are not staged; the finish kernel re-derives
+            // that scan tile's records from the input.
+            if (warp_total && run + warp_off < p.ws_cap)
+                emit_records(wbase, lane, w, esc, off, run + warp_off, rec, 3ull * p.ws_cap);
+            run += sub_esc;
         }
+        if (!aborted && tid == 0) p.ws_count[st] = run;
+    }
+    if (aborted && tid == 0) {
+        if (p.status) atomicMax(p.status, kStatusTimeout);
+        // Copies in flight must land before the block exits (bounded).
+        for (uint32_t k = waited; k < issued; k++)
+            if (!(p.skip_first && blockIdx.x == 0 && k == 0))
+                mbar_wait(&S.full[k % kEncStages], (k / kEncStages) & 1u, p.wait_limit_ns);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Finish: escape offsets, record copy-out, chunk headers, stream size.
+// Block b owns the contiguous scan-tile range [b T / F, (b+1) T / F).
+// ---------------------------------------------------------------------------
+constexpr uint32_t kFinThreads = 256;
+
+template <bool CONTIG>
+__global__ void __launch_bounds__(kFinThreads) finish_bf16_kernel(const EncodeParams p) {
+    __shared__ uint32_t s_sum[kFinThreads / 32];
+    __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
+    __shared__ uint8_t s_code[256];
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint32_t T = p.num_tiles, F = gridDim.x;
+    const uint32_t t0 = (uint32_t)((uint64_t)blockIdx.x * T / F), t1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * T / F);
+    {
+        uint32_t code = 0x10u;
+#pragma unroll
+        for (int k = 0; k < kCodes; k++)
+            if (p.cb[k] == tid) code = (uint32_t)k;
+        s_code[tid] = (uint8_t)code;
+    }
+    // Escapes in all scan tiles before this block's range.
+    uint32_t part = 0;
+    for (uint32_t t = tid; t < t0; t += kFinThreads) part += p.ws_count[t];
+    part = __reduce_add_sync(0xFFFFFFFFu, part);
+    if (lane == 0) s_sum[warp] = part;
+    __syncthreads();
+    uint32_t base = 0;
+#pragma unroll
+    for (uint32_t v = 0; v < kFinThreads / 32; v++) base += s_sum[v];
+    __syncthreads();
+
+    const uint32_t lane_add = ((0x100u - p.cb[0]) & 0xFFu) * 0x01010101u;
+    for (uint32_t c0 = t0; c0 < t1; c0 += kFinThreads) {
+        const uint32_t t = c0 + tid;
+        const uint32_t cnt = t < t1 ? p.ws_count[t] : 0u;
+        // Block-wide exclusive scan of the counts of this batch.
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= (uint32_t)d) incl += a;
+        }
+        if (lane == 31) s_sum[warp] = incl;
+        __syncthreads();
+        uint32_t wbase = 0, total = 0;
+#pragma unroll
+        for (uint32_t v = 0; v < kFinThreads / 32; v++) {
+            wbase += v < warp ? s_sum[v] : 0u;
+            total += s_sum[v];
+        }
+        const uint32_t prefix = base + wbase + incl - cnt;
+        s_prefix[tid] = prefix;
+        s_count[tid] = cnt;
+        if (t < t1) {
+            const bool last = t == T - 1;
+            // A chunk's last scan tile writes the chunk's header.
+            if ((t % kScansPerChunk == kScansPerChunk - 1 || last) && p.L.num_chunks > 0) {
+                const uint32_t c = t / kScansPerChunk;
+                const bool has_prev = t % kScansPerChunk != 0;  // the chunk's first scan tile is t - 1
+                const uint32_t prev = has_prev ? p.ws_count[t - 1] : 0u;
+                store_u32_le(p.out + p.L.hdr_off + 8ull * c, prefix - prev);
+                store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, prev + cnt);
+            }
+            if (last) {
+                const unsigned long long size = p.L.rec_off + 3ull * (prefix + cnt);
+                *p.out_bytes = size;
+                if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
+            }
+        }
+        __syncthreads();
+        // One warp per scan tile: copy the staged records, or re-derive them.
+        const uint32_t batch = min(kFinThreads, t1 - c0);
+        for (uint32_t j = warp; j < batch; j += kFinThreads / 32) {
+            const uint32_t st = c0 + j, c = s_count[j];
+            const uint64_t dst = p.L.rec_off + 3ull * s_prefix[j];
+            if (c <= p.ws_cap) {
+                const uint8_t* src = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
+                for (uint32_t b = lane; b < 3 * c; b += 32)
+                    if (dst + b < p.capacity) p.out[dst + b] = src[b];
+            } else {
+                // More escapes than staged: walk the scan tile again, 1,024
+                // elements per step in the encoder's (k, lane, j) order.
+                const uint64_t n = p.L.n;
+                uint32_t run = 0;
+                for (uint64_t wb = (uint64_t)st * kScanTile; wb < n && wb < (uint64_t)(st + 1) * kScanTile; wb += 1024) {
+                    uint32_t w[4][4], cnt4[4], esc[4], off[4];
+                    load_groups_global(p, wb, lane, w, cnt4);
+#pragma unroll
+                    for (int k = 0; k < 4; k++) esc[k] = code_group<CONTIG, false>(w[k], cnt4[k], lane_add, s_code).esc;
+                    const uint32_t wt = warp_escape_ranks(esc, lane, off);
+                    emit_records(wb, lane, w, esc, off, run, p.out + dst, p.capacity > dst ? p.capacity - dst : 0);
+                    run += wt;
+                }
+            }
+        }
+        base += total;
+        __syncthreads();
     }
 }
 
@@ -731,16 +712,19 @@ cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
     int dev = 0, sms = 0, per_sm = 0;
     if (err == cudaSuccess) err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kEncThreads, smem);
+    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kComputeThreads, smem);
     if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    // All blocks must be co-resident: a tile waits for its predecessors,
-    // which belong to other blocks.  The cooperative launch guarantees it.
     EncodeParams q = p;
-    q.grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)per_sm * sms);
+    q.grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
     void* args[] = {&q};
-    err = cudaLaunchCooperativeKernel(kern, q.grid, kEncThreads, args, smem, s);
-    return err == cudaSuccess ? cudaGetLastError() : err;
+    err = cudaLaunchKernel(kern, q.grid, kComputeThreads, args, smem, s);
+    if (err != cudaSuccess) return err;
+    const uint32_t fin_grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)2 * sms);
+    if (p.contig)
+        finish_bf16_kernel<true><<<fin_grid, kFinThreads, 0, s>>>(q);
+    else
+        finish_bf16_kernel<false><<<fin_grid, kFinThreads, 0, s>>>(q);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {

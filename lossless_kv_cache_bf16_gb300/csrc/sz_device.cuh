@@ -167,92 +167,6 @@ __device__ __forceinline__ uint32_t lookback_prefix(uint64_t* status, uint32_t t
     return prefix;
 }
 
-// Wide look-back, run by one full warp, for a tile whose aggregate has
-// already been published (by whoever knew it first).  Each step examines the
-// 256 nearest unexamined predecessors with 8 independent loads per lane, so
-// one memory round trip covers 256 tiles: the look-back keeps up as long as
-// fewer than ~256 tiles are published per round trip (a 32-wide step caps
-// the rate at 32 per round trip, far below what HBM needs with 16 KB tiles).
-// Publishes the tile's prefix and returns it, or on a timeout or predecessor
-// error publishes kFlagError and sets *failed.
-// Also returns in *agg_prev the aggregate of tile - 1 (0 for tile 0).
-__device__ __forceinline__ uint32_t lookback_prefix_wide(uint64_t* status, uint32_t tile, uint32_t aggregate,
-                                                         uint64_t limit_ns, bool* failed, uint32_t* agg_prev) {
-    constexpr int kPer = 8;
-    const uint32_t lane = threadIdx.x & 31u;
-    *failed = false;
-    *agg_prev = 0;
-    uint32_t prefix = 0;
-    if (tile > 0) {
-        bool first_window = true;
-        int64_t first = (int64_t)tile - 1;  // nearest unexamined predecessor
-        uint64_t t0 = 0;
-        bool clock_started = false;
-        while (true) {
-            uint64_t w[kPer];
-            uint32_t invalid = 0;
-            bool error = false;
-#pragma unroll
-            for (int u = 0; u < kPer; u++) {
-                const int64_t idx = first - (int64_t)(kPer * lane + u);
-                w[u] = idx >= 0 ? ld_relaxed_u64(status + idx) : pack_status(kFlagPrefix, 0, 0);
-            }
-            while (true) {
-                invalid = 0;
-#pragma unroll
-                for (int u = 0; u < kPer; u++) {
-                    const uint32_t f = status_flag(w[u]);
-                    error |= f == kFlagError;
-                    invalid |= (uint32_t)(f == kFlagNone) << u;
-                }
-                if (__any_sync(0xFFFFFFFFu, error)) {
-                    *failed = true;
-                    break;
-                }
-                if (!__any_sync(0xFFFFFFFFu, invalid != 0)) break;
-                if (!clock_started) {
-                    t0 = globaltimer_ns();
-                    clock_started = true;
-                } else if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > limit_ns)) {
-                    *failed = true;
-                    break;
-                }
-                // Predecessors are other blocks' tiles in flight: poll every
-                // few hundred ns rather than spin (spinning costs issue slots).
-                __nanosleep(256);
-#pragma unroll
-                for (int u = 0; u < kPer; u++)
-                    if ((invalid >> u) & 1u) w[u] = ld_relaxed_u64(status + (first - (int64_t)(kPer * lane + u)));
-            }
-            if (*failed) break;
-            if (first_window) *agg_prev = __shfl_sync(0xFFFFFFFFu, status_aggregate(w[0]), 0);
-            first_window = false;
-            // Nearest published prefix inside this lane's 8, and the sum up to it.
-            int nearest = -1;
-            uint32_t part = 0;
-#pragma unroll
-            for (int u = kPer - 1; u >= 0; u--)
-                if (status_flag(w[u]) == kFlagPrefix) nearest = u;
-#pragma unroll
-            for (int u = 0; u < kPer; u++) {
-                if (nearest < 0 || u < nearest) part += status_aggregate(w[u]);
-                if (u == nearest) part += status_aggregate(w[u]) + status_prefix(w[u]);
-            }
-            const uint32_t have = __ballot_sync(0xFFFFFFFFu, nearest >= 0);
-            if (have) {
-                const uint32_t lead = __ffs(have) - 1;
-                prefix += __reduce_add_sync(0xFFFFFFFFu, lane <= lead ? part : 0u);
-                break;
-            }
-            prefix += __reduce_add_sync(0xFFFFFFFFu, part);
-            first -= 32 * kPer;
-        }
-    }
-    if (lane == 0)
-        st_relaxed_u64(status + tile, *failed ? pack_status(kFlagError, 0, 0) : pack_status(kFlagPrefix, aggregate, prefix));
-    return *failed ? 0u : prefix;
-}
-
 // Little-endian byte stores for the few unaligned header fields.
 __device__ __forceinline__ void store_u32_le(uint8_t* p, uint32_t v) {
     p[0] = (uint8_t)v;

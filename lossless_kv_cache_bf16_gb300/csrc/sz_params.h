@@ -31,9 +31,12 @@ struct EncodeParams {
     int* status;             // nullable
     uint64_t wait_limit_ns;
     int vec;                 // 1 when the aligned vector path may be used
-    uint32_t grid;           // persistent kernels: blocks in the (cooperative) launch
-    uint32_t skip_first;     // test hook: tile 0 is never processed
+    uint32_t grid;           // persistent kernels: blocks in the launch
+    uint32_t skip_first;     // test hook: a wait that never completes
     int contig;              // codebook is 16 consecutive exponents cb[0]..cb[0]+15
+    uint32_t* ws_count;      // two-phase encode: escapes per scan tile
+    uint8_t* ws_rec;         // two-phase encode: staged records, ws_cap per scan tile
+    uint32_t ws_cap;         // records staged per scan tile
     uint8_t cb[16];          // ascending
 };
 

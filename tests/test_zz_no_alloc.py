@@ -67,7 +67,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(64, dtype=torch.uint8, device="cuda")
     ob = torch.zeros(1, dtype=torch.int64, device="cuda")
-    too_many = (1 << 30) + 1                  # the static scratch covers 2^30 elements
+    too_many = (1 << 28) + 1                  # the static scratch covers 2^28 elements
     with pytest.raises(S.SplitZipError) as e:
         S.sz_encode_noalloc(S.SZ_BF16, CB_MID, x, out, ob, None, n=too_many)
     assert e.value.status == S.SZ_ERR_CAPACITY
