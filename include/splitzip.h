@@ -92,13 +92,12 @@ typedef struct sz_codebook {
  * Host only; returns 0 for an unknown dtype. */
 size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes);
 
-/* Bytes of device workspace that sz_encode needs for n elements.  BF16: the
- * escape count of every 32,768-element scan tile and up to 1,024 staged
- * escape records per scan tile (about 4.7% of the input size); E5M2: one
- * look-back word per 16,384-element tile plus a tile counter.  The workspace
- * is scratch: its contents on entry do not matter, and it must not be shared
- * by encodes that can run at the same time.  Host only; returns 0 for an
- * unknown dtype. */
+/* Bytes of device workspace that sz_encode needs for n elements: the escape
+ * count of every 32,768-element scan tile and up to 1,024 staged escape
+ * records (3 bytes each) per scan tile -- about 4.7% of a BF16 input, 9.4%
+ * of an E5M2 input.  The workspace is scratch: its contents on entry do not
+ * matter, and it must not be shared by encodes that can run at the same
+ * time.  Host only; returns 0 for an unknown dtype. */
 size_t sz_workspace_size(sz_dtype dt, size_t n);
 
 /* Number of exponent bins: 256 (BF16) or 32 (E5M2); 0 for an unknown dtype. */
@@ -187,11 +186,11 @@ sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_
                             int* d_status, cudaStream_t stream);
 
 /* Testing hook, not for production use: sz_encode, except that one wait
- * inside the encode never completes -- BF16: the first input copy of block 0
- * is never issued, so that block's wait for it runs out; E5M2: tile 0 is never
- * processed, so its successors' wait for its escape count runs out.  The wait
- * gives up after wait_limit_ns.  Lets a test check that the wait ends with
- * SZ_ERR_TIMEOUT in *d_status instead of hanging.  d_status must not be NULL. */
+ * inside the encode never completes: the first input copy of block 0 is never
+ * issued, so that block's wait for it gives up after wait_limit_ns.  Lets a
+ * test check that the wait ends with SZ_ERR_TIMEOUT in *d_status instead of
+ * hanging.  BF16 only (the E5M2 encoder has no in-kernel wait; E5M2 returns
+ * SZ_ERR_UNSUPPORTED).  d_status must not be NULL. */
 sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const void* d_in,
                                   size_t n, void* d_out, size_t out_capacity,
                                   unsigned long long* d_out_bytes, int* d_status,

@@ -18,20 +18,18 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded inter-block waits: 
 bool dtype_ok(int dt) { return dt == SZ_BF16 || dt == SZ_FP8_E5M2; }
 uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 uint64_t dense_bytes(sz_dtype dt, uint64_t n) { return dt == SZ_BF16 ? n + cdiv(n, 2) : 7 * cdiv(n, 8); }
-// Elements per look-back tile of the encoder (one workspace word each).
-uint64_t tile_elems(sz_dtype dt) { return dt == SZ_BF16 ? kBf16ScanTile : kE5Tile; }
-uint64_t tiles_for(sz_dtype dt, uint64_t n) { return std::max<uint64_t>(1, cdiv(n, tile_elems(dt))); }
+// Encode scan tiles (both dtypes): one escape count and one record staging
+// area each in the workspace.
+uint64_t scan_tiles_for(uint64_t n) { return std::max<uint64_t>(1, cdiv(n, kScanTile)); }
 
-// BF16 encode stages up to this many escape records per scan tile in the
+// The encoders stage up to this many escape records per scan tile in the
 // workspace; scan tiles with more are re-derived by the finish kernel.
 constexpr uint32_t kStageRecs = 1024;
 uint64_t align16(uint64_t x) { return (x + 15) & ~15ull; }
-// BF16: [u32 count per scan tile][3 * cap bytes of records per scan tile].
-// E5M2: [tile counter, 16 bytes][u64 look-back word per tile].
-uint64_t workspace_bytes(sz_dtype dt, uint64_t n, uint32_t cap = kStageRecs) {
-    const uint64_t tiles = tiles_for(dt, n);
-    if (dt == SZ_BF16) return align16(4 * tiles) + 3ull * cap * tiles;
-    return 16 + 8 * tiles;
+// Workspace: [u32 count per scan tile][3 * cap bytes of records per scan tile].
+uint64_t workspace_bytes(uint64_t n, uint32_t cap = kStageRecs) {
+    const uint64_t tiles = scan_tiles_for(n);
+    return align16(4 * tiles) + 3ull * cap * tiles;
 }
 // Tiles of the decoder (independent of the encoder's look-back tiles).
 uint64_t decode_tiles_for(sz_dtype dt, uint64_t n) {
@@ -85,7 +83,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     if (!aligned(d_ws, 16) || !aligned(d_out_bytes, 8) || (d_status && !aligned(d_status, 4))) return SZ_ERR_INVALID_ARG;
     if (!codebook_ok(dt, h_cb->exp)) return SZ_ERR_INVALID_ARG;
     if (out_capacity < sz_encoded_size(dt, n, 0)) return SZ_ERR_CAPACITY;
-    const uint64_t ws_need = workspace_bytes(dt, n, stage_recs);
+    const uint64_t ws_need = workspace_bytes(n, stage_recs);
     if (ws_bytes < ws_need) return SZ_ERR_CAPACITY;
 
     EncodeParams p{};
@@ -93,9 +91,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     p.in = static_cast<const uint8_t*>(d_in);
     p.out = static_cast<uint8_t*>(d_out);
     p.capacity = out_capacity;
-    p.num_tiles = (uint32_t)tiles_for(dt, n);
-    p.ticket = static_cast<uint32_t*>(d_ws);
-    p.tile_status = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(d_ws) + 16);
+    p.num_tiles = (uint32_t)scan_tiles_for(n);
     p.ws_count = static_cast<uint32_t*>(d_ws);
     p.ws_rec = static_cast<uint8_t*>(d_ws) + align16(4 * (uint64_t)p.num_tiles);
     p.ws_cap = stage_recs;
@@ -111,10 +107,9 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     else
         p.vec = aligned(d_in, 16) && aligned(d_out, 16);
 
-    // BF16 writes every count it reads, so only the E5M2 look-back words need clearing.
-    cudaError_t err = dt == SZ_BF16 ? cudaSuccess : cudaMemsetAsync(d_ws, 0, ws_need, stream);
-    if (err == cudaSuccess && first_ticket && dt != SZ_BF16) err = cudaMemsetAsync(d_ws, (int)first_ticket, 1, stream);
-    if (err == cudaSuccess && d_status) err = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
+    // The workspace needs no clearing: the encoders write every count that
+    // the finish kernel reads.
+    cudaError_t err = d_status ? cudaMemsetAsync(d_status, 0, sizeof(int), stream) : cudaSuccess;
     if (err != cudaSuccess) return from_cuda(err);
     err = dt == SZ_BF16 ? launch_encode_bf16(p, stream) : launch_encode_e5m2(p, stream);
     return from_cuda(err);
@@ -128,10 +123,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
 // rest are re-derived): 6.1 MiB.
 constexpr uint64_t kNoAllocMaxElems = 1ull << 28;
 constexpr uint32_t kNoAllocStageRecs = 256;
-constexpr uint64_t kNoAllocScratchBytes =
-    ((kNoAllocMaxElems / kBf16ScanTile) * (4 + 3ull * kNoAllocStageRecs)) > (16 + 8 * (kNoAllocMaxElems / kE5Tile))
-        ? (kNoAllocMaxElems / kBf16ScanTile) * (4 + 3ull * kNoAllocStageRecs)
-        : (16 + 8 * (kNoAllocMaxElems / kE5Tile));
+constexpr uint64_t kNoAllocScratchBytes = (kNoAllocMaxElems / kScanTile) * (4 + 3ull * kNoAllocStageRecs);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Host code cannot use g_noalloc_scratch as a device address (in host code the
@@ -168,7 +160,7 @@ size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes) {
 
 size_t sz_workspace_size(sz_dtype dt, size_t n) {
     if (!dtype_ok(dt)) return 0;
-    return workspace_bytes(dt, n);
+    return workspace_bytes(n);
 }
 
 size_t sz_histogram_bins(sz_dtype dt) {
@@ -225,7 +217,7 @@ sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size
 sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                             size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, cudaStream_t stream) {
     if (!dtype_ok(dt)) return SZ_ERR_INVALID_ARG;
-    if ((uint64_t)n > kNoAllocMaxElems || workspace_bytes(dt, n, kNoAllocStageRecs) > kNoAllocScratchBytes)
+    if ((uint64_t)n > kNoAllocMaxElems || workspace_bytes(n, kNoAllocStageRecs) > kNoAllocScratchBytes)
         return SZ_ERR_CAPACITY;  // beyond the static scratch
     void* ws = nullptr;
     const sz_status st = noalloc_scratch_for_current_device(&ws);
@@ -239,6 +231,7 @@ sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const vo
                                   size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
                                   size_t ws_bytes, unsigned long long wait_limit_ns, cudaStream_t stream) {
     if (!d_status || wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs) return SZ_ERR_INVALID_ARG;
+    if (dt == SZ_FP8_E5M2) return SZ_ERR_UNSUPPORTED;  // the E5M2 encoder has no in-kernel wait
     return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 1,
                        wait_limit_ns, stream);
 }

@@ -38,11 +38,10 @@ constexpr uint32_t kWarps = kBf16Threads / 32;
 //    streams, and ranks the escapes (ballot/popc warp scans, then a block
 //    scan).  Each scan tile's escape count and its first ws_cap records, in
 //    element order, go to the workspace.  Blocks never wait for each other.
-// 2. finish_bf16_kernel turns the counts into escape offsets (a block-wide
-//    scan over each block's range of scan tiles, on top of the sum of all
-//    earlier counts), copies the staged records into the stream, writes the
-//    chunk headers and the stream size, and re-derives the records of any
-//    scan tile with more than ws_cap escapes from the input.
+// 2. finish_kernel (sz_finish.cu) turns the counts into escape offsets,
+//    copies the staged records into the stream, writes the chunk headers and
+//    the stream size, and re-derives the records of any scan tile with more
+//    than ws_cap escapes from the input.
 // The records cost 6 extra bytes of traffic per escape (staged, read back),
 // a small price for a streaming pass without inter-block waits.
 // ---------------------------------------------------------------------------
@@ -56,12 +55,9 @@ namespace {
 #endif
 constexpr uint32_t kEncStages = SZ_ENC_STAGES;   // input ring depth (16 KB sub-tiles)
 constexpr uint32_t kSubsPerScan = 4;
-constexpr uint32_t kScanTile = kBf16Tile * kSubsPerScan;      // 32768 elements
-constexpr uint32_t kScansPerChunk = kChunk / kScanTile;       // 2
 constexpr uint32_t kComputeThreads = kBf16Threads;           // 256
 constexpr uint32_t kTileBytes = kBf16Tile * 2;               // 16 KB of BF16 per sub-tile
-static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
-static_assert(kScanTile == kBf16ScanTile, "scan tile size shared with the host");
+static_assert(kBf16Tile * kSubsPerScan == kScanTile, "four sub-tiles per scan tile");
 
 struct EncodeSmem {
     alignas(128) uint8_t in[kEncStages][kTileBytes];
@@ -347,107 +343,6 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
 }
 
 // ---------------------------------------------------------------------------
-// Finish: escape offsets, record copy-out, chunk headers, stream size.
-// Block b owns the contiguous scan-tile range [b T / F, (b+1) T / F).
-// ---------------------------------------------------------------------------
-constexpr uint32_t kFinThreads = 256;
-
-template <bool CONTIG>
-__global__ void __launch_bounds__(kFinThreads) finish_bf16_kernel(const EncodeParams p) {
-    __shared__ uint32_t s_sum[kFinThreads / 32];
-    __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
-    __shared__ uint8_t s_code[256];
-    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint32_t T = p.num_tiles, F = gridDim.x;
-    const uint32_t t0 = (uint32_t)((uint64_t)blockIdx.x * T / F), t1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * T / F);
-    {
-        uint32_t code = 0x10u;
-#pragma unroll
-        for (int k = 0; k < kCodes; k++)
-            if (p.cb[k] == tid) code = (uint32_t)k;
-        s_code[tid] = (uint8_t)code;
-    }
-    // Escapes in all scan tiles before this block's range.
-    uint32_t part = 0;
-    for (uint32_t t = tid; t < t0; t += kFinThreads) part += p.ws_count[t];
-    part = __reduce_add_sync(0xFFFFFFFFu, part);
-    if (lane == 0) s_sum[warp] = part;
-    __syncthreads();
-    uint32_t base = 0;
-#pragma unroll
-    for (uint32_t v = 0; v < kFinThreads / 32; v++) base += s_sum[v];
-    __syncthreads();
-
-    const uint32_t lane_add = ((0x100u - p.cb[0]) & 0xFFu) * 0x01010101u;
-    for (uint32_t c0 = t0; c0 < t1; c0 += kFinThreads) {
-        const uint32_t t = c0 + tid;
-        const uint32_t cnt = t < t1 ? p.ws_count[t] : 0u;
-        // Block-wide exclusive scan of the counts of this batch.
-        uint32_t incl = cnt;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-            if (lane >= (uint32_t)d) incl += a;
-        }
-        if (lane == 31) s_sum[warp] = incl;
-        __syncthreads();
-        uint32_t wbase = 0, total = 0;
-#pragma unroll
-        for (uint32_t v = 0; v < kFinThreads / 32; v++) {
-            wbase += v < warp ? s_sum[v] : 0u;
-            total += s_sum[v];
-        }
-        const uint32_t prefix = base + wbase + incl - cnt;
-        s_prefix[tid] = prefix;
-        s_count[tid] = cnt;
-        if (t < t1) {
-            const bool last = t == T - 1;
-            // A chunk's last scan tile writes the chunk's header.
-            if ((t % kScansPerChunk == kScansPerChunk - 1 || last) && p.L.num_chunks > 0) {
-                const uint32_t c = t / kScansPerChunk;
-                const bool has_prev = t % kScansPerChunk != 0;  // the chunk's first scan tile is t - 1
-                const uint32_t prev = has_prev ? p.ws_count[t - 1] : 0u;
-                store_u32_le(p.out + p.L.hdr_off + 8ull * c, prefix - prev);
-                store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, prev + cnt);
-            }
-            if (last) {
-                const unsigned long long size = p.L.rec_off + 3ull * (prefix + cnt);
-                *p.out_bytes = size;
-                if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
-            }
-        }
-        __syncthreads();
-        // One warp per scan tile: copy the staged records, or re-derive them.
-        const uint32_t batch = min(kFinThreads, t1 - c0);
-        for (uint32_t j = warp; j < batch; j += kFinThreads / 32) {
-            const uint32_t st = c0 + j, c = s_count[j];
-            const uint64_t dst = p.L.rec_off + 3ull * s_prefix[j];
-            if (c <= p.ws_cap) {
-                const uint8_t* src = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
-                for (uint32_t b = lane; b < 3 * c; b += 32)
-                    if (dst + b < p.capacity) p.out[dst + b] = src[b];
-            } else {
-                // More escapes than staged: walk the scan tile again, 1,024
-                // elements per step in the encoder's (k, lane, j) order.
-                const uint64_t n = p.L.n;
-                uint32_t run = 0;
-                for (uint64_t wb = (uint64_t)st * kScanTile; wb < n && wb < (uint64_t)(st + 1) * kScanTile; wb += 1024) {
-                    uint32_t w[4][4], cnt4[4], esc[4], off[4];
-                    load_groups_global(p, wb, lane, w, cnt4);
-#pragma unroll
-                    for (int k = 0; k < 4; k++) esc[k] = code_group<CONTIG, false>(w[k], cnt4[k], lane_add, s_code).esc;
-                    const uint32_t wt = warp_escape_ranks(esc, lane, off);
-                    emit_records(wb, lane, w, esc, off, run, p.out + dst, p.capacity > dst ? p.capacity - dst : 0);
-                    run += wt;
-                }
-            }
-        }
-        base += total;
-        __syncthreads();
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Decode: a persistent kernel; block b owns the contiguous tile range
 // [bT/G, (b+1)T/G).  Because escape records are stored in element order, a
 // block's records also form one contiguous run of the stream: one block
@@ -719,12 +614,7 @@ cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
     void* args[] = {&q};
     err = cudaLaunchKernel(kern, q.grid, kComputeThreads, args, smem, s);
     if (err != cudaSuccess) return err;
-    const uint32_t fin_grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)2 * sms);
-    if (p.contig)
-        finish_bf16_kernel<true><<<fin_grid, kFinThreads, 0, s>>>(q);
-    else
-        finish_bf16_kernel<false><<<fin_grid, kFinThreads, 0, s>>>(q);
-    return cudaGetLastError();
+    return launch_finish(q, true, s);
 }
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {

@@ -1,19 +1,6 @@
-// sz_device.cuh -- device-side building blocks shared by the SplitZip kernels.
-//
-// Ordered escape compaction ([MET] "Flujo de Escape": escapes are written in
-// element order) uses a single-pass decoupled look-back over tiles.  Every
-// tile publishes a 64-bit status word:
-//
-//   [63:62] flag   0 = nothing yet, 1 = aggregate known, 2 = prefix known,
-//                  3 = error (a wait gave up; successors stop waiting)
-//   [61:32] aggregate: escapes inside this tile
-//   [31: 0] exclusive prefix: escapes in all earlier tiles (flag 2 only)
-//
-// The data travels inside the word, so relaxed gpu-scope loads and stores are
-// enough.  Tiles are handed out by an atomic counter in launch order, so every
-// tile a block waits for belongs to a block that is already running: the wait
-// always ends, and it is bounded anyway (globaltimer) so that a fault can only
-// end in SZ_ERR_TIMEOUT, never in a hung GPU.
+// sz_device.cuh -- device-side building blocks shared by the SplitZip kernels:
+// streaming loads/stores, the global timer for bounded waits, little-endian
+// helpers, and the decoders' per-tile escape search and validation.
 #pragma once
 
 #include <cstdint>
@@ -27,31 +14,11 @@ namespace sz {
 constexpr uint32_t kChunk = 65536;  // elements per escape chunk (u16 positions)
 constexpr int kCodes = 16;          // top-16 codebook
 
-constexpr uint64_t kFlagNone = 0;
-constexpr uint64_t kFlagAggregate = 1;
-constexpr uint64_t kFlagPrefix = 2;
-constexpr uint64_t kFlagError = 3;
-
 // Device status codes (same values as sz_status in splitzip.h).
 constexpr int kStatusCapacity = 3;
 constexpr int kStatusCorrupt = 4;
 constexpr int kStatusTimeout = 5;
 
-__device__ __forceinline__ uint64_t pack_status(uint64_t flag, uint32_t aggregate, uint32_t prefix) {
-    return (flag << 62) | ((uint64_t)(aggregate & 0x3FFFFFFFu) << 32) | prefix;
-}
-__device__ __forceinline__ uint32_t status_flag(uint64_t w) { return (uint32_t)(w >> 62); }
-__device__ __forceinline__ uint32_t status_aggregate(uint64_t w) { return (uint32_t)(w >> 32) & 0x3FFFFFFFu; }
-__device__ __forceinline__ uint32_t status_prefix(uint64_t w) { return (uint32_t)w; }
-
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -87,84 +54,6 @@ __device__ __forceinline__ void st_stream_v2(void* p, uint2 v) {
 }
 __device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
     asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Wait (bounded) until tile `idx` has published its prefix; returns the word,
-// or a word with kFlagError if the wait ran out or the tile reported an error.
-__device__ __forceinline__ uint64_t wait_for_prefix(const uint64_t* status, uint32_t idx, uint64_t limit_ns) {
-    uint64_t w = ld_relaxed_u64(status + idx);
-    if (status_flag(w) == kFlagPrefix || status_flag(w) == kFlagError) return w;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        __nanosleep(100);
-        w = ld_relaxed_u64(status + idx);
-        const uint32_t f = status_flag(w);
-        if (f == kFlagPrefix || f == kFlagError) return w;
-        if (globaltimer_ns() - t0 > limit_ns) return pack_status(kFlagError, 0, 0);
-    }
-}
-
-// Decoupled look-back, run by one full warp of the block that owns `tile`.
-// Publishes the tile's aggregate, sums predecessors' aggregates back to the
-// nearest published prefix (32 tiles per step), publishes the tile's own
-// prefix and returns it (same value in every lane).  On a timeout or a
-// predecessor error it publishes kFlagError and sets *failed.
-__device__ __forceinline__ uint32_t lookback_prefix(uint64_t* status, uint32_t tile, uint32_t aggregate,
-                                                    uint64_t limit_ns, bool* failed) {
-    const uint32_t lane = threadIdx.x & 31u;
-    *failed = false;
-    if (tile == 0) {
-        if (lane == 0) st_relaxed_u64(status, pack_status(kFlagPrefix, aggregate, 0));
-        return 0;
-    }
-    if (lane == 0) st_relaxed_u64(status + tile, pack_status(kFlagAggregate, aggregate, 0));
-
-    uint32_t prefix = 0;
-    int64_t first = (int64_t)tile - 1;  // predecessor examined by lane 0
-    uint64_t t0 = 0;
-    bool clock_started = false;
-    while (true) {
-        const int64_t idx = first - (int64_t)lane;
-        uint64_t w;
-        while (true) {
-            // Lanes past tile 0 read as "prefix 0"; tile 0 always publishes a
-            // prefix, so no window ever needs to look beyond it.
-            w = idx >= 0 ? ld_relaxed_u64(status + idx) : pack_status(kFlagPrefix, 0, 0);
-            const uint32_t f = status_flag(w);
-            if (__any_sync(0xFFFFFFFFu, f == kFlagError)) {
-                *failed = true;
-                break;
-            }
-            if (__all_sync(0xFFFFFFFFu, f != kFlagNone)) break;
-            if (!clock_started) {
-                t0 = globaltimer_ns();
-                clock_started = true;
-            } else if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > limit_ns)) {  // warp-uniform
-                *failed = true;
-                break;
-            }
-            __nanosleep(64);
-        }
-        if (*failed) break;
-        const uint32_t have_prefix = __ballot_sync(0xFFFFFFFFu, status_flag(w) == kFlagPrefix);
-        const uint32_t agg = status_aggregate(w);
-        if (have_prefix) {
-            const uint32_t nearest = __ffs(have_prefix) - 1;
-            uint32_t part = 0;
-            if (lane < nearest) part = agg;
-            if (lane == nearest) part = agg + status_prefix(w);
-            prefix += __reduce_add_sync(0xFFFFFFFFu, part);
-            break;
-        }
-        prefix += __reduce_add_sync(0xFFFFFFFFu, agg);
-        first -= 32;
-    }
-    if (*failed) {
-        if (lane == 0) st_relaxed_u64(status + tile, pack_status(kFlagError, 0, 0));
-        return 0;
-    }
-    if (lane == 0) st_relaxed_u64(status + tile, pack_status(kFlagPrefix, aggregate, prefix));
-    return prefix;
 }
 
 // Little-endian byte stores for the few unaligned header fields.

@@ -7,14 +7,15 @@
 // a 56-bit little-endian word stored as 7 bytes; escapes use the same
 // (u16 position, u8 exponent) stream as BF16.
 //
-// Work layout.  A block of 128 threads owns a tile of 16,384 elements (four
-// tiles per chunk); thread t owns the 128 contiguous elements [128t, 128t+128)
-// of the tile = 16 groups = 128 input bytes and 112 packed bytes.  A warp's
-// 4 KB of elements and 3.5 KB of packed bytes move between global and
-// registers through a per-warp shared-memory transpose, so every global
-// access is a fully coalesced 16 B/lane instruction and every shared access
-// is free of bank conflicts (XOR swizzle for 8-piece rows; the 7-piece rows
-// need none because 7 is odd).
+// Work layout.  Thread t of a block owns 128 contiguous elements = 16 groups
+// = 128 input bytes and 112 packed bytes.  A warp's 4 KB of elements and
+// 3.5 KB of packed bytes move between global memory and registers through a
+// per-warp shared-memory transpose, so every global access is a fully
+// coalesced 16 B/lane instruction and every shared access is free of bank
+// conflicts (XOR swizzle for 8-piece rows; the 7-piece rows need none
+// because 7 is odd).  The encoder's block of 256 threads owns one
+// 32,768-element scan tile; the decoder's block of 128 threads owns a
+// 16,384-element tile.
 #include "sz_device.cuh"
 #include "sz_params.h"
 
@@ -22,11 +23,11 @@ namespace sz {
 
 namespace {
 
-constexpr uint32_t kTilesPerChunk = kChunk / kE5Tile;  // 4
 static_assert(kChunk % kE5Tile == 0, "tiles must not straddle chunks");
-constexpr uint32_t kWarps = kE5Threads / 32;
+constexpr uint32_t kWarps = kE5Threads / 32;           // decode warps
 constexpr uint32_t kWarpElems = 32 * kE5PerThread;     // 4096
-constexpr uint32_t kStageRecs = 2048;                   // records staged in shared memory per tile
+constexpr uint32_t kEncThreads = kScanTile / kE5PerThread;  // 256: one scan tile per encode block
+constexpr uint32_t kEncWarps = kEncThreads / 32;
 
 // 16-byte slot of piece s (0..7) of thread-row r in an 8-piece swizzled row set.
 __device__ __forceinline__ uint32_t swz8(uint32_t r, uint32_t s) { return r * 8u + (s ^ (r & 7u)); }
@@ -34,26 +35,33 @@ __device__ __forceinline__ uint32_t swz8(uint32_t r, uint32_t s) { return r * 8u
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Encode (same single-pass escape compaction as BF16; see sz_bf16.cu).
-//
-// The warp's input bytes stay in shared memory (swizzled rows, one per
-// thread) for the whole tile: packing reads them 16 bytes at a time and the
-// escape records read the exponents of escaped elements back from there, so
-// no thread holds its 128 input bytes in registers.  Packed bytes go to a
-// second per-warp buffer (7 pieces per row) and leave with coalesced stores.
+// Encode, first phase: one scan tile per block.  The warp's input bytes stay
+// in shared memory (swizzled rows, one per thread) for the whole tile:
+// packing reads them 16 bytes at a time and the escape records read the
+// exponents of escaped elements back from there, so no thread holds its 128
+// input bytes in registers.  Packed bytes go to a second per-warp buffer
+// (7 pieces per row) and leave with coalesced stores.  The tile's escape
+// count and its first ws_cap records (element order: thread, then element)
+// go to the workspace; finish_kernel (sz_finish.cu) places them.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kE5Threads) encode_e5m2_kernel(const EncodeParams p) {
-    __shared__ uint8_t s_field[256];                    // byte -> field; 0x80 marks an escape
-    __shared__ __align__(16) uint4 s_in[kWarps][256];   // 8 swizzled pieces per thread
-    __shared__ __align__(16) uint4 s_out[kWarps][224];  // 7 pieces per thread
-    __shared__ uint8_t s_rec[3 * kStageRecs];
-    __shared__ uint32_t s_warp_esc[kWarps];
-    __shared__ uint32_t s_tile, s_prefix;
-    __shared__ int s_failed;
+struct EncodeE5Smem {
+    uint4 in[kEncWarps][256];   // 8 swizzled pieces per thread
+    uint4 out[kEncWarps][224];  // 7 pieces per thread
+    uint32_t warp_esc[kEncWarps];
+    uint8_t field[256];         // byte -> field; 0x80 marks an escape
+};
+
+__global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodeParams p) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
+    auto& s_field = S.field;
+    auto& s_in = S.in;
+    auto& s_out = S.out;
+    auto& s_warp_esc = S.warp_esc;
 
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    for (uint32_t x = tid; x < 256; x += kE5Threads) {
-        const uint32_t e = (x >> 2) & 31u;
+    {
+        const uint32_t x = tid, e = (x >> 2) & 31u;
         uint32_t code = 0xFFu;
 #pragma unroll
         for (int k = 0; k < kCodes; k++)
@@ -61,12 +69,11 @@ __global__ void __launch_bounds__(kE5Threads) encode_e5m2_kernel(const EncodePar
         const uint32_t sm3 = ((x >> 7) << 2) | (x & 3u);
         s_field[x] = (uint8_t)(code == 0xFFu ? (0x80u | (sm3 << 4)) : (code | (sm3 << 4)));
     }
-    if (tid == 0) s_tile = atomicAdd(p.ticket, 1u);
+    if (blockIdx.x == 0 && tid < kCodes) p.out[p.L.cb_off + tid] = p.cb[tid];
     __syncthreads();
-    const uint32_t tile = s_tile;
-    if (tile >= p.num_tiles) return;  // only with the stalled-predecessor test hook
+    const uint32_t st = blockIdx.x;
     const uint64_t n = p.L.n;
-    const uint64_t warp_base = (uint64_t)tile * kE5Tile + warp * kWarpElems;
+    const uint64_t warp_base = (uint64_t)st * kScanTile + warp * kWarpElems;
     const uint64_t thread_base = warp_base + lane * kE5PerThread;
     const bool warp_full = p.vec && warp_base + kWarpElems <= n;
     const uint32_t cnt = thread_base >= n ? 0u : (n - thread_base >= kE5PerThread ? kE5PerThread : (uint32_t)(n - thread_base));
@@ -172,17 +179,18 @@ __global__ void __launch_bounds__(kE5Threads) encode_e5m2_kernel(const EncodePar
     __syncthreads();
     uint32_t rank = incl - mine, tile_esc = 0;
 #pragma unroll
-    for (uint32_t v = 0; v < kWarps; v++) {
+    for (uint32_t v = 0; v < kEncWarps; v++) {
         const uint32_t c = s_warp_esc[v];
         if (v < warp) rank += c;
         tile_esc += c;
     }
-    const bool staged = tile_esc <= kStageRecs;
-
-    // Writes this thread's records, in element order, from record `rank` on;
-    // exponents come back from the input row in shared memory.
-    const uint8_t* row = reinterpret_cast<const uint8_t*>(&s_in[warp][0]);
-    auto emit = [&](uint8_t* dst_base, uint64_t limit) {
+    if (tid == 0) p.ws_count[st] = tile_esc;
+    // Stage this thread's records (those ranked below ws_cap); exponents come
+    // back from the input row in shared memory.
+    if (mine && rank < p.ws_cap) {
+        const uint8_t* row = reinterpret_cast<const uint8_t*>(&s_in[warp][0]);
+        uint8_t* dst = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
+        const uint64_t limit = 3ull * p.ws_cap;
         uint64_t at = 3ull * rank;
 #pragma unroll
         for (int q = 0; q < 4; q++) {
@@ -193,74 +201,14 @@ __global__ void __launch_bounds__(kE5Threads) encode_e5m2_kernel(const EncodePar
                 const uint32_t byte = row[swz8(lane, j >> 4) * 16u + (j & 15u)];
                 const uint32_t pos = (uint32_t)(thread_base + j) & 0xFFFFu;
                 if (at + 3 <= limit) {
-                    dst_base[at] = (uint8_t)pos;
-                    dst_base[at + 1] = (uint8_t)(pos >> 8);
-                    dst_base[at + 2] = (uint8_t)((byte >> 2) & 31u);
+                    dst[at] = (uint8_t)pos;
+                    dst[at + 1] = (uint8_t)(pos >> 8);
+                    dst[at + 2] = (uint8_t)((byte >> 2) & 31u);
                 }
                 at += 3;
             }
         }
-    };
-    if (mine && staged) emit(s_rec, sizeof(s_rec));
-
-    if (warp == 0) {
-        bool failed;
-        const uint32_t prefix = lookback_prefix(p.tile_status, tile, tile_esc, p.wait_limit_ns, &failed);
-        if (lane == 0) s_prefix = prefix, s_failed = failed;
     }
-    __syncthreads();
-    if (s_failed) {
-        if (tid == 0 && p.status) atomicMax(p.status, kStatusTimeout);
-        return;
-    }
-    const uint32_t prefix = s_prefix;
-    const uint64_t dst = p.L.rec_off + 3ull * prefix;
-    if (staged) {
-        const uint32_t nbytes = 3u * tile_esc;
-        for (uint32_t b = tid; b < nbytes; b += kE5Threads)
-            if (dst + b < p.capacity) p.out[dst + b] = s_rec[b];
-    } else if (mine) {
-        // Too many escapes to stage: write them straight to their place.
-        emit(p.out + dst, p.capacity > dst ? p.capacity - dst : 0);
-    }
-
-    if (tid == 0) {
-        if (tile % kTilesPerChunk == 0 && tile > 0) {
-            const uint64_t wprev = wait_for_prefix(p.tile_status, tile - kTilesPerChunk, p.wait_limit_ns);
-            if (status_flag(wprev) == kFlagError) {
-                if (p.status) atomicMax(p.status, kStatusTimeout);
-            } else {
-                const uint32_t c = tile / kTilesPerChunk - 1;
-                const uint32_t first = status_prefix(wprev);
-                store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
-                store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, prefix - first);
-            }
-        }
-        if (tile == p.num_tiles - 1) {
-            const uint32_t total = prefix + tile_esc;
-            const unsigned long long size = p.L.rec_off + 3ull * total;
-            *p.out_bytes = size;
-            if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
-            if (p.L.num_chunks > 0) {
-                const uint32_t c = p.L.num_chunks - 1;
-                const uint32_t first_tile = c * kTilesPerChunk;
-                uint32_t first = prefix;
-                bool ok = true;
-                if (first_tile != tile) {
-                    const uint64_t wf = wait_for_prefix(p.tile_status, first_tile, p.wait_limit_ns);
-                    ok = status_flag(wf) != kFlagError;
-                    first = status_prefix(wf);
-                }
-                if (ok) {
-                    store_u32_le(p.out + p.L.hdr_off + 8ull * c, first);
-                    store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, total - first);
-                } else if (p.status) {
-                    atomicMax(p.status, kStatusTimeout);
-                }
-            }
-        }
-    }
-    if (tile == 0 && tid < kCodes) p.out[p.L.cb_off + tid] = p.cb[tid];
 }
 
 // ---------------------------------------------------------------------------
@@ -373,8 +321,12 @@ __global__ void __launch_bounds__(kE5Threads) decode_e5m2_kernel(const DecodePar
 }
 
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
-    encode_e5m2_kernel<<<p.num_tiles, kE5Threads, 0, s>>>(p);
-    return cudaGetLastError();
+    const size_t smem = sizeof(EncodeE5Smem);
+    cudaError_t err = cudaFuncSetAttribute(encode_e5m2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    encode_e5m2_kernel<<<p.num_tiles, kEncThreads, smem, s>>>(p);
+    err = cudaGetLastError();
+    return err != cudaSuccess ? err : launch_finish(p, false, s);
 }
 
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {

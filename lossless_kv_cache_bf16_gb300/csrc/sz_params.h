@@ -24,9 +24,7 @@ struct EncodeParams {
     const uint8_t* in;
     uint8_t* out;
     uint64_t capacity;
-    uint32_t num_tiles;
-    uint32_t* ticket;        // workspace: tile counter
-    uint64_t* tile_status;   // workspace: one look-back word per tile
+    uint32_t num_tiles;      // scan tiles
     unsigned long long* out_bytes;
     int* status;             // nullable
     uint64_t wait_limit_ns;
@@ -34,8 +32,8 @@ struct EncodeParams {
     uint32_t grid;           // persistent kernels: blocks in the launch
     uint32_t skip_first;     // test hook: a wait that never completes
     int contig;              // codebook is 16 consecutive exponents cb[0]..cb[0]+15
-    uint32_t* ws_count;      // two-phase encode: escapes per scan tile
-    uint8_t* ws_rec;         // two-phase encode: staged records, ws_cap per scan tile
+    uint32_t* ws_count;      // workspace: escapes per scan tile
+    uint8_t* ws_rec;         // workspace: staged records, ws_cap per scan tile
     uint32_t ws_cap;         // records staged per scan tile
     uint8_t cb[16];          // ascending
 };
@@ -62,15 +60,17 @@ struct HistogramParams {
 constexpr uint32_t kBf16Threads = 256;
 constexpr uint32_t kBf16PerThread = 32;
 constexpr uint32_t kBf16Tile = kBf16Threads * kBf16PerThread;   // 8192
-constexpr uint32_t kBf16ScanTile = 4 * kBf16Tile;                // encode look-back unit: 32768
-constexpr uint32_t kE5Threads = 128;
+constexpr uint32_t kE5Threads = 128;                            // E5M2 decode block
 constexpr uint32_t kE5PerThread = 128;                          // 16 groups of 8
-constexpr uint32_t kE5Tile = kE5Threads * kE5PerThread;         // 16384
+constexpr uint32_t kE5Tile = kE5Threads * kE5PerThread;         // 16384: E5M2 decode tile
+// Encode (both dtypes): escape counts and staged records per scan tile.
+constexpr uint32_t kScanTile = 32768;
 
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_histogram(const HistogramParams& p, cudaStream_t s);
+cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s);
 
 }  // namespace sz

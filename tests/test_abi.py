@@ -45,17 +45,14 @@ def test_encoded_size_matches_oracle(S, orc):
 
 
 def test_workspace_size(S):
-    # BF16: a u32 count (16-byte aligned block) and 1,024 staged 3-byte records
-    # per 32,768-element scan tile.
-    bf16 = lambda tiles: ((4 * tiles + 15) // 16) * 16 + 3072 * tiles
-    assert S.sz_workspace_size(S.SZ_BF16, 0) == bf16(1)
-    assert S.sz_workspace_size(S.SZ_BF16, 32768) == bf16(1)
-    assert S.sz_workspace_size(S.SZ_BF16, 32769) == bf16(2)
-    assert S.sz_workspace_size(S.SZ_BF16, 939524096) == bf16(939524096 // 32768)
-    # E5M2: a tile counter and one look-back word per 16,384-element tile.
-    assert S.sz_workspace_size(S.SZ_FP8_E5M2, 0) == 16 + 8
-    assert S.sz_workspace_size(S.SZ_FP8_E5M2, 16385) == 16 + 16
-    assert S.sz_workspace_size(S.SZ_FP8_E5M2, 1 << 30) == 16 + 8 * ((1 << 30) // 16384)
+    # A u32 count (16-byte aligned block) and 1,024 staged 3-byte records per
+    # 32,768-element scan tile, for either dtype.
+    ws = lambda tiles: ((4 * tiles + 15) // 16) * 16 + 3072 * tiles
+    for dt in (S.SZ_BF16, S.SZ_FP8_E5M2):
+        assert S.sz_workspace_size(dt, 0) == ws(1)
+        assert S.sz_workspace_size(dt, 32768) == ws(1)
+        assert S.sz_workspace_size(dt, 32769) == ws(2)
+        assert S.sz_workspace_size(dt, 939524096) == ws(939524096 // 32768)
 
 
 def test_codebook_selection_matches_oracle(S, orc):

@@ -26,19 +26,19 @@ def test_link_model():
 
 
 def test_traffic_is_null_without_matching_profile(tmp_path, monkeypatch):
-    assert bench.profiled_traffic("encode_bf16_kernel", "no_such_workload") is None
+    assert bench.profiled_traffic("encode_bf16", "no_such_workload") is None
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     os.makedirs(tmp_path / "profiles")
     csrc = tmp_path / "lossless_kv_cache_bf16_gb300" / "csrc"
     os.makedirs(csrc)
-    for name in bench.KERNEL_SOURCES["encode_bf16_kernel"]:
+    for name in bench.KERNEL_SOURCES["encode_bf16"]:
         (csrc / name).write_text("v1")
-    h = bench.kernel_source_hash("encode_bf16_kernel")
-    (tmp_path / "profiles" / "encode_bf16_kernel_w.txt").write_text(
+    h = bench.kernel_source_hash("encode_bf16")
+    (tmp_path / "profiles" / "encode_bf16_w.txt").write_text(
         f"kernel_source_sha256_16: {h}\ndram_bytes_per_launch: 1234\n")
-    assert bench.profiled_traffic("encode_bf16_kernel", "w") == 1234
+    assert bench.profiled_traffic("encode_bf16", "w") == 1234
     (csrc / "sz_bf16.cu").write_text("v2")   # kernel changed since the capture
-    assert bench.profiled_traffic("encode_bf16_kernel", "w") is None
+    assert bench.profiled_traffic("encode_bf16", "w") is None
 
 
 def _free_port():

@@ -2,10 +2,9 @@
 
 A corrupted stream must give SZ_ERR_CORRUPT exactly when the oracle's
 validator rejects it, and decode must never write outside its output.  The
-encode's wait for a predecessor tile is bounded: a test hook starts the tile
-counter at 1 so tile 0 never publishes, and the wait must end in
-SZ_ERR_TIMEOUT with the CUDA context still usable.  Nothing here faults,
-traps or hangs the GPU.
+encode's waits are bounded: a test hook never issues one input copy, and the
+wait for it must end in SZ_ERR_TIMEOUT with the CUDA context still usable.
+Nothing here faults, traps or hangs the GPU.
 """
 import time
 
@@ -113,25 +112,32 @@ def test_host_rejects_bad_arguments():
     assert e.value.status == S.SZ_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("kind", ["bf16", "e5m2"])
-def test_stalled_predecessor_times_out(orc, kind):
-    dt = G.DT[kind]
-    n = 5 * (8192 if kind == "bf16" else 16384) + 7
-    x = (torch.randn(n, device="cuda") * 100).to(torch.bfloat16) if kind == "bf16" else \
-        torch.randint(0, 256, (n,), device="cuda", dtype=torch.uint8)
-    cb = CB_MID if kind == "bf16" else CB_E5_MID
-    out = torch.empty(S.sz_encoded_size(dt, n, n), dtype=torch.uint8, device="cuda")
-    ws = torch.empty(S.sz_workspace_size(dt, n), dtype=torch.uint8, device="cuda")
+def test_stall_hook_refuses_e5m2():
+    x = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    out = torch.empty(S.sz_encoded_size(S.SZ_FP8_E5M2, 64, 64), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(S.sz_workspace_size(S.SZ_FP8_E5M2, 64), dtype=torch.uint8, device="cuda")
+    ob = torch.zeros(1, dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(S.SplitZipError) as e:
+        S.sz_debug_encode_stalled(S.SZ_FP8_E5M2, CB_E5_MID, x, out, ob, st, ws, wait_limit_ns=1000)
+    assert e.value.status == S.SZ_ERR_UNSUPPORTED
+
+
+def test_stalled_wait_times_out(orc):
+    n = 5 * 32768 + 7
+    x = (torch.randn(n, device="cuda") * 100).to(torch.bfloat16)
+    out = torch.empty(S.sz_encoded_size(S.SZ_BF16, n, n), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(S.sz_workspace_size(S.SZ_BF16, n), dtype=torch.uint8, device="cuda")
     ob = torch.zeros(1, dtype=torch.int64, device="cuda")
     st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
     t0 = time.time()
-    S.sz_debug_encode_stalled(dt, cb, x, out, ob, st, ws, wait_limit_ns=50_000_000)
+    S.sz_debug_encode_stalled(S.SZ_BF16, CB_MID, x, out, ob, st, ws, wait_limit_ns=50_000_000)
     torch.cuda.synchronize()
     elapsed = time.time() - t0
     assert int(st.item()) == S.SZ_ERR_TIMEOUT
     assert elapsed < 10.0
     # The context is still usable: a normal encode right after is exact.
-    got, status, _ = G.encode(dt, cb, x)
+    got, status, _ = G.encode(S.SZ_BF16, CB_MID, x)
     assert status == 0
-    assert np.array_equal(got, orc.encode(O.BF16 if kind == "bf16" else O.E5M2, cb, G.as_bytes(x)))
+    assert np.array_equal(got, orc.encode(O.BF16, CB_MID, G.as_bytes(x)))
