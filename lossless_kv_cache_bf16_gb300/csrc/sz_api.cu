@@ -24,7 +24,8 @@ uint64_t scan_tiles_for(uint64_t n) { return std::max<uint64_t>(1, cdiv(n, kScan
 
 // The encoders stage up to this many escape records per scan tile in the
 // workspace; scan tiles with more are re-derived by the finish kernel.
-constexpr uint32_t kStageRecs = 1024;
+constexpr uint32_t kStageRecs = kMaxStageRecs;
+static_assert(kStageRecs <= kMaxStageRecs && kStageRecs % 16 == 0, "finish kernel staging limits");
 uint64_t align16(uint64_t x) { return (x + 15) & ~15ull; }
 // Workspace: [u32 count per scan tile][3 * cap bytes of records per scan tile].
 uint64_t workspace_bytes(uint64_t n, uint32_t cap = kStageRecs) {
@@ -123,6 +124,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
 // rest are re-derived): 6.1 MiB.
 constexpr uint64_t kNoAllocMaxElems = 1ull << 28;
 constexpr uint32_t kNoAllocStageRecs = 256;
+static_assert(kNoAllocStageRecs <= kMaxStageRecs && kNoAllocStageRecs % 16 == 0, "finish kernel staging limits");
 constexpr uint64_t kNoAllocScratchBytes = (kNoAllocMaxElems / kScanTile) * (4 + 3ull * kNoAllocStageRecs);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

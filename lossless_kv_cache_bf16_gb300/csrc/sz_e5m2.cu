@@ -32,6 +32,63 @@ constexpr uint32_t kEncWarps = kEncThreads / 32;
 // 16-byte slot of piece s (0..7) of thread-row r in an 8-piece swizzled row set.
 __device__ __forceinline__ uint32_t swz8(uint32_t r, uint32_t s) { return r * 8u + (s ^ (r & 7u)); }
 
+// Four E5M2 bytes -> their four 7-bit fields (one per byte), for a codebook of
+// 16 consecutive exponents cb0..cb0+15 (cb0 <= 16).  Per byte,
+// d = 0x20 + exponent - cb0 has no borrow; bit 4 of d is set exactly when
+// exponent - cb0 falls outside 0..15, i.e. for an escape, whose code is 0.
+// esc4 receives those bit-4 flags.
+__device__ __forceinline__ uint32_t fields4_contig(uint32_t w, uint32_t cb0x4, uint32_t& esc4) {
+    const uint32_t d = (((w >> 2) & 0x1F1F1F1Fu) | 0x20202020u) - cb0x4;
+    esc4 = d & 0x10101010u;
+    const uint32_t keep = 0x0F0F0F0Fu ^ (esc4 - (esc4 >> 4));  // 0x0F per byte, 0x00 for escapes
+    return (d & keep) | ((w >> 1) & 0x40404040u) | ((w << 4) & 0x30303030u);
+}
+
+// Four 7-bit fields held one per byte -> 28 bits, field 0 lowest.
+__device__ __forceinline__ uint32_t pack28(uint32_t f) {
+    const uint32_t x = (f & 0x007F007Fu) | ((f >> 1) & 0x3F803F80u);  // two 14-bit pairs
+    return (x & 0x3FFFu) | ((x >> 2) & 0x0FFFC000u);
+}
+
+// Bit-4 flags of four bytes -> a 4-bit mask, byte 0 lowest (the partial
+// products of the multiply land on distinct bits, so nothing carries).
+__device__ __forceinline__ uint32_t gather4(uint32_t esc4) { return ((esc4 >> 4) * 0x10204080u) >> 28; }
+
+// One group of 8 elements (two little-endian words of input bytes) -> the
+// 56-bit packed word (lo: bits 0..31, hi: bits 32..55) and the 8-bit escape
+// mask.  CONTIG: byte-parallel arithmetic; otherwise a 256-entry table maps a
+// byte to its field, with 0x80 marking an escape.
+template <bool CONTIG>
+__device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t cb0x4, const uint8_t* field, uint32_t& lo,
+                                           uint32_t& hi, uint32_t& esc8) {
+    if (CONTIG) {
+        uint32_t ea, eb;
+        const uint32_t pa = pack28(fields4_contig(a, cb0x4, ea)), pb = pack28(fields4_contig(b, cb0x4, eb));
+        lo = pa | (pb << 28);
+        hi = pb >> 4;
+        esc8 = gather4(ea) | (gather4(eb) << 4);
+    } else {
+        lo = 0;
+        hi = 0;
+        esc8 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t f = field[((j < 4 ? a : b) >> (8 * (j & 3))) & 0xFFu];
+            esc8 |= (f >> 7) << j;
+            const uint32_t f7 = f & 0x7Fu;
+            const int bit = 7 * j;
+            if (bit + 7 <= 32) {
+                lo |= f7 << bit;
+            } else if (bit >= 32) {
+                hi |= f7 << (bit - 32);
+            } else {
+                lo |= f7 << bit;
+                hi |= f7 >> (32 - bit);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -51,6 +108,7 @@ struct EncodeE5Smem {
     uint8_t field[256];         // byte -> field; 0x80 marks an escape
 };
 
+template <bool CONTIG>
 __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodeParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
@@ -109,6 +167,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodePa
     // accumulator; each append completes at most one 32-bit word, and every
     // fourth word completes one 16-byte piece of the row's 7.
     uint32_t escm[4] = {0, 0, 0, 0};
+    const uint32_t cb0x4 = (uint32_t)p.cb[0] * 0x01010101u;
     {
         uint64_t acc = 0;
         uint32_t nbits = 0, nwords = 0;
@@ -119,23 +178,10 @@ __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodePa
             const uint32_t in4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int h = 0; h < 2; h++) {  // group 2s + h
-                uint32_t lo = 0, hi = 0;
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const int e = 16 * s + 8 * h + j;  // element inside the thread
-                    const uint32_t f = s_field[(in4[2 * h + (j >> 2)] >> (8 * (j & 3))) & 0xFFu];
-                    escm[e >> 5] |= (f >> 7) << (e & 31);
-                    const uint32_t f7 = f & 0x7Fu;
-                    const int bit = 7 * j;
-                    if (bit + 7 <= 32) {
-                        lo |= f7 << bit;
-                    } else if (bit >= 32) {
-                        hi |= f7 << (bit - 32);
-                    } else {
-                        lo |= f7 << bit;
-                        hi |= f7 >> (32 - bit);
-                    }
-                }
+                const int e = 16 * s + 8 * h;  // first element of the group inside the thread
+                uint32_t lo, hi, esc8;
+                code_group<CONTIG>(in4[2 * h], in4[2 * h + 1], cb0x4, s_field, lo, hi, esc8);
+                escm[e >> 5] |= esc8 << (e & 31);
 #pragma unroll
                 for (int part = 0; part < 2; part++) {
                     acc |= (uint64_t)(part == 0 ? lo : hi) << nbits;
@@ -322,9 +368,10 @@ __global__ void __launch_bounds__(kE5Threads) decode_e5m2_kernel(const DecodePar
 
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(EncodeE5Smem);
-    cudaError_t err = cudaFuncSetAttribute(encode_e5m2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = p.contig ? encode_e5m2_kernel<true> : encode_e5m2_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    encode_e5m2_kernel<<<p.num_tiles, kEncThreads, smem, s>>>(p);
+    kern<<<p.num_tiles, kEncThreads, smem, s>>>(p);
     err = cudaGetLastError();
     return err != cudaSuccess ? err : launch_finish(p, false, s);
 }

@@ -4,11 +4,15 @@
 // tile, the number of escapes and (up to ws_cap of) the tile's escape
 // records in element order in the workspace.  This kernel places them:
 //  * block b owns the contiguous scan-tile range [bT/F, (b+1)T/F); it sums
-//    the counts of all earlier scan tiles, then scans its own counts in
-//    batches of 256, giving every scan tile its escape offset;
+//    the counts of all earlier scan tiles (16-byte loads, several in flight
+//    per thread), then scans its own counts in batches of 256, giving every
+//    scan tile its escape offset;
 //  * one warp per scan tile copies the staged records to offset * 3 in the
-//    escape stream, or, when the tile had more than ws_cap escapes, walks the
-//    tile's elements again in order and writes the records directly;
+//    escape stream: 16-byte loads of the whole staged run into shared memory,
+//    then aligned 4-byte stores (a funnel shift realigns the bytes) with at
+//    most 3 single bytes at either end.  When the tile had more than ws_cap
+//    escapes, the warp walks the tile's elements again in order and writes
+//    the records directly;
 //  * a chunk's last scan tile writes the chunk's header (offset = escapes
 //    before the chunk, count = escapes in it); the last scan tile writes the
 //    stream size.
@@ -23,7 +27,11 @@ namespace sz {
 namespace {
 
 constexpr uint32_t kFinThreads = 256;
+constexpr uint32_t kFinWarps = kFinThreads / 32;
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;
+constexpr uint32_t kStageBytes = 3 * kMaxStageRecs;      // staged records of one scan tile
+constexpr uint32_t kStageLoads = kStageBytes / 512;       // 16-byte loads per lane
+static_assert(kStageBytes % 512 == 0, "whole warp-wide 16-byte loads");
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
 
 // Exponent of element i: bits 14..7 of a BF16, bits 6..2 of an E5M2 byte.
@@ -37,7 +45,8 @@ __device__ __forceinline__ uint32_t exponent_at(const uint8_t* in, uint64_t i) {
 
 template <bool BF16>
 __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams p) {
-    __shared__ uint32_t s_sum[kFinThreads / 32];
+    __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 16];  // +16: realignment reads past the end
+    __shared__ uint32_t s_sum[kFinWarps];
     __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
     __shared__ uint8_t s_member[256];  // exponent is in the codebook
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -49,17 +58,28 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
         for (int k = 0; k < kCodes; k++) member |= p.cb[k] == tid;
         s_member[tid] = (uint8_t)member;
     }
-    // Escapes in all scan tiles before this block's range.
+    // Escapes in all scan tiles before this block's range.  ws_count is
+    // 16-byte aligned.
     uint32_t part = 0;
-    for (uint32_t t = tid; t < t0; t += kFinThreads) part += p.ws_count[t];
+    {
+        const uint4* c4 = reinterpret_cast<const uint4*>(p.ws_count);
+        const uint32_t q_end = t0 / 4;
+#pragma unroll 8
+        for (uint32_t q = tid; q < q_end; q += kFinThreads) {
+            const uint4 v = c4[q];
+            part += v.x + v.y + v.z + v.w;
+        }
+        if (tid < (t0 & 3u)) part += p.ws_count[(t0 & ~3u) + tid];
+    }
     part = __reduce_add_sync(0xFFFFFFFFu, part);
     if (lane == 0) s_sum[warp] = part;
     __syncthreads();
     uint32_t base = 0;
 #pragma unroll
-    for (uint32_t v = 0; v < kFinThreads / 32; v++) base += s_sum[v];
+    for (uint32_t v = 0; v < kFinWarps; v++) base += s_sum[v];
     __syncthreads();
 
+    uint8_t* const stage = s_stage[warp];
     for (uint32_t c0 = t0; c0 < t1; c0 += kFinThreads) {
         const uint32_t t = c0 + tid;
         const uint32_t cnt = t < t1 ? p.ws_count[t] : 0u;
@@ -73,7 +93,7 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
         __syncthreads();
         uint32_t wbase = 0, total = 0;
 #pragma unroll
-        for (uint32_t v = 0; v < kFinThreads / 32; v++) {
+        for (uint32_t v = 0; v < kFinWarps; v++) {
             wbase += v < warp ? s_sum[v] : 0u;
             total += s_sum[v];
         }
@@ -99,13 +119,45 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
         __syncthreads();
         // One warp per scan tile: copy the staged records, or re-derive them.
         const uint32_t batch = min(kFinThreads, t1 - c0);
-        for (uint32_t j = warp; j < batch; j += kFinThreads / 32) {
+        for (uint32_t j = warp; j < batch; j += kFinWarps) {
             const uint32_t st = c0 + j, c = s_count[j];
             const uint64_t dst = p.L.rec_off + 3ull * s_prefix[j];
             if (c <= p.ws_cap) {
-                const uint8_t* src = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
-                for (uint32_t b = lane; b < 3 * c; b += 32)
-                    if (dst + b < p.capacity) p.out[dst + b] = src[b];
+                // Staged run: 3c bytes at a 16-byte aligned address, inside a
+                // region of 3 * ws_cap bytes (a multiple of 16).
+                const uint32_t nbytes = 3 * c;
+                const uint4* src = reinterpret_cast<const uint4*>(p.ws_rec + (uint64_t)st * 3 * p.ws_cap);
+                uint4 v[kStageLoads];
+#pragma unroll
+                for (uint32_t k = 0; k < kStageLoads; k++)
+                    if (16 * lane + 512 * k < nbytes) v[k] = src[lane + 32 * k];
+#pragma unroll
+                for (uint32_t k = 0; k < kStageLoads; k++)
+                    if (16 * lane + 512 * k < nbytes) reinterpret_cast<uint4*>(stage)[lane + 32 * k] = v[k];
+                __syncwarp();
+                // out + dst + head is 4-byte aligned; bytes before it, and the
+                // 0..3 bytes after the last whole word, go one at a time.
+                uint8_t* const o = p.out + dst;
+                const uint32_t head = min((uint32_t)((4u - (uint32_t)(reinterpret_cast<uintptr_t>(o) & 3u)) & 3u), nbytes);
+                const uint32_t words = (nbytes - head) / 4, tail = (nbytes - head) & 3u;
+                const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage);
+                const uint32_t shift = 8u * (head & 3u);
+                for (uint32_t w = lane; w < words; w += 32) {
+                    const uint32_t off = head + 4 * w;
+                    const uint32_t val = __funnelshift_r(sw[off >> 2], sw[(off >> 2) + 1], shift);
+                    if (dst + off + 4 <= p.capacity) {
+                        *reinterpret_cast<uint32_t*>(o + off) = val;
+                    } else {
+#pragma unroll
+                        for (uint32_t b = 0; b < 4; b++)
+                            if (dst + off + b < p.capacity) o[off + b] = (uint8_t)(val >> (8 * b));
+                    }
+                }
+                if (lane < head + tail) {
+                    const uint32_t off = lane < head ? lane : head + 4 * words + (lane - head);
+                    if (dst + off < p.capacity) o[off] = stage[off];
+                }
+                __syncwarp();  // the buffer is reused by the warp's next scan tile
             } else {
                 // More escapes than staged: walk the tile in element order,
                 // 8 consecutive elements per lane, 256 per step.
@@ -150,7 +202,8 @@ cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s) {
     cudaError_t err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    const uint64_t want = (uint64_t)2 * sms;
+    // Several blocks per SM: the record copies are latency bound.
+    const uint64_t want = (uint64_t)4 * sms;
     const uint32_t grid = (uint32_t)(p.num_tiles < want ? p.num_tiles : want);
     if (bf16)
         finish_kernel<true><<<grid, kFinThreads, 0, s>>>(p);

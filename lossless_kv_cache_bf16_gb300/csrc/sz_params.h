@@ -65,6 +65,9 @@ constexpr uint32_t kE5PerThread = 128;                          // 16 groups of 
 constexpr uint32_t kE5Tile = kE5Threads * kE5PerThread;         // 16384: E5M2 decode tile
 // Encode (both dtypes): escape counts and staged records per scan tile.
 constexpr uint32_t kScanTile = 32768;
+// Most records staged per scan tile (EncodeParams::ws_cap <= this, and a
+// multiple of 16 so that every tile's staged run starts 16-byte aligned).
+constexpr uint32_t kMaxStageRecs = 1024;
 
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);

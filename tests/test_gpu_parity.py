@@ -66,25 +66,32 @@ def test_e5m2_edge_sizes(orc, n):
 
 def test_bf16_bruteforce_all_patterns(orc):
     x = torch.arange(65536, dtype=torch.int32, device="cuda").to(torch.int16).view(torch.bfloat16)
-    for cb in (CB_MID, CB_EDGES):
+    # Contiguous codebooks (byte-parallel coding path) including both ends of
+    # the exponent range, and a non-contiguous one (table path).
+    cbs = (CB_MID, np.arange(0, 16, dtype=np.uint8), np.arange(240, 256, dtype=np.uint8), CB_EDGES)
+    for cb in cbs:
         s = roundtrip_vs_oracle(orc, "bf16", cb, x)
         assert s.size == 282648
     # Every pattern in a shuffled order across several tiles and chunks.
     g = torch.Generator(device="cuda")
     g.manual_seed(5)
     perm = torch.cat([torch.randperm(65536, generator=g, device="cuda") for _ in range(5)])
-    roundtrip_vs_oracle(orc, "bf16", CB_EDGES, x[perm].contiguous())
+    for cb in (CB_MID, CB_EDGES):
+        roundtrip_vs_oracle(orc, "bf16", cb, x[perm].contiguous())
 
 
 def test_e5m2_bruteforce_all_patterns(orc):
     x = torch.arange(256, dtype=torch.int32, device="cuda").to(torch.uint8)
-    for cb in (CB_E5_MID, CB_E5_EDGES):
+    cbs = (CB_E5_MID, np.arange(0, 16, dtype=np.uint8), np.arange(16, 32, dtype=np.uint8), CB_E5_EDGES)
+    for cb in cbs:
         s = roundtrip_vs_oracle(orc, "e5m2", cb, x)
         assert s.size == 632
+    # Shuffled across several scan tiles and chunks (whole-warp load path).
     g = torch.Generator(device="cuda")
     g.manual_seed(6)
     perm = torch.randint(0, 256, (5 * 65536 + 77,), generator=g, device="cuda")
-    roundtrip_vs_oracle(orc, "e5m2", CB_E5_EDGES, x[perm].contiguous())
+    for cb in cbs:
+        roundtrip_vs_oracle(orc, "e5m2", cb, x[perm].contiguous())
 
 
 def test_unaligned_buffers(orc):
