@@ -33,44 +33,46 @@ constexpr uint32_t kEncWarps = kEncThreads / 32;
 __device__ __forceinline__ uint32_t swz8(uint32_t r, uint32_t s) { return r * 8u + (s ^ (r & 7u)); }
 
 // Four E5M2 bytes -> their four 7-bit fields (one per byte), for a codebook of
-// 16 consecutive exponents cb0..cb0+15 (cb0 <= 16).  Per byte,
-// d = 0x20 + exponent - cb0 has no borrow; bit 4 of d is set exactly when
-// exponent - cb0 falls outside 0..15, i.e. for an escape, whose code is 0.
-// esc4 receives those bit-4 flags.
-__device__ __forceinline__ uint32_t fields4_contig(uint32_t w, uint32_t cb0x4, uint32_t& esc4) {
-    const uint32_t d = (((w >> 2) & 0x1F1F1F1Fu) | 0x20202020u) - cb0x4;
+// 16 consecutive exponents cb0..cb0+15 (cb0 <= 16).  With add = 0x20 - cb0 in
+// every byte, d = exponent + add has no carry between bytes, and bit 4 of d
+// is set exactly when exponent - cb0 falls outside 0..15, i.e. for an escape,
+// whose code is 0.  esc4 receives those bit-4 flags.  The parts of a field
+// occupy disjoint bits, so the mantissa joins with a multiply-add.
+__device__ __forceinline__ uint32_t fields4_contig(uint32_t w, uint32_t add, uint32_t& esc4) {
+    const uint32_t d = ((w >> 2) & 0x1F1F1F1Fu) + add;
     esc4 = d & 0x10101010u;
-    const uint32_t keep = 0x0F0F0F0Fu ^ (esc4 - (esc4 >> 4));  // 0x0F per byte, 0x00 for escapes
-    return (d & keep) | ((w >> 1) & 0x40404040u) | ((w << 4) & 0x30303030u);
+    const uint32_t kill = (esc4 >> 4) * 0x0Fu;                     // 0x0F in escaped bytes
+    const uint32_t code_sign = (d & 0x0F0F0F0Fu & ~kill) | ((w >> 1) & 0x40404040u);
+    return (w & 0x03030303u) * 16u + code_sign;
 }
 
-// Four 7-bit fields held one per byte -> 28 bits, field 0 lowest.
+// Four 7-bit fields held one per byte -> 28 bits, field 0 lowest.  Each step
+// moves the upper half of every lane down by subtracting a multiple of it.
 __device__ __forceinline__ uint32_t pack28(uint32_t f) {
-    const uint32_t x = (f & 0x007F007Fu) | ((f >> 1) & 0x3F803F80u);  // two 14-bit pairs
-    return (x & 0x3FFFu) | ((x >> 2) & 0x0FFFC000u);
+    const uint32_t x = f - ((f >> 8) & 0x007F007Fu) * 128u;     // 16-bit lanes: f0 | f1 << 7
+    return x - ((x >> 2) & 0x0FFFC000u) * 3u;                     // f0 | f1 << 7 | f2 << 14 | f3 << 21
 }
-
-// Bit-4 flags of four bytes -> a 4-bit mask, byte 0 lowest (the partial
-// products of the multiply land on distinct bits, so nothing carries).
-__device__ __forceinline__ uint32_t gather4(uint32_t esc4) { return ((esc4 >> 4) * 0x10204080u) >> 28; }
 
 // One group of 8 elements (two little-endian words of input bytes) -> the
-// 56-bit packed word (lo: bits 0..31, hi: bits 32..55) and the 8-bit escape
-// mask.  CONTIG: byte-parallel arithmetic; otherwise a 256-entry table maps a
-// byte to its field, with 0x80 marking an escape.
+// 56-bit packed word (lo: bits 0..31, hi: bits 32..55) and, in bits 24..31 of
+// esc_hi, the escape mask (element j at bit 24 + j; the lower bits are junk).
+// CONTIG: byte-parallel arithmetic, the eight bit-4 flags gathered by one
+// multiply whose partial products land below bit 24 or above bit 31;
+// otherwise a 256-entry table maps a byte to its field, with 0x80 marking an
+// escape.
 template <bool CONTIG>
-__device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t cb0x4, const uint8_t* field, uint32_t& lo,
-                                           uint32_t& hi, uint32_t& esc8) {
+__device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t add, const uint8_t* field, uint32_t& lo,
+                                           uint32_t& hi, uint32_t& esc_hi) {
     if (CONTIG) {
         uint32_t ea, eb;
-        const uint32_t pa = pack28(fields4_contig(a, cb0x4, ea)), pb = pack28(fields4_contig(b, cb0x4, eb));
-        lo = pa | (pb << 28);
+        const uint32_t pa = pack28(fields4_contig(a, add, ea)), pb = pack28(fields4_contig(b, add, eb));
+        lo = pb * (1u << 28) + pa;
         hi = pb >> 4;
-        esc8 = gather4(ea) | (gather4(eb) << 4);
+        esc_hi = ((ea >> 4) | eb) * 0x01020408u;  // a_j at 8j, b_j at 8j + 4 -> bit 24 + j, 28 + j
     } else {
         lo = 0;
         hi = 0;
-        esc8 = 0;
+        uint32_t esc8 = 0;
 #pragma unroll
         for (int j = 0; j < 8; j++) {
             const uint32_t f = field[((j < 4 ? a : b) >> (8 * (j & 3))) & 0xFFu];
@@ -86,6 +88,7 @@ __device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t cb0x
                 hi |= f7 >> (32 - bit);
             }
         }
+        esc_hi = esc8 << 24;
     }
 }
 
@@ -163,39 +166,36 @@ __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodePa
     }
     __syncwarp();
 
-    // Pack: each group's 56 bits are appended (32 + 24 bits) to a bit
-    // accumulator; each append completes at most one 32-bit word, and every
-    // fourth word completes one 16-byte piece of the row's 7.
-    uint32_t escm[4] = {0, 0, 0, 0};
-    const uint32_t cb0x4 = (uint32_t)p.cb[0] * 0x01010101u;
+    // Pack: four groups (224 bits) make seven 32-bit words; a thread's 16
+    // groups make its 28 words = 7 pieces of 16 bytes.  escm[q] holds the
+    // escape flags of elements 32q..32q+31 of the thread.
+    uint32_t escm[4];
     {
-        uint64_t acc = 0;
-        uint32_t nbits = 0, nwords = 0;
-        uint32_t words[4] = {0, 0, 0, 0};
+        const uint32_t add = 0x20202020u - (uint32_t)p.cb[0] * 0x01010101u;
+        uint32_t words[28];
 #pragma unroll
-        for (int s = 0; s < 8; s++) {
-            const uint4 v = s_in[warp][swz8(lane, s)];
-            const uint32_t in4[4] = {v.x, v.y, v.z, v.w};
+        for (int q = 0; q < 4; q++) {
+            uint32_t lo[4], hi[4], eh[4];
 #pragma unroll
-            for (int h = 0; h < 2; h++) {  // group 2s + h
-                const int e = 16 * s + 8 * h;  // first element of the group inside the thread
-                uint32_t lo, hi, esc8;
-                code_group<CONTIG>(in4[2 * h], in4[2 * h + 1], cb0x4, s_field, lo, hi, esc8);
-                escm[e >> 5] |= esc8 << (e & 31);
-#pragma unroll
-                for (int part = 0; part < 2; part++) {
-                    acc |= (uint64_t)(part == 0 ? lo : hi) << nbits;
-                    nbits += part == 0 ? 32 : 24;
-                    if (nbits >= 32) {
-                        words[nwords & 3] = (uint32_t)acc;
-                        acc >>= 32;
-                        nbits -= 32;
-                        if ((++nwords & 3) == 0)
-                            s_out[warp][lane * 7 + (nwords >> 2) - 1] = make_uint4(words[0], words[1], words[2], words[3]);
-                    }
-                }
+            for (int hs = 0; hs < 2; hs++) {
+                const uint4 v = s_in[warp][swz8(lane, 2 * q + hs)];
+                code_group<CONTIG>(v.x, v.y, add, s_field, lo[2 * hs], hi[2 * hs], eh[2 * hs]);
+                code_group<CONTIG>(v.z, v.w, add, s_field, lo[2 * hs + 1], hi[2 * hs + 1], eh[2 * hs + 1]);
             }
+            // Byte 3 of each group's eh, in group order.
+            escm[q] = __byte_perm(__byte_perm(eh[0], eh[1], 0x0073u), __byte_perm(eh[2], eh[3], 0x7300u), 0x7610u);
+            uint32_t* w = words + 7 * q;
+            w[0] = lo[0];
+            w[1] = lo[1] * (1u << 24) + hi[0];
+            w[2] = __funnelshift_r(lo[1], hi[1], 8);
+            w[3] = lo[2] * (1u << 16) + (hi[1] >> 8);
+            w[4] = __funnelshift_r(lo[2], hi[2], 16);
+            w[5] = lo[3] * (1u << 8) + (hi[2] >> 16);
+            w[6] = __funnelshift_r(lo[3], hi[3], 24);
         }
+#pragma unroll
+        for (int k = 0; k < 7; k++)
+            s_out[warp][lane * 7 + k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
     }
     __syncwarp();
 
