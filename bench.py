@@ -245,7 +245,7 @@ def main():
         value = args.steps * n_s * elem_bytes / t / 1e9
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16" if is_bf16 else "u8",
                 "data": "synthetic", "config": {"workload": args.config, "elements_per_step": n_s},
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                                  "sample": f"first {n_s} elements of {args.config} per step (encode + decode)"},

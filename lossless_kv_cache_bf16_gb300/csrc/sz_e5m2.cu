@@ -95,29 +95,28 @@ __device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t add,
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Encode, first phase: one scan tile per block.  The warp's input bytes stay
-// in shared memory (swizzled rows, one per thread) for the whole tile:
-// packing reads them 16 bytes at a time and the escape records read the
-// exponents of escaped elements back from there, so no thread holds its 128
-// input bytes in registers.  Packed bytes go to a second per-warp buffer
-// (7 pieces per row) and leave with coalesced stores.  The tile's escape
-// count and its first ws_cap records (element order: thread, then element)
-// go to the workspace; finish_kernel (sz_finish.cu) places them.
+// Encode, first phase: one scan tile per block.  Each warp stages its 4 KB
+// of input in shared memory (swizzled rows, one per thread), so that global
+// loads stay coalesced while each thread codes its own 128 contiguous bytes.
+// The packed bytes (7 pieces of 16 bytes per thread) reuse the same buffer
+// once the whole warp has read its rows, and leave with coalesced stores.
+// Before that, the tile's escape count and its first ws_cap records (element
+// order: thread, then element; exponents read back from the rows) go to the
+// workspace; finish_kernel (sz_finish.cu) places the records.
 // ---------------------------------------------------------------------------
 struct EncodeE5Smem {
-    uint4 in[kEncWarps][256];   // 8 swizzled pieces per thread
-    uint4 out[kEncWarps][224];  // 7 pieces per thread
+    uint4 buf[kEncWarps][256];  // input: 8 swizzled pieces per thread; then output: 7 pieces per thread
     uint32_t warp_esc[kEncWarps];
     uint8_t field[256];         // byte -> field; 0x80 marks an escape
 };
 
 template <bool CONTIG>
-__global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kernel(const EncodeParams p) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
     auto& s_field = S.field;
-    auto& s_in = S.in;
-    auto& s_out = S.out;
+    auto& s_in = S.buf;
+    auto& s_out = S.buf;
     auto& s_warp_esc = S.warp_esc;
 
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -169,10 +168,9 @@ __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodePa
     // Pack: four groups (224 bits) make seven 32-bit words; a thread's 16
     // groups make its 28 words = 7 pieces of 16 bytes.  escm[q] holds the
     // escape flags of elements 32q..32q+31 of the thread.
-    uint32_t escm[4];
+    uint32_t escm[4], words[28];
     {
         const uint32_t add = 0x20202020u - (uint32_t)p.cb[0] * 0x01010101u;
-        uint32_t words[28];
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             uint32_t lo[4], hi[4], eh[4];
@@ -193,24 +191,6 @@ __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodePa
             w[5] = lo[3] * (1u << 8) + (hi[2] >> 16);
             w[6] = __funnelshift_r(lo[3], hi[3], 24);
         }
-#pragma unroll
-        for (int k = 0; k < 7; k++)
-            s_out[warp][lane * 7 + k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
-    }
-    __syncwarp();
-
-    const uint64_t out_base = warp_base / 8 * 7;  // packed bytes before this warp
-    if (warp_full) {
-#pragma unroll
-        for (uint32_t i = 0; i < 7; i++) {
-            const uint32_t piece = lane + 32 * i;
-            st_stream_v4(p.out + out_base + 16 * piece, s_out[warp][piece]);
-        }
-    } else if (cnt > 0) {
-        const uint32_t nbytes = 7 * ((cnt + 7) / 8);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(&s_out[warp][lane * 7]);
-        uint8_t* dst = p.out + out_base + lane * 112u;
-        for (uint32_t b = 0; b < nbytes; b++) dst[b] = src[b];
     }
 
     // Rank escapes: thread order, then element order inside the thread.
@@ -231,8 +211,8 @@ __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodePa
         tile_esc += c;
     }
     if (tid == 0) p.ws_count[st] = tile_esc;
-    // Stage this thread's records (those ranked below ws_cap); exponents come
-    // back from the input row in shared memory.
+    // Stage this thread's records (those ranked below ws_cap); the exponents
+    // come from the thread's input row, still in shared memory.
     if (mine && rank < p.ws_cap) {
         const uint8_t* row = reinterpret_cast<const uint8_t*>(&s_in[warp][0]);
         uint8_t* dst = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
@@ -254,6 +234,26 @@ __global__ void __launch_bounds__(kEncThreads) encode_e5m2_kernel(const EncodePa
                 at += 3;
             }
         }
+    }
+
+    // Every row of the warp has been read: the buffer takes the output.
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 7; k++)
+        s_out[warp][lane * 7 + k] = make_uint4(words[4 * k], words[4 * k + 1], words[4 * k + 2], words[4 * k + 3]);
+    __syncwarp();
+    const uint64_t out_base = warp_base / 8 * 7;  // packed bytes before this warp
+    if (warp_full) {
+#pragma unroll
+        for (uint32_t i = 0; i < 7; i++) {
+            const uint32_t piece = lane + 32 * i;
+            st_stream_v4(p.out + out_base + 16 * piece, s_out[warp][piece]);
+        }
+    } else if (cnt > 0) {
+        const uint32_t nbytes = 7 * ((cnt + 7) / 8);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(&s_out[warp][lane * 7]);
+        uint8_t* dst = p.out + out_base + lane * 112u;
+        for (uint32_t b = 0; b < nbytes; b++) dst[b] = src[b];
     }
 }
 
