@@ -32,7 +32,7 @@ uint64_t workspace_bytes(uint64_t n, uint32_t cap = kStageRecs) {
     const uint64_t tiles = scan_tiles_for(n);
     return align16(4 * tiles) + 3ull * cap * tiles;
 }
-// Tiles of the decoder (independent of the encoder's look-back tiles).
+// Tiles of the decoder (independent of the encoder's scan tiles).
 uint64_t decode_tiles_for(sz_dtype dt, uint64_t n) {
     return std::max<uint64_t>(1, cdiv(n, dt == SZ_BF16 ? kBf16Tile : kE5Tile));
 }
@@ -76,7 +76,7 @@ bool codebook_ok(sz_dtype dt, const uint8_t* cb) {
 
 sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                       size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
-                      size_t ws_bytes, uint32_t first_ticket, uint64_t wait_ns, cudaStream_t stream,
+                      size_t ws_bytes, uint32_t skip_first, uint64_t wait_ns, cudaStream_t stream,
                       uint32_t stage_recs = kStageRecs) {
     if (!dtype_ok(dt) || !h_cb || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
     if ((n > 0 && !d_in) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
@@ -102,7 +102,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     std::memcpy(p.cb, h_cb->exp, SZ_CODEBOOK_SIZE);
     std::sort(p.cb, p.cb + SZ_CODEBOOK_SIZE);  // code k = k-th smallest exponent
     p.contig = p.cb[SZ_CODEBOOK_SIZE - 1] - p.cb[0] == SZ_CODEBOOK_SIZE - 1;
-    p.skip_first = first_ticket;
+    p.skip_first = skip_first;
     if (dt == SZ_BF16)
         p.vec = aligned(d_in, 16) && aligned(d_out, 8) && aligned(static_cast<uint8_t*>(d_out) + n, 4);
     else
