@@ -350,9 +350,19 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
 // chunk), then a cursor walks the records through a shared-memory window.
 // Dense input (sign|mantissa bytes and nibbles) arrives through a 4-stage ring
 // of TMA bulk copies.  Per tile: nibble byte -> two exponents via a 256-entry
-// LUT, joined with the sm bytes; the tile's escapes are spread into a bitmap
-// and an exponent table and applied in registers, so every output byte is
+// LUT, joined with the sm bytes; the tile's escapes, gathered into a bitmap
+// and an exponent table, are applied in registers, so every output byte is
 // stored once.
+//
+// One block barrier per tile.  The escapes are gathered one tile ahead into
+// the other of two bitmap/table buffers: while tile t is decoded from buffer
+// t % 2, every thread takes one of the next (up to 256) records and, if it
+// lies below tile t+1's end, checks it and enters it into buffer (t+1) % 2.
+// The tile's closing barrier (__syncthreads_count) both publishes those
+// entries and counts them, which advances the cursor; only a tile with more
+// than 256 escapes takes further counted steps.  A bitmap word is read only
+// by its owning thread, which clears it right after reading.  Chunk headers
+// are read two tiles ahead, also ahead of a closing barrier.
 //
 // Validation: every record is consumed by exactly one tile and checked there
 // (position inside the tile, above the previous one); a chunk's last tile
@@ -371,11 +381,13 @@ struct DecodeSmem {
     alignas(128) uint8_t nib[kDecStages][kBf16Tile / 2];
     uint64_t full[kDecStages];
     uint32_t lut[256];
-    uint32_t bits[kDecThreads];
-    uint8_t patch[kBf16Tile];
+    uint32_t bits[2][kDecThreads];  // escape bitmaps: word tid belongs to thread tid
+    uint8_t patch[2][kBf16Tile];    // escape exponents by position in the tile
     uint8_t win[3 * kWindowRecs];
+    uint32_t hdr[2][2];             // {offset, count} of a chunk, by chunk parity
     uint32_t scratch[8];
     int bad;
+    int abort;
 };
 
 }  // namespace
@@ -397,9 +409,12 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_bf16_kernel(const Decod
     if (tid == 0) {
         for (uint32_t s = 0; s < kDecStages; s++) mbar_init(&S.full[s], 1);
         S.bad = 0;
+        S.abort = 0;
         fence_mbar_init();
     }
     S.lut[tid] = ((uint32_t)cb[tid & 15u] << 7) | ((uint32_t)cb[tid >> 4] << 23);
+    S.bits[0][tid] = 0;
+    S.bits[1][tid] = 0;
     if (tid < kCodes) {  // a codebook is 16 distinct exponents
         bool dup = false;
         for (int k = 0; k < kCodes; k++) dup |= (k != (int)tid) && cb[k] == cb[tid];
@@ -421,7 +436,16 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_bf16_kernel(const Decod
     if (tid == 0)
         for (uint32_t t = t_begin; t < t_end && t < t_begin + kDecStages; t++, issued++) issue((t - t_begin) % kDecStages, t);
 
-    // Record window [win_lo, win_lo + win_len) and the walk state.
+    auto tile_p0 = [&](uint32_t t) { return (t % kTilesPerChunk) * kBf16Tile; };
+    auto tile_len_of = [&](uint32_t t) {
+        const uint64_t b = (uint64_t)t * kBf16Tile;
+        return n - b >= kBf16Tile ? kBf16Tile : (uint32_t)(n - b);
+    };
+    auto last_of_chunk = [&](uint32_t t) { return t % kTilesPerChunk == kTilesPerChunk - 1 || t == T - 1; };
+
+    // Record window [win_lo, win_lo + win_len) and the walk state (the chunk
+    // of the tile whose escapes are gathered next).  All of it is
+    // block-uniform, so every thread reaches the same barriers.
     uint32_t win_lo = 0, win_len = 0;
     uint32_t chunk_o = 0, chunk_end = 0, cursor = 0;
     auto win_pos = [&](uint32_t j) {
@@ -435,160 +459,219 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_bf16_kernel(const Decod
         for (uint32_t b = tid; b < 3 * win_len; b += kDecThreads) S.win[b] = rec[3ull * from + b];
         __syncthreads();
     };
+    // The window must hold the next step's records [cursor, cursor + 256).
+    auto cover = [&]() {
+        const uint32_t nb = min(kDecThreads, chunk_end - cursor);
+        if (nb > 0 && (cursor < win_lo || cursor + nb > win_lo + win_len)) refill(cursor);
+    };
+    // Chunk header {o, m} of chunk c into S.hdr[c & 1], after its checks;
+    // prev_end is o + m of chunk c - 1 (used only at a chunk's first tile).
+    // Thread 0 only.
+    auto store_header = [&](uint32_t c, uint32_t o, uint32_t m, bool at_chunk_start, uint64_t prev_end) {
+        const uint64_t rest = n - (uint64_t)c * kChunk;
+        const uint64_t chunk_len = rest < kChunk ? rest : kChunk;
+        bool bad = m > chunk_len || o > p.n_esc || m > p.n_esc - o;
+        if (at_chunk_start) {
+            bad |= (uint64_t)o != (c == 0 ? 0ull : prev_end);
+            if (c == p.L.num_chunks - 1) bad |= (uint64_t)o + m != p.n_esc;
+        }
+        if (bad) S.bad = 1;
+        S.hdr[c & 1][0] = o;
+        S.hdr[c & 1][1] = bad ? 0u : m;
+        return (uint64_t)o + (bad ? 0u : m);
+    };
+    // A tile at a chunk start takes the chunk's records from its header.
+    auto begin_tile = [&](uint32_t tw) {
+        if (p.L.num_chunks > 0 && tw % kTilesPerChunk == 0) {
+            const uint32_t c = tw / kTilesPerChunk;
+            chunk_o = S.hdr[c & 1][0];
+            chunk_end = chunk_o + S.hdr[c & 1][1];
+            cursor = chunk_o;
+        }
+    };
+    // One gathering step for tile tw into buffer b: thread tid takes record
+    // cursor + tid.  Returns whether that record belongs to the tile (its
+    // position is below the tile's end); such a record is checked, and a good
+    // one is entered.  prev: position of the tile's record before the cursor,
+    // or ~0 at the tile's start.
+    auto gather = [&](uint32_t tw, uint32_t b, uint32_t prev) {
+        const uint32_t r = cursor + tid;
+        if (r >= chunk_end) return false;
+        const uint32_t p0 = tile_p0(tw);
+        const uint32_t pos = win_pos(r);
+        if (pos >= p0 + kBf16Tile) return false;
+        const uint32_t before = tid == 0 ? prev : win_pos(r - 1);
+        if (pos < p0 || pos - p0 >= tile_len_of(tw) || (before != 0xFFFFFFFFu && pos <= before)) {
+            S.bad = 1;
+            return true;
+        }
+        const uint32_t q = pos - p0;
+        S.patch[b][q] = S.win[3 * (r - win_lo) + 2];
+        atomicOr(&S.bits[b][(q >> 10) * 32u + ((q >> 3) & 31u)], 1u << (((q >> 8) & 3u) * 8u + (q & 7u)));
+        return true;
+    };
+    // After a counted step that took k records: further steps while a step
+    // was full, then the chunk-end and hand-off checks of tile tw.
+    auto end_tile = [&](uint32_t tw, uint32_t b, uint32_t k) {
+        cursor += k;
+        while (k == kDecThreads && cursor < chunk_end) {
+            const uint32_t prev = win_pos(cursor - 1);  // still in the window
+            cover();
+            k = (uint32_t)__syncthreads_count(gather(tw, b, prev));
+            cursor += k;
+        }
+        if (last_of_chunk(tw) && cursor != chunk_end && tid == 0) S.bad = 1;
+        if (tw == t_end - 1 && !last_of_chunk(tw) && chunk_end > chunk_o) {
+            // Hand-off: the next block starts its walk where its search says.
+            const uint32_t e = tile_p0(tw) + kBf16Tile;
+            uint32_t a, bb;
+            block_lower_bounds<kDecThreads>(rec, chunk_o, chunk_end - chunk_o, e, e, S.scratch, &a, &bb);
+            if (tid == 0 && a != cursor) S.bad = 1;
+        }
+    };
+
+    // Prologue: the first chunk's header (and the next one's when tile
+    // t_begin + 1 starts a chunk), where the range's records start, and the
+    // escapes of tile t_begin.
+    if (t_begin < t_end) {
+        if (p.L.num_chunks > 0) {
+            const uint32_t c = t_begin / kTilesPerChunk;
+            const bool at_start = t_begin % kTilesPerChunk == 0;
+            if (tid == 0) {
+                const uint8_t* h = p.in + p.L.hdr_off + 8ull * c;
+                const uint64_t prev_end =
+                    (c > 0 && at_start) ? (uint64_t)load_u32_le(h - 8) + load_u32_le(h - 4) : 0ull;
+                const uint64_t end = store_header(c, load_u32_le(h), load_u32_le(h + 4), at_start, prev_end);
+                if (t_begin + 1 < t_end && (t_begin + 1) % kTilesPerChunk == 0)
+                    store_header(c + 1, load_u32_le(h + 8), load_u32_le(h + 12), true, end);
+            }
+            __syncthreads();
+            chunk_o = S.hdr[c & 1][0];
+            chunk_end = chunk_o + S.hdr[c & 1][1];
+            cursor = chunk_o;
+            if (!at_start && chunk_end > chunk_o) {
+                uint32_t a, b;
+                const uint32_t p0 = tile_p0(t_begin);
+                block_lower_bounds<kDecThreads>(rec, chunk_o, chunk_end - chunk_o, p0, p0, S.scratch, &a, &b);
+                cursor = a;
+            }
+        }
+        cover();
+        end_tile(t_begin, 0, (uint32_t)__syncthreads_count(gather(t_begin, 0, 0xFFFFFFFFu)));
+    }
 
     bool aborted = false;
     uint32_t i = 0;
     for (uint32_t t = t_begin; t < t_end; t++, i++) {
-        const uint32_t slot = i % kDecStages;
+        const uint32_t slot = i % kDecStages, buf = i & 1u;
         const uint64_t base = (uint64_t)t * kBf16Tile;
-        const uint32_t chunk = t / kTilesPerChunk;
-        const uint32_t p0 = (t % kTilesPerChunk) * kBf16Tile;
-        const uint32_t tile_len = n - base >= kBf16Tile ? kBf16Tile : (uint32_t)(n - base);
-        const bool first_of_chunk = t % kTilesPerChunk == 0;
-        const bool last_of_chunk = t % kTilesPerChunk == kTilesPerChunk - 1 || t == T - 1;
 
-        // Chunk header: at each chunk start and at the start of the range
-        // (n = 0 has no chunk and no header).
-        if (p.L.num_chunks > 0 && (first_of_chunk || t == t_begin)) {
-            if (tid == 0) {
-                const uint8_t* h = p.in + p.L.hdr_off + 8ull * chunk;
-                const uint32_t o = load_u32_le(h), m = load_u32_le(h + 4);
-                const uint64_t rest = n - (uint64_t)chunk * kChunk;
-                const uint64_t chunk_len = rest < kChunk ? rest : kChunk;
-                bool bad = m > chunk_len || o > p.n_esc || m > p.n_esc - o;
-                if (first_of_chunk) {
-                    if (chunk == 0) {
-                        bad |= o != 0;
-                    } else {
-                        const uint64_t po = load_u32_le(h - 8), pm = load_u32_le(h - 4);
-                        bad |= (uint64_t)o != po + pm;
-                    }
-                    if (chunk == p.L.num_chunks - 1) bad |= (uint64_t)o + m != p.n_esc;
-                }
-                if (bad) S.bad = 1;
-                S.scratch[6] = o;
-                S.scratch[7] = bad ? 0u : m;
-            }
-            __syncthreads();
-            const uint32_t o = S.scratch[6], m = S.scratch[7];
-            chunk_o = o;
-            chunk_end = o + m;
-            cursor = o;
-            if (!first_of_chunk && m > 0) {  // range starts inside the chunk
-                uint32_t a, b;
-                block_lower_bounds<kDecThreads>(rec, o, m, p0, p0, S.scratch, &a, &b);
-                cursor = a;
-            }
-            __syncthreads();
+        // The header of the chunk that starts at tile t + 2: loaded now,
+        // checked and stored before this tile's closing barrier.  Its
+        // predecessor is the chunk of tiles t and t + 1.
+        const bool prefetch = tid == 0 && p.L.num_chunks > 0 && t + 2 < t_end && (t + 2) % kTilesPerChunk == 0;
+        uint32_t next_o = 0, next_m = 0;
+        if (prefetch) {
+            const uint8_t* h = p.in + p.L.hdr_off + 8ull * ((t + 2) / kTilesPerChunk);
+            next_o = load_u32_le(h);
+            next_m = load_u32_le(h + 4);
         }
 
-        S.bits[tid] = 0;  // the previous tile's reads ended at its final barrier
-        // This tile's records: the prefix of the run with position < tile end.
-        uint32_t prev = 0xFFFFFFFFu;  // position of the tile's previous record
-        while (cursor < chunk_end) {
-            const uint32_t nb = min(kDecThreads, chunk_end - cursor);
-            if (cursor < win_lo || cursor + nb > win_lo + win_len) refill(cursor);
-            uint32_t pos = 0xFFFFFFFFu, e = 0;
-            if (tid < nb) {
-                pos = win_pos(cursor + tid);
-                e = S.win[3 * (cursor + tid - win_lo) + 2];
-            }
-            const bool mine = tid < nb && pos < p0 + kBf16Tile;
-            const uint32_t k = (uint32_t)__syncthreads_count(mine);
-            if (tid < k) {
-                const uint32_t before = tid == 0 ? prev : win_pos(cursor + tid - 1);
-                const bool ok = pos >= p0 && pos - p0 < tile_len && (before == 0xFFFFFFFFu || pos > before);
-                if (!ok) {
-                    S.bad = 1;
-                } else {
-                    const uint32_t q = pos - p0;
-                    S.patch[q] = (uint8_t)e;
-                    atomicOr(&S.bits[(q >> 10) * 32u + ((q >> 3) & 31u)], 1u << (((q >> 8) & 3u) * 8u + (q & 7u)));
-                }
-            }
-            if (k > 0) prev = win_pos(cursor + k - 1);
-            cursor += k;
-            if (k < nb) break;  // the barrier after the input wait orders the applies
-            __syncthreads();    // window reads done before the next batch may refill it
-        }
-        if (last_of_chunk && cursor != chunk_end && tid == 0) S.bad = 1;
-        if (t == t_end - 1 && !last_of_chunk && chunk_end > chunk_o) {
-            // Hand-off: the next block starts its walk where its search says.
-            uint32_t a, b;
-            block_lower_bounds<kDecThreads>(rec, chunk_o, chunk_end - chunk_o, p0 + kBf16Tile, p0 + kBf16Tile,
-                                            S.scratch, &a, &b);
-            if (tid == 0 && a != cursor) S.bad = 1;
-        }
-
-        // Dense input of this tile.
+        // Tile t: dense input, with the escapes gathered into buffer buf.
         const bool failed_wait = !mbar_wait(&S.full[slot], (i / kDecStages) & 1u, p.wait_limit_ns);
-        if (!failed_wait) waited = i + 1;
-        if (__syncthreads_or(failed_wait)) {
+        if (!failed_wait) {
+            waited = i + 1;
+            const uint32_t bits = S.bits[buf][tid];
+            S.bits[buf][tid] = 0;  // only this thread reads this word
+            const uint32_t qt = warp * 1024u + lane * 8u;  // the thread's first element in the tile
+            // Group k of the thread: sm bytes (2 words), nibbles (1 word) -> 4 output words.
+            auto decode_group = [&](int k, uint2 smv, uint32_t nibv, uint32_t (&y)[4]) {
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    // Each sm byte twice per 16-bit half: the high copy keeps the
+                    // sign (bit 15), the low copy the mantissa (bits 0..6).
+                    const uint32_t smw = q < 2 ? smv.x : smv.y;
+                    const uint32_t tt = __byte_perm(smw, 0, (q & 1) ? 0x3322 : 0x1100);
+                    y[q] = (tt & 0x807F807Fu) | S.lut[(nibv >> (8 * q)) & 0xFFu];
+                }
+                const uint32_t gb = (bits >> (8 * k)) & 0xFFu;
+                if (gb) {
+                    const uint8_t* pt = S.patch[buf] + qt + k * 256u;
+#pragma unroll
+                    for (int jj = 0; jj < 8; jj++) {
+                        if ((gb >> jj) & 1u) {
+                            const uint32_t sh = 7 + 16 * (jj & 1);
+                            y[jj >> 1] = (y[jj >> 1] & ~(0xFFu << sh)) | ((uint32_t)pt[jj] << sh);
+                        }
+                    }
+                }
+            };
+            if (full_tile(t)) {
+                // Whole tile in the stage slot: no bounds to check.
+                const uint8_t* ssm = S.sm[slot] + qt;
+                const uint8_t* snb = S.nib[slot] + qt / 2;
+                uint8_t* o = p.out + 2 * (base + qt);
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    uint32_t y[4];
+                    decode_group(k, *reinterpret_cast<const uint2*>(ssm + k * 256),
+                                 *reinterpret_cast<const uint32_t*>(snb + k * 128), y);
+                    st_stream_v4(o + k * 512, make_uint4(y[0], y[1], y[2], y[3]));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint64_t i0 = base + qt + k * 256u;
+                    const uint32_t cnt = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
+                    uint2 smv;
+                    uint32_t nibv;
+                    if (p.vec && cnt == 8) {
+                        smv = ld_stream_v2(p.in + i0);
+                        nibv = ld_stream_u32(p.in + p.L.nib_off + i0 / 2);
+                    } else {
+                        uint64_t sv = 0;
+                        uint32_t nb = 0;
+                        for (uint32_t jj = 0; jj < cnt; jj++) sv |= (uint64_t)p.in[i0 + jj] << (8 * jj);
+                        for (uint32_t b = 0; b < (cnt + 1) / 2; b++)
+                            nb |= (uint32_t)p.in[p.L.nib_off + i0 / 2 + b] << (8 * b);
+                        smv = make_uint2((uint32_t)sv, (uint32_t)(sv >> 32));
+                        nibv = nb;
+                    }
+                    uint32_t y[4];
+                    decode_group(k, smv, nibv, y);
+                    if (p.vec && cnt == 8) {
+                        st_stream_v4(p.out + 2 * i0, make_uint4(y[0], y[1], y[2], y[3]));
+                    } else {
+#pragma unroll
+                        for (uint32_t jj = 0; jj < 8; jj++) {
+                            if (jj < cnt) {
+                                const uint32_t v = y[jj >> 1] >> (16 * (jj & 1));
+                                p.out[2 * (i0 + jj)] = (uint8_t)v;
+                                p.out[2 * (i0 + jj) + 1] = (uint8_t)(v >> 8);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+
+        // Tile t + 1: its first gathering step, into the other buffer.
+        bool mine = false;
+        if (t + 1 < t_end) {
+            begin_tile(t + 1);
+            cover();
+            mine = gather(t + 1, buf ^ 1u, 0xFFFFFFFFu);
+        }
+        if (prefetch) store_header((t + 2) / kTilesPerChunk, next_o, next_m, true, chunk_end);
+        if (failed_wait) S.abort = 1;
+        // Closing barrier: stage slot and buffer buf free, buffer buf ^ 1 and
+        // the next header published, the step counted.
+        const uint32_t k = (uint32_t)__syncthreads_count(mine);
+        if (S.abort) {
             aborted = true;
             break;
         }
-        const bool from_smem = full_tile(t);
-        uint2 smv[4];
-        uint32_t nibv[4], cnt[4];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
-            const uint64_t i0 = base + q0;
-            cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
-            if (from_smem) {
-                smv[k] = *reinterpret_cast<const uint2*>(&S.sm[slot][q0]);
-                nibv[k] = *reinterpret_cast<const uint32_t*>(&S.nib[slot][q0 / 2]);
-            } else if (p.vec && cnt[k] == 8) {
-                smv[k] = ld_stream_v2(p.in + i0);
-                nibv[k] = ld_stream_u32(p.in + p.L.nib_off + i0 / 2);
-            } else {
-                uint64_t sv = 0;
-                uint32_t nb = 0;
-                for (uint32_t jj = 0; jj < cnt[k]; jj++) sv |= (uint64_t)p.in[i0 + jj] << (8 * jj);
-                for (uint32_t b = 0; b < (cnt[k] + 1) / 2; b++) nb |= (uint32_t)p.in[p.L.nib_off + i0 / 2 + b] << (8 * b);
-                smv[k] = make_uint2((uint32_t)sv, (uint32_t)(sv >> 32));
-                nibv[k] = nb;
-            }
-        }
-
-        const uint32_t bits = S.bits[tid];
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint64_t i0 = base + warp * 1024u + k * 256u + lane * 8u;
-            uint32_t y[4];
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                // Each sm byte twice per 16-bit half: the high copy keeps the
-                // sign (bit 15), the low copy the mantissa (bits 0..6).
-                const uint32_t smw = q < 2 ? smv[k].x : smv[k].y;
-                const uint32_t tt = __byte_perm(smw, 0, (q & 1) ? 0x3322 : 0x1100);
-                y[q] = (tt & 0x807F807Fu) | S.lut[(nibv[k] >> (8 * q)) & 0xFFu];
-            }
-            const uint32_t gb = (bits >> (8 * k)) & 0xFFu;
-            if (gb) {
-                const uint32_t qbase = warp * 1024u + k * 256u + lane * 8u;
-#pragma unroll
-                for (int jj = 0; jj < 8; jj++) {
-                    if ((gb >> jj) & 1u) {
-                        const uint32_t sh = 7 + 16 * (jj & 1);
-                        y[jj >> 1] = (y[jj >> 1] & ~(0xFFu << sh)) | ((uint32_t)S.patch[qbase + jj] << sh);
-                    }
-                }
-            }
-            if (p.vec && cnt[k] == 8) {
-                st_stream_v4(p.out + 2 * i0, make_uint4(y[0], y[1], y[2], y[3]));
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < 8; jj++) {
-                    if ((uint32_t)jj < cnt[k]) {
-                        const uint32_t v = y[jj >> 1] >> (16 * (jj & 1));
-                        p.out[2 * (i0 + jj)] = (uint8_t)v;
-                        p.out[2 * (i0 + jj) + 1] = (uint8_t)(v >> 8);
-                    }
-                }
-            }
-        }
-        __syncthreads();  // stage slot, bitmap and patch table free again
+        if (t + 1 < t_end) end_tile(t + 1, buf ^ 1u, k);
         if (tid == 0 && t + kDecStages < t_end) issue(slot, t + kDecStages), issued++;
     }
     if (tid == 0 && aborted) {
