@@ -274,17 +274,19 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
             if (!failed_wait) waited = i + 1;
             uint32_t w[4][4], cnt[4], esc[4];
             if (full_sub(u)) {
-                // Whole sub-tile in range, buffers aligned: no bounds logic.
+                // Whole sub-tile in range, buffers aligned: no bounds logic;
+                // lane's group k sits at constant offsets from its group 0.
+                const uint8_t* src = S.in[slot] + 2 * (warp * 1024u + lane * 8u);
+                uint8_t* o_sm = p.out + wbase + lane * 8u;
+                uint8_t* o_nib = p.out + p.L.nib_off + (wbase + lane * 8u) / 2;
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
-                    const uint32_t q0 = warp * 1024u + k * 256u + lane * 8u;
-                    const uint4 v = *reinterpret_cast<const uint4*>(S.in[slot] + 2 * q0);
+                    const uint4 v = *reinterpret_cast<const uint4*>(src + k * 512);
                     w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
                     const GroupOut o = code_group<CONTIG, true>(w[k], 8, lane_add, S.code);
                     esc[k] = o.esc;
-                    const uint64_t i0 = wbase + k * 256u + lane * 8u;
-                    st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
-                    st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
+                    st_stream_v2(o_sm + k * 256, make_uint2(o.sm_lo, o.sm_hi));
+                    st_stream_u32(o_nib + k * 128, o.nib);
                 }
             } else {
                 load_groups_global(p, wbase, lane, w, cnt);
