@@ -33,7 +33,7 @@ constexpr uint32_t kWarps = kBf16Threads / 32;
 //
 // 1. encode_bf16_kernel streams the tensor: a persistent kernel whose blocks
 //    take 32,768-element "scan tiles" (four 8,192-element sub-tiles) in
-//    round-robin order.  Sub-tiles arrive through a 4-stage ring of TMA bulk
+//    round-robin order.  Sub-tiles arrive through a 2-stage ring of TMA bulk
 //    copies; per sub-tile the block splits, codes and packs, stores the dense
 //    streams, and ranks the escapes (ballot/popc warp scans, then a block
 //    scan).  Each scan tile's escape count and its first ws_cap records, in
@@ -48,10 +48,10 @@ constexpr uint32_t kWarps = kBf16Threads / 32;
 namespace {
 
 #ifndef SZ_ENC_STAGES
-#define SZ_ENC_STAGES 3
+#define SZ_ENC_STAGES 2
 #endif
 #ifndef SZ_ENC_MIN_BLOCKS
-#define SZ_ENC_MIN_BLOCKS 3
+#define SZ_ENC_MIN_BLOCKS 4
 #endif
 constexpr uint32_t kEncStages = SZ_ENC_STAGES;   // input ring depth (16 KB sub-tiles)
 constexpr uint32_t kSubsPerScan = 4;
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
 // block's records also form one contiguous run of the stream: one block
 // search finds where the run starts (only when the range starts inside a
 // chunk), then a cursor walks the records through a shared-memory window.
-// Dense input (sign|mantissa bytes and nibbles) arrives through a 4-stage ring
+// Dense input (sign|mantissa bytes and nibbles) arrives through a 2-stage ring
 // of TMA bulk copies.  Per tile: nibble byte -> two exponents via a 256-entry
 // LUT, joined with the sm bytes; the tile's escapes, gathered into a bitmap
 // and an exponent table, are applied in registers, so every output byte is
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr uint32_t kDecStages = 4;
+constexpr uint32_t kDecStages = 2;
 constexpr uint32_t kDecThreads = kBf16Threads;  // 256
 constexpr uint32_t kWindowRecs = 1024;
 
@@ -394,7 +394,7 @@ struct DecodeSmem {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kDecThreads, 3) decode_bf16_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;

@@ -16,15 +16,17 @@
 // because 7 is odd).  The encoder's block of 256 threads owns one
 // 32,768-element scan tile; the decoder's block of 128 threads owns a
 // 16,384-element tile.
+#include <algorithm>
+
 #include "sz_device.cuh"
 #include "sz_params.h"
+#include "sz_pipeline.cuh"
 
 namespace sz {
 
 namespace {
 
 static_assert(kChunk % kE5Tile == 0, "tiles must not straddle chunks");
-constexpr uint32_t kWarps = kE5Threads / 32;           // decode warps
 constexpr uint32_t kWarpElems = 32 * kE5PerThread;     // 4096
 constexpr uint32_t kEncThreads = kScanTile / kE5PerThread;  // 256: one scan tile per encode block
 constexpr uint32_t kEncWarps = kEncThreads / 32;
@@ -112,7 +114,7 @@ struct EncodeE5Smem {
 
 template <bool CONTIG>
 __global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kernel(const EncodeParams p) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
     auto& s_field = S.field;
     auto& s_in = S.buf;
@@ -258,112 +260,358 @@ __global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kerne
 }
 
 // ---------------------------------------------------------------------------
-// Decode: packed groups -> fields -> bytes through a 128-entry LUT, staged in
-// the warp's transpose buffer where the tile's escapes patch the exponent
-// bits, then stored with coalesced 16-byte writes.
+// Decode: a persistent kernel; block b owns the contiguous tile range
+// [bT/G, (b+1)T/G) of 16,384-element tiles (4 per chunk).  The packed bytes
+// of a tile (14,336) arrive through a 2-stage ring of TMA bulk copies (four
+// blocks per SM keep eight tiles in flight per SM); thread
+// t decodes elements 64t..64t+63 of the tile from its 56 bytes (7 8-byte
+// shared loads, conflict-free because the 14-word row stride is an odd
+// multiple of 2 words) into its row of the warp's output buffer (4 pieces of
+// 16 bytes per row, XOR-swizzled so that the row writes are conflict-free).
+// A field becomes a byte by arithmetic when the codebook is 16 consecutive
+// exponents (exponent = cb0 + code), else through a 128-entry table.  The
+// tile's records are walked as in the BF16 decoder (block search only where
+// a range starts inside a chunk, then a cursor through a shared window, one
+// record per thread per step); after the step's counting barrier the holders
+// patch the exponent bits of their bytes in the output rows, and after a
+// second barrier the rows leave with coalesced 16-byte stores.  Validation is
+// the BF16 decoder's, plus exponents below 32 in the codebook and records.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kE5Threads) decode_e5m2_kernel(const DecodeParams p) {
-    __shared__ uint8_t s_dec[128];  // field -> E5M2 byte
-    __shared__ __align__(16) uint4 s_xpose[kWarps][256];
-    __shared__ uint32_t s_cnt[6];
-    __shared__ int s_bad;
+namespace {
 
-    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    const uint32_t tile = blockIdx.x;
-    const uint64_t n = p.L.n;
-    const uint64_t warp_base = (uint64_t)tile * kE5Tile + warp * kWarpElems;
-    const uint64_t thread_base = warp_base + lane * kE5PerThread;
-    const bool warp_full = p.vec && warp_base + kWarpElems <= n;
-    const uint32_t cnt = thread_base >= n ? 0u : (n - thread_base >= kE5PerThread ? kE5PerThread : (uint32_t)(n - thread_base));
-    const uint8_t* cb = p.in + p.L.cb_off;
+constexpr uint32_t kE5DecThreads = 256;
+constexpr uint32_t kE5DecWarps = kE5DecThreads / 32;
+constexpr uint32_t kE5DecTile = kE5Tile;                      // 16384 elements
+constexpr uint32_t kE5DecPer = kE5DecTile / kE5DecThreads;    // 64 elements = 8 groups = 56 bytes
+constexpr uint32_t kE5DecTileBytes = kE5DecTile / 8 * 7;      // 14336
+constexpr uint32_t kE5DecStages = 2;
+constexpr uint32_t kE5TilesPerChunk = kChunk / kE5DecTile;    // 4
+constexpr uint32_t kE5WindowRecs = 1024;
+static_assert(kChunk % kE5DecTile == 0 && kE5DecTileBytes % 16 == 0, "tile layout");
 
-    {
-        const uint32_t f = tid;  // 128 threads, one field value each
-        const uint32_t sm3 = f >> 4;
-        s_dec[f] = (uint8_t)(((sm3 >> 2) << 7) | ((uint32_t)cb[f & 15u] << 2) | (sm3 & 3u));
-    }
-    if (tid == 0) s_bad = 0;
+struct DecodeE5Smem {
+    alignas(128) uint8_t in[kE5DecStages][kE5DecTileBytes];
+    alignas(16) uint4 out[kE5DecWarps][32 * 4];  // per warp: 32 rows of 4 swizzled pieces
+    uint64_t full[kE5DecStages];
+    uint8_t dec[128];                            // field -> byte
+    uint8_t win[3 * kE5WindowRecs];
+    uint32_t hdr[2][2];                          // {offset, count} of a chunk, by chunk parity
+    uint32_t scratch[8];
+    int bad;
+    int abort;
+    int contig;
+};
 
-    // Packed bytes of this thread: 28 words (16 groups).
-    uint32_t pw[28];
-    const uint64_t in_base = warp_base / 8 * 7;
-    if (warp_full) {
-#pragma unroll
-        for (uint32_t i = 0; i < 7; i++) {
-            const uint32_t piece = lane + 32 * i;
-            s_xpose[warp][piece] = ld_stream_v4(p.in + in_base + 16 * piece);
-        }
-        __syncwarp();
-#pragma unroll
-        for (uint32_t i = 0; i < 7; i++) {
-            const uint4 v = s_xpose[warp][lane * 7 + i];
-            pw[4 * i] = v.x, pw[4 * i + 1] = v.y, pw[4 * i + 2] = v.z, pw[4 * i + 3] = v.w;
-        }
+// 16-byte slot of piece s (0..3) of row r in a 4-piece swizzled row set.
+__device__ __forceinline__ uint32_t swz4(uint32_t r, uint32_t s) { return r * 4u + (s ^ ((r >> 1) & 3u)); }
+
+// 28 bits holding four 7-bit fields -> the fields one per byte (inverse of
+// the encoder's compaction): each step moves the upper half of every lane up.
+__device__ __forceinline__ uint32_t spread28(uint32_t y) {
+    const uint32_t x = y + (y & 0x0FFFC000u) * 3u;  // 16-bit lanes: f0 | f1 << 7
+    return x + (x & 0x3F803F80u);                   // bytes: f0, f1, f2, f3
+}
+
+// Four fields (one per byte) -> four E5M2 bytes, codebook cb0..cb0+15:
+// sign (field bit 6) to bit 7, exponent cb0 + code to bits 2..6, mantissa
+// (field bits 4..5) to bits 0..1; the parts are disjoint, so they add.
+__device__ __forceinline__ uint32_t bytes4_contig(uint32_t f, uint32_t cb0x4) {
+    return (f & 0x40404040u) * 2u + ((f & 0x0F0F0F0Fu) + cb0x4) * 4u + ((f >> 4) & 0x03030303u);
+}
+
+// One group (56 bits: lo = bits 0..31, hi = bits 32..55) -> 8 bytes.
+template <bool CONTIG>
+__device__ __forceinline__ void decode_group(uint32_t lo, uint32_t hi, uint32_t cb0x4, const uint8_t* dec,
+                                             uint32_t& y0, uint32_t& y1) {
+    const uint32_t a = lo & 0x0FFFFFFFu, b = __funnelshift_r(lo, hi, 28) & 0x0FFFFFFFu;
+    if (CONTIG) {
+        y0 = bytes4_contig(spread28(a), cb0x4);
+        y1 = bytes4_contig(spread28(b), cb0x4);
     } else {
-        const uint32_t nbytes = 7 * ((cnt + 7) / 8);
-        const uint8_t* src = p.in + in_base + lane * 112u;
+        y0 = 0;
+        y1 = 0;
 #pragma unroll
-        for (int k = 0; k < 28; k++) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int t = 0; t < 4; t++)
-                if ((uint32_t)(4 * k + t) < nbytes) v |= (uint32_t)src[4 * k + t] << (8 * t);
-            pw[k] = v;
+        for (int j = 0; j < 4; j++) {
+            y0 |= (uint32_t)dec[(a >> (7 * j)) & 0x7Fu] << (8 * j);
+            y1 |= (uint32_t)dec[(b >> (7 * j)) & 0x7Fu] << (8 * j);
         }
     }
-    __syncthreads();  // s_dec, s_bad ready; transpose buffer free again
+}
 
+// Byte j (0..6) of a group that starts at byte 7g of the 14 words pw.
+template <int G>
+__device__ __forceinline__ void group_words(const uint32_t (&pw)[14], uint32_t& lo, uint32_t& hi) {
+    constexpr int b0 = 7 * G, w0 = b0 / 4, sh = 8 * (b0 % 4);
+    const uint32_t x0 = pw[w0], x1 = w0 + 1 < 14 ? pw[w0 + 1] : 0u, x2 = w0 + 2 < 14 ? pw[w0 + 2] : 0u;
+    lo = sh ? __funnelshift_r(x0, x1, sh) : x0;
+    hi = (sh ? __funnelshift_r(x1, x2, sh) : x1) & 0x00FFFFFFu;
+}
+
+}  // namespace
+
+template <bool CONTIG>
+__device__ __forceinline__ void decode_rows(const uint32_t (&pw)[14], uint32_t cb0x4, const uint8_t* dec, uint4* rows,
+                                            uint32_t lane) {
+    uint32_t y[16];
+#define SZ_E5_GROUP(G)                                                  \
+    {                                                                   \
+        uint32_t lo, hi;                                                \
+        group_words<G>(pw, lo, hi);                                     \
+        decode_group<CONTIG>(lo, hi, cb0x4, dec, y[2 * G], y[2 * G + 1]); \
+    }
+    SZ_E5_GROUP(0) SZ_E5_GROUP(1) SZ_E5_GROUP(2) SZ_E5_GROUP(3)
+    SZ_E5_GROUP(4) SZ_E5_GROUP(5) SZ_E5_GROUP(6) SZ_E5_GROUP(7)
+#undef SZ_E5_GROUP
+#pragma unroll
+    for (uint32_t s = 0; s < 4; s++) rows[swz4(lane, s)] = make_uint4(y[4 * s], y[4 * s + 1], y[4 * s + 2], y[4 * s + 3]);
+}
+
+__global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const DecodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    DecodeE5Smem& S = *reinterpret_cast<DecodeE5Smem*>(smem_raw);
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint64_t n = p.L.n;
+    const uint32_t T = p.num_tiles, G = gridDim.x;
+    const uint32_t t_begin = (uint32_t)((uint64_t)blockIdx.x * T / G);
+    const uint32_t t_end = (uint32_t)((uint64_t)(blockIdx.x + 1) * T / G);
+    const uint8_t* cb = p.in + p.L.cb_off;
+    const uint8_t* rec = p.in + p.L.rec_off;
+    const bool tma = p.vec && (reinterpret_cast<uintptr_t>(p.in) % 16 == 0);
+
+    if (tid == 0) {
+        for (uint32_t s = 0; s < kE5DecStages; s++) mbar_init(&S.full[s], 1);
+        S.bad = 0;
+        S.abort = 0;
+        S.contig = 1;
+        fence_mbar_init();
+    }
+    if (tid < 128) {
+        const uint32_t sm3 = tid >> 4;
+        S.dec[tid] = (uint8_t)(((sm3 >> 2) << 7) | ((uint32_t)cb[tid & 15u] << 2) | (sm3 & 3u));
+    }
+    __syncthreads();
     if (tid < kCodes) {  // 16 distinct exponents that fit in 5 bits
         bool bad = cb[tid] >= 32;
         for (int k = 0; k < kCodes; k++) bad |= (k != (int)tid) && cb[k] == cb[tid];
-        if (bad) s_bad = 1;
+        if (bad) S.bad = 1;
+        if ((uint32_t)cb[tid] != (uint32_t)cb[0] + tid) S.contig = 0;
     }
-
-    // Dense pass into the transpose buffer (this thread's row, swizzled).
-#pragma unroll
-    for (int s = 0; s < 8; s++) {
-        uint32_t y[4];
-#pragma unroll
-        for (int w = 0; w < 4; w++) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int t = 0; t < 4; t++) {
-                const int j = 16 * s + 4 * w + t;  // element inside the thread
-                const int g = j / 8, bit = 7 * (j % 8);
-                // 56-bit group value starts at byte 7g of the thread's packed bytes.
-                const int byte0 = 7 * g + bit / 8, sh = bit % 8;
-                const uint32_t lo = (pw[byte0 / 4] >> (8 * (byte0 % 4))) & 0xFFu;
-                const int byte1 = byte0 + 1;
-                const uint32_t hi = byte1 < 7 * (g + 1) ? (pw[byte1 / 4] >> (8 * (byte1 % 4))) & 0xFFu : 0u;
-                const uint32_t f = ((lo | (hi << 8)) >> sh) & 0x7Fu;
-                v |= (uint32_t)s_dec[f] << (8 * t);
-            }
-            y[w] = v;
-        }
-        s_xpose[warp][swz8(lane, s)] = make_uint4(y[0], y[1], y[2], y[3]);
-    }
-
-    // Escapes: patch the exponent bits of the staged bytes.
-    uint8_t* staged = reinterpret_cast<uint8_t*>(&s_xpose[0][0]);
-    for_each_tile_escape<kE5Threads, kE5Tile, true>(p, tile, s_cnt, &s_bad, [&](uint32_t q, uint32_t e) {
-        const uint32_t t = q >> 7, b = q & 127u;  // owning thread of the tile, byte inside its row
-        const uint32_t w = t >> 5, l = t & 31u;
-        uint8_t* at = staged + (w * 256u + swz8(l, b >> 4)) * 16u + (b & 15u);
-        *at = (uint8_t)((*at & 0x83u) | (e << 2));
-    });
     __syncthreads();
+    const bool contig = S.contig != 0;
+    const uint32_t cb0x4 = (uint32_t)cb[0] * 0x01010101u;
 
-    if (warp_full) {
-#pragma unroll
-        for (uint32_t i = 0; i < 8; i++) {
-            const uint32_t piece = lane + 32 * i;
-            st_stream_v4(p.out + warp_base + 16 * piece, s_xpose[warp][swz8(piece >> 3, piece & 7u)]);
+    auto full_tile = [&](uint32_t t) { return tma && (uint64_t)(t + 1) * kE5DecTile <= n; };
+    auto issue = [&](uint32_t slot, uint32_t t) {  // thread 0 only
+        if (full_tile(t)) {
+            mbar_arrive_expect_tx(&S.full[slot], kE5DecTileBytes);
+            bulk_g2s(S.in[slot], p.in + (uint64_t)t * kE5DecTileBytes, kE5DecTileBytes, &S.full[slot]);
+        } else {
+            mbar_arrive(&S.full[slot]);
         }
-    } else {
-        for (uint32_t b = 0; b < cnt; b++)
-            p.out[thread_base + b] = staged[(warp * 256u + swz8(lane, b >> 4)) * 16u + (b & 15u)];
+    };
+    uint32_t issued = 0, waited = 0;
+    if (tid == 0)
+        for (uint32_t t = t_begin; t < t_end && t < t_begin + kE5DecStages; t++, issued++)
+            issue((t - t_begin) % kE5DecStages, t);
+
+    auto tile_p0 = [&](uint32_t t) { return (t % kE5TilesPerChunk) * kE5DecTile; };
+    auto tile_len_of = [&](uint32_t t) {
+        const uint64_t b = (uint64_t)t * kE5DecTile;
+        return n - b >= kE5DecTile ? kE5DecTile : (uint32_t)(n - b);
+    };
+    auto last_of_chunk = [&](uint32_t t) { return t % kE5TilesPerChunk == kE5TilesPerChunk - 1 || t == T - 1; };
+
+    // Record window and walk state (block-uniform).
+    uint32_t win_lo = 0, win_len = 0;
+    uint32_t chunk_o = 0, chunk_end = 0, cursor = 0;
+    auto win_pos = [&](uint32_t j) {
+        const uint8_t* r = S.win + 3 * (j - win_lo);
+        return (uint32_t)r[0] | ((uint32_t)r[1] << 8);
+    };
+    auto refill = [&](uint32_t from) {  // block-wide; ends with a barrier
+        __syncthreads();
+        win_lo = from;
+        win_len = min(kE5WindowRecs, p.n_esc - from);
+        for (uint32_t b = tid; b < 3 * win_len; b += kE5DecThreads) S.win[b] = rec[3ull * from + b];
+        __syncthreads();
+    };
+    auto cover = [&]() {
+        const uint32_t nb = min(kE5DecThreads, chunk_end - cursor);
+        if (nb > 0 && (cursor < win_lo || cursor + nb > win_lo + win_len)) refill(cursor);
+    };
+    // Chunk header checks and store (thread 0), as in the BF16 decoder.
+    auto store_header = [&](uint32_t c, uint32_t o, uint32_t m, bool at_chunk_start, uint64_t prev_end) {
+        const uint64_t rest = n - (uint64_t)c * kChunk;
+        const uint64_t chunk_len = rest < kChunk ? rest : kChunk;
+        bool bad = m > chunk_len || o > p.n_esc || m > p.n_esc - o;
+        if (at_chunk_start) {
+            bad |= (uint64_t)o != (c == 0 ? 0ull : prev_end);
+            if (c == p.L.num_chunks - 1) bad |= (uint64_t)o + m != p.n_esc;
+        }
+        if (bad) S.bad = 1;
+        S.hdr[c & 1][0] = o;
+        S.hdr[c & 1][1] = bad ? 0u : m;
+    };
+    // One step: thread tid takes record cursor + tid; returns whether it lies
+    // below the tile's end.  A good one leaves its byte position q in the tile
+    // and its exponent e for the patch.
+    auto gather = [&](uint32_t tw, uint32_t prev, bool& ok, uint32_t& q, uint32_t& e) {
+        ok = false;
+        const uint32_t r = cursor + tid;
+        if (r >= chunk_end) return false;
+        const uint32_t p0 = tile_p0(tw);
+        const uint32_t pos = win_pos(r);
+        if (pos >= p0 + kE5DecTile) return false;
+        const uint32_t before = tid == 0 ? prev : win_pos(r - 1);
+        e = S.win[3 * (r - win_lo) + 2];
+        if (pos < p0 || pos - p0 >= tile_len_of(tw) || (before != 0xFFFFFFFFu && pos <= before) || e >= 32) {
+            S.bad = 1;
+            return true;
+        }
+        ok = true;
+        q = pos - p0;
+        return true;
+    };
+    // Byte q of the tile lives in row q / 64 (warp q / 2048), byte q % 64.
+    auto patch = [&](uint32_t q, uint32_t e) {
+        const uint32_t t = q >> 6, b = q & 63u;
+        uint8_t* at = reinterpret_cast<uint8_t*>(&S.out[t >> 5][swz4(t & 31u, b >> 4)]) + (b & 15u);
+        *at = (uint8_t)((*at & 0x83u) | (e << 2));
+    };
+
+    // Prologue: the first chunk's header and where the range's records start.
+    if (p.L.num_chunks > 0) {
+        const uint32_t c = t_begin / kE5TilesPerChunk;
+        const bool at_start = t_begin % kE5TilesPerChunk == 0;
+        if (tid == 0) {
+            const uint8_t* h = p.in + p.L.hdr_off + 8ull * c;
+            const uint64_t prev_end = (c > 0 && at_start) ? (uint64_t)load_u32_le(h - 8) + load_u32_le(h - 4) : 0ull;
+            store_header(c, load_u32_le(h), load_u32_le(h + 4), at_start, prev_end);
+        }
+        __syncthreads();
+        chunk_o = S.hdr[c & 1][0];
+        chunk_end = chunk_o + S.hdr[c & 1][1];
+        cursor = chunk_o;
+        if (!at_start && chunk_end > chunk_o) {
+            uint32_t a, b;
+            const uint32_t p0 = tile_p0(t_begin);
+            block_lower_bounds<kE5DecThreads>(rec, chunk_o, chunk_end - chunk_o, p0, p0, S.scratch, &a, &b);
+            cursor = a;
+        }
     }
-    if (tid == 0 && s_bad && p.status) atomicMax(p.status, kStatusCorrupt);
+
+    uint4* const rows = S.out[warp];
+    bool aborted = false;
+    uint32_t i = 0;
+    for (uint32_t t = t_begin; t < t_end; t++, i++) {
+        const uint32_t slot = i % kE5DecStages;
+        const uint64_t base = (uint64_t)t * kE5DecTile;
+        const uint32_t chunk = t / kE5TilesPerChunk;
+        if (p.L.num_chunks > 0 && t % kE5TilesPerChunk == 0 && t != t_begin) {
+            chunk_o = S.hdr[chunk & 1][0];
+            chunk_end = chunk_o + S.hdr[chunk & 1][1];
+            cursor = chunk_o;
+        }
+        // The next chunk's header, when tile t + 1 starts one: loaded now,
+        // stored before this tile's second barrier.
+        const bool prefetch = tid == 0 && p.L.num_chunks > 0 && t + 1 < t_end && (t + 1) % kE5TilesPerChunk == 0;
+        uint32_t next_o = 0, next_m = 0;
+        if (prefetch) {
+            const uint8_t* h = p.in + p.L.hdr_off + 8ull * (chunk + 1);
+            next_o = load_u32_le(h);
+            next_m = load_u32_le(h + 4);
+        }
+
+        // Dense pass into this thread's output row.
+        const bool failed_wait = !mbar_wait(&S.full[slot], (i / kE5DecStages) & 1u, p.wait_limit_ns);
+        const uint64_t thread_base = base + (uint64_t)tid * kE5DecPer;
+        const uint32_t cnt =
+            thread_base >= n ? 0u : (n - thread_base >= kE5DecPer ? kE5DecPer : (uint32_t)(n - thread_base));
+        if (!failed_wait) {
+            waited = i + 1;
+            uint32_t pw[14];
+            if (full_tile(t)) {
+                const uint2* src = reinterpret_cast<const uint2*>(S.in[slot] + 56u * tid);
+#pragma unroll
+                for (int k = 0; k < 7; k++) {
+                    const uint2 v = src[k];
+                    pw[2 * k] = v.x;
+                    pw[2 * k + 1] = v.y;
+                }
+            } else {
+                const uint32_t nbytes = 7 * ((cnt + 7) / 8);
+                const uint8_t* src = p.in + thread_base / 8 * 7;
+#pragma unroll
+                for (int k = 0; k < 14; k++) {
+                    uint32_t v = 0;
+#pragma unroll
+                    for (int b = 0; b < 4; b++)
+                        if ((uint32_t)(4 * k + b) < nbytes) v |= (uint32_t)src[4 * k + b] << (8 * b);
+                    pw[k] = v;
+                }
+            }
+            if (contig)
+                decode_rows<true>(pw, cb0x4, S.dec, rows, lane);
+            else
+                decode_rows<false>(pw, cb0x4, S.dec, rows, lane);
+        }
+
+        // This tile's records: one per thread, counted at the first barrier
+        // (which also completes the rows); the holders then patch them.
+        bool ok = false;
+        uint32_t q = 0, e = 0;
+        cover();
+        const bool mine = gather(t, 0xFFFFFFFFu, ok, q, e);
+        if (failed_wait) S.abort = 1;
+        uint32_t k = (uint32_t)__syncthreads_count(mine);
+        if (S.abort) {
+            aborted = true;
+            break;
+        }
+        // The dense pass has consumed the ring slot: refill it now.
+        if (tid == 0 && t + kE5DecStages < t_end) issue(slot, t + kE5DecStages), issued++;
+        if (ok) patch(q, e);
+        cursor += k;
+        while (k == kE5DecThreads && cursor < chunk_end) {  // a full step: maybe more records
+            const uint32_t prev = win_pos(cursor - 1);
+            cover();
+            const bool more = gather(t, prev, ok, q, e);
+            k = (uint32_t)__syncthreads_count(more);
+            if (ok) patch(q, e);
+            cursor += k;
+        }
+        if (last_of_chunk(t) && cursor != chunk_end && tid == 0) S.bad = 1;
+        if (t == t_end - 1 && !last_of_chunk(t) && chunk_end > chunk_o) {
+            const uint32_t end = tile_p0(t) + kE5DecTile;
+            uint32_t a, b;
+            block_lower_bounds<kE5DecThreads>(rec, chunk_o, chunk_end - chunk_o, end, end, S.scratch, &a, &b);
+            if (tid == 0 && a != cursor) S.bad = 1;
+        }
+        if (prefetch) store_header(chunk + 1, next_o, next_m, true, chunk_end);
+        __syncthreads();  // patches done
+
+        // The warp's rows -> global memory.
+        const uint64_t wbase = base + warp * (32u * kE5DecPer);
+        if (p.vec && wbase + 32u * kE5DecPer <= n) {
+            uint8_t* o = p.out + wbase;
+#pragma unroll
+            for (uint32_t r = 0; r < 4; r++) {
+                const uint32_t piece = lane + 32 * r;
+                st_stream_v4(o + 16 * piece, rows[swz4(piece >> 2, piece & 3u)]);
+            }
+        } else {
+            const uint8_t* row = reinterpret_cast<const uint8_t*>(rows);
+            for (uint32_t b = 0; b < cnt; b++) p.out[thread_base + b] = row[swz4(lane, b >> 4) * 16u + (b & 15u)];
+        }
+        __syncwarp();  // the rows are rewritten by the next tile
+    }
+    if (tid == 0 && aborted) {
+        for (uint32_t k = waited; k < issued; k++)
+            mbar_wait(&S.full[k % kE5DecStages], (k / kE5DecStages) & 1u, p.wait_limit_ns);
+        if (p.status) atomicMax(p.status, kStatusTimeout);
+    }
+    __syncthreads();
+    if (tid == 0 && S.bad && p.status) atomicMax(p.status, kStatusCorrupt);
 }
 
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
@@ -377,7 +625,16 @@ cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {
-    decode_e5m2_kernel<<<p.num_tiles, kE5Threads, 0, s>>>(p);
+    const size_t smem = sizeof(DecodeE5Smem);
+    cudaError_t err = cudaFuncSetAttribute(decode_e5m2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (err == cudaSuccess) err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_e5m2_kernel, kE5DecThreads, smem);
+    if (err != cudaSuccess) return err;
+    const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
+    decode_e5m2_kernel<<<grid, kE5DecThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
