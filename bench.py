@@ -164,6 +164,20 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def e2e_segments(n: int, parts: int):
+    """[start, end) element ranges of at most `parts` segments of whole
+    65,536-element chunks (the last one may be partial) covering n elements."""
+    chunk = 65536
+    chunks = max(1, -(-n // chunk))
+    per = -(-chunks // max(1, parts))
+    out = []
+    for c0 in range(0, chunks, per):
+        a0, a1 = c0 * chunk, min(n, (c0 + per) * chunk)
+        if a1 > a0:
+            out.append((a0, a1))
+    return out or [(0, 0)]
+
+
 # ---- the reference arm: the CPU oracle ------------------------------------------
 
 def time_oracle(orc, dt_oracle, cb, xb, n):
@@ -188,6 +202,8 @@ def main():
                     choices=["llama8b_prefill", "long_ctx_gqa", "fp8_e5m2", "escape_sweep", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-segments", type=int, default=8,
+                    help="whole-chunk segments the end-to-end leg pipelines across three streams")
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first L layers of a layered workload (smaller captures for ncu)")
     ap.add_argument("--profile", action="store_true",
@@ -340,32 +356,74 @@ def main():
     e2e = None
     memcpy_gbs = None
     if not args.profile and args.e2e_steps > 0:
-        # End to end through the C ABI with host buffers: pinned H2D of the input,
-        # encode, decode, D2H of the decoded tensor, every step.
+        # End to end through the C ABI with host buffers, every step: pinned H2D
+        # of the input, encode, decode, D2H of the decoded tensor.  The tensor
+        # is cut into segments of whole 65,536-element chunks, each encoded as
+        # its own self-contained stream (the layout of an independent shard),
+        # so that the H2D copy of one segment, the codec on the previous one
+        # and the D2H copy of the one before overlap on three streams.
         xh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
         xh.copy_(x.view(torch.uint8).reshape(-1))
         yh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
-        xv = x.view(torch.uint8).reshape(-1)
-        yv = y.view(torch.uint8).reshape(-1)
+        segs = e2e_segments(n, args.e2e_segments)
+        xf, yf = x.reshape(-1), y.reshape(-1)
+        seg_cap = [S.sz_encoded_size(dt, a1 - a0, a1 - a0) for a0, a1 in segs]
+        seg_at = [sum((c + 255) // 256 * 256 for c in seg_cap[:i]) for i in range(len(segs))]
+        seg_buf = torch.empty(seg_at[-1] + seg_cap[-1], dtype=torch.uint8, device=dev)
+        seg_out = [seg_buf[o:o + c] for o, c in zip(seg_at, seg_cap)]
+        seg_size = []  # per-segment stream sizes (fixed for this input)
+        for (a0, a1), o in zip(segs, seg_out):
+            S.sz_encode(dt, cb, xf[a0:a1], o, ob, est, ws)
+            torch.cuda.synchronize()
+            seg_size.append(int(ob.item()))
+        s_in, s_cod, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()
+        in_done = [ev() for _ in segs]     # H2D of segment i landed
+        enc_done = [ev() for _ in segs]    # encode of segment i has read its input
+        dec_done = [ev() for _ in segs]    # decode of segment i wrote its output
+        out_done = [ev() for _ in segs]    # D2H of segment i has read its output
+        started = [False]
+
+        def e2e_step():
+            for i, ((a0, a1), o, sz) in enumerate(zip(segs, seg_out, seg_size)):
+                b0, b1 = a0 * elem_bytes, a1 * elem_bytes
+                with torch.cuda.stream(s_in):
+                    if started[0]:
+                        s_in.wait_event(enc_done[i])  # the previous step's encode has read it
+                    x.view(torch.uint8).reshape(-1)[b0:b1].copy_(xh[b0:b1], non_blocking=True)
+                    in_done[i].record(s_in)
+                with torch.cuda.stream(s_cod):
+                    s_cod.wait_event(in_done[i])
+                    if started[0]:
+                        s_cod.wait_event(out_done[i])  # the previous step's D2H has read it
+                    S.sz_encode(dt, cb, xf[a0:a1], o, ob, est, ws)
+                    enc_done[i].record(s_cod)
+                    S.sz_decode(dt, o, sz, a1 - a0, yf[a0:a1], dst)
+                    dec_done[i].record(s_cod)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(dec_done[i])
+                    yh[b0:b1].copy_(y.view(torch.uint8).reshape(-1)[b0:b1], non_blocking=True)
+                    out_done[i].record(s_out)
+            started[0] = True
+
         for _ in range(2):
-            xv.copy_(xh, non_blocking=True)
-            encode()
-            decode(size)
-            yh.copy_(yv, non_blocking=True)
+            e2e_step()
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e_a.record(stream)
+        for s_ in (s_in, s_cod, s_out):
+            s_.wait_event(e_a)
         for _ in range(args.e2e_steps):
-            xv.copy_(xh, non_blocking=True)
-            encode()
-            decode(size)
-            yh.copy_(yv, non_blocking=True)
+            e2e_step()
+        for s_ in (s_in, s_cod, s_out):
+            stream.wait_stream(s_)
         e_b.record(stream)
         torch.cuda.synchronize()
         e2e_t = e_a.elapsed_time(e_b) / 1e3
         e2e_value, _ = aggregate(args.e2e_steps * n_bytes, gather_elapsed(dist, e2e_t, dev))
+        assert int(est.item()) == 0 and int(dst.item()) == 0, "codec reported an error"
         assert torch.equal(yh, xh), "end-to-end round trip is not bit-exact"
 
         # Device-to-device copy bandwidth in the same run (bytes = read + write).
@@ -383,7 +441,8 @@ def main():
         del a, b
 
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": n_bytes, "d2h_bytes_per_step": n_bytes,
-               "steps": args.e2e_steps}
+               "steps": args.e2e_steps, "segments": len(segs), "streams": 3,
+               "stream_bytes_per_step": sum(seg_size)}
     te, td = statistics.mean(t_enc), statistics.mean(t_dec)
     enc_gbs, dec_gbs = n_bytes / te / 1e9, n_bytes / td / 1e9
     peak, peak_src = measured_peaks()
