@@ -353,6 +353,40 @@ def main():
 
     value, t_max = aggregate(K * n_bytes, gather_elapsed(dist, elapsed, dev))
 
+    online = None
+    if not args.profile:
+        # Online (per-tensor) calibration on the device, the alternative to the
+        # offline codebook that the pages' calibration ablation weighs: the
+        # histogram of every s-th group of 8 elements plus the top-16, then an
+        # encode that reads that codebook from device memory.
+        dcb = torch.empty(16, dtype=torch.uint8, device=dev)
+        dhist = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device=dev)
+        online = {}
+        for stride in (1, 16):
+            for _ in range(3):
+                S.sz_calibrate_device(dt, x, dhist, dcb, sample_stride=stride)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for _ in range(20):
+                S.sz_calibrate_device(dt, x, dhist, dcb, sample_stride=stride)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            online[f"calibrate_us_stride{stride}"] = c0.elapsed_time(c1) / 20 * 1e3
+        for _ in range(3):
+            S.sz_encode_dcb(dt, dcb, x, out, ob, est, ws)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(20):
+            S.sz_encode_dcb(dt, dcb, x, out, ob, est, ws)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        assert int(est.item()) == 0
+        online_size = int(ob.item())
+        online.update({"sample": "every 16th group of 8 elements of the tensor itself",
+                       "encode_dcb_gbs": n_bytes / (c0.elapsed_time(c1) / 20 / 1e3) / 1e9,
+                       "codebook": dcb.cpu().tolist(), "offline_codebook": [int(v) for v in cb],
+                       "ratio": n_bytes / online_size, "ratio_offline": n_bytes / size})
+
     e2e = None
     memcpy_gbs = None
     if not args.profile and args.e2e_steps > 0:
@@ -489,7 +523,7 @@ def main():
         "link_model": link_model(n_bytes, size, te, td),
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
                           "hardware": "not named on the pages"},
-        "roofline": roofline, "cpu_baseline": cpu,
+        "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online,
         "e2e": e2e,
         "gpu_launches": sum(len(OPS[op][0]) for op in ops) * K, "clocks": clocks,
     }

@@ -117,6 +117,25 @@ sz_status sz_histogram(sz_dtype dt, const void* d_sample, size_t n,
 sz_status sz_codebook_from_histogram(sz_dtype dt, const unsigned long long* h_hist,
                                      sz_codebook* h_cb);
 
+/* Top-16 selection on the device: the same rule as
+ * sz_codebook_from_histogram, from sz_histogram_bins(dt) counts in device
+ * memory (d_hist, 8-byte aligned) to 16 ascending exponents in device memory
+ * (d_cb, 16 bytes, 16-byte aligned).  One block; asynchronous, no host
+ * synchronisation.  The pages calibrate offline; this is the device
+ * counterpart for per-tensor (online) calibration, whose cost the pages'
+ * calibration ablation ([RES] "Calibracion") weighs. */
+sz_status sz_codebook_from_histogram_device(sz_dtype dt, const unsigned long long* d_hist,
+                                            uint8_t* d_cb, cudaStream_t stream);
+
+/* Online calibration, all on the device: the exponent histogram of every
+ * sample_stride-th group of 8 elements of d_x (groups g with g % stride == 0,
+ * i.e. elements [8g, 8g + 8) of those groups; stride 1 = every element), then
+ * sz_codebook_from_histogram_device into d_cb.  d_hist as for sz_histogram.
+ * Asynchronous, no host synchronisation: an sz_encode_dcb can follow on the
+ * same stream (and both can be captured in a CUDA graph). */
+sz_status sz_calibrate_device(sz_dtype dt, const void* d_x, size_t n, uint32_t sample_stride,
+                              unsigned long long* d_hist, uint8_t* d_cb, cudaStream_t stream);
+
 /* Offline calibration = sz_histogram, a device-to-host copy of the counts,
  * and sz_codebook_from_histogram.  Synchronises `stream` (the only call that
  * does).  d_hist is the same caller-owned scratch as for sz_histogram. */
@@ -134,11 +153,23 @@ sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n,
  *  d_out_bytes   device u64, receives the stream size (also on
  *                SZ_ERR_CAPACITY, where it is the size that was needed)
  *  d_status      device int or NULL: SZ_OK, SZ_ERR_CAPACITY or SZ_ERR_TIMEOUT
+ *                (sz_encode_dcb also SZ_ERR_INVALID_ARG for a bad codebook)
  *  d_ws          device workspace of ws_bytes >= sz_workspace_size(dt, n)
  * Asynchronous; the stream is byte-for-byte the layout above. */
 sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n,
                     void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
                     int* d_status, void* d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/* sz_encode with the codebook in device memory (d_cb: 16 bytes, 16-byte
+ * aligned, read on the device when the kernels run), e.g. as written by
+ * sz_calibrate_device.  The stream is the one sz_encode gives for the same
+ * 16 exponents.  The codebook must be 16 strictly ascending exponents (below
+ * 32 for E5M2); otherwise *d_status becomes SZ_ERR_INVALID_ARG and the stream
+ * is meaningless.  The pages calibrate offline; this entry point serves
+ * per-tensor calibration without a host round trip. */
+sz_status sz_encode_dcb(sz_dtype dt, const uint8_t* d_cb, const void* d_in, size_t n,
+                        void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
+                        int* d_status, void* d_ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Decode ([MET] "Estrategia de Decodificacion"): dense LUT pass, then the
  * escape overwrite.

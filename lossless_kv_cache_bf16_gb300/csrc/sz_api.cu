@@ -74,15 +74,18 @@ bool codebook_ok(sz_dtype dt, const uint8_t* cb) {
     return true;
 }
 
+// Exactly one of h_cb (host codebook, checked here) and d_cb (device
+// codebook, 16-byte aligned, checked by the kernels) is set.
 sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                       size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
                       size_t ws_bytes, uint32_t skip_first, uint64_t wait_ns, cudaStream_t stream,
-                      uint32_t stage_recs = kStageRecs) {
-    if (!dtype_ok(dt) || !h_cb || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
+                      uint32_t stage_recs = kStageRecs, const uint8_t* d_cb = nullptr) {
+    if (!dtype_ok(dt) || (!h_cb == !d_cb) || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
     if ((n > 0 && !d_in) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
     if (dt == SZ_BF16 && !aligned(d_in, 2)) return SZ_ERR_INVALID_ARG;
     if (!aligned(d_ws, 16) || !aligned(d_out_bytes, 8) || (d_status && !aligned(d_status, 4))) return SZ_ERR_INVALID_ARG;
-    if (!codebook_ok(dt, h_cb->exp)) return SZ_ERR_INVALID_ARG;
+    if (h_cb && !codebook_ok(dt, h_cb->exp)) return SZ_ERR_INVALID_ARG;
+    if (d_cb && !aligned(d_cb, 16)) return SZ_ERR_INVALID_ARG;
     if (out_capacity < sz_encoded_size(dt, n, 0)) return SZ_ERR_CAPACITY;
     const uint64_t ws_need = workspace_bytes(n, stage_recs);
     if (ws_bytes < ws_need) return SZ_ERR_CAPACITY;
@@ -99,9 +102,12 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     p.out_bytes = d_out_bytes;
     p.status = d_status;
     p.wait_limit_ns = wait_ns;
-    std::memcpy(p.cb, h_cb->exp, SZ_CODEBOOK_SIZE);
-    std::sort(p.cb, p.cb + SZ_CODEBOOK_SIZE);  // code k = k-th smallest exponent
-    p.contig = p.cb[SZ_CODEBOOK_SIZE - 1] - p.cb[0] == SZ_CODEBOOK_SIZE - 1;
+    if (h_cb) {
+        std::memcpy(p.cb, h_cb->exp, SZ_CODEBOOK_SIZE);
+        std::sort(p.cb, p.cb + SZ_CODEBOOK_SIZE);  // code k = k-th smallest exponent
+        p.contig = p.cb[SZ_CODEBOOK_SIZE - 1] - p.cb[0] == SZ_CODEBOOK_SIZE - 1;
+    }
+    p.cb_dev = d_cb;
     p.skip_first = skip_first;
     if (dt == SZ_BF16)
         p.vec = aligned(d_in, 16) && aligned(d_out, 8) && aligned(static_cast<uint8_t*>(d_out) + n, 4);
@@ -178,8 +184,28 @@ sz_status sz_histogram(sz_dtype dt, const void* d_sample, size_t n, unsigned lon
     cudaError_t err = cudaMemsetAsync(d_hist, 0, sz_histogram_bins(dt) * sizeof(unsigned long long), stream);
     if (err != cudaSuccess) return from_cuda(err);
     if (n == 0) return SZ_OK;
-    HistogramParams p{static_cast<const uint8_t*>(d_sample), n, d_hist, dt == SZ_BF16};
+    HistogramParams p{static_cast<const uint8_t*>(d_sample), n, d_hist, dt == SZ_BF16, 1u};
     return from_cuda(launch_histogram(p, stream));
+}
+
+sz_status sz_codebook_from_histogram_device(sz_dtype dt, const unsigned long long* d_hist, uint8_t* d_cb,
+                                            cudaStream_t stream) {
+    if (!dtype_ok(dt) || !d_hist || !d_cb || !aligned(d_hist, 8) || !aligned(d_cb, 16)) return SZ_ERR_INVALID_ARG;
+    return from_cuda(launch_select(d_hist, (uint32_t)sz_histogram_bins(dt), d_cb, stream));
+}
+
+sz_status sz_calibrate_device(sz_dtype dt, const void* d_x, size_t n, uint32_t sample_stride,
+                              unsigned long long* d_hist, uint8_t* d_cb, cudaStream_t stream) {
+    if (!dtype_ok(dt) || !d_hist || !d_cb || (n > 0 && !d_x) || sample_stride == 0) return SZ_ERR_INVALID_ARG;
+    if (dt == SZ_BF16 && !aligned(d_x, 2)) return SZ_ERR_INVALID_ARG;
+    if (!aligned(d_hist, 8) || !aligned(d_cb, 16)) return SZ_ERR_INVALID_ARG;
+    cudaError_t err = cudaMemsetAsync(d_hist, 0, sz_histogram_bins(dt) * sizeof(unsigned long long), stream);
+    if (err == cudaSuccess && n > 0) {
+        HistogramParams p{static_cast<const uint8_t*>(d_x), n, d_hist, dt == SZ_BF16, sample_stride};
+        err = launch_histogram(p, stream);
+    }
+    if (err == cudaSuccess) err = launch_select(d_hist, (uint32_t)sz_histogram_bins(dt), d_cb, stream);
+    return from_cuda(err);
 }
 
 sz_status sz_codebook_from_histogram(sz_dtype dt, const unsigned long long* h_hist, sz_codebook* h_cb) {
@@ -216,6 +242,14 @@ sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size
                        kWaitLimitNs, stream);
 }
 
+sz_status sz_encode_dcb(sz_dtype dt, const uint8_t* d_cb, const void* d_in, size_t n, void* d_out,
+                        size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
+                        size_t ws_bytes, cudaStream_t stream) {
+    if (!d_cb) return SZ_ERR_INVALID_ARG;
+    return encode_impl(dt, nullptr, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
+                       kWaitLimitNs, stream, kStageRecs, d_cb);
+}
+
 sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                             size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, cudaStream_t stream) {
     if (!dtype_ok(dt)) return SZ_ERR_INVALID_ARG;
@@ -224,7 +258,7 @@ sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_
     void* ws = nullptr;
     const sz_status st = noalloc_scratch_for_current_device(&ws);
     if (st != SZ_OK) return st;
-    // encode_impl clears the part of the scratch the kernel uses before launching.
+    // The two-phase encode needs no cleared workspace.
     return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, ws, kNoAllocScratchBytes, 0,
                        kWaitLimitNs, stream, kNoAllocStageRecs);
 }

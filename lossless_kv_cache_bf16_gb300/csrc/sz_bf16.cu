@@ -212,7 +212,7 @@ __device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const
 }
 
 template <bool CONTIG>
-__global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_kernel(const EncodeParams p) {
+__device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const uint8_t (&cb)[16]) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -236,13 +236,16 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
         uint32_t code = 0x10u;
 #pragma unroll
         for (int k = 0; k < kCodes; k++)
-            if (p.cb[k] == tid) code = (uint32_t)k;
+            if (cb[k] == tid) code = (uint32_t)k;
         S.code[tid] = (uint8_t)code;
     }
-    if (blockIdx.x == 0 && tid < kCodes) p.out[p.L.cb_off + tid] = p.cb[tid];
+    if (blockIdx.x == 0 && tid == 0) {
+#pragma unroll
+        for (int k = 0; k < kCodes; k++) p.out[p.L.cb_off + k] = cb[k];
+    }
     __syncthreads();
 
-    const uint32_t lane_add = ((0x100u - p.cb[0]) & 0xFFu) * 0x01010101u;  // (256 - cb0) per byte
+    const uint32_t lane_add = ((0x100u - cb[0]) & 0xFFu) * 0x01010101u;  // (256 - cb0) per byte
     auto issue = [&](uint32_t i) {  // thread 0 only: sub-tile i of this block into ring slot i % S
         const uint32_t u = sub_of(i), slot = i % kEncStages;
         if (p.skip_first && blockIdx.x == 0 && i == 0) return;  // test hook: this slot never fills
@@ -341,6 +344,25 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
         for (uint32_t k = waited; k < issued; k++)
             if (!(p.skip_first && blockIdx.x == 0 && k == 0))
                 mbar_wait(&S.full[k % kEncStages], (k / kEncStages) & 1u, p.wait_limit_ns);
+    }
+}
+
+// MODE 0: codebook in the parameters, table coding; 1: in the parameters,
+// contiguous; 2: in device memory, checked (a bad one sets SZ_ERR_INVALID_ARG
+// in *status) and the coding chosen on the device.
+template <int MODE>
+__global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_kernel(const EncodeParams p) {
+    uint8_t cb[16];
+    bool contig;
+    const bool ok = load_codebook(p.cb, MODE == 2 ? p.cb_dev : nullptr, 256u, cb, contig);
+    if (MODE == 2) {
+        if (!ok && blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicMax(p.status, kStatusInvalid);
+        if (contig)
+            encode_bf16_body<true>(p, cb);
+        else
+            encode_bf16_body<false>(p, cb);
+    } else {
+        encode_bf16_body<MODE == 1>(p, cb);
     }
 }
 
@@ -687,7 +709,9 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
 
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(EncodeSmem);
-    const void* kern = p.contig ? (const void*)encode_bf16_kernel<true> : (const void*)encode_bf16_kernel<false>;
+    const void* kern = p.cb_dev   ? (const void*)encode_bf16_kernel<2>
+                       : p.contig ? (const void*)encode_bf16_kernel<1>
+                                  : (const void*)encode_bf16_kernel<0>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int dev = 0, sms = 0, per_sm = 0;
     if (err == cudaSuccess) err = cudaGetDevice(&dev);

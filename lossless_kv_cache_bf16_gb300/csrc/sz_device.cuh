@@ -15,6 +15,7 @@ constexpr uint32_t kChunk = 65536;  // elements per escape chunk (u16 positions)
 constexpr int kCodes = 16;          // top-16 codebook
 
 // Device status codes (same values as sz_status in splitzip.h).
+constexpr int kStatusInvalid = 1;  // a codebook read from device memory is not valid
 constexpr int kStatusCapacity = 3;
 constexpr int kStatusCorrupt = 4;
 constexpr int kStatusTimeout = 5;
@@ -213,6 +214,32 @@ __device__ void for_each_tile_escape(const DecodeParams& p, uint32_t tile, uint3
         }
     }
     __syncthreads();
+}
+
+// The codebook of an encode in registers: the 16 bytes of the parameters, or,
+// when cb_dev is set, 16 bytes of device memory (16-byte aligned) that are
+// checked here.  Returns whether they are 16 strictly ascending exponents
+// below `limit`; contig: cb[k] = cb[0] + k for every k.
+__device__ __forceinline__ bool load_codebook(const uint8_t (&param_cb)[16], const uint8_t* cb_dev, uint32_t limit,
+                                              uint8_t (&cb)[16], bool& contig) {
+    if (cb_dev) {
+        const uint4 v = *reinterpret_cast<const uint4*>(cb_dev);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 16; k++) cb[k] = (uint8_t)(w[k >> 2] >> (8 * (k & 3)));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 16; k++) cb[k] = param_cb[k];
+    }
+    bool ok = true;
+    contig = true;
+#pragma unroll
+    for (int k = 0; k < 16; k++) {
+        ok &= cb[k] < limit;
+        if (k > 0) ok &= cb[k] > cb[k - 1];
+        contig &= (uint32_t)cb[k] == (uint32_t)cb[0] + k;
+    }
+    return ok;
 }
 
 }  // namespace sz

@@ -113,7 +113,7 @@ struct EncodeE5Smem {
 };
 
 template <bool CONTIG>
-__global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kernel(const EncodeParams p) {
+__device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const uint8_t (&cb)[16]) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
     auto& s_field = S.field;
@@ -127,11 +127,14 @@ __global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kerne
         uint32_t code = 0xFFu;
 #pragma unroll
         for (int k = 0; k < kCodes; k++)
-            if (p.cb[k] == e) code = (uint32_t)k;
+            if (cb[k] == e) code = (uint32_t)k;
         const uint32_t sm3 = ((x >> 7) << 2) | (x & 3u);
         s_field[x] = (uint8_t)(code == 0xFFu ? (0x80u | (sm3 << 4)) : (code | (sm3 << 4)));
     }
-    if (blockIdx.x == 0 && tid < kCodes) p.out[p.L.cb_off + tid] = p.cb[tid];
+    if (blockIdx.x == 0 && tid == 0) {
+#pragma unroll
+        for (int k = 0; k < kCodes; k++) p.out[p.L.cb_off + k] = cb[k];
+    }
     __syncthreads();
     const uint32_t st = blockIdx.x;
     const uint64_t n = p.L.n;
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kerne
             s_in[warp][swz8(piece >> 3, piece & 7u)] = ld_stream_v4(p.in + warp_base + 16 * piece);
         }
     } else {
-        const uint32_t pad = (uint32_t)p.cb[0] << 2;
+        const uint32_t pad = (uint32_t)cb[0] << 2;
         for (uint32_t s = 0; s < 8; s++) {
             uint32_t w[4];
 #pragma unroll
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kerne
     // escape flags of elements 32q..32q+31 of the thread.
     uint32_t escm[4], words[28];
     {
-        const uint32_t add = 0x20202020u - (uint32_t)p.cb[0] * 0x01010101u;
+        const uint32_t add = 0x20202020u - (uint32_t)cb[0] * 0x01010101u;
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             uint32_t lo[4], hi[4], eh[4];
@@ -256,6 +259,26 @@ __global__ void __launch_bounds__(kEncThreads, CONTIG ? 5 : 3) encode_e5m2_kerne
         const uint8_t* src = reinterpret_cast<const uint8_t*>(&s_out[warp][lane * 7]);
         uint8_t* dst = p.out + out_base + lane * 112u;
         for (uint32_t b = 0; b < nbytes; b++) dst[b] = src[b];
+    }
+}
+
+// MODE 0: codebook in the parameters, table coding; 1: in the parameters,
+// contiguous; 2: in device memory, checked (a bad one sets SZ_ERR_INVALID_ARG
+// in *status) and the coding chosen on the device.
+template <int MODE>
+__global__ void __launch_bounds__(kEncThreads, MODE == 1 ? 4 : 3) encode_e5m2_kernel(const EncodeParams p) {
+    uint8_t cb[16];
+    bool contig;
+    const bool ok = load_codebook(p.cb, MODE == 2 ? p.cb_dev : nullptr, 32u, cb, contig);
+    if (MODE == 2) {
+        if (!ok && blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicMax(p.status, kStatusInvalid);
+        // A contiguous run must also stay within 5 bits for the byte-parallel coding.
+        if (contig && cb[0] <= 16)
+            encode_e5m2_body<true>(p, cb);
+        else
+            encode_e5m2_body<false>(p, cb);
+    } else {
+        encode_e5m2_body<MODE == 1>(p, cb);
     }
 }
 
@@ -616,7 +639,7 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
 
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(EncodeE5Smem);
-    auto kern = p.contig ? encode_e5m2_kernel<true> : encode_e5m2_kernel<false>;
+    auto kern = p.cb_dev ? encode_e5m2_kernel<2> : p.contig ? encode_e5m2_kernel<1> : encode_e5m2_kernel<0>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     kern<<<p.num_tiles, kEncThreads, smem, s>>>(p);

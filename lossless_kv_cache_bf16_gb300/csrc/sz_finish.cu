@@ -53,9 +53,12 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
     const uint32_t T = p.num_tiles, F = gridDim.x;
     const uint32_t t0 = (uint32_t)((uint64_t)blockIdx.x * T / F), t1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * T / F);
     {
+        uint8_t cb[16];
+        bool contig;
+        load_codebook(p.cb, p.cb_dev, BF16 ? 256u : 32u, cb, contig);
         uint32_t member = 0;
 #pragma unroll
-        for (int k = 0; k < kCodes; k++) member |= p.cb[k] == tid;
+        for (int k = 0; k < kCodes; k++) member |= cb[k] == tid;
         s_member[tid] = (uint8_t)member;
     }
     // Escapes in all scan tiles before this block's range.  ws_count is

@@ -35,6 +35,7 @@ struct EncodeParams {
     uint32_t* ws_count;      // workspace: escapes per scan tile
     uint8_t* ws_rec;         // workspace: staged records, ws_cap per scan tile
     uint32_t ws_cap;         // records staged per scan tile
+    const uint8_t* cb_dev;   // nullable: codebook in device memory instead of cb
     uint8_t cb[16];          // ascending
 };
 
@@ -54,6 +55,7 @@ struct HistogramParams {
     uint64_t n;
     unsigned long long* hist;
     int bf16;
+    uint32_t stride;  // count the elements of every stride-th group of 8 (1: all)
 };
 
 // Tile sizes (elements).  Both divide the 65,536-element chunk.
@@ -74,6 +76,8 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_histogram(const HistogramParams& p, cudaStream_t s);
+// Top-16 of a device histogram -> 16 ascending exponents in device memory.
+cudaError_t launch_select(const unsigned long long* hist, uint32_t bins, uint8_t* cb_out, cudaStream_t s);
 cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s);
 
 }  // namespace sz

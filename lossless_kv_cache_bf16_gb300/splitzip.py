@@ -60,6 +60,9 @@ def _load() -> ctypes.CDLL:
         "sz_status_string": (ctypes.c_char_p, [i32]),
         "sz_debug_encode_stalled": (i32, [i32, cbp, vp, sz, vp, sz, vp, vp, vp, sz, ctypes.c_ulonglong, vp]),
         "sz_encode_noalloc": (i32, [i32, cbp, vp, sz, vp, sz, vp, vp, vp]),
+        "sz_codebook_from_histogram_device": (i32, [i32, vp, vp, vp]),
+        "sz_calibrate_device": (i32, [i32, vp, sz, ctypes.c_uint32, vp, vp, vp]),
+        "sz_encode_dcb": (i32, [i32, vp, vp, sz, vp, sz, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -150,6 +153,37 @@ def sz_calibrate(dt: int, sample: torch.Tensor, hist: torch.Tensor, stream=None)
     _check("sz_calibrate", LIB.sz_calibrate(dt, _dev_ptr(sample, "sample"), _elements(dt, sample),
                                             _dev_ptr(hist, "hist"), ctypes.byref(cb), _stream(stream)))
     return list(cb.exp)
+
+
+def sz_codebook_from_histogram_device(dt: int, hist: torch.Tensor, cb: torch.Tensor, stream=None) -> None:
+    """Top-16 of a device histogram into cb (16 uint8 on the device); asynchronous."""
+    assert hist.numel() == sz_histogram_bins(dt) and hist.element_size() == 8
+    assert cb.numel() * cb.element_size() >= SZ_CODEBOOK_SIZE
+    _check("sz_codebook_from_histogram_device",
+           LIB.sz_codebook_from_histogram_device(dt, _dev_ptr(hist, "hist"), _dev_ptr(cb, "cb"), _stream(stream)))
+
+
+def sz_calibrate_device(dt: int, x: torch.Tensor, hist: torch.Tensor, cb: torch.Tensor, sample_stride: int = 1,
+                        stream=None, n: int | None = None) -> None:
+    """Online calibration on the device (histogram of every sample_stride-th
+    group of 8 elements, then top-16) into cb (16 uint8 on the device);
+    asynchronous, no host synchronisation."""
+    assert hist.numel() == sz_histogram_bins(dt) and hist.element_size() == 8
+    assert cb.numel() * cb.element_size() >= SZ_CODEBOOK_SIZE
+    n = _elements(dt, x) if n is None else n
+    _check("sz_calibrate_device",
+           LIB.sz_calibrate_device(dt, _dev_ptr(x, "x"), n, sample_stride, _dev_ptr(hist, "hist"),
+                                   _dev_ptr(cb, "cb"), _stream(stream)))
+
+
+def sz_encode_dcb(dt: int, cb: torch.Tensor, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
+                  status: torch.Tensor | None, ws: torch.Tensor, stream=None, n: int | None = None) -> None:
+    """sz_encode with the codebook in device memory (cb: 16 uint8 on the device)."""
+    n = _elements(dt, x) if n is None else n
+    _check("sz_encode_dcb", LIB.sz_encode_dcb(dt, _dev_ptr(cb, "cb"), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
+                                              out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                              _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
+                                              ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def sz_encode(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
