@@ -387,6 +387,22 @@ def main():
                        "codebook": dcb.cpu().tolist(), "offline_codebook": [int(v) for v in cb],
                        "ratio": n_bytes / online_size, "ratio_offline": n_bytes / size})
 
+    ablation = None
+    if not args.profile:
+        # Codebook ablation on this tensor: exact stream sizes under Top-16
+        # (this format), Top-8 and Top-15 + sentinel, from the device
+        # histogram of the whole tensor.
+        fh = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device=dev)
+        S.sz_histogram(dt, x, fh)
+        counts = fh.cpu().tolist()
+        s16, s8, s15 = S.sz_ablation_sizes(dt, counts, n)
+        top = sorted(counts, reverse=True)
+        ablation = {"ratio_top16": n_bytes / s16, "ratio_top8": n_bytes / s8, "ratio_top15_sentinel": n_bytes / s15,
+                    "coverage_top16": sum(top[:16]) / n, "coverage_top8": sum(top[:8]) / n,
+                    "coverage_top15": sum(top[:15]) / n,
+                    "note": "sizes from the whole-tensor exponent histogram; the Top-8 and sentinel layouts are "
+                            "readings (codes + same escapes/headers), their codecs are not built"}
+
     e2e = None
     memcpy_gbs = None
     if not args.profile and args.e2e_steps > 0:
@@ -523,7 +539,7 @@ def main():
         "link_model": link_model(n_bytes, size, te, td),
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
                           "hardware": "not named on the pages"},
-        "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online,
+        "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online, "ablation": ablation,
         "e2e": e2e,
         "gpu_launches": sum(len(OPS[op][0]) for op in ops) * K, "clocks": clocks,
     }

@@ -136,6 +136,20 @@ sz_status sz_codebook_from_histogram_device(sz_dtype dt, const unsigned long lon
 sz_status sz_calibrate_device(sz_dtype dt, const void* d_x, size_t n, uint32_t sample_stride,
                               unsigned long long* d_hist, uint8_t* d_cb, cudaStream_t stream);
 
+/* Codebook ablation ([RES] "Estudios de Ablacion": Top-16 vs Top-8, and
+ * explicit escape positions vs a Top-15 sentinel).  From the exponent
+ * histogram h_hist (sz_histogram_bins(dt) counts) of n elements, the stream
+ * sizes in bytes of (h_sizes[0]) this format with its top-16 codebook,
+ * (h_sizes[1]) 3-bit Top-8 codes (BF16: sm bytes + 8 codes in 3 bytes; E5M2:
+ * 6-bit code|sm3 fields, 4 in 3 bytes) with the same 3-byte escape records,
+ * an 8-byte codebook and the same headers, and (h_sizes[2]) Top-15 codes
+ * with code 15 as an escape sentinel, each escape storing only its exponent
+ * byte, a 15-byte codebook and the same headers.  The pages name these
+ * designs but not their layouts; these are the plainest ones that keep the
+ * rest of the format.  Host only. */
+sz_status sz_ablation_sizes(sz_dtype dt, const unsigned long long* h_hist, size_t n,
+                            unsigned long long* h_sizes);
+
 /* Offline calibration = sz_histogram, a device-to-host copy of the counts,
  * and sz_codebook_from_histogram.  Synchronises `stream` (the only call that
  * does).  d_hist is the same caller-owned scratch as for sz_histogram. */

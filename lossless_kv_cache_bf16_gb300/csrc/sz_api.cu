@@ -222,6 +222,24 @@ sz_status sz_codebook_from_histogram(sz_dtype dt, const unsigned long long* h_hi
     return SZ_OK;
 }
 
+sz_status sz_ablation_sizes(sz_dtype dt, const unsigned long long* h_hist, size_t n, unsigned long long* h_sizes) {
+    if (!dtype_ok(dt) || !h_hist || !h_sizes) return SZ_ERR_INVALID_ARG;
+    const int bins = (int)sz_histogram_bins(dt);
+    int order[256];
+    for (int e = 0; e < bins; e++) order[e] = e;
+    std::stable_sort(order, order + bins, [&](int a, int b) { return h_hist[a] > h_hist[b]; });
+    // covered[k] = elements whose exponent is among the k most frequent.
+    unsigned long long covered[17] = {};
+    for (int k = 1; k <= 16; k++) covered[k] = covered[k - 1] + h_hist[order[k - 1]];
+    const uint64_t chunks = cdiv(n, SZ_CHUNK_ELEMS);
+    const uint64_t e16 = n - covered[16], e8 = n - covered[8], e15 = n - covered[15];
+    const uint64_t codes8 = dt == SZ_BF16 ? n + 3 * cdiv(n, 8) : 3 * cdiv(n, 4);
+    h_sizes[0] = sz_encoded_size(dt, n, e16);
+    h_sizes[1] = codes8 + 3 * e8 + 8 + 8 * chunks;
+    h_sizes[2] = dense_bytes(dt, n) + e15 + 15 + 8 * chunks;
+    return SZ_OK;
+}
+
 sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n, unsigned long long* d_hist, sz_codebook* h_cb,
                        cudaStream_t stream) {
     if (!h_cb) return SZ_ERR_INVALID_ARG;

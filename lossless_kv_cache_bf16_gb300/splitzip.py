@@ -63,6 +63,7 @@ def _load() -> ctypes.CDLL:
         "sz_codebook_from_histogram_device": (i32, [i32, vp, vp, vp]),
         "sz_calibrate_device": (i32, [i32, vp, sz, ctypes.c_uint32, vp, vp, vp]),
         "sz_encode_dcb": (i32, [i32, vp, vp, sz, vp, sz, vp, vp, vp, sz, vp]),
+        "sz_ablation_sizes": (i32, [i32, u64p, sz, u64p]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -145,6 +146,15 @@ def sz_codebook_from_histogram(dt: int, hist) -> list[int]:
     cb = sz_codebook()
     _check("sz_codebook_from_histogram", LIB.sz_codebook_from_histogram(dt, arr, ctypes.byref(cb)))
     return list(cb.exp)
+
+
+def sz_ablation_sizes(dt: int, hist, n: int) -> tuple[int, int, int]:
+    """Stream sizes under Top-16 (this format), Top-8 and Top-15 + sentinel."""
+    vals = [int(v) for v in (hist.tolist() if hasattr(hist, "tolist") else hist)]
+    arr = (ctypes.c_ulonglong * len(vals))(*vals)
+    out = (ctypes.c_ulonglong * 3)()
+    _check("sz_ablation_sizes", LIB.sz_ablation_sizes(dt, arr, n, out))
+    return int(out[0]), int(out[1]), int(out[2])
 
 
 def sz_calibrate(dt: int, sample: torch.Tensor, hist: torch.Tensor, stream=None) -> list[int]:

@@ -95,6 +95,7 @@ class Oracle:
             "orc_encode": (i32, [i32, vp, vp, u64, vp, u64, ctypes.POINTER(u64)]),
             "orc_validate": (i32, [i32, vp, u64, u64, ctypes.POINTER(u64)]),
             "orc_decode": (i32, [i32, vp, u64, u64, vp]),
+            "orc_ablation_sizes": (i32, [i32, vp, u64, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -173,6 +174,16 @@ class Oracle:
         y = np.zeros(max(2 * n if dt == BF16 else n, 1), dtype=np.uint8)
         st = self.lib.orc_decode(dt, _ptr(s), s.size, n, _ptr(y))
         return int(st), y[: (2 * n if dt == BF16 else n)]
+
+
+    # -- ablation ------------------------------------------------------------
+    def ablation_sizes(self, dt: int, hist: np.ndarray, n: int) -> tuple[int, int, int]:
+        """Stream sizes under Top-16 (this format), Top-8 and Top-15 + sentinel."""
+        h = np.ascontiguousarray(hist, dtype=np.uint64)
+        assert h.size == (256 if dt == BF16 else 32)
+        out = np.zeros(3, dtype=np.uint64)
+        self.lib.orc_ablation_sizes(dt, _ptr(h), n, _ptr(out))
+        return int(out[0]), int(out[1]), int(out[2])
 
 
 _DEFAULT: Oracle | None = None

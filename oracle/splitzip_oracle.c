@@ -41,6 +41,18 @@
  *      E5M2 dense = [7 bytes x ceil(N/8)].  No global header, no padding.
  *  R10 zero, subnormal, Inf and NaN need no special case: an exponent field
  *      is just a value.
+ *
+ * The codebook ablation ([RES] "Estudios de Ablacion": Top-16 vs Top-8, and
+ * explicit positions vs a Top-15 sentinel) names the alternative designs but
+ * not their layouts; orc_ablation_sizes counts them under the plainest
+ * layouts that keep everything else of this format:
+ *  A1  Top-8: 3-bit codes; BF16 keeps the sm bytes and packs 8 codes in 3
+ *      bytes; E5M2 packs 6-bit code|sm3 fields, 4 in 3 bytes; escapes as R6;
+ *      the codebook takes 8 bytes.
+ *  A2  Top-15 + sentinel: 4-bit codes with 15 marking an escape; an escape
+ *      stores only its exponent byte, in element order; the codebook takes
+ *      15 bytes; the chunk headers stay (they give each chunk's first escape).
+ *  A3  top-k selection follows R4 with k in place of 16.
  */
 #include <stddef.h>
 #include <stdint.h>
@@ -98,11 +110,11 @@ void orc_histogram(int dt, const uint8_t *x, uint64_t n, uint64_t *hist) {
 
 /* Pick the 16 most frequent exponents (R4: ties toward the smaller exponent,
  * unseen exponents fill up from the smallest), then list them ascending (R3). */
-int orc_codebook_from_histogram(int dt, const uint64_t *hist, uint8_t *cb) {
-    int taken[256];
+/* taken[e] = 1 for the k most frequent exponents (R4 for any k <= bins). */
+static void pick_most_frequent(int dt, const uint64_t *hist, int k, int *taken) {
     int bins = exponent_bins(dt);
     for (int e = 0; e < 256; e++) taken[e] = 0;
-    for (int k = 0; k < ORC_CB; k++) {
+    for (int r = 0; r < k; r++) {
         int best = -1;
         for (int e = 0; e < bins; e++) {
             if (taken[e]) continue;
@@ -110,6 +122,12 @@ int orc_codebook_from_histogram(int dt, const uint64_t *hist, uint8_t *cb) {
         }
         taken[best] = 1;
     }
+}
+
+int orc_codebook_from_histogram(int dt, const uint64_t *hist, uint8_t *cb) {
+    int taken[256];
+    int bins = exponent_bins(dt);
+    pick_most_frequent(dt, hist, ORC_CB, taken);
     int k = 0;
     for (int e = 0; e < bins; e++)
         if (taken[e]) cb[k++] = (uint8_t)e;
@@ -345,5 +363,41 @@ int orc_decode(int dt, const uint8_t *in, uint64_t in_bytes, uint64_t n, uint8_t
             }
         }
     }
+    return ORC_OK;
+}
+
+/* ---- codebook ablation sizes ([RES] "Estudios de Ablacion") -------------- */
+
+/* Elements whose exponent is outside the k most frequent ones (the same
+ * selection rule as the codebook: repeated arg-max, ties toward the smaller
+ * exponent, unseen exponents eligible). */
+static uint64_t outside_top_k(int dt, const uint64_t *hist, uint64_t n, int k) {
+    int taken[256];
+    uint64_t covered = 0;
+    pick_most_frequent(dt, hist, k, taken);
+    for (int e = 0; e < exponent_bins(dt); e++)
+        if (taken[e]) covered += hist[e];
+    return n - covered;
+}
+
+/* Stream sizes of n elements under the three codebook designs the ablation
+ * compares (readings A1-A3):
+ *   sizes[0]  Top-16, this format: 4-bit codes, escapes as (u16 position,
+ *             u8 exponent) records; = orc_encoded_size with the top-16 set;
+ *   sizes[1]  Top-8: 3-bit codes (BF16: 8 codes in 3 bytes next to the sm
+ *             bytes; E5M2: 6-bit code|sm3 fields, 4 in 3 bytes), escapes as
+ *             above, an 8-byte codebook and the same chunk headers;
+ *   sizes[2]  Top-15 + sentinel: code 15 marks an escape, which stores only
+ *             its exponent byte (positions are implied), a 15-byte codebook
+ *             and the same chunk headers (escape offsets per chunk). */
+int orc_ablation_sizes(int dt, const uint64_t *hist, uint64_t n, uint64_t *sizes) {
+    uint64_t chunks = orc_num_chunks(n);
+    uint64_t e16 = outside_top_k(dt, hist, n, 16);
+    uint64_t e8 = outside_top_k(dt, hist, n, 8);
+    uint64_t e15 = outside_top_k(dt, hist, n, 15);
+    uint64_t dense8 = dt == ORC_BF16 ? n + 3 * ((n + 7) / 8) : 3 * ((n + 3) / 4);
+    sizes[0] = orc_encoded_size(dt, n, e16);
+    sizes[1] = dense8 + 3 * e8 + 8 + 8 * chunks;
+    sizes[2] = orc_dense_bytes(dt, n) + e15 + 15 + 8 * chunks;
     return ORC_OK;
 }

@@ -336,6 +336,35 @@ def check_invalid_codebook_refused(orc):
     raise AssertionError("encode accepted a codebook with a repeated exponent")
 
 
+def check_ablation_hand(orc):
+    """Stream sizes under Top-16 / Top-8 / Top-15 + sentinel (golden)."""
+    for g in G.load("ablation_hand.txt"):
+        dt = O.BF16 if g["dtype"] == "bf16" else O.E5M2
+        n = int(g["n"])
+        if g["case"] == "bf16_all":
+            x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+        elif g["case"] == "e5m2_all":
+            x = np.arange(256, dtype=np.uint32).astype(np.uint8)
+        else:  # exponents ramp_from.. seen 20, 19, ..., 1 times
+            e0 = int(g["ramp_from"])
+            exps = np.concatenate([np.full(20 - k, e0 + k) for k in range(20)]).astype(np.uint32)
+            x = (exps << 7).astype(np.uint16) if dt == O.BF16 else (exps << 2).astype(np.uint8)
+        assert O.Oracle.element_count(dt, x) == n
+        want = tuple(int(v) for v in g["sizes"].split())
+        assert orc.ablation_sizes(dt, orc.histogram(dt, x), n) == want, g["case"]
+
+
+def check_ablation_top16_is_the_stream(orc):
+    """The Top-16 size of the ablation is the size of this format's stream."""
+    rng = np.random.default_rng(12)
+    for dt, x in ((O.BF16, (rng.standard_normal(70_001) * 40).astype(np.float32).view(np.uint32) >> 16),
+                  (O.E5M2, rng.integers(0, 256, 9_999))):
+        x = x.astype(np.uint16 if dt == O.BF16 else np.uint8)
+        cb = orc.calibrate(dt, x)
+        n = O.Oracle.element_count(dt, x)
+        assert orc.ablation_sizes(dt, orc.histogram(dt, x), n)[0] == orc.encode(dt, cb, x).size
+
+
 CHECKS = [
     check_hand_bf16,
     check_hand_e5m2,
@@ -351,4 +380,6 @@ CHECKS = [
     check_dense_pass_then_overwrite,
     check_corrupt_rejected,
     check_invalid_codebook_refused,
+    check_ablation_hand,
+    check_ablation_top16_is_the_stream,
 ]

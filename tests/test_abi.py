@@ -96,3 +96,24 @@ def test_status_strings(S):
     assert S.sz_status_string(0) == "SZ_OK"
     assert S.sz_status_string(5) == "SZ_ERR_TIMEOUT"
     assert S.sz_status_string(99) == "SZ_ERR_UNKNOWN"
+
+
+def test_ablation_sizes_match_oracle(S, orc):
+    """The library's ablation arithmetic is written independently of the
+    oracle's; they must agree on every histogram, ties and zeros included."""
+    from oracle import oracle as O
+
+    rng = np.random.default_rng(9)
+    for dt, odt in ((S.SZ_BF16, O.BF16), (S.SZ_FP8_E5M2, O.E5M2)):
+        bins = S.sz_histogram_bins(dt)
+        for trial in range(60):
+            if trial % 3 == 0:
+                h = rng.integers(0, 3, size=bins)
+            elif trial % 3 == 1:
+                h = rng.integers(0, 1 << 30, size=bins)
+            else:
+                h = np.zeros(bins, dtype=np.int64)
+                h[rng.integers(0, bins, size=5)] = rng.integers(1, 100, size=5)
+            h = h.astype(np.uint64)
+            n = int(h.sum())
+            assert S.sz_ablation_sizes(dt, h, n) == orc.ablation_sizes(odt, h, n)

@@ -189,3 +189,20 @@ def test_online_chain_in_a_cuda_graph(orc, kind):
         torch.cuda.synchronize()
         assert int(dst.item()) == 0
         assert torch.equal(y.view(torch.uint8), x.view(torch.uint8))
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e5m2"])
+def test_ablation_sizes_from_the_device_histogram(orc, kind):
+    """Device histogram + the library's ablation arithmetic = the oracle's
+    ablation sizes of the same tensor; the Top-16 size is the real stream's."""
+    from lossless_kv_cache_bf16_gb300 import workloads as W
+
+    dt = _dt(kind)
+    x = (W.kv_tiny("cuda", 4) if kind == "bf16" else W.fp8_e5m2_kv("cuda", 4, layers=1, tokens=128)).reshape(-1)
+    n = x.numel()
+    hist = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device="cuda")
+    S.sz_histogram(dt, x, hist)
+    got = S.sz_ablation_sizes(dt, hist.cpu().tolist(), n)
+    xb = G.as_bytes(x)
+    assert got == orc.ablation_sizes(ODT[kind], orc.histogram(ODT[kind], xb), n)
+    assert got[0] == orc.encode(ODT[kind], orc.calibrate(ODT[kind], xb), xb).size
