@@ -387,6 +387,42 @@ def main():
                        "codebook": dcb.cpu().tolist(), "offline_codebook": [int(v) for v in cb],
                        "ratio": n_bytes / online_size, "ratio_offline": n_bytes / size})
 
+    paged = None
+    if not args.profile:
+        # Paged KV: the tensor seen as a pool of pages of 16 tokens (x heads x
+        # head_dim elements), a shuffled block table over all of them, encoded
+        # straight from the pages and decoded straight into a second pool.
+        page_elems = 16 * x.shape[-1] * x.shape[-2] if x.dim() == 5 else 16384
+        if n % page_elems == 0:
+            pages = n // page_elems
+            gperm = torch.Generator(device="cpu")
+            gperm.manual_seed(7)
+            ids = torch.randperm(pages, generator=gperm).to(torch.int32).to(dev)
+            pout = torch.empty(S.sz_encoded_size(dt, n, n), dtype=torch.uint8, device=dev)
+            for _ in range(3):
+                S.sz_encode_paged(dt, cb, x, page_elems, ids, n, pout, ob, est, ws)
+            torch.cuda.synchronize()
+            psize = int(ob.item())
+            for _ in range(3):
+                S.sz_decode_paged(dt, pout, psize, n, y, page_elems, ids, dst)
+            ev3 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev3[0].record(stream)
+            for _ in range(20):
+                S.sz_encode_paged(dt, cb, x, page_elems, ids, n, pout, ob, est, ws)
+            ev3[1].record(stream)
+            for _ in range(20):
+                S.sz_decode_paged(dt, pout, psize, n, y, page_elems, ids, dst)
+            ev3[2].record(stream)
+            torch.cuda.synchronize()
+            assert int(est.item()) == 0 and int(dst.item()) == 0
+            assert torch.equal(y.view(torch.uint8), x.view(torch.uint8)), "paged round trip is not bit-exact"
+            paged = {"page_elems": page_elems, "pages": pages, "block_table": "random permutation of all pages",
+                     "encode_gbs": n_bytes / (ev3[0].elapsed_time(ev3[1]) / 20 / 1e3) / 1e9,
+                     "decode_gbs": n_bytes / (ev3[1].elapsed_time(ev3[2]) / 20 / 1e3) / 1e9,
+                     "stream_bytes": psize}
+            # Restore y as the plain decode of the contiguous stream for what follows.
+            S.sz_decode(dt, out, size, n, y, dst)
+
     ablation = None
     if not args.profile:
         # Codebook ablation on this tensor: exact stream sizes under Top-16
@@ -539,7 +575,7 @@ def main():
         "link_model": link_model(n_bytes, size, te, td),
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
                           "hardware": "not named on the pages"},
-        "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online, "ablation": ablation,
+        "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online, "ablation": ablation, "paged": paged,
         "e2e": e2e,
         "gpu_launches": sum(len(OPS[op][0]) for op in ops) * K, "clocks": clocks,
     }

@@ -201,6 +201,31 @@ sz_status sz_encode_dcb(sz_dtype dt, const uint8_t* d_cb, const void* d_in, size
 sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n,
                     void* d_out, int* d_status, cudaStream_t stream);
 
+/* Paged KV tensors.  Serving engines keep a KV cache as a pool of equal
+ * pages and each sequence as a block table of page ids; these two calls
+ * encode such a tensor straight from its pages and decode straight into
+ * them, with no contiguous copy.  The pages describe the codec for a
+ * contiguous tensor; this is the gather/scatter step around it.
+ *  d_pool        the pool (device, 16-byte aligned): pool_pages pages of
+ *                page_elems elements each, page q at d_pool + q * page_elems
+ *                * element size
+ *  page_elems    a power of two, 16 <= page_elems <= 2^30
+ *  d_block_ids   device int32[ceil(n / page_elems)]: element e of the logical
+ *                tensor is element e % page_elems of page d_block_ids[e /
+ *                page_elems].  An id outside [0, pool_pages) is never
+ *                dereferenced: *d_status becomes SZ_ERR_INVALID_ARG and the
+ *                result is meaningless.  Decode writes only the pages the
+ *                table names (ids must not repeat for decode).
+ * The stream is byte for byte the sz_encode stream of the logical tensor;
+ * other arguments and errors as for sz_encode / sz_decode. */
+sz_status sz_encode_paged(sz_dtype dt, const sz_codebook* h_cb, const void* d_pool, size_t pool_pages,
+                          size_t page_elems, const int32_t* d_block_ids, size_t n,
+                          void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
+                          int* d_status, void* d_ws, size_t ws_bytes, cudaStream_t stream);
+sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n,
+                          void* d_pool, size_t pool_pages, size_t page_elems,
+                          const int32_t* d_block_ids, int* d_status, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* sz_status_string(int status);
 

@@ -79,7 +79,7 @@ bool codebook_ok(sz_dtype dt, const uint8_t* cb) {
 sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                       size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
                       size_t ws_bytes, uint32_t skip_first, uint64_t wait_ns, cudaStream_t stream,
-                      uint32_t stage_recs = kStageRecs, const uint8_t* d_cb = nullptr) {
+                      uint32_t stage_recs = kStageRecs, const uint8_t* d_cb = nullptr, PageMap pm = PageMap{}) {
     if (!dtype_ok(dt) || (!h_cb == !d_cb) || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
     if ((n > 0 && !d_in) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
     if (dt == SZ_BF16 && !aligned(d_in, 2)) return SZ_ERR_INVALID_ARG;
@@ -108,6 +108,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
         p.contig = p.cb[SZ_CODEBOOK_SIZE - 1] - p.cb[0] == SZ_CODEBOOK_SIZE - 1;
     }
     p.cb_dev = d_cb;
+    p.pm = pm;
     p.skip_first = skip_first;
     if (dt == SZ_BF16)
         p.vec = aligned(d_in, 16) && aligned(d_out, 8) && aligned(static_cast<uint8_t*>(d_out) + n, 4);
@@ -290,8 +291,8 @@ sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const vo
                        wait_limit_ns, stream);
 }
 
-sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_out, int* d_status,
-                    cudaStream_t stream) {
+sz_status decode_impl(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_out, int* d_status,
+                      cudaStream_t stream, PageMap pm) {
     if (!dtype_ok(dt) || !d_in || (n > 0 && !d_out) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
     if (dt == SZ_BF16 && !aligned(d_out, 2)) return SZ_ERR_INVALID_ARG;
     if (d_status && !aligned(d_status, 4)) return SZ_ERR_INVALID_ARG;
@@ -308,6 +309,7 @@ sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, vo
     p.n_esc = (uint32_t)n_esc;
     p.status = d_status;
     p.wait_limit_ns = kWaitLimitNs;
+    p.pm = pm;
     if (dt == SZ_BF16)
         p.vec = aligned(d_in, 8) && aligned(static_cast<const uint8_t*>(d_in) + n, 4) && aligned(d_out, 16);
     else
@@ -318,6 +320,45 @@ sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, vo
         if (err != cudaSuccess) return from_cuda(err);
     }
     return from_cuda(dt == SZ_BF16 ? launch_decode_bf16(p, stream) : launch_decode_e5m2(p, stream));
+}
+
+// A page pool: page_elems a power of two in [16, 2^30], the pool 16-byte
+// aligned (so every page is), pool_pages in [1, 2^31).  Ids are checked on
+// the device.
+bool page_map_for(const void* d_pool, size_t pool_pages, size_t page_elems, const int32_t* d_ids, size_t n,
+                  PageMap* pm) {
+    if (page_elems < 16 || page_elems > (1ull << 30) || (page_elems & (page_elems - 1)) != 0) return false;
+    if (pool_pages == 0 || pool_pages >= (1ull << 31) || !d_pool || !aligned(d_pool, 16)) return false;
+    if (n > 0 && (!d_ids || !aligned(d_ids, 4))) return false;
+    uint32_t lg = 0;
+    while ((1ull << lg) < page_elems) lg++;
+    pm->ids = d_ids;
+    pm->pool_pages = (uint32_t)pool_pages;
+    pm->lg = lg;
+    return true;
+}
+
+sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_out, int* d_status,
+                    cudaStream_t stream) {
+    return decode_impl(dt, d_in, in_bytes, n, d_out, d_status, stream, PageMap{});
+}
+
+sz_status sz_encode_paged(sz_dtype dt, const sz_codebook* h_cb, const void* d_pool, size_t pool_pages,
+                          size_t page_elems, const int32_t* d_block_ids, size_t n, void* d_out, size_t out_capacity,
+                          unsigned long long* d_out_bytes, int* d_status, void* d_ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+    PageMap pm{};
+    if (!page_map_for(d_pool, pool_pages, page_elems, d_block_ids, n, &pm)) return SZ_ERR_INVALID_ARG;
+    if (n > 0 && cdiv(n, page_elems) > (1ull << 31)) return SZ_ERR_INVALID_ARG;
+    return encode_impl(dt, h_cb, d_pool, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
+                       kWaitLimitNs, stream, kStageRecs, nullptr, pm);
+}
+
+sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_pool, size_t pool_pages,
+                          size_t page_elems, const int32_t* d_block_ids, int* d_status, cudaStream_t stream) {
+    PageMap pm{};
+    if (!page_map_for(d_pool, pool_pages, page_elems, d_block_ids, n, &pm)) return SZ_ERR_INVALID_ARG;
+    return decode_impl(dt, d_in, in_bytes, n, d_pool, d_status, stream, pm);
 }
 
 const char* sz_status_string(int status) {

@@ -163,6 +163,9 @@ __device__ __forceinline__ uint32_t warp_escape_ranks(const uint32_t (&esc)[4], 
 
 // Loads lane's 4 groups of 8 elements of one warp's 1,024 elements starting
 // at element `base` (= sub-tile start + 1024 warp), from global memory.
+// A group of 8 never straddles a page (pages hold a power of two >= 16
+// elements), so one page lookup serves the whole group.
+template <bool PAGED>
 __device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64_t base, uint32_t lane,
                                                    uint32_t (&w)[4][4], uint32_t (&cnt)[4]) {
     const uint64_t n = p.L.n;
@@ -170,8 +173,9 @@ __device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64
     for (int k = 0; k < 4; k++) {
         const uint64_t i0 = base + k * 256u + lane * 8u;
         cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
+        const uint8_t* g = p.in + (cnt[k] ? elem_offset<PAGED>(p.pm, i0, 2, p.status) : 2 * i0);
         if (p.vec && cnt[k] == 8) {
-            const uint4 v = ld_stream_v4(p.in + 2 * i0);
+            const uint4 v = ld_stream_v4(g);
             w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
         } else {
 #pragma unroll
@@ -179,7 +183,7 @@ __device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64
 #pragma unroll
             for (int jj = 0; jj < 8; jj++) {
                 if ((uint32_t)jj < cnt[k]) {
-                    const uint8_t* e = p.in + 2 * (i0 + jj);
+                    const uint8_t* e = g + 2 * jj;
                     w[k][jj >> 1] |= ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) << (16 * (jj & 1));
                 }
             }
@@ -211,7 +215,7 @@ __device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const
     }
 }
 
-template <bool CONTIG>
+template <bool CONTIG, bool PAGED>
 __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const uint8_t (&cb)[16]) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
@@ -226,7 +230,12 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
     // Sub-tiles of this block, in order: index i -> scan tile i/4, part i%4.
     const uint32_t my_subs = my_scans == 0 ? 0u : (my_scans - 1) * kSubsPerScan + subs_in(scan_of(my_scans - 1));
     auto sub_of = [&](uint32_t i) { return scan_of(i / kSubsPerScan) * kSubsPerScan + i % kSubsPerScan; };
-    auto full_sub = [&](uint32_t u) { return p.vec && (uint64_t)(u + 1) * kBf16Tile <= n; };
+    // Paged input goes through the ring when a sub-tile is at most 8 page
+    // pieces (pages of >= 1,024 elements); smaller pages are read directly.
+    const uint32_t piece_lg = PAGED ? min(p.pm.lg, 13u) : 13u;  // 2^13 = one sub-tile
+    auto full_sub = [&](uint32_t u) {
+        return p.vec && (uint64_t)(u + 1) * kBf16Tile <= n && (!PAGED || p.pm.lg >= 10);
+    };
 
     if (tid == 0) {
         for (uint32_t s = 0; s < kEncStages; s++) mbar_init(&S.full[s], 1);
@@ -251,7 +260,14 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
         if (p.skip_first && blockIdx.x == 0 && i == 0) return;  // test hook: this slot never fills
         if (full_sub(u)) {
             mbar_arrive_expect_tx(&S.full[slot], kTileBytes);
-            bulk_g2s(S.in[slot], p.in + (uint64_t)u * kTileBytes, kTileBytes, &S.full[slot]);
+            if (PAGED) {
+                const uint32_t piece = 1u << piece_lg;  // elements per copy
+                for (uint32_t e = 0; e < kBf16Tile; e += piece)
+                    bulk_g2s(S.in[slot] + 2 * e, p.in + elem_offset<true>(p.pm, (uint64_t)u * kBf16Tile + e, 2, p.status),
+                             2 * piece, &S.full[slot]);
+            } else {
+                bulk_g2s(S.in[slot], p.in + (uint64_t)u * kTileBytes, kTileBytes, &S.full[slot]);
+            }
         } else {
             mbar_arrive(&S.full[slot]);  // read straight from global instead
         }
@@ -292,7 +308,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
                     st_stream_u32(o_nib + k * 128, o.nib);
                 }
             } else {
-                load_groups_global(p, wbase, lane, w, cnt);
+                load_groups_global<PAGED>(p, wbase, lane, w, cnt);
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     const uint64_t i0 = wbase + k * 256u + lane * 8u;
@@ -350,7 +366,8 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
 // MODE 0: codebook in the parameters, table coding; 1: in the parameters,
 // contiguous; 2: in device memory, checked (a bad one sets SZ_ERR_INVALID_ARG
 // in *status) and the coding chosen on the device.
-template <int MODE>
+// PAGED: the input is a paged tensor (EncodeParams::pm).
+template <int MODE, bool PAGED = false>
 __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_kernel(const EncodeParams p) {
     uint8_t cb[16];
     bool contig;
@@ -358,11 +375,11 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
     if (MODE == 2) {
         if (!ok && blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicMax(p.status, kStatusInvalid);
         if (contig)
-            encode_bf16_body<true>(p, cb);
+            encode_bf16_body<true, false>(p, cb);
         else
-            encode_bf16_body<false>(p, cb);
+            encode_bf16_body<false, false>(p, cb);
     } else {
-        encode_bf16_body<MODE == 1>(p, cb);
+        encode_bf16_body<MODE == 1, PAGED>(p, cb);
     }
 }
 
@@ -416,6 +433,8 @@ struct DecodeSmem {
 
 }  // namespace
 
+// PAGED: the output is a paged tensor (DecodeParams::pm).
+template <bool PAGED>
 __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
@@ -640,7 +659,9 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     uint32_t y[4];
                     decode_group(k, *reinterpret_cast<const uint2*>(ssm + k * 256),
                                  *reinterpret_cast<const uint32_t*>(snb + k * 128), y);
-                    st_stream_v4(o + k * 512, make_uint4(y[0], y[1], y[2], y[3]));
+                    // A group of 8 never straddles a page.
+                    uint8_t* dst = PAGED ? p.out + elem_offset<true>(p.pm, base + qt + k * 256u, 2, p.status) : o + k * 512;
+                    st_stream_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
                 }
             } else {
 #pragma unroll
@@ -663,15 +684,16 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     }
                     uint32_t y[4];
                     decode_group(k, smv, nibv, y);
+                    uint8_t* dst = p.out + (cnt ? elem_offset<PAGED>(p.pm, i0, 2, p.status) : 2 * i0);
                     if (p.vec && cnt == 8) {
-                        st_stream_v4(p.out + 2 * i0, make_uint4(y[0], y[1], y[2], y[3]));
+                        st_stream_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
                     } else {
 #pragma unroll
                         for (uint32_t jj = 0; jj < 8; jj++) {
                             if (jj < cnt) {
                                 const uint32_t v = y[jj >> 1] >> (16 * (jj & 1));
-                                p.out[2 * (i0 + jj)] = (uint8_t)v;
-                                p.out[2 * (i0 + jj) + 1] = (uint8_t)(v >> 8);
+                                dst[2 * jj] = (uint8_t)v;
+                                dst[2 * jj + 1] = (uint8_t)(v >> 8);
                             }
                         }
                     }
@@ -709,9 +731,10 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
 
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(EncodeSmem);
+    const bool paged = p.pm.ids != nullptr;  // host codebooks only
     const void* kern = p.cb_dev   ? (const void*)encode_bf16_kernel<2>
-                       : p.contig ? (const void*)encode_bf16_kernel<1>
-                                  : (const void*)encode_bf16_kernel<0>;
+                       : p.contig ? (paged ? (const void*)encode_bf16_kernel<1, true> : (const void*)encode_bf16_kernel<1>)
+                                  : (paged ? (const void*)encode_bf16_kernel<0, true> : (const void*)encode_bf16_kernel<0>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int dev = 0, sms = 0, per_sm = 0;
     if (err == cudaSuccess) err = cudaGetDevice(&dev);
@@ -728,15 +751,15 @@ cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
 
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(DecodeSmem);
-    cudaError_t err = cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = p.pm.ids ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int dev = 0, sms = 0, per_sm = 0;
     if (err == cudaSuccess) err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess)
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_bf16_kernel, kDecThreads, smem);
+    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem);
     if (err != cudaSuccess) return err;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
-    decode_bf16_kernel<<<grid, kDecThreads, smem, s>>>(p);
+    kern<<<grid, kDecThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -242,4 +242,25 @@ __device__ __forceinline__ bool load_codebook(const uint8_t (&param_cb)[16], con
     return ok;
 }
 
+// Byte offset of element e in a paged tensor (see PageMap), elements of
+// `esize` bytes.  An id outside the pool maps to page 0 (so that nothing
+// outside the pool is touched) and clears ok.
+__device__ __forceinline__ uint64_t paged_offset(const PageMap& m, uint64_t e, uint32_t esize, bool& ok) {
+    const int32_t id = m.ids[e >> m.lg];
+    ok = (uint32_t)id < m.pool_pages;
+    const uint64_t page = ok ? (uint64_t)(uint32_t)id : 0ull;
+    return ((page << m.lg) + (e & ((1ull << m.lg) - 1ull))) * esize;
+}
+
+// Byte offset of element e: linear, or through the page map.  A bad page id
+// raises SZ_ERR_INVALID_ARG in *status.
+template <bool PAGED>
+__device__ __forceinline__ uint64_t elem_offset(const PageMap& m, uint64_t e, uint32_t esize, int* status) {
+    if (!PAGED) return e * esize;
+    bool ok;
+    const uint64_t off = paged_offset(m, e, esize, ok);
+    if (!ok && status) atomicMax(status, kStatusInvalid);
+    return off;
+}
+
 }  // namespace sz

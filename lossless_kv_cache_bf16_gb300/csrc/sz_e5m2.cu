@@ -112,7 +112,7 @@ struct EncodeE5Smem {
     uint8_t field[256];         // byte -> field; 0x80 marks an escape
 };
 
-template <bool CONTIG>
+template <bool CONTIG, bool PAGED>
 __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const uint8_t (&cb)[16]) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
@@ -149,7 +149,9 @@ __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const ui
 #pragma unroll
         for (uint32_t i = 0; i < 8; i++) {
             const uint32_t piece = lane + 32 * i;
-            s_in[warp][swz8(piece >> 3, piece & 7u)] = ld_stream_v4(p.in + warp_base + 16 * piece);
+            // A 16-element piece never straddles a page.
+            s_in[warp][swz8(piece >> 3, piece & 7u)] =
+                ld_stream_v4(p.in + elem_offset<PAGED>(p.pm, warp_base + 16 * piece, 1, p.status));
         }
     } else {
         const uint32_t pad = (uint32_t)cb[0] << 2;
@@ -161,7 +163,8 @@ __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const ui
 #pragma unroll
                 for (uint32_t t = 0; t < 4; t++) {
                     const uint32_t j = 16 * s + 4 * q + t;
-                    v |= (j < cnt ? (uint32_t)p.in[thread_base + j] : pad) << (8 * t);
+                    v |= (j < cnt ? (uint32_t)p.in[elem_offset<PAGED>(p.pm, thread_base + j, 1, p.status)] : pad)
+                         << (8 * t);
                 }
                 w[q] = v;
             }
@@ -265,7 +268,8 @@ __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const ui
 // MODE 0: codebook in the parameters, table coding; 1: in the parameters,
 // contiguous; 2: in device memory, checked (a bad one sets SZ_ERR_INVALID_ARG
 // in *status) and the coding chosen on the device.
-template <int MODE>
+// PAGED: the input is a paged tensor (EncodeParams::pm).
+template <int MODE, bool PAGED = false>
 __global__ void __launch_bounds__(kEncThreads, MODE == 1 ? 4 : 3) encode_e5m2_kernel(const EncodeParams p) {
     uint8_t cb[16];
     bool contig;
@@ -274,11 +278,11 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 1 ? 4 : 3) encode_e5m2_ke
         if (!ok && blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicMax(p.status, kStatusInvalid);
         // A contiguous run must also stay within 5 bits for the byte-parallel coding.
         if (contig && cb[0] <= 16)
-            encode_e5m2_body<true>(p, cb);
+            encode_e5m2_body<true, false>(p, cb);
         else
-            encode_e5m2_body<false>(p, cb);
+            encode_e5m2_body<false, false>(p, cb);
     } else {
-        encode_e5m2_body<MODE == 1>(p, cb);
+        encode_e5m2_body<MODE == 1, PAGED>(p, cb);
     }
 }
 
@@ -389,6 +393,8 @@ __device__ __forceinline__ void decode_rows(const uint32_t (&pw)[14], uint32_t c
     for (uint32_t s = 0; s < 4; s++) rows[swz4(lane, s)] = make_uint4(y[4 * s], y[4 * s + 1], y[4 * s + 2], y[4 * s + 3]);
 }
 
+// PAGED: the output is a paged tensor (DecodeParams::pm).
+template <bool PAGED>
 __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeE5Smem& S = *reinterpret_cast<DecodeE5Smem*>(smem_raw);
@@ -616,15 +622,16 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
         // The warp's rows -> global memory.
         const uint64_t wbase = base + warp * (32u * kE5DecPer);
         if (p.vec && wbase + 32u * kE5DecPer <= n) {
-            uint8_t* o = p.out + wbase;
 #pragma unroll
             for (uint32_t r = 0; r < 4; r++) {
-                const uint32_t piece = lane + 32 * r;
-                st_stream_v4(o + 16 * piece, rows[swz4(piece >> 2, piece & 3u)]);
+                const uint32_t piece = lane + 32 * r;  // 16 elements: never straddles a page
+                st_stream_v4(p.out + elem_offset<PAGED>(p.pm, wbase + 16 * piece, 1, p.status),
+                             rows[swz4(piece >> 2, piece & 3u)]);
             }
         } else {
             const uint8_t* row = reinterpret_cast<const uint8_t*>(rows);
-            for (uint32_t b = 0; b < cnt; b++) p.out[thread_base + b] = row[swz4(lane, b >> 4) * 16u + (b & 15u)];
+            for (uint32_t b = 0; b < cnt; b++)
+                p.out[elem_offset<PAGED>(p.pm, thread_base + b, 1, p.status)] = row[swz4(lane, b >> 4) * 16u + (b & 15u)];
         }
         __syncwarp();  // the rows are rewritten by the next tile
     }
@@ -639,7 +646,10 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
 
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(EncodeE5Smem);
-    auto kern = p.cb_dev ? encode_e5m2_kernel<2> : p.contig ? encode_e5m2_kernel<1> : encode_e5m2_kernel<0>;
+    const bool paged = p.pm.ids != nullptr;  // host codebooks only
+    auto kern = p.cb_dev   ? encode_e5m2_kernel<2>
+                : p.contig ? (paged ? encode_e5m2_kernel<1, true> : encode_e5m2_kernel<1>)
+                           : (paged ? encode_e5m2_kernel<0, true> : encode_e5m2_kernel<0>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     kern<<<p.num_tiles, kEncThreads, smem, s>>>(p);
@@ -649,15 +659,15 @@ cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
 
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(DecodeE5Smem);
-    cudaError_t err = cudaFuncSetAttribute(decode_e5m2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = p.pm.ids ? decode_e5m2_kernel<true> : decode_e5m2_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int dev = 0, sms = 0, per_sm = 0;
     if (err == cudaSuccess) err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess)
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_e5m2_kernel, kE5DecThreads, smem);
+    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kE5DecThreads, smem);
     if (err != cudaSuccess) return err;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
-    decode_e5m2_kernel<<<grid, kE5DecThreads, smem, s>>>(p);
+    kern<<<grid, kE5DecThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -34,16 +34,18 @@ constexpr uint32_t kStageLoads = kStageBytes / 512;       // 16-byte loads per l
 static_assert(kStageBytes % 512 == 0, "whole warp-wide 16-byte loads");
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
 
-// Exponent of element i: bits 14..7 of a BF16, bits 6..2 of an E5M2 byte.
-template <bool BF16>
-__device__ __forceinline__ uint32_t exponent_at(const uint8_t* in, uint64_t i) {
-    if (BF16) return (((uint32_t)in[2 * i] | ((uint32_t)in[2 * i + 1] << 8)) >> 7) & 0xFFu;
-    return ((uint32_t)in[i] >> 2) & 0x1Fu;
+// Exponent of element i (linear or paged input): bits 14..7 of a BF16, bits
+// 6..2 of an E5M2 byte.
+template <bool BF16, bool PAGED>
+__device__ __forceinline__ uint32_t exponent_at(const EncodeParams& p, uint64_t i) {
+    const uint8_t* e = p.in + elem_offset<PAGED>(p.pm, i, BF16 ? 2u : 1u, p.status);
+    if (BF16) return (((uint32_t)e[0] | ((uint32_t)e[1] << 8)) >> 7) & 0xFFu;
+    return ((uint32_t)e[0] >> 2) & 0x1Fu;
 }
 
 }  // namespace
 
-template <bool BF16>
+template <bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams p) {
     __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 16];  // +16: realignment reads past the end
     __shared__ uint32_t s_sum[kFinWarps];
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
                     uint32_t m = 0;
 #pragma unroll
                     for (int jj = 0; jj < 8; jj++)
-                        if (i0 + jj < end && !s_member[exponent_at<BF16>(p.in, i0 + jj)]) m |= 1u << jj;
+                        if (i0 + jj < end && !s_member[exponent_at<BF16, PAGED>(p, i0 + jj)]) m |= 1u << jj;
                     const uint32_t c8 = __popc(m);
                     uint32_t x = c8;
 #pragma unroll
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
                         if (r + 3 <= p.capacity) {
                             p.out[r] = (uint8_t)pos;
                             p.out[r + 1] = (uint8_t)(pos >> 8);
-                            p.out[r + 2] = (uint8_t)exponent_at<BF16>(p.in, i0 + jj);
+                            p.out[r + 2] = (uint8_t)exponent_at<BF16, PAGED>(p, i0 + jj);
                         }
                         r += 3;
                     }
@@ -208,10 +210,13 @@ cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s) {
     // Several blocks per SM: the record copies are latency bound.
     const uint64_t want = (uint64_t)4 * sms;
     const uint32_t grid = (uint32_t)(p.num_tiles < want ? p.num_tiles : want);
+    const bool paged = p.pm.ids != nullptr;
     if (bf16)
-        finish_kernel<true><<<grid, kFinThreads, 0, s>>>(p);
+        paged ? finish_kernel<true, true><<<grid, kFinThreads, 0, s>>>(p)
+              : finish_kernel<true, false><<<grid, kFinThreads, 0, s>>>(p);
     else
-        finish_kernel<false><<<grid, kFinThreads, 0, s>>>(p);
+        paged ? finish_kernel<false, true><<<grid, kFinThreads, 0, s>>>(p)
+              : finish_kernel<false, false><<<grid, kFinThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -19,6 +19,15 @@ struct StreamLayout {
     uint32_t num_chunks;
 };
 
+// Paged tensor (a block table over a pool of equal pages): element e lives in
+// page ids[e >> lg] at offset e & (2^lg - 1); page q starts at byte
+// (q << lg) * element size of the pool.  ids == nullptr: contiguous tensor.
+struct PageMap {
+    const int32_t* ids;
+    uint32_t pool_pages;
+    uint32_t lg;
+};
+
 struct EncodeParams {
     StreamLayout L;
     const uint8_t* in;
@@ -36,6 +45,7 @@ struct EncodeParams {
     uint8_t* ws_rec;         // workspace: staged records, ws_cap per scan tile
     uint32_t ws_cap;         // records staged per scan tile
     const uint8_t* cb_dev;   // nullable: codebook in device memory instead of cb
+    PageMap pm;              // paged input (in = the pool) when pm.ids is set
     uint8_t cb[16];          // ascending
 };
 
@@ -48,6 +58,7 @@ struct DecodeParams {
     int* status;             // nullable
     int vec;
     uint64_t wait_limit_ns;  // bounded waits for in-kernel copies
+    PageMap pm;              // paged output (out = the pool) when pm.ids is set
 };
 
 struct HistogramParams {

@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
         "sz_calibrate_device": (i32, [i32, vp, sz, ctypes.c_uint32, vp, vp, vp]),
         "sz_encode_dcb": (i32, [i32, vp, vp, sz, vp, sz, vp, vp, vp, sz, vp]),
         "sz_ablation_sizes": (i32, [i32, u64p, sz, u64p]),
+        "sz_encode_paged": (i32, [i32, cbp, vp, sz, sz, vp, sz, vp, sz, vp, vp, vp, sz, vp]),
+        "sz_decode_paged": (i32, [i32, vp, sz, sz, vp, sz, sz, vp, vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -216,6 +218,40 @@ def sz_decode(dt: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, y: tor
         raise ValueError("output buffer too small")
     _check("sz_decode", LIB.sz_decode(dt, _dev_ptr(stream_bytes, "stream"), in_bytes, n, _dev_ptr(y, "y"),
                                       _dev_ptr(status, "status"), _stream(stream)))
+
+
+def _pool_pages(dt: int, pool: torch.Tensor, page_elems: int) -> int:
+    page_bytes = page_elems * ELEMENT_BYTES[dt]
+    return (pool.numel() * pool.element_size()) // page_bytes if page_bytes else 0
+
+
+def sz_encode_paged(dt: int, cb, pool: torch.Tensor, page_elems: int, block_ids: torch.Tensor, n: int,
+                    out: torch.Tensor, out_bytes: torch.Tensor, status: torch.Tensor | None, ws: torch.Tensor,
+                    stream=None) -> None:
+    """Encode the n-element tensor whose element e is element e % page_elems
+    of page block_ids[e // page_elems] of `pool` (pages of page_elems)."""
+    if block_ids.dtype != torch.int32:
+        raise ValueError("block_ids must be int32")
+    c = _codebook(cb)
+    _check("sz_encode_paged",
+           LIB.sz_encode_paged(dt, ctypes.byref(c), _dev_ptr(pool, "pool"), _pool_pages(dt, pool, page_elems),
+                               page_elems, _dev_ptr(block_ids, "block_ids"), n, _dev_ptr(out, "out"),
+                               out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                               _dev_ptr(status, "status"), _dev_ptr(ws, "ws"), ws.numel() * ws.element_size(),
+                               _stream(stream)))
+
+
+def sz_decode_paged(dt: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, pool: torch.Tensor, page_elems: int,
+                    block_ids: torch.Tensor, status: torch.Tensor | None, stream=None) -> None:
+    """Decode into the pages of `pool` that block_ids names (see sz_encode_paged)."""
+    if block_ids.dtype != torch.int32:
+        raise ValueError("block_ids must be int32")
+    if in_bytes > stream_bytes.numel() * stream_bytes.element_size():
+        raise ValueError("in_bytes exceeds the stream buffer")
+    _check("sz_decode_paged",
+           LIB.sz_decode_paged(dt, _dev_ptr(stream_bytes, "stream"), in_bytes, n, _dev_ptr(pool, "pool"),
+                               _pool_pages(dt, pool, page_elems), page_elems, _dev_ptr(block_ids, "block_ids"),
+                               _dev_ptr(status, "status"), _stream(stream)))
 
 
 def sz_encode_noalloc(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
