@@ -63,6 +63,7 @@ struct EncodeSmem {
     alignas(128) uint8_t in[kEncStages][kTileBytes];
     uint64_t full[kEncStages];        // TMA -> compute: sub-tile landed
     alignas(16) uint32_t warp_esc[2][kWarps];
+    alignas(16) uint8_t rec[3 * kMaxStageRecs];  // the scan tile's staged records
     uint8_t code[256];                // exponent -> code; 0x10 marks an escape
 };
 
@@ -281,7 +282,6 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
     for (uint32_t ks = 0; ks < my_scans && !aborted; ks++) {
         const uint32_t st = scan_of(ks);
         const uint32_t subs = subs_in(st);
-        uint8_t* rec = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
         uint32_t run = 0;  // escapes so far in this scan tile
         for (uint32_t part = 0; part < subs; part++, i++) {
             const uint32_t slot = i % kEncStages;
@@ -347,12 +347,25 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
                 }
             }
             // Records beyond ws_cap are not staged; the finish kernel re-derives
-            // that scan tile's records from the input.
+            // that scan tile's records from the input.  They are gathered in
+            // shared memory and leave once per scan tile, in 16-byte stores.
             if (warp_total && run + warp_off < p.ws_cap)
-                emit_records(wbase, lane, w, esc, off, run + warp_off, rec, 3ull * p.ws_cap);
+                emit_records(wbase, lane, w, esc, off, run + warp_off, S.rec, 3ull * p.ws_cap);
             run += sub_esc;
         }
-        if (!aborted && tid == 0) p.ws_count[st] = run;
+        if (aborted) break;  // block-uniform
+        if (tid == 0) p.ws_count[st] = run;
+        __syncthreads();  // every record of the scan tile is in S.rec
+        {
+            // The workspace region (3 ws_cap bytes, a multiple of 16) starts
+            // 16-byte aligned, so whole 16-byte pieces stay inside it.
+            const uint32_t nbytes = 3 * min(run, p.ws_cap);
+            uint8_t* dst = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
+            for (uint32_t b = 16 * tid; b < nbytes; b += 16 * kComputeThreads)
+                *reinterpret_cast<uint4*>(dst + b) = *reinterpret_cast<const uint4*>(S.rec + b);
+        }
+        // The next scan tile writes S.rec only after its first sub-tile's
+        // barrier, which every thread reaches after this copy.
     }
     if (aborted && tid == 0) {
         if (p.status) atomicMax(p.status, kStatusTimeout);

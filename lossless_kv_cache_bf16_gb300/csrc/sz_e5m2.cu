@@ -108,6 +108,7 @@ __device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t add,
 // ---------------------------------------------------------------------------
 struct EncodeE5Smem {
     uint4 buf[kEncWarps][256];  // input: 8 swizzled pieces per thread; then output: 7 pieces per thread
+    alignas(16) uint8_t rec[3 * kMaxStageRecs];  // the scan tile's staged records
     uint32_t warp_esc[kEncWarps];
     uint8_t field[256];         // byte -> field; 0x80 marks an escape
 };
@@ -221,9 +222,10 @@ __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const ui
     if (tid == 0) p.ws_count[st] = tile_esc;
     // Stage this thread's records (those ranked below ws_cap); the exponents
     // come from the thread's input row, still in shared memory.
+    // They are gathered in shared memory and leave in 16-byte stores.
     if (mine && rank < p.ws_cap) {
         const uint8_t* row = reinterpret_cast<const uint8_t*>(&s_in[warp][0]);
-        uint8_t* dst = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
+        uint8_t* dst = S.rec;
         const uint64_t limit = 3ull * p.ws_cap;
         uint64_t at = 3ull * rank;
 #pragma unroll
@@ -242,6 +244,16 @@ __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const ui
                 at += 3;
             }
         }
+    }
+
+    __syncthreads();  // every record of the scan tile is in S.rec
+    {
+        // The workspace region (3 ws_cap bytes, a multiple of 16) starts
+        // 16-byte aligned, so whole 16-byte pieces stay inside it.
+        const uint32_t nbytes = 3 * min(tile_esc, p.ws_cap);
+        uint8_t* dst = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
+        for (uint32_t b = 16 * tid; b < nbytes; b += 16 * kEncThreads)
+            *reinterpret_cast<uint4*>(dst + b) = *reinterpret_cast<const uint4*>(S.rec + b);
     }
 
     // Every row of the warp has been read: the buffer takes the output.
