@@ -71,13 +71,6 @@ struct GroupOut {
     uint32_t sm_lo, sm_hi, nib, esc;
 };
 
-// Exponent of element j (0..7) of a group from its four BF16-pair words.
-__device__ __forceinline__ uint32_t group_exponent(const uint32_t (&w)[4], uint32_t j) {
-    const uint32_t lo = (j & 2) ? w[1] : w[0], hi = (j & 2) ? w[3] : w[2];
-    const uint32_t word = (j & 4) ? hi : lo;
-    return (word >> (7 + 16 * (j & 1))) & 0xFFu;
-}
-
 // Split and code one group of 8 elements (four 32-bit words of BF16 pairs).
 // The low bytes (exponent bit 0 | mantissa) and high bytes (sign | exponent
 // bits 7..1) of four elements are gathered with byte permutes; the
@@ -194,24 +187,35 @@ __device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64
 
 // Writes the records of lane's escapes among one warp's 1,024 elements
 // starting at element `base`: record index first + off[k] + rank in group.
+// One loop over all of the lane's escape bits (group k = bit / 8), so the
+// warp iterates as often as its busiest lane has escapes, not once per group.
 __device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const uint32_t (&w)[4][4],
                                              const uint32_t (&esc)[4], const uint32_t (&off)[4], uint64_t first,
                                              uint8_t* dst, uint64_t limit) {
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        uint32_t msk = esc[k];
-        const uint32_t pos0 = (uint32_t)(base + k * 256u + lane * 8u) & 0xFFFFu;
-        uint64_t at = 3ull * (first + off[k]);
-        while (msk) {  // only the set bits; usually one iteration
-            const uint32_t jj = __ffs(msk) - 1;
-            msk &= msk - 1;
-            const uint32_t pos = pos0 + jj;  // a group never straddles a chunk
-            if (at + 3 <= limit) {
-                dst[at] = (uint8_t)pos;
-                dst[at + 1] = (uint8_t)(pos >> 8);
-                dst[at + 2] = (uint8_t)group_exponent(w[k], jj);
-            }
-            at += 3;
+    const uint32_t all = esc[0] | (esc[1] << 8) | (esc[2] << 16) | (esc[3] << 24);
+    uint32_t m = all;
+    const uint32_t pos_base = (uint32_t)(base + lane * 8u) & 0xFFFFu;  // a warp never straddles a chunk
+    while (m) {
+        const uint32_t b = __ffs(m) - 1;
+        m &= m - 1;
+        const uint32_t k = b >> 3, jj = b & 7u;
+        const uint32_t offk = k < 2 ? (k == 0 ? off[0] : off[1]) : (k == 2 ? off[2] : off[3]);
+        const uint32_t before = __popc(all & ((1u << b) - 1u) & (0xFFu << (8 * k)));  // earlier in the group
+        // Exponent of element jj of group k: bits 7..14 of its 16-bit half.
+        const uint32_t q = jj >> 1;
+        uint32_t g0, g1, g2, g3;
+        g0 = q < 2 ? (q == 0 ? w[0][0] : w[0][1]) : (q == 2 ? w[0][2] : w[0][3]);
+        g1 = q < 2 ? (q == 0 ? w[1][0] : w[1][1]) : (q == 2 ? w[1][2] : w[1][3]);
+        g2 = q < 2 ? (q == 0 ? w[2][0] : w[2][1]) : (q == 2 ? w[2][2] : w[2][3]);
+        g3 = q < 2 ? (q == 0 ? w[3][0] : w[3][1]) : (q == 2 ? w[3][2] : w[3][3]);
+        const uint32_t word = k < 2 ? (k == 0 ? g0 : g1) : (k == 2 ? g2 : g3);
+        const uint32_t e = (word >> (7 + 16 * (jj & 1u))) & 0xFFu;
+        const uint32_t pos = pos_base + k * 256u + jj;
+        const uint64_t at = 3ull * (first + offk + before);
+        if (at + 3 <= limit) {
+            dst[at] = (uint8_t)pos;
+            dst[at + 1] = (uint8_t)(pos >> 8);
+            dst[at + 2] = (uint8_t)e;
         }
     }
 }
