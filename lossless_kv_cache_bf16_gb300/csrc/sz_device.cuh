@@ -1,6 +1,7 @@
 // sz_device.cuh -- device-side building blocks shared by the SplitZip kernels:
 // streaming loads/stores, the global timer for bounded waits, little-endian
-// helpers, and the decoders' per-tile escape search and validation.
+// helpers, the decoders' block search for where a range's escape records
+// start, the encoders' codebook loader, and paged-tensor addressing.
 #pragma once
 
 #include <cstdint>
@@ -132,89 +133,6 @@ __device__ void block_lower_bounds(const uint8_t* rec, uint32_t o, uint32_t m, u
 }  // namespace sz
 
 namespace sz {
-
-// Decode side: the escape records that fall in one tile.
-//
-// Checks the tile's chunk header against the stream (count fits the chunk,
-// offset + count within the E records the stream size implies; the first
-// tile of a chunk also checks that offsets are the running sum of counts and
-// that the last chunk ends at E), finds the tile's run [r0, r1) of the chunk's
-// sorted records, and calls apply(q, exponent) for every record of the run
-// whose position lies in the tile (q = element index inside the tile) and is
-// above the previous position of its chunk.  Any failed check sets *s_bad.
-// The runs of a chunk's tiles meet exactly (same search, same keys), so every
-// record of a valid stream is applied once and every record of a corrupt one
-// is checked once.  For E5M2 an exponent must also fit in 5 bits.
-//
-// Must be called by all THREADS threads; ends with a block barrier, so what
-// apply() wrote to shared memory is visible afterwards.  *s_bad must be
-// initialised (and a barrier passed) before the call.
-template <uint32_t THREADS, uint32_t TILE, bool FP8, typename Apply>
-__device__ void for_each_tile_escape(const DecodeParams& p, uint32_t tile, uint32_t* s_scratch, int* s_bad,
-                                     Apply apply) {
-    constexpr uint32_t kTilesPerChunk = kChunk / TILE;
-    static_assert(kChunk % TILE == 0, "tiles must not straddle chunks");
-    const uint32_t tid = threadIdx.x;
-    const uint64_t n = p.L.n;
-    const uint64_t base = (uint64_t)tile * TILE;
-    const uint32_t chunk = tile / kTilesPerChunk;
-    const uint32_t p0 = (tile % kTilesPerChunk) * TILE;
-    const uint32_t tile_len = base >= n ? 0u : (n - base >= TILE ? TILE : (uint32_t)(n - base));
-    const uint8_t* rec = p.in + p.L.rec_off;
-
-    if (tid == 0) {
-        uint32_t o = 0, m = 0;
-        if (p.L.num_chunks > 0) {
-            const uint8_t* h = p.in + p.L.hdr_off + 8ull * chunk;
-            o = load_u32_le(h);
-            m = load_u32_le(h + 4);
-            const uint64_t rest = n - (uint64_t)chunk * kChunk;
-            const uint64_t chunk_len = rest < kChunk ? rest : kChunk;
-            bool bad = m > chunk_len || o > p.n_esc || m > p.n_esc - o;
-            if (tile % kTilesPerChunk == 0) {
-                if (chunk == 0) {
-                    bad |= o != 0;
-                } else {
-                    const uint64_t po = load_u32_le(h - 8), pm = load_u32_le(h - 4);
-                    bad |= (uint64_t)o != po + pm;
-                }
-                if (chunk == p.L.num_chunks - 1) bad |= (uint64_t)o + m != p.n_esc;
-            }
-            if (bad) *s_bad = 1, m = 0;
-        }
-        s_scratch[4] = o;
-        s_scratch[5] = m;
-    }
-    __syncthreads();
-    const uint32_t o = s_scratch[4], m = s_scratch[5];
-    if (m == 0) return;  // block-uniform
-
-    const bool first_in_chunk = tile % kTilesPerChunk == 0;
-    const bool last_in_chunk = tile % kTilesPerChunk == kTilesPerChunk - 1 || tile == p.num_tiles - 1;
-    uint32_t r0 = o, r1 = o + m;
-    if (!(first_in_chunk && last_in_chunk)) {
-        uint32_t a, b;
-        block_lower_bounds<THREADS>(rec, o, m, p0, p0 + TILE, s_scratch, &a, &b);
-        if (!first_in_chunk) r0 = a;
-        if (!last_in_chunk) r1 = b;
-    }
-    if (r1 < r0) {
-        if (tid == 0) *s_bad = 1;
-    } else {
-        for (uint32_t j = r0 + tid; j < r1; j += THREADS) {
-            const uint32_t pos = rec_pos(rec, j);
-            const uint32_t e = rec[3ull * j + 2];
-            const bool in_tile = pos >= p0 && pos - p0 < tile_len;
-            const bool ordered = j == o || pos > rec_pos(rec, j - 1);
-            if (!in_tile || !ordered || (FP8 && e >= 32)) {
-                *s_bad = 1;
-                continue;
-            }
-            apply(pos - p0, e);
-        }
-    }
-    __syncthreads();
-}
 
 // The codebook of an encode in registers: the 16 bytes of the parameters, or,
 // when cb_dev is set, 16 bytes of device memory (16-byte aligned) that are

@@ -73,9 +73,8 @@ struct HistogramParams {
 constexpr uint32_t kBf16Threads = 256;
 constexpr uint32_t kBf16PerThread = 32;
 constexpr uint32_t kBf16Tile = kBf16Threads * kBf16PerThread;   // 8192
-constexpr uint32_t kE5Threads = 128;                            // E5M2 decode block
-constexpr uint32_t kE5PerThread = 128;                          // 16 groups of 8
-constexpr uint32_t kE5Tile = kE5Threads * kE5PerThread;         // 16384: E5M2 decode tile
+constexpr uint32_t kE5PerThread = 128;                          // E5M2 encode: 16 groups of 8 per thread
+constexpr uint32_t kE5Tile = 16384;                             // E5M2 decode tile
 // Encode (both dtypes): escape counts and staged records per scan tile.
 constexpr uint32_t kScanTile = 32768;
 // Most records staged per scan tile (EncodeParams::ws_cap <= this, and a

@@ -64,22 +64,4 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  : "memory");
 }
 
-// Named barrier over the first `threads` threads of the block (id != 0).
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Named barrier that also ORs a predicate over the participating threads, so
-// that every thread takes the same decision (e.g. to abort after a timeout).
-__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t threads, bool pred) {
-    uint32_t out;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, %2, %3, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(out)
-        : "r"((uint32_t)pred), "r"(id), "r"(threads)
-        : "memory");
-    return out != 0;
-}
-
 }  // namespace sz
