@@ -6,6 +6,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "splitzip.h"
 #include "sz_params.h"
 
@@ -14,6 +16,15 @@ namespace {
 using namespace sz;
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded inter-block waits: 1 s
+
+// An NVTX range around a public call, so that profilers can attribute the
+// kernels it launches (free when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool dtype_ok(int dt) { return dt == SZ_BF16 || dt == SZ_FP8_E5M2; }
 uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
@@ -179,6 +190,7 @@ size_t sz_histogram_bins(sz_dtype dt) {
 
 sz_status sz_histogram(sz_dtype dt, const void* d_sample, size_t n, unsigned long long* d_hist,
                        cudaStream_t stream) {
+    const NvtxRange range("sz_histogram");
     if (!dtype_ok(dt) || !d_hist || (n > 0 && !d_sample)) return SZ_ERR_INVALID_ARG;
     if (dt == SZ_BF16 && !aligned(d_sample, 2)) return SZ_ERR_INVALID_ARG;
     if (!aligned(d_hist, 8)) return SZ_ERR_INVALID_ARG;
@@ -191,12 +203,14 @@ sz_status sz_histogram(sz_dtype dt, const void* d_sample, size_t n, unsigned lon
 
 sz_status sz_codebook_from_histogram_device(sz_dtype dt, const unsigned long long* d_hist, uint8_t* d_cb,
                                             cudaStream_t stream) {
+    const NvtxRange range("sz_codebook_from_histogram_device");
     if (!dtype_ok(dt) || !d_hist || !d_cb || !aligned(d_hist, 8) || !aligned(d_cb, 16)) return SZ_ERR_INVALID_ARG;
     return from_cuda(launch_select(d_hist, (uint32_t)sz_histogram_bins(dt), d_cb, stream));
 }
 
 sz_status sz_calibrate_device(sz_dtype dt, const void* d_x, size_t n, uint32_t sample_stride,
                               unsigned long long* d_hist, uint8_t* d_cb, cudaStream_t stream) {
+    const NvtxRange range("sz_calibrate_device");
     if (!dtype_ok(dt) || !d_hist || !d_cb || (n > 0 && !d_x) || sample_stride == 0) return SZ_ERR_INVALID_ARG;
     if (dt == SZ_BF16 && !aligned(d_x, 2)) return SZ_ERR_INVALID_ARG;
     if (!aligned(d_hist, 8) || !aligned(d_cb, 16)) return SZ_ERR_INVALID_ARG;
@@ -243,6 +257,7 @@ sz_status sz_ablation_sizes(sz_dtype dt, const unsigned long long* h_hist, size_
 
 sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n, unsigned long long* d_hist, sz_codebook* h_cb,
                        cudaStream_t stream) {
+    const NvtxRange range("sz_calibrate");
     if (!h_cb) return SZ_ERR_INVALID_ARG;
     sz_status st = sz_histogram(dt, d_sample, n, d_hist, stream);
     if (st != SZ_OK) return st;
@@ -257,6 +272,7 @@ sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n, unsigned lon
 sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                     size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws, size_t ws_bytes,
                     cudaStream_t stream) {
+    const NvtxRange range("sz_encode");
     return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
                        kWaitLimitNs, stream);
 }
@@ -264,6 +280,7 @@ sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size
 sz_status sz_encode_dcb(sz_dtype dt, const uint8_t* d_cb, const void* d_in, size_t n, void* d_out,
                         size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
                         size_t ws_bytes, cudaStream_t stream) {
+    const NvtxRange range("sz_encode_dcb");
     if (!d_cb) return SZ_ERR_INVALID_ARG;
     return encode_impl(dt, nullptr, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
                        kWaitLimitNs, stream, kStageRecs, d_cb);
@@ -271,6 +288,7 @@ sz_status sz_encode_dcb(sz_dtype dt, const uint8_t* d_cb, const void* d_in, size
 
 sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                             size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, cudaStream_t stream) {
+    const NvtxRange range("sz_encode_noalloc");
     if (!dtype_ok(dt)) return SZ_ERR_INVALID_ARG;
     if ((uint64_t)n > kNoAllocMaxElems || workspace_bytes(n, kNoAllocStageRecs) > kNoAllocScratchBytes)
         return SZ_ERR_CAPACITY;  // beyond the static scratch
@@ -340,6 +358,7 @@ bool page_map_for(const void* d_pool, size_t pool_pages, size_t page_elems, cons
 
 sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_out, int* d_status,
                     cudaStream_t stream) {
+    const NvtxRange range("sz_decode");
     return decode_impl(dt, d_in, in_bytes, n, d_out, d_status, stream, PageMap{});
 }
 
@@ -347,6 +366,7 @@ sz_status sz_encode_paged(sz_dtype dt, const sz_codebook* h_cb, const void* d_po
                           size_t page_elems, const int32_t* d_block_ids, size_t n, void* d_out, size_t out_capacity,
                           unsigned long long* d_out_bytes, int* d_status, void* d_ws, size_t ws_bytes,
                           cudaStream_t stream) {
+    const NvtxRange range("sz_encode_paged");
     PageMap pm{};
     if (!page_map_for(d_pool, pool_pages, page_elems, d_block_ids, n, &pm)) return SZ_ERR_INVALID_ARG;
     if (n > 0 && cdiv(n, page_elems) > (1ull << 31)) return SZ_ERR_INVALID_ARG;
@@ -356,6 +376,7 @@ sz_status sz_encode_paged(sz_dtype dt, const sz_codebook* h_cb, const void* d_po
 
 sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_pool, size_t pool_pages,
                           size_t page_elems, const int32_t* d_block_ids, int* d_status, cudaStream_t stream) {
+    const NvtxRange range("sz_decode_paged");
     PageMap pm{};
     if (!page_map_for(d_pool, pool_pages, page_elems, d_block_ids, n, &pm)) return SZ_ERR_INVALID_ARG;
     return decode_impl(dt, d_in, in_bytes, n, d_pool, d_status, stream, pm);
