@@ -32,6 +32,9 @@ CORRUPT = 4
 
 CHUNK = 65536
 
+ABL_TOP8 = 1       # ablation codecs (BF16): Top-8 with 3-bit codes
+ABL_SENTINEL = 2   # Top-15 codes with 15 as an escape sentinel
+
 
 def _digest(source_text: str, flags) -> str:
     h = hashlib.sha256()
@@ -96,6 +99,10 @@ class Oracle:
             "orc_validate": (i32, [i32, vp, u64, u64, ctypes.POINTER(u64)]),
             "orc_decode": (i32, [i32, vp, u64, u64, vp]),
             "orc_ablation_sizes": (i32, [i32, vp, u64, vp]),
+            "orc_abl_size": (u64, [i32, u64, u64]),
+            "orc_abl_codebook": (i32, [i32, vp, vp]),
+            "orc_abl_encode": (i32, [i32, vp, vp, u64, vp, u64, ctypes.POINTER(u64)]),
+            "orc_abl_decode": (i32, [i32, vp, u64, u64, vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -184,6 +191,37 @@ class Oracle:
         out = np.zeros(3, dtype=np.uint64)
         self.lib.orc_ablation_sizes(dt, _ptr(h), n, _ptr(out))
         return int(out[0]), int(out[1]), int(out[2])
+
+
+    # -- ablation codecs (BF16): ABL_TOP8, ABL_SENTINEL ------------------------
+    def abl_size(self, variant: int, n: int, n_escapes: int) -> int:
+        return int(self.lib.orc_abl_size(variant, n, n_escapes))
+
+    def abl_codebook(self, variant: int, hist: np.ndarray) -> np.ndarray:
+        h = np.ascontiguousarray(hist, dtype=np.uint64)
+        assert h.size == 256
+        cb = np.zeros(8 if variant == ABL_TOP8 else 15, dtype=np.uint8)
+        assert self.lib.orc_abl_codebook(variant, _ptr(h), _ptr(cb)) == OK
+        return cb
+
+    def abl_encode(self, variant: int, cb, x: np.ndarray) -> np.ndarray:
+        c = np.ascontiguousarray(cb, dtype=np.uint8)
+        xb = _u8(x)
+        n = xb.size // 2
+        size = ctypes.c_uint64(0)
+        st = self.lib.orc_abl_encode(variant, _ptr(c), _ptr(xb), n, None, 0, ctypes.byref(size))
+        if st not in (OK, CAPACITY):
+            raise ValueError(f"ablation encode failed ({st})")
+        out = np.empty(max(size.value, 1), dtype=np.uint8)
+        st = self.lib.orc_abl_encode(variant, _ptr(c), _ptr(xb), n, _ptr(out), out.size, ctypes.byref(size))
+        assert st == OK
+        return out[: size.value]
+
+    def abl_decode(self, variant: int, stream: np.ndarray, n: int):
+        s = _u8(stream)
+        y = np.zeros(max(2 * n, 1), dtype=np.uint8)
+        st = self.lib.orc_abl_decode(variant, _ptr(s), s.size, n, _ptr(y))
+        return int(st), y[: 2 * n]
 
 
 _DEFAULT: Oracle | None = None

@@ -53,6 +53,11 @@
  *      stores only its exponent byte, in element order; the codebook takes
  *      15 bytes; the chunk headers stay (they give each chunk's first escape).
  *  A3  top-k selection follows R4 with k in place of 16.
+ *  A4  as full codecs (orc_abl_*): Top-8 puts element j of group g at bits
+ *      3j..3j+2 of the 24-bit little-endian word at byte 3g; the sentinel's
+ *      escape exponent is the next byte of its chunk's run; both decoders
+ *      check what keeps them in bounds (closed-form size, running-sum
+ *      headers, Top-8 record positions as R11, sentinel counts per chunk).
  */
 #include <stddef.h>
 #include <stdint.h>
@@ -69,6 +74,8 @@
 #define ORC_CHUNK 65536u   /* a u16 position addresses 65,536 elements [MET] */
 #define ORC_CB 16          /* top-16 codebook, 4-bit codes [MET] */
 #define ORC_NO_CODE 0xFFu
+#define ORC_ABL_TOP8 1
+#define ORC_ABL_SENTINEL 2
 
 static uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 
@@ -399,5 +406,182 @@ int orc_ablation_sizes(int dt, const uint64_t *hist, uint64_t n, uint64_t *sizes
     sizes[0] = orc_encoded_size(dt, n, e16);
     sizes[1] = dense8 + 3 * e8 + 8 + 8 * chunks;
     sizes[2] = orc_dense_bytes(dt, n) + e15 + 15 + 8 * chunks;
+    return ORC_OK;
+}
+
+/* ---- ablation codecs (BF16; readings A1, A2, A4) -------------------------- */
+
+/* The two alternative designs of the ablation as full codecs, so that their
+ * decoding can be compared, not just their sizes.  Variant ORC_ABL_TOP8 (A1):
+ * [sm N][codes 3 ceil(N/8)][codebook 8][headers 8C][records 3E]; element j of
+ * group g has its 3-bit code at bits 3j..3j+2 of the 24-bit little-endian
+ * word at byte 3g, an escape gets code 0 and an R6 record.  Variant
+ * ORC_ABL_SENTINEL (A2): [sm N][nibbles ceil(N/2)][codebook 15][headers 8C]
+ * [exponent bytes E]; code 15 marks an escape, whose exponent is the next
+ * byte of its chunk's run (headers as R7).  Codes follow ascending exponent
+ * order (R3).  A4: the decoders check the closed-form size, the headers as
+ * running sums, and (Top-8) the record positions as R11 or (sentinel) that
+ * each chunk holds as many sentinels as its header counts. */
+
+static int abl_k(int variant) { return variant == ORC_ABL_TOP8 ? 8 : 15; }
+
+uint64_t orc_abl_size(int variant, uint64_t n, uint64_t n_escapes) {
+    uint64_t chunks = orc_num_chunks(n);
+    if (variant == ORC_ABL_TOP8) return n + 3 * ceil_div(n, 8) + 8 + 8 * chunks + 3 * n_escapes;
+    return n + ceil_div(n, 2) + 15 + 8 * chunks + n_escapes;
+}
+
+/* The k most frequent exponents (A3), ascending. */
+int orc_abl_codebook(int variant, const uint64_t *hist, uint8_t *cb) {
+    int taken[256];
+    if (variant != ORC_ABL_TOP8 && variant != ORC_ABL_SENTINEL) return ORC_INVALID_ARG;
+    pick_most_frequent(ORC_BF16, hist, abl_k(variant), taken);
+    int k = 0;
+    for (int e = 0; e < 256; e++)
+        if (taken[e]) cb[k++] = (uint8_t)e;
+    return ORC_OK;
+}
+
+int orc_abl_encode(int variant, const uint8_t *cb, const uint8_t *x, uint64_t n,
+                   uint8_t *out, uint64_t capacity, uint64_t *out_bytes) {
+    if (variant != ORC_ABL_TOP8 && variant != ORC_ABL_SENTINEL) return ORC_INVALID_ARG;
+    if (n >= ((uint64_t)1 << 32)) return ORC_INVALID_ARG;
+    int k = abl_k(variant);
+    uint8_t inv[256];
+    for (int e = 0; e < 256; e++) inv[e] = ORC_NO_CODE;
+    for (int c = 0; c < k; c++) {
+        if (inv[cb[c]] != ORC_NO_CODE) return ORC_INVALID_ARG;
+        inv[cb[c]] = (uint8_t)c;
+    }
+    uint64_t n_esc = 0;
+    for (uint64_t i = 0; i < n; i++)
+        if (inv[exponent_at(ORC_BF16, x, i)] == ORC_NO_CODE) n_esc++;
+    uint64_t size = orc_abl_size(variant, n, n_esc);
+    *out_bytes = size;
+    if (size > capacity) return ORC_CAPACITY;
+
+    uint64_t chunks = orc_num_chunks(n);
+    uint64_t dense = variant == ORC_ABL_TOP8 ? n + 3 * ceil_div(n, 8) : n + ceil_div(n, 2);
+    uint8_t *codes = out + n;
+    uint8_t *cb_out = out + dense;
+    uint8_t *hdr = cb_out + k;
+    uint8_t *esc = hdr + 8 * chunks;
+    memset(out, 0, dense);
+
+    uint64_t j = 0; /* escapes so far */
+    for (uint64_t i = 0; i < n; i++) {
+        unsigned v = bf16_at(x, i);
+        unsigned e = (v >> 7) & 0xFFu;
+        unsigned code = inv[e];
+        out[i] = (uint8_t)((((v >> 15) & 1u) << 7) | (v & 0x7Fu)); /* R1 */
+        if (variant == ORC_ABL_TOP8) {
+            if (code == ORC_NO_CODE) {
+                put_u16(esc + 3 * j, (unsigned)(i % ORC_CHUNK));
+                esc[3 * j + 2] = (uint8_t)e;
+                j++;
+                code = 0u; /* A1: an escape keeps code 0 */
+            }
+            /* 3-bit code j of group g: bits 3j..3j+2 of the 24-bit word. */
+            unsigned bit = 3 * (unsigned)(i % 8);
+            uint64_t g = i / 8;
+            for (unsigned b = 0; b < 3; b++) {
+                unsigned lo = 8 * b;
+                if (bit + 3 <= lo || bit >= lo + 8) continue;
+                if (bit >= lo)
+                    codes[3 * g + b] |= (uint8_t)((code << (bit - lo)) & 0xFFu);
+                else
+                    codes[3 * g + b] |= (uint8_t)((code >> (lo - bit)) & 0xFFu);
+            }
+        } else {
+            if (code == ORC_NO_CODE) {
+                esc[j++] = (uint8_t)e;
+                code = 15;
+            }
+            codes[i / 2] |= (uint8_t)(code << (4 * (i % 2))); /* R2 */
+        }
+    }
+    memcpy(cb_out, cb, (size_t)k);
+    uint64_t before = 0; /* escapes in earlier chunks */
+    for (uint64_t c = 0; c < chunks; c++) {
+        uint64_t lo = c * ORC_CHUNK;
+        uint64_t hi = lo + ORC_CHUNK < n ? lo + ORC_CHUNK : n;
+        uint64_t in_chunk = 0;
+        for (uint64_t i = lo; i < hi; i++)
+            if (inv[exponent_at(ORC_BF16, x, i)] == ORC_NO_CODE) in_chunk++;
+        put_u32(hdr + 8 * c, before);
+        put_u32(hdr + 8 * c + 4, in_chunk);
+        before += in_chunk;
+    }
+    return ORC_OK;
+}
+
+int orc_abl_decode(int variant, const uint8_t *in, uint64_t in_bytes, uint64_t n, uint8_t *y) {
+    if (variant != ORC_ABL_TOP8 && variant != ORC_ABL_SENTINEL) return ORC_INVALID_ARG;
+    if (n >= ((uint64_t)1 << 32)) return ORC_INVALID_ARG;
+    int k = abl_k(variant);
+    uint64_t fixed = orc_abl_size(variant, n, 0);
+    unsigned per_escape = variant == ORC_ABL_TOP8 ? 3u : 1u;
+    if (in_bytes < fixed || (in_bytes - fixed) % per_escape != 0) return ORC_CORRUPT;
+    uint64_t n_esc = (in_bytes - fixed) / per_escape;
+    uint64_t chunks = orc_num_chunks(n);
+    uint64_t dense = variant == ORC_ABL_TOP8 ? n + 3 * ceil_div(n, 8) : n + ceil_div(n, 2);
+    const uint8_t *codes = in + n;
+    const uint8_t *cb = in + dense;
+    const uint8_t *hdr = cb + k;
+    const uint8_t *esc = hdr + 8 * chunks;
+
+    /* Headers: a running sum that ends at E; each count fits its chunk. */
+    uint64_t running = 0;
+    for (uint64_t c = 0; c < chunks; c++) {
+        uint64_t offset = get_u32(hdr + 8 * c), count = get_u32(hdr + 8 * c + 4);
+        uint64_t lo = c * ORC_CHUNK;
+        uint64_t len = (lo + ORC_CHUNK < n ? lo + ORC_CHUNK : n) - lo;
+        if (offset != running || count > len || running + count > n_esc) return ORC_CORRUPT;
+        if (variant == ORC_ABL_TOP8) {
+            for (uint64_t q = 0; q < count; q++) {
+                unsigned pos = get_u16(esc + 3 * (offset + q));
+                if (pos >= len || (q > 0 && pos <= get_u16(esc + 3 * (offset + q - 1)))) return ORC_CORRUPT;
+            }
+        } else {
+            uint64_t sentinels = 0;
+            for (uint64_t i = lo; i < lo + len; i++)
+                if (((codes[i / 2] >> (4 * (i % 2))) & 0xFu) == 15u) sentinels++;
+            if (sentinels != count) return ORC_CORRUPT;
+        }
+        running += count;
+    }
+    if (running != n_esc) return ORC_CORRUPT;
+
+    for (uint64_t c = 0; c < chunks; c++) {
+        uint64_t offset = get_u32(hdr + 8 * c);
+        uint64_t lo = c * ORC_CHUNK;
+        uint64_t hi = lo + ORC_CHUNK < n ? lo + ORC_CHUNK : n;
+        uint64_t seen = 0; /* sentinels so far in this chunk */
+        for (uint64_t i = lo; i < hi; i++) {
+            unsigned sm = in[i], e;
+            if (variant == ORC_ABL_TOP8) {
+                uint64_t g = i / 8;
+                unsigned word = (unsigned)codes[3 * g] | ((unsigned)codes[3 * g + 1] << 8) |
+                                ((unsigned)codes[3 * g + 2] << 16);
+                e = cb[(word >> (3 * (unsigned)(i % 8))) & 7u];
+            } else {
+                unsigned code = (codes[i / 2] >> (4 * (i % 2))) & 0xFu;
+                e = code == 15u ? esc[offset + seen++] : cb[code];
+            }
+            unsigned v = ((sm >> 7) << 15) | (e << 7) | (sm & 0x7Fu);
+            y[2 * i] = (uint8_t)(v & 0xFFu);
+            y[2 * i + 1] = (uint8_t)(v >> 8);
+        }
+        if (variant == ORC_ABL_TOP8) { /* escape overwrite */
+            uint64_t count = get_u32(hdr + 8 * c + 4);
+            for (uint64_t q = 0; q < count; q++) {
+                uint64_t i = lo + get_u16(esc + 3 * (offset + q));
+                unsigned v = (unsigned)y[2 * i] | ((unsigned)y[2 * i + 1] << 8);
+                v = (v & 0x807Fu) | ((unsigned)esc[3 * (offset + q) + 2] << 7);
+                y[2 * i] = (uint8_t)(v & 0xFFu);
+                y[2 * i + 1] = (uint8_t)(v >> 8);
+            }
+        }
+    }
     return ORC_OK;
 }

@@ -365,6 +365,55 @@ def check_ablation_top16_is_the_stream(orc):
         assert orc.ablation_sizes(dt, orc.histogram(dt, x), n)[0] == orc.encode(dt, cb, x).size
 
 
+def check_ablation_codecs_hand(orc):
+    """The Top-8 and sentinel streams of the five-element tensor (golden)."""
+    for g in G.load("ablation_codecs_hand.txt"):
+        variant = O.ABL_TOP8 if g["case"] == "top8" else O.ABL_SENTINEL
+        x = np.array([int(v, 16) for v in g["x"].split()], dtype=np.uint16)
+        cb = np.array([int(v) for v in g["codebook"].split()], dtype=np.uint8)
+        want = np.array([int(v, 16) for v in g["stream"].split()], dtype=np.uint8)
+        s = orc.abl_encode(variant, cb, x)
+        assert np.array_equal(s, want), g["case"]
+        st, y = orc.abl_decode(variant, s, 5)
+        assert st == O.OK and y.tobytes() == x.tobytes()
+
+
+def check_ablation_codecs_bruteforce(orc):
+    """Every BF16 pattern: round trip, and the sizes arithmetic fixes (each
+    exponent owns 256 patterns: E8 = 63,488, E15 = 61,696)."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    rng = np.random.default_rng(21)
+    for variant, k, size in ((O.ABL_TOP8, 8, 280592), (O.ABL_SENTINEL, 15, 160023)):
+        for cb in (np.arange(120, 120 + k), np.sort(rng.choice(256, k, replace=False)),
+                   np.array(list(range(k - 1)) + [255])):
+            s = orc.abl_encode(variant, cb.astype(np.uint8), x)
+            assert s.size == size
+            st, y = orc.abl_decode(variant, s, 65536)
+            assert st == O.OK and y.tobytes() == x.tobytes()
+        # A shuffled tensor over three chunks: the order of escapes matters here.
+        xs = x[rng.permutation(65536)][: 3 * 65536 // 2]
+        xs = np.concatenate([xs, x[rng.permutation(65536)]])
+        cb = orc.abl_codebook(variant, orc.histogram(O.BF16, xs))
+        s = orc.abl_encode(variant, cb, xs)
+        st, y = orc.abl_decode(variant, s, xs.size)
+        assert st == O.OK and y.tobytes() == xs.tobytes()
+        assert s.size == orc.ablation_sizes(O.BF16, orc.histogram(O.BF16, xs), xs.size)[1 if k == 8 else 2]
+
+
+def check_ablation_codecs_reject_corruption(orc):
+    x = (np.random.default_rng(5).standard_normal(70_000) * 50).astype(np.float32).view(np.uint32) >> 16
+    x = x.astype(np.uint16)
+    for variant in (O.ABL_TOP8, O.ABL_SENTINEL):
+        cb = orc.abl_codebook(variant, orc.histogram(O.BF16, x))
+        s = orc.abl_encode(variant, cb, x)
+        assert orc.abl_decode(variant, s[:-1], x.size)[0] == O.CORRUPT       # size off
+        k = 8 if variant == O.ABL_TOP8 else 15
+        hdr = x.size + (3 * ((x.size + 7) // 8) if variant == O.ABL_TOP8 else (x.size + 1) // 2) + k
+        bad = s.copy()
+        bad[hdr + 4] ^= 1                                                     # chunk 0 count
+        assert orc.abl_decode(variant, bad, x.size)[0] == O.CORRUPT
+
+
 CHECKS = [
     check_hand_bf16,
     check_hand_e5m2,
@@ -382,4 +431,7 @@ CHECKS = [
     check_invalid_codebook_refused,
     check_ablation_hand,
     check_ablation_top16_is_the_stream,
+    check_ablation_codecs_hand,
+    check_ablation_codecs_bruteforce,
+    check_ablation_codecs_reject_corruption,
 ]

@@ -65,6 +65,12 @@ MUTANTS = [
     ("E5M2 decode drops the mantissa",
      "y[i] = (uint8_t)(((sm3 >> 2) << 7) | ((unsigned)cb[code] << 2) | (sm3 & 0x3u));",
      "y[i] = (uint8_t)(((sm3 >> 2) << 7) | ((unsigned)cb[code] << 2));"),
+    ("Top-8 ablation codes packed 4 bits apart",
+     "unsigned bit = 3 * (unsigned)(i % 8);",
+     "unsigned bit = 4 * (unsigned)(i % 8);"),
+    ("sentinel ablation marks escapes with code 14",
+     "                code = 15;",
+     "                code = 14;"),
 ]
 
 
