@@ -437,7 +437,33 @@ def main():
                     "coverage_top16": sum(top[:16]) / n, "coverage_top8": sum(top[:8]) / n,
                     "coverage_top15": sum(top[:15]) / n,
                     "note": "sizes from the whole-tensor exponent histogram; the Top-8 and sentinel layouts are "
-                            "readings (codes + same escapes/headers), their codecs are not built"}
+                            "readings (codes + the same headers; Top-8 keeps position records, the sentinel "
+                            "stores only exponent bytes)"}
+        if is_bf16:
+            # Decode speed of the alternative designs on this tensor (their
+            # encoders are plain and not timed).
+            speeds = {"top16": n_bytes / statistics.mean(t_dec) / 1e9}
+            for variant, name in ((S.SZ_ABL_TOP8, "top8"), (S.SZ_ABL_SENTINEL, "top15_sentinel")):
+                acb = S.sz_ablation_codebook(variant, counts)
+                aout = torch.empty(S.sz_ablation_encoded_size(variant, n, n), dtype=torch.uint8, device=dev)
+                aws = torch.empty(S.sz_ablation_workspace_size(n), dtype=torch.uint8, device=dev)
+                S.sz_ablation_encode(variant, acb, x, aout, ob, aws)
+                torch.cuda.synchronize()
+                asize = int(ob.item())
+                for _ in range(3):
+                    S.sz_ablation_decode(variant, aout, asize, n, y, dst)
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                for _ in range(20):
+                    S.sz_ablation_decode(variant, aout, asize, n, y, dst)
+                a1.record(stream)
+                torch.cuda.synchronize()
+                assert int(dst.item()) == 0 and torch.equal(y.view(torch.uint8), x.view(torch.uint8)), name
+                speeds[name] = n_bytes / (a0.elapsed_time(a1) / 20 / 1e3) / 1e9
+                del aout, aws
+            ablation["decode_gbs"] = speeds
+            ablation["decode_slowdown_vs_top16"] = {k: speeds["top16"] / v for k, v in speeds.items()}
+            S.sz_decode(dt, out, size, n, y, dst)
 
     e2e = None
     memcpy_gbs = None

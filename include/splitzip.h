@@ -226,6 +226,37 @@ sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t
                           void* d_pool, size_t pool_pages, size_t page_elems,
                           const int32_t* d_block_ids, int* d_status, cudaStream_t stream);
 
+/* The codebook ablation's two alternative designs as working BF16 codecs,
+ * for measuring their decode speed against this format ([RES] "Estudios de
+ * Ablacion": Top-8 is reported to decode 3x slower, a Top-15 sentinel 3.5x
+ * slower; [MET] "Decision de Diseno").  Not part of the SplitZip format; the
+ * pages give no layouts, so these are readings:
+ *  SZ_ABL_TOP8      [sm N][codes 3 ceil(N/8)][codebook 8][headers 8C]
+ *                   [records 3E]: code j of group g at bits 3j..3j+2 of the
+ *                   24-bit little-endian word at byte 3g; escapes as in the
+ *                   SplitZip stream (code 0 + a position/exponent record).
+ *  SZ_ABL_SENTINEL  [sm N][nibbles ceil(N/2)][codebook 15][headers 8C]
+ *                   [exponent bytes E]: code 15 marks an escape, whose
+ *                   exponent is the next byte of its chunk's run.
+ * h_cb: 8 or 15 distinct exponents, code c = h_cb[c].  out_capacity must be
+ * at least sz_ablation_encoded_size(variant, n, n); d_ws at least
+ * sz_ablation_workspace_size(n) bytes, 4-byte aligned.  Decode reports
+ * SZ_ERR_CORRUPT in *d_status for headers that are not running sums, a
+ * sentinel count that disagrees with its chunk's header, or (Top-8) record
+ * positions out of order; it writes nothing outside d_out[0, 2n).
+ * Asynchronous; encode writes the stream size to *d_out_bytes. */
+enum sz_ablation { SZ_ABL_TOP8 = 1, SZ_ABL_SENTINEL = 2 };
+size_t sz_ablation_encoded_size(int variant, size_t n, size_t n_escapes);
+/* The 8 (Top-8) or 15 (sentinel) most frequent exponents of a BF16 histogram
+ * (256 counts), chosen as for sz_codebook_from_histogram, ascending.  Host. */
+sz_status sz_ablation_codebook(int variant, const unsigned long long* h_hist, uint8_t* h_cb);
+size_t sz_ablation_workspace_size(size_t n);
+sz_status sz_ablation_encode(int variant, const uint8_t* h_cb, const void* d_in, size_t n,
+                             void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
+                             void* d_ws, size_t ws_bytes, cudaStream_t stream);
+sz_status sz_ablation_decode(int variant, const void* d_in, size_t in_bytes, size_t n,
+                             void* d_out, int* d_status, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* sz_status_string(int status);
 

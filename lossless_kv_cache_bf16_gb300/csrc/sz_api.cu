@@ -382,6 +382,98 @@ sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t
     return decode_impl(dt, d_in, in_bytes, n, d_pool, d_status, stream, pm);
 }
 
+// ---- the codebook ablation's alternative codecs (BF16) ----------------------
+namespace {
+bool ablation_ok(int v) { return v == SZ_ABL_TOP8 || v == SZ_ABL_SENTINEL; }
+uint32_t ablation_k(int v) { return v == SZ_ABL_TOP8 ? 8u : 15u; }
+uint64_t ablation_dense(int v, uint64_t n) { return v == SZ_ABL_TOP8 ? n + 3 * cdiv(n, 8) : n + cdiv(n, 2); }
+}  // namespace
+
+size_t sz_ablation_encoded_size(int variant, size_t n, size_t n_escapes) {
+    if (!ablation_ok(variant)) return 0;
+    return ablation_dense(variant, n) + ablation_k(variant) + 8 * cdiv(n, SZ_CHUNK_ELEMS) +
+           (variant == SZ_ABL_TOP8 ? 3 : 1) * (uint64_t)n_escapes;
+}
+
+sz_status sz_ablation_codebook(int variant, const unsigned long long* h_hist, uint8_t* h_cb) {
+    if (!ablation_ok(variant) || !h_hist || !h_cb) return SZ_ERR_INVALID_ARG;
+    int order[256];
+    for (int e = 0; e < 256; e++) order[e] = e;
+    std::stable_sort(order, order + 256, [&](int a, int b) { return h_hist[a] > h_hist[b]; });
+    const uint32_t k = ablation_k(variant);
+    for (uint32_t c = 0; c < k; c++) h_cb[c] = (uint8_t)order[c];
+    std::sort(h_cb, h_cb + k);
+    return SZ_OK;
+}
+
+size_t sz_ablation_workspace_size(size_t n) { return 8 * std::max<uint64_t>(1, cdiv(n, SZ_CHUNK_ELEMS)); }
+
+sz_status sz_ablation_encode(int variant, const uint8_t* h_cb, const void* d_in, size_t n, void* d_out,
+                             size_t out_capacity, unsigned long long* d_out_bytes, void* d_ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+    const NvtxRange range("sz_ablation_encode");
+    if (!ablation_ok(variant) || !h_cb || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
+    if ((n > 0 && !d_in) || (uint64_t)n >= (1ull << 32) || !aligned(d_in, 2) || !aligned(d_ws, 4) ||
+        !aligned(d_out_bytes, 8))
+        return SZ_ERR_INVALID_ARG;
+    const uint32_t k = ablation_k(variant);
+    bool seen[256] = {};
+    for (uint32_t c = 0; c < k; c++) {
+        if (seen[h_cb[c]]) return SZ_ERR_INVALID_ARG;
+        seen[h_cb[c]] = true;
+    }
+    if (out_capacity < sz_ablation_encoded_size(variant, n, n)) return SZ_ERR_CAPACITY;
+    if (ws_bytes < sz_ablation_workspace_size(n)) return SZ_ERR_CAPACITY;
+    AblationParams p{};
+    p.in = static_cast<const uint8_t*>(d_in);
+    p.out = static_cast<uint8_t*>(d_out);
+    p.n = n;
+    p.chunks = (uint32_t)cdiv(n, SZ_CHUNK_ELEMS);
+    p.k = k;
+    p.top8 = variant == SZ_ABL_TOP8;
+    p.cb_off = ablation_dense(variant, n);
+    p.hdr_off = p.cb_off + k;
+    p.rec_off = p.hdr_off + 8ull * p.chunks;
+    p.counts = static_cast<uint32_t*>(d_ws);
+    p.offsets = p.counts + std::max<uint32_t>(p.chunks, 1u);
+    p.out_bytes = d_out_bytes;
+    std::memcpy(p.cb, h_cb, k);
+    return from_cuda(launch_ablation_encode(p, stream));
+}
+
+sz_status sz_ablation_decode(int variant, const void* d_in, size_t in_bytes, size_t n, void* d_out, int* d_status,
+                             cudaStream_t stream) {
+    const NvtxRange range("sz_ablation_decode");
+    if (!ablation_ok(variant) || !d_in || (n > 0 && !d_out) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
+    if (!aligned(d_out, 2) || (d_status && !aligned(d_status, 4))) return SZ_ERR_INVALID_ARG;
+    const uint64_t fixed = sz_ablation_encoded_size(variant, n, 0);
+    const uint64_t per = variant == SZ_ABL_TOP8 ? 3 : 1;
+    if (in_bytes < fixed || (in_bytes - fixed) % per != 0) return SZ_ERR_CORRUPT;
+    const uint64_t n_esc = (in_bytes - fixed) / per;
+    if (n_esc > n) return SZ_ERR_CORRUPT;
+    DecodeParams p{};
+    p.L.n = n;
+    p.L.dense = ablation_dense(variant, n);
+    p.L.nib_off = n;
+    p.L.cb_off = p.L.dense;
+    p.L.num_chunks = (uint32_t)cdiv(n, SZ_CHUNK_ELEMS);
+    p.L.hdr_off = p.L.cb_off + ablation_k(variant);
+    p.L.rec_off = p.L.hdr_off + 8ull * p.L.num_chunks;
+    p.in = static_cast<const uint8_t*>(d_in);
+    p.out = static_cast<uint8_t*>(d_out);
+    p.num_tiles = (uint32_t)decode_tiles_for(SZ_BF16, n);
+    p.n_esc = (uint32_t)n_esc;
+    p.status = d_status;
+    p.wait_limit_ns = kWaitLimitNs;
+    // 16-byte input when the dense streams start 16-byte aligned; 16-byte output.
+    p.vec = aligned(d_in, 16) && aligned(static_cast<const uint8_t*>(d_in) + n, 16) && aligned(d_out, 16);
+    if (d_status) {
+        const cudaError_t err = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
+        if (err != cudaSuccess) return from_cuda(err);
+    }
+    return from_cuda(variant == SZ_ABL_TOP8 ? launch_decode_bf16(p, stream, true) : launch_decode_sentinel(p, stream));
+}
+
 const char* sz_status_string(int status) {
     switch (status) {
         case SZ_OK: return "SZ_OK";

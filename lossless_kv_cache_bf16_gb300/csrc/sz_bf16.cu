@@ -451,8 +451,12 @@ struct DecodeSmem {
 }  // namespace
 
 // PAGED: the output is a paged tensor (DecodeParams::pm).
-template <bool PAGED>
+// TOP8: the Top-8 layout of the codebook ablation (3-bit codes, 8 per 3
+// bytes, an 8-entry codebook); everything else is shared.
+template <bool PAGED, bool TOP8 = false>
 __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const DecodeParams p) {
+    constexpr uint32_t kCodeBytes = TOP8 ? kBf16Tile / 8 * 3 : kBf16Tile / 2;  // code bytes per tile
+    constexpr int kEntries = TOP8 ? 8 : kCodes;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -472,12 +476,17 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
         S.abort = 0;
         fence_mbar_init();
     }
-    S.lut[tid] = ((uint32_t)cb[tid & 15u] << 7) | ((uint32_t)cb[tid >> 4] << 23);
+    // Two codes -> their two exponents, pre-shifted into both 16-bit halves:
+    // a nibble byte (Top-16) or 6 bits (Top-8).
+    if (TOP8)
+        S.lut[tid] = tid < 64 ? ((uint32_t)cb[tid & 7u] << 7) | ((uint32_t)cb[tid >> 3] << 23) : 0u;
+    else
+        S.lut[tid] = ((uint32_t)cb[tid & 15u] << 7) | ((uint32_t)cb[tid >> 4] << 23);
     S.bits[0][tid] = 0;
     S.bits[1][tid] = 0;
-    if (tid < kCodes) {  // a codebook is 16 distinct exponents
+    if (tid < (uint32_t)kEntries) {  // a codebook holds distinct exponents
         bool dup = false;
-        for (int k = 0; k < kCodes; k++) dup |= (k != (int)tid) && cb[k] == cb[tid];
+        for (int k = 0; k < kEntries; k++) dup |= (k != (int)tid) && cb[k] == cb[tid];
         if (dup) S.bad = 1;  // ordered before the reads by the barriers below
     }
     __syncthreads();
@@ -485,9 +494,9 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
     auto full_tile = [&](uint32_t t) { return tma && (uint64_t)(t + 1) * kBf16Tile <= n; };
     auto issue = [&](uint32_t slot, uint32_t t) {  // thread 0 only
         if (full_tile(t)) {
-            mbar_arrive_expect_tx(&S.full[slot], kBf16Tile + kBf16Tile / 2);
+            mbar_arrive_expect_tx(&S.full[slot], kBf16Tile + kCodeBytes);
             bulk_g2s(S.sm[slot], p.in + (uint64_t)t * kBf16Tile, kBf16Tile, &S.full[slot]);
-            bulk_g2s(S.nib[slot], p.in + p.L.nib_off + (uint64_t)t * (kBf16Tile / 2), kBf16Tile / 2, &S.full[slot]);
+            bulk_g2s(S.nib[slot], p.in + p.L.nib_off + (uint64_t)t * kCodeBytes, kCodeBytes, &S.full[slot]);
         } else {
             mbar_arrive(&S.full[slot]);
         }
@@ -652,7 +661,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     // sign (bit 15), the low copy the mantissa (bits 0..6).
                     const uint32_t smw = q < 2 ? smv.x : smv.y;
                     const uint32_t tt = __byte_perm(smw, 0, (q & 1) ? 0x3322 : 0x1100);
-                    y[q] = (tt & 0x807F807Fu) | S.lut[(nibv >> (8 * q)) & 0xFFu];
+                    y[q] = (tt & 0x807F807Fu) | S.lut[TOP8 ? (nibv >> (6 * q)) & 63u : (nibv >> (8 * q)) & 0xFFu];
                 }
                 const uint32_t gb = (bits >> (8 * k)) & 0xFFu;
                 if (gb) {
@@ -670,12 +679,20 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                 // Whole tile in the stage slot: no bounds to check.
                 const uint8_t* ssm = S.sm[slot] + qt;
                 const uint8_t* snb = S.nib[slot] + qt / 2;
+                const uint32_t* scw = reinterpret_cast<const uint32_t*>(S.nib[slot]);
                 uint8_t* o = p.out + 2 * (base + qt);
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
-                    uint32_t y[4];
-                    decode_group(k, *reinterpret_cast<const uint2*>(ssm + k * 256),
-                                 *reinterpret_cast<const uint32_t*>(snb + k * 128), y);
+                    uint32_t y[4], codes;
+                    if (TOP8) {
+                        // 24 code bits at byte 3g of the tile's codes (g = the
+                        // group's index in the tile); two aligned words hold them.
+                        const uint32_t at = 3 * (qt / 8 + 32 * k);
+                        codes = __funnelshift_r(scw[at >> 2], scw[(at >> 2) + 1], 8 * (at & 3)) & 0xFFFFFFu;
+                    } else {
+                        codes = *reinterpret_cast<const uint32_t*>(snb + k * 128);
+                    }
+                    decode_group(k, *reinterpret_cast<const uint2*>(ssm + k * 256), codes, y);
                     // A group of 8 never straddles a page.
                     uint8_t* dst = PAGED ? p.out + elem_offset<true>(p.pm, base + qt + k * 256u, 2, p.status) : o + k * 512;
                     st_stream_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
@@ -687,15 +704,20 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     const uint32_t cnt = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
                     uint2 smv;
                     uint32_t nibv;
-                    if (p.vec && cnt == 8) {
+                    if (p.vec && cnt == 8 && !TOP8) {
                         smv = ld_stream_v2(p.in + i0);
                         nibv = ld_stream_u32(p.in + p.L.nib_off + i0 / 2);
                     } else {
                         uint64_t sv = 0;
                         uint32_t nb = 0;
                         for (uint32_t jj = 0; jj < cnt; jj++) sv |= (uint64_t)p.in[i0 + jj] << (8 * jj);
-                        for (uint32_t b = 0; b < (cnt + 1) / 2; b++)
-                            nb |= (uint32_t)p.in[p.L.nib_off + i0 / 2 + b] << (8 * b);
+                        if (TOP8) {  // a started group has all 3 of its code bytes
+                            if (cnt)
+                                for (uint32_t b = 0; b < 3; b++) nb |= (uint32_t)p.in[p.L.nib_off + 3 * (i0 / 8) + b] << (8 * b);
+                        } else {
+                            for (uint32_t b = 0; b < (cnt + 1) / 2; b++)
+                                nb |= (uint32_t)p.in[p.L.nib_off + i0 / 2 + b] << (8 * b);
+                        }
                         smv = make_uint2((uint32_t)sv, (uint32_t)(sv >> 32));
                         nibv = nb;
                     }
@@ -766,9 +788,9 @@ cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
     return launch_finish(q, true, s);
 }
 
-cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8) {
     const size_t smem = sizeof(DecodeSmem);
-    auto kern = p.pm.ids ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
+    auto kern = top8 ? decode_bf16_kernel<false, true> : p.pm.ids ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int dev = 0, sms = 0, per_sm = 0;
     if (err == cudaSuccess) err = cudaGetDevice(&dev);

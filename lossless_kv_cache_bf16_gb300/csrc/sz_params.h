@@ -69,6 +69,21 @@ struct HistogramParams {
     uint32_t stride;  // count the elements of every stride-th group of 8 (1: all)
 };
 
+// The codebook ablation's alternative BF16 codecs (sz_ablation.cu).
+struct AblationParams {
+    const uint8_t* in;
+    uint8_t* out;
+    uint64_t n;
+    uint32_t chunks;
+    uint32_t k;                      // codebook entries: 8 (Top-8) or 15 (sentinel)
+    int top8;
+    uint64_t cb_off, hdr_off, rec_off;
+    uint32_t* counts;                // workspace: escapes per chunk
+    uint32_t* offsets;               // workspace: escapes before each chunk
+    unsigned long long* out_bytes;
+    uint8_t cb[16];                  // code c -> exponent, as given
+};
+
 // Tile sizes (elements).  Both divide the 65,536-element chunk.
 constexpr uint32_t kBf16Threads = 256;
 constexpr uint32_t kBf16PerThread = 32;
@@ -82,12 +97,15 @@ constexpr uint32_t kScanTile = 32768;
 constexpr uint32_t kMaxStageRecs = 1024;
 
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s);
-cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s);
+// top8: the Top-8 layout of the codebook ablation (see sz_ablation_decode).
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8 = false);
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_histogram(const HistogramParams& p, cudaStream_t s);
 // Top-16 of a device histogram -> 16 ascending exponents in device memory.
 cudaError_t launch_select(const unsigned long long* hist, uint32_t bins, uint8_t* cb_out, cudaStream_t s);
 cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s);
+cudaError_t launch_ablation_encode(const AblationParams& p, cudaStream_t s);
+cudaError_t launch_decode_sentinel(const DecodeParams& p, cudaStream_t s);
 
 }  // namespace sz

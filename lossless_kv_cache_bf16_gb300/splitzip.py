@@ -24,6 +24,9 @@ SZ_ERR_CUDA = 6
 
 SZ_BF16 = 0
 SZ_FP8_E5M2 = 1
+
+SZ_ABL_TOP8 = 1        # codebook ablation: Top-8, 3-bit codes
+SZ_ABL_SENTINEL = 2    # codebook ablation: Top-15 codes, 15 = escape sentinel
 SZ_CHUNK_ELEMS = 65536
 SZ_CODEBOOK_SIZE = 16
 
@@ -65,6 +68,11 @@ def _load() -> ctypes.CDLL:
         "sz_encode_dcb": (i32, [i32, vp, vp, sz, vp, sz, vp, vp, vp, sz, vp]),
         "sz_ablation_sizes": (i32, [i32, u64p, sz, u64p]),
         "sz_encode_paged": (i32, [i32, cbp, vp, sz, sz, vp, sz, vp, sz, vp, vp, vp, sz, vp]),
+        "sz_ablation_encoded_size": (sz, [i32, sz, sz]),
+        "sz_ablation_workspace_size": (sz, [sz]),
+        "sz_ablation_codebook": (i32, [i32, u64p, vp]),
+        "sz_ablation_encode": (i32, [i32, vp, vp, sz, vp, sz, vp, vp, sz, vp]),
+        "sz_ablation_decode": (i32, [i32, vp, sz, sz, vp, vp, vp]),
         "sz_decode_paged": (i32, [i32, vp, sz, sz, vp, sz, sz, vp, vp, vp]),
     }
     for name, (res, args) in sigs.items():
@@ -252,6 +260,44 @@ def sz_decode_paged(dt: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, 
            LIB.sz_decode_paged(dt, _dev_ptr(stream_bytes, "stream"), in_bytes, n, _dev_ptr(pool, "pool"),
                                _pool_pages(dt, pool, page_elems), page_elems, _dev_ptr(block_ids, "block_ids"),
                                _dev_ptr(status, "status"), _stream(stream)))
+
+
+def sz_ablation_encoded_size(variant: int, n: int, n_escapes: int) -> int:
+    return int(LIB.sz_ablation_encoded_size(variant, n, n_escapes))
+
+
+def sz_ablation_workspace_size(n: int) -> int:
+    return int(LIB.sz_ablation_workspace_size(n))
+
+
+def sz_ablation_codebook(variant: int, hist) -> list[int]:
+    vals = [int(v) for v in (hist.tolist() if hasattr(hist, "tolist") else hist)]
+    assert len(vals) == 256
+    arr = (ctypes.c_ulonglong * 256)(*vals)
+    cb = (ctypes.c_uint8 * 15)()
+    _check("sz_ablation_codebook", LIB.sz_ablation_codebook(variant, arr, cb))
+    return list(cb)[: 8 if variant == SZ_ABL_TOP8 else 15]
+
+
+def sz_ablation_encode(variant: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
+                       ws: torch.Tensor, stream=None) -> None:
+    """Encode BF16 x in one of the ablation's alternative layouts (cb: 8 or 15 exponents)."""
+    vals = [int(v) for v in (cb.tolist() if hasattr(cb, "tolist") else cb)]
+    arr = (ctypes.c_uint8 * 16)(*vals)
+    _check("sz_ablation_encode",
+           LIB.sz_ablation_encode(variant, arr, _dev_ptr(x, "x"), _elements(SZ_BF16, x), _dev_ptr(out, "out"),
+                                  out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                  _dev_ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def sz_ablation_decode(variant: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, y: torch.Tensor,
+                       status: torch.Tensor | None, stream=None) -> None:
+    if in_bytes > stream_bytes.numel() * stream_bytes.element_size():
+        raise ValueError("in_bytes exceeds the stream buffer")
+    if 2 * n > y.numel() * y.element_size():
+        raise ValueError("output buffer too small")
+    _check("sz_ablation_decode", LIB.sz_ablation_decode(variant, _dev_ptr(stream_bytes, "stream"), in_bytes, n,
+                                                        _dev_ptr(y, "y"), _dev_ptr(status, "status"), _stream(stream)))
 
 
 def sz_encode_noalloc(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,

@@ -117,3 +117,17 @@ def test_ablation_sizes_match_oracle(S, orc):
             h = h.astype(np.uint64)
             n = int(h.sum())
             assert S.sz_ablation_sizes(dt, h, n) == orc.ablation_sizes(odt, h, n)
+
+
+def test_ablation_codebook_and_sizes_match_oracle(S, orc):
+    """Top-8 / Top-15 selection and the alternative layouts' closed-form
+    sizes, written independently in the library and in the oracle."""
+    from oracle import oracle as O
+
+    rng = np.random.default_rng(17)
+    for variant, ov in ((S.SZ_ABL_TOP8, O.ABL_TOP8), (S.SZ_ABL_SENTINEL, O.ABL_SENTINEL)):
+        for trial in range(40):
+            h = (rng.integers(0, 3, size=256) if trial % 2 else rng.integers(0, 1 << 30, size=256)).astype(np.uint64)
+            assert S.sz_ablation_codebook(variant, h) == [int(v) for v in orc.abl_codebook(ov, h)]
+        for n, e in ((0, 0), (1, 1), (65536, 9), (65537, 65537), (10 ** 6, 123)):
+            assert S.sz_ablation_encoded_size(variant, n, e) == orc.abl_size(ov, n, e)
