@@ -88,8 +88,10 @@ __device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t 
     const uint32_t L1 = __byte_perm(w[2], w[3], 0x6420), H1 = __byte_perm(w[2], w[3], 0x7531);
     o.sm_lo = (H0 & 0x80808080u) | (L0 & 0x7F7F7F7Fu);
     o.sm_hi = (H1 & 0x80808080u) | (L1 & 0x7F7F7F7Fu);
-    const uint32_t e0 = ((H0 << 1) & 0xFEFEFEFEu) | ((L0 >> 7) & 0x01010101u);  // exponents 0..3
-    const uint32_t e1 = ((H1 << 1) & 0xFEFEFEFEu) | ((L1 >> 7) & 0x01010101u);  // exponents 4..7
+    // Exponent byte = (high byte << 1) | (low byte >> 7): disjoint fields, so
+    // a multiply-add and a high multiply (FMA pipe; the coding is ALU-bound).
+    const uint32_t e0 = mad_lo<2u>(H0 & 0x7F7F7F7Fu, mul_hi<1u << 25>(L0 & 0x80808080u));  // exponents 0..3
+    const uint32_t e1 = mad_lo<2u>(H1 & 0x7F7F7F7Fu, mul_hi<1u << 25>(L1 & 0x80808080u));  // exponents 4..7
     uint32_t m = 0;
     if (CONTIG) {
         // sub_lo = (256 - cb0) mod 256 in every byte.
@@ -107,7 +109,8 @@ __device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t 
             c0 &= ~(f0 * 0xFFu), c1 &= ~(f1 * 0xFFu);
             m = ((f0 * 0x01020408u) >> 24) | (((f1 * 0x01020408u) >> 20) & 0xF0u);
         }
-        const uint32_t p0 = c0 | (c0 >> 4), p1 = c1 | (c1 >> 4);  // bytes 0, 2: code pairs
+        // Bytes 0, 2: code pairs (every byte of c is < 16, so c + (c >> 4) = c | (c >> 4)).
+        const uint32_t p0 = mad_hi<1u << 28>(c0, c0), p1 = mad_hi<1u << 28>(c1, c1);
         o.nib = __byte_perm(p0, p1, 0x6420);
     } else {
         uint32_t nib = 0, flags = 0;

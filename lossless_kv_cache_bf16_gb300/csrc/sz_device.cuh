@@ -181,4 +181,27 @@ __device__ __forceinline__ uint64_t elem_offset(const PageMap& m, uint64_t e, ui
     return off;
 }
 
+// Integer multiply-adds with a constant multiplier (IMAD, on the FMA pipe).
+// A right shift by k of a word whose low k bits are masked off is a high
+// multiply by 2^(32-k), and adding disjoint bit fields equals OR-ing them, so
+// bit packing can be split between the integer ALU and FMA pipes.
+template <uint32_t B>
+__device__ __forceinline__ uint32_t mad_lo(uint32_t a, uint32_t c) {  // a * B + c
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "n"(B), "r"(c));
+    return d;
+}
+template <uint32_t B>
+__device__ __forceinline__ uint32_t mad_hi(uint32_t a, uint32_t c) {  // (a * B >> 32) + c
+    uint32_t d;
+    asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "n"(B), "r"(c));
+    return d;
+}
+template <uint32_t B>
+__device__ __forceinline__ uint32_t mul_hi(uint32_t a) {  // a * B >> 32
+    uint32_t d;
+    asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "n"(B));
+    return d;
+}
+
 }  // namespace sz

@@ -41,18 +41,20 @@ __device__ __forceinline__ uint32_t swz8(uint32_t r, uint32_t s) { return r * 8u
 // whose code is 0.  esc4 receives those bit-4 flags.  The parts of a field
 // occupy disjoint bits, so the mantissa joins with a multiply-add.
 __device__ __forceinline__ uint32_t fields4_contig(uint32_t w, uint32_t add, uint32_t& esc4) {
-    const uint32_t d = ((w >> 2) & 0x1F1F1F1Fu) + add;
+    // Shifts of masked words as high multiplies, joins as multiply-adds (see
+    // mad_hi): the coding is ALU-bound, the FMA pipe is not.
+    const uint32_t d = mad_hi<0x40000000u>(w & 0x7C7C7C7Cu, add);   // exponent + add per byte
     esc4 = d & 0x10101010u;
-    const uint32_t kill = (esc4 >> 4) * 0x0Fu;                     // 0x0F in escaped bytes
-    const uint32_t code_sign = (d & 0x0F0F0F0Fu & ~kill) | ((w >> 1) & 0x40404040u);
-    return (w & 0x03030303u) * 16u + code_sign;
+    const uint32_t kill = mul_hi<0xF0000000u>(esc4);                 // 0x0F in escaped bytes
+    const uint32_t code_sign = mad_hi<0x80000000u>(w & 0x80808080u, d & 0x0F0F0F0Fu & ~kill);  // sign to bit 6
+    return mad_lo<16u>(w & 0x03030303u, code_sign);                  // mantissa to bits 4..5
 }
 
 // Four 7-bit fields held one per byte -> 28 bits, field 0 lowest.  Each step
 // moves the upper half of every lane down by subtracting a multiple of it.
 __device__ __forceinline__ uint32_t pack28(uint32_t f) {
-    const uint32_t x = f - ((f >> 8) & 0x007F007Fu) * 128u;     // 16-bit lanes: f0 | f1 << 7
-    return x - ((x >> 2) & 0x0FFFC000u) * 3u;                     // f0 | f1 << 7 | f2 << 14 | f3 << 21
+    const uint32_t x = mad_lo<0xFFFFFF80u>(mul_hi<1u << 24>(f & 0x7F007F00u), f);  // f0 | f1 << 7 per 16-bit lane
+    return mad_lo<0xFFFFFFFDu>(mul_hi<1u << 30>(x & 0x3FFF0000u), x);             // f0 | f1 << 7 | f2 << 14 | f3 << 21
 }
 
 // One group of 8 elements (two little-endian words of input bytes) -> the
@@ -68,9 +70,9 @@ __device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t add,
     if (CONTIG) {
         uint32_t ea, eb;
         const uint32_t pa = pack28(fields4_contig(a, add, ea)), pb = pack28(fields4_contig(b, add, eb));
-        lo = pb * (1u << 28) + pa;
-        hi = pb >> 4;
-        esc_hi = ((ea >> 4) | eb) * 0x01020408u;  // a_j at 8j, b_j at 8j + 4 -> bit 24 + j, 28 + j
+        lo = mad_lo<1u << 28>(pb, pa);
+        hi = mul_hi<1u << 28>(pb);                                  // pb >> 4
+        esc_hi = mad_hi<1u << 28>(ea, eb) * 0x01020408u;  // a_j at 8j, b_j at 8j + 4 -> bit 24 + j, 28 + j
     } else {
         lo = 0;
         hi = 0;
@@ -193,11 +195,11 @@ __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const ui
             escm[q] = __byte_perm(__byte_perm(eh[0], eh[1], 0x0073u), __byte_perm(eh[2], eh[3], 0x7300u), 0x7610u);
             uint32_t* w = words + 7 * q;
             w[0] = lo[0];
-            w[1] = lo[1] * (1u << 24) + hi[0];
+            w[1] = mad_lo<1u << 24>(lo[1], hi[0]);
             w[2] = __funnelshift_r(lo[1], hi[1], 8);
-            w[3] = lo[2] * (1u << 16) + (hi[1] >> 8);
+            w[3] = mad_lo<1u << 16>(lo[2], mul_hi<1u << 24>(hi[1]));   // lo2 << 16 | hi1 >> 8
             w[4] = __funnelshift_r(lo[2], hi[2], 16);
-            w[5] = lo[3] * (1u << 8) + (hi[2] >> 16);
+            w[5] = mad_lo<1u << 8>(lo[3], mul_hi<1u << 16>(hi[2]));    // lo3 << 8 | hi2 >> 16
             w[6] = __funnelshift_r(lo[3], hi[3], 24);
         }
     }
