@@ -178,6 +178,57 @@ def e2e_segments(n: int, parts: int):
     return out or [(0, 0)]
 
 
+SWEEP_POINTS = (("p=0.001", 0.001), ("p=0.01", 0.01), ("p=0.05", 0.05), ("adversarial", None),
+                ("all_escape", None))
+
+
+def escape_sweep_leg(S, W, dt, cb, x, out, ob, est, ws, dst, dev, stream, peak, iters=20):
+    """Encode and decode throughput as the escape share grows: the sweep's
+    planted-escape tensors (same size and codebook as the p = 0 tensor x),
+    uniformly random non-NaN patterns, and a tensor with every exponent
+    outside the codebook.  Each point is checked bit-exact before it is
+    timed; the roofline fraction uses the point's own stream size."""
+    import torch
+
+    n = x.numel()
+    n_bytes = 2 * n
+    y = torch.empty_like(x)
+    res = {}
+    for name, p in SWEEP_POINTS:
+        if p is not None:
+            t = W.escape_sweep(p, cb, dev, n=n)
+        elif name == "adversarial":
+            t = W.adversarial(dev, n=n)
+        else:
+            t = W.all_escape(cb, dev, n=n)
+        S.sz_encode(dt, cb, t, out, ob, est, ws)
+        torch.cuda.synchronize()
+        size = int(ob.item())
+        S.sz_decode(dt, out, size, n, y, dst)
+        torch.cuda.synchronize()
+        assert int(est.item()) == 0 and int(dst.item()) == 0, name
+        assert torch.equal(y.view(torch.uint8), t.view(torch.uint8)), f"{name}: round trip is not bit-exact"
+        for _ in range(3):
+            S.sz_encode(dt, cb, t, out, ob, est, ws)
+            S.sz_decode(dt, out, size, n, y, dst)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        for _ in range(iters):
+            S.sz_encode(dt, cb, t, out, ob, est, ws)
+        e[1].record(stream)
+        for _ in range(iters):
+            S.sz_decode(dt, out, size, n, y, dst)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        te, td = e[0].elapsed_time(e[1]) / iters / 1e3, e[1].elapsed_time(e[2]) / iters / 1e3
+        res[name] = {"escape_rate": (size - S.sz_encoded_size(dt, n, 0)) / 3 / n, "ratio": n_bytes / size,
+                     "encode_gbs": n_bytes / te / 1e9, "decode_gbs": n_bytes / td / 1e9,
+                     "encode_frac_of_codec_roofline": (n_bytes + size) / te / 1e9 / peak,
+                     "decode_frac_of_codec_roofline": (n_bytes + size) / td / 1e9 / peak}
+        del t
+    return res
+
+
 # ---- the reference arm: the CPU oracle ------------------------------------------
 
 def time_oracle(orc, dt_oracle, cb, xb, n):
@@ -357,7 +408,7 @@ def main():
     if not args.profile:
         # Online (per-tensor) calibration on the device, the alternative to the
         # offline codebook that the pages' calibration ablation weighs: the
-        # histogram of every s-th group of 8 elements plus the top-16, then an
+        # histogram of one 128-byte line in every run of s lines plus the top-16, then an
         # encode that reads that codebook from device memory.
         dcb = torch.empty(16, dtype=torch.uint8, device=dev)
         dhist = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device=dev)
@@ -382,7 +433,7 @@ def main():
         torch.cuda.synchronize()
         assert int(est.item()) == 0
         online_size = int(ob.item())
-        online.update({"sample": "every 16th group of 8 elements of the tensor itself",
+        online.update({"sample": "one 128-byte line in every run of 16 lines (hashed position) of the tensor itself",
                        "encode_dcb_gbs": n_bytes / (c0.elapsed_time(c1) / 20 / 1e3) / 1e9,
                        "codebook": dcb.cpu().tolist(), "offline_codebook": [int(v) for v in cb],
                        "ratio": n_bytes / online_size, "ratio_offline": n_bytes / size})
@@ -464,6 +515,12 @@ def main():
             ablation["decode_gbs"] = speeds
             ablation["decode_slowdown_vs_top16"] = {k: speeds["top16"] / v for k, v in speeds.items()}
             S.sz_decode(dt, out, size, n, y, dst)
+
+    sweep = None
+    if not args.profile and args.config == "escape_sweep":
+        sweep = escape_sweep_leg(S, W, dt, cb, x, out, ob, est, ws, dst, dev, stream, peak=measured_peaks()[0])
+        S.sz_encode(dt, cb, x, out, ob, est, ws)
+        S.sz_decode(dt, out, size, n, y, dst)
 
     e2e = None
     memcpy_gbs = None
@@ -602,7 +659,7 @@ def main():
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
                           "hardware": "not named on the pages"},
         "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online, "ablation": ablation, "paged": paged,
-        "e2e": e2e,
+        "escape_sweep": sweep, "e2e": e2e,
         "gpu_launches": sum(len(OPS[op][0]) for op in ops) * K, "clocks": clocks,
     }
     print(json.dumps(line))

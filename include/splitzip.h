@@ -127,10 +127,16 @@ sz_status sz_codebook_from_histogram(sz_dtype dt, const unsigned long long* h_hi
 sz_status sz_codebook_from_histogram_device(sz_dtype dt, const unsigned long long* d_hist,
                                             uint8_t* d_cb, cudaStream_t stream);
 
-/* Online calibration, all on the device: the exponent histogram of every
- * sample_stride-th group of 8 elements of d_x (groups g with g % stride == 0,
- * i.e. elements [8g, 8g + 8) of those groups; stride 1 = every element), then
- * sz_codebook_from_histogram_device into d_cb.  d_hist as for sz_histogram.
+/* Online calibration, all on the device: the exponent histogram of a sample
+ * of d_x, then sz_codebook_from_histogram_device into d_cb.  The sample is
+ * made of 128-byte lines (line k = elements [64k, 64k + 64) for BF16,
+ * [128k, 128k + 128) for E5M2, clipped to n).  With S = sample_stride, the
+ * lines form runs w = 0, 1, ... of S lines (the last run may be shorter, L
+ * lines); run w contributes line wS + floor(lowbias32(w) * L / 2^32), where
+ * lowbias32 is C. Wellons' 32-bit integer hash (x ^= x >> 16; x *= 0x7feb352d;
+ * x ^= x >> 15; x *= 0x846ca68b; x ^= x >> 16).  S = 1 takes every element.
+ * One line in S costs about 1/S of a full read and does not alias with a
+ * periodic KV layout.  d_hist as for sz_histogram.
  * Asynchronous, no host synchronisation: an sz_encode_dcb can follow on the
  * same stream (and both can be captured in a CUDA graph). */
 sz_status sz_calibrate_device(sz_dtype dt, const void* d_x, size_t n, uint32_t sample_stride,

@@ -115,66 +115,18 @@ struct EncodeE5Smem {
     uint8_t field[256];         // byte -> field; 0x80 marks an escape
 };
 
-template <bool CONTIG, bool PAGED>
-__device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const uint8_t (&cb)[16]) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
+// Everything after the input rows are in shared memory: coding, escape
+// ranks, staged records, packed output.
+template <bool CONTIG>
+__device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5Smem& S, const uint8_t (&cb)[16],
+                                                 uint64_t warp_base, uint64_t thread_base, bool warp_full,
+                                                 uint32_t cnt) {
     auto& s_field = S.field;
     auto& s_in = S.buf;
     auto& s_out = S.buf;
     auto& s_warp_esc = S.warp_esc;
-
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
-    {
-        const uint32_t x = tid, e = (x >> 2) & 31u;
-        uint32_t code = 0xFFu;
-#pragma unroll
-        for (int k = 0; k < kCodes; k++)
-            if (cb[k] == e) code = (uint32_t)k;
-        const uint32_t sm3 = ((x >> 7) << 2) | (x & 3u);
-        s_field[x] = (uint8_t)(code == 0xFFu ? (0x80u | (sm3 << 4)) : (code | (sm3 << 4)));
-    }
-    if (blockIdx.x == 0 && tid == 0) {
-#pragma unroll
-        for (int k = 0; k < kCodes; k++) p.out[p.L.cb_off + k] = cb[k];
-    }
-    __syncthreads();
     const uint32_t st = blockIdx.x;
-    const uint64_t n = p.L.n;
-    const uint64_t warp_base = (uint64_t)st * kScanTile + warp * kWarpElems;
-    const uint64_t thread_base = warp_base + lane * kE5PerThread;
-    const bool warp_full = p.vec && warp_base + kWarpElems <= n;
-    const uint32_t cnt = thread_base >= n ? 0u : (n - thread_base >= kE5PerThread ? kE5PerThread : (uint32_t)(n - thread_base));
-
-    // Input bytes into this thread's row.  Bytes past n read as exponent
-    // cb[0] with sign and mantissa 0, which packs to field 0 and is no escape.
-    if (warp_full) {
-#pragma unroll
-        for (uint32_t i = 0; i < 8; i++) {
-            const uint32_t piece = lane + 32 * i;
-            // A 16-element piece never straddles a page.
-            s_in[warp][swz8(piece >> 3, piece & 7u)] =
-                ld_stream_v4(p.in + elem_offset<PAGED>(p.pm, warp_base + 16 * piece, 1, p.status));
-        }
-    } else {
-        const uint32_t pad = (uint32_t)cb[0] << 2;
-        for (uint32_t s = 0; s < 8; s++) {
-            uint32_t w[4];
-#pragma unroll
-            for (uint32_t q = 0; q < 4; q++) {
-                uint32_t v = 0;
-#pragma unroll
-                for (uint32_t t = 0; t < 4; t++) {
-                    const uint32_t j = 16 * s + 4 * q + t;
-                    v |= (j < cnt ? (uint32_t)p.in[elem_offset<PAGED>(p.pm, thread_base + j, 1, p.status)] : pad)
-                         << (8 * t);
-                }
-                w[q] = v;
-            }
-            s_in[warp][swz8(lane, s)] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-    __syncwarp();
 
     // Pack: four groups (224 bits) make seven 32-bit words; a thread's 16
     // groups make its 28 words = 7 pieces of 16 bytes.  escm[q] holds the
@@ -280,23 +232,88 @@ __device__ __forceinline__ void encode_e5m2_body(const EncodeParams& p, const ui
 }
 
 // MODE 0: codebook in the parameters, table coding; 1: in the parameters,
-// contiguous; 2: in device memory, checked (a bad one sets SZ_ERR_INVALID_ARG
-// in *status) and the coding chosen on the device.
+// contiguous; 2: in device memory, checked (a bad one sets
+// SZ_ERR_INVALID_ARG in *status), the coding chosen per block.  The device
+// codebook is loaded first and examined only once this thread's input loads
+// are in flight, so its latency hides behind theirs.
 // PAGED: the input is a paged tensor (EncodeParams::pm).
 template <int MODE, bool PAGED = false>
-__global__ void __launch_bounds__(kEncThreads, MODE == 1 ? 4 : 3) encode_e5m2_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_kernel(const EncodeParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    EncodeE5Smem& S = *reinterpret_cast<EncodeE5Smem*>(smem_raw);
+    auto& s_in = S.buf;
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    uint4 cbv = make_uint4(0, 0, 0, 0);
+    if (MODE == 2) cbv = *reinterpret_cast<const uint4*>(p.cb_dev);
+    const uint64_t n = p.L.n;
+    const uint64_t warp_base = (uint64_t)blockIdx.x * kScanTile + warp * kWarpElems;
+    const uint64_t thread_base = warp_base + lane * kE5PerThread;
+    const bool warp_full = p.vec && warp_base + kWarpElems <= n;
+    const uint32_t cnt = thread_base >= n ? 0u : (n - thread_base >= kE5PerThread ? kE5PerThread : (uint32_t)(n - thread_base));
+
+    // Input bytes into this thread's row.
+    if (warp_full) {
+#pragma unroll
+        for (uint32_t i = 0; i < 8; i++) {
+            const uint32_t piece = lane + 32 * i;
+            // A 16-element piece never straddles a page.
+            s_in[warp][swz8(piece >> 3, piece & 7u)] =
+                ld_stream_v4(p.in + elem_offset<PAGED>(p.pm, warp_base + 16 * piece, 1, p.status));
+        }
+    }
     uint8_t cb[16];
     bool contig;
-    const bool ok = load_codebook(p.cb, MODE == 2 ? p.cb_dev : nullptr, 32u, cb, contig);
+    bool ok;
     if (MODE == 2) {
-        if (!ok && blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicMax(p.status, kStatusInvalid);
-        // A contiguous run must also stay within 5 bits for the byte-parallel coding.
-        if (contig && cb[0] <= 16)
-            encode_e5m2_body<true, false>(p, cb);
-        else
-            encode_e5m2_body<false, false>(p, cb);
+        const uint32_t w[4] = {cbv.x, cbv.y, cbv.z, cbv.w};
+        uint8_t dcb[16];
+#pragma unroll
+        for (int k = 0; k < 16; k++) dcb[k] = (uint8_t)(w[k >> 2] >> (8 * (k & 3)));
+        ok = load_codebook(dcb, nullptr, 32u, cb, contig);
     } else {
-        encode_e5m2_body<MODE == 1, PAGED>(p, cb);
+        ok = load_codebook(p.cb, nullptr, 32u, cb, contig);
+    }
+    if (MODE == 2 && !ok && blockIdx.x == 0 && tid == 0 && p.status) atomicMax(p.status, kStatusInvalid);
+    if (blockIdx.x == 0 && tid == 0) {
+#pragma unroll
+        for (int k = 0; k < kCodes; k++) p.out[p.L.cb_off + k] = cb[k];
+    }
+    if (!warp_full) {
+        // Bytes past n read as exponent cb[0] with sign and mantissa 0, which
+        // packs to field 0 and is no escape.
+        const uint32_t pad = (uint32_t)cb[0] << 2;
+        for (uint32_t s = 0; s < 8; s++) {
+            uint32_t w[4];
+#pragma unroll
+            for (uint32_t q = 0; q < 4; q++) {
+                uint32_t v = 0;
+#pragma unroll
+                for (uint32_t t = 0; t < 4; t++) {
+                    const uint32_t j = 16 * s + 4 * q + t;
+                    v |= (j < cnt ? (uint32_t)p.in[elem_offset<PAGED>(p.pm, thread_base + j, 1, p.status)] : pad)
+                         << (8 * t);
+                }
+                w[q] = v;
+            }
+            s_in[warp][swz8(lane, s)] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    __syncwarp();
+    // A contiguous run must also stay within 5 bits for the byte-parallel coding.
+    const bool use_contig = MODE == 1 || (MODE == 2 && contig && cb[0] <= 16);
+    if (use_contig) {
+        encode_e5m2_code<true>(p, S, cb, warp_base, thread_base, warp_full, cnt);
+    } else {
+        // The byte -> field table (block-uniform branch).
+        const uint32_t x = tid, e = (x >> 2) & 31u;
+        uint32_t code = 0xFFu;
+#pragma unroll
+        for (int k = 0; k < kCodes; k++)
+            if (cb[k] == e) code = (uint32_t)k;
+        const uint32_t sm3 = ((x >> 7) << 2) | (x & 3u);
+        S.field[x] = (uint8_t)(code == 0xFFu ? (0x80u | (sm3 << 4)) : (code | (sm3 << 4)));
+        __syncthreads();
+        encode_e5m2_code<false>(p, S, cb, warp_base, thread_base, warp_full, cnt);
     }
 }
 
@@ -668,7 +685,8 @@ cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
     if (err != cudaSuccess) return err;
     kern<<<p.num_tiles, kEncThreads, smem, s>>>(p);
     err = cudaGetLastError();
-    return err != cudaSuccess ? err : launch_finish(p, false, s);
+    if (err != cudaSuccess) return err;
+    return launch_finish(p, false, s);
 }
 
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {

@@ -10,9 +10,14 @@
 //  * one warp per scan tile copies the staged records to offset * 3 in the
 //    escape stream: 16-byte loads of the whole staged run into shared memory,
 //    then aligned 4-byte stores (a funnel shift realigns the bytes) with at
-//    most 3 single bytes at either end.  When the tile had more than ws_cap
-//    escapes, the warp walks the tile's elements again in order and writes
-//    the records directly;
+//    most 3 single bytes at either end;
+//  * a scan tile with more than ws_cap escapes has its ws_cap staged records
+//    copied by the whole block, which then walks the rest of the tile (after
+//    the last staged position) again, in element order, 4,096 (BF16) or
+//    8,192 (E5M2) elements per step: 16-byte loads (all of a step's in
+//    flight at once), a block scan of the escape counts, the step's records
+//    assembled in shared memory and written with the same aligned word
+//    stores;
 //  * a chunk's last scan tile writes the chunk's header (offset = escapes
 //    before the chunk, count = escapes in it); the last scan tile writes the
 //    stream size.
@@ -31,24 +36,162 @@ constexpr uint32_t kFinWarps = kFinThreads / 32;
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;
 constexpr uint32_t kStageBytes = 3 * kMaxStageRecs;      // staged records of one scan tile
 constexpr uint32_t kStageLoads = kStageBytes / 512;       // 16-byte loads per lane
+constexpr uint32_t kRederiveU = 2;  // 16-byte pieces per thread per re-derivation step
+static_assert(3 * kFinThreads * 16 * kRederiveU + 16 <= kFinWarps * (kStageBytes + 16),
+              "a step's records fit the staging space");
 static_assert(kStageBytes % 512 == 0, "whole warp-wide 16-byte loads");
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
 
-// Exponent of element i (linear or paged input): bits 14..7 of a BF16, bits
-// 6..2 of an E5M2 byte.
+// Copy nbytes from shared memory (src, 4-byte aligned, readable up to 4 bytes
+// past the end) to out + dst with aligned 4-byte stores; the 0..3 bytes
+// before the first aligned word and after the last go one at a time.  Bytes
+// at or beyond `capacity` are not written.  Threads tid = 0, step, 2 step, ...
+// share the work.
+__device__ __forceinline__ void copy_out(const uint8_t* src, uint32_t nbytes, uint8_t* out, uint64_t dst,
+                                         uint64_t capacity, uint32_t tid, uint32_t step) {
+    uint8_t* const o = out + dst;
+    const uint32_t head = min((uint32_t)((4u - (uint32_t)(reinterpret_cast<uintptr_t>(o) & 3u)) & 3u), nbytes);
+    const uint32_t words = (nbytes - head) / 4, tail = (nbytes - head) & 3u;
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(src);
+    const uint32_t shift = 8u * (head & 3u);
+    for (uint32_t w = tid; w < words; w += step) {
+        const uint32_t off = head + 4 * w;
+        const uint32_t val = __funnelshift_r(sw[off >> 2], sw[(off >> 2) + 1], shift);
+        if (dst + off + 4 <= capacity) {
+            *reinterpret_cast<uint32_t*>(o + off) = val;
+        } else {
+#pragma unroll
+            for (uint32_t b = 0; b < 4; b++)
+                if (dst + off + b < capacity) o[off + b] = (uint8_t)(val >> (8 * b));
+        }
+    }
+    if (tid < head + tail) {
+        const uint32_t off = tid < head ? tid : head + 4 * words + (tid - head);
+        if (dst + off < capacity) o[off] = src[off];
+    }
+}
+
+// The records of scan tile st, which has more escapes than the ws_cap it
+// staged, written by the whole block at byte offset dst of the stream
+// (element order): the staged records first (they are the tile's first
+// ws_cap escapes), then the ones after the last staged position, re-derived
+// from the input.  A step covers kU pieces of 16 bytes per thread (piece
+// u * 256 + tid of the step), all loaded before any is examined.  buf: shared
+// scratch of at least 3 * max(elements per step, ws_cap) + 16 bytes, 16-byte
+// aligned; s_warp: kU * 8 words.
 template <bool BF16, bool PAGED>
-__device__ __forceinline__ uint32_t exponent_at(const EncodeParams& p, uint64_t i) {
-    const uint8_t* e = p.in + elem_offset<PAGED>(p.pm, i, BF16 ? 2u : 1u, p.status);
-    if (BF16) return (((uint32_t)e[0] | ((uint32_t)e[1] << 8)) >> 7) & 0xFFu;
-    return ((uint32_t)e[0] >> 2) & 0x1Fu;
+__device__ void rederive_tile(const EncodeParams& p, uint32_t st, uint64_t dst, const uint8_t* s_member, uint8_t* buf,
+                              uint32_t* s_warp) {
+    constexpr uint32_t kPer = BF16 ? 8u : 16u;  // elements in 16 bytes
+    constexpr uint32_t kEsize = BF16 ? 2u : 1u;
+    constexpr uint32_t kU = kRederiveU;
+    constexpr uint32_t kStep = kU * kFinThreads * kPer;  // elements per step (divides the scan tile)
+    static_assert(kScanTile % kStep == 0, "whole steps per scan tile");
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint64_t n = p.L.n, begin = (uint64_t)st * kScanTile;
+    const uint64_t end = min(begin + kScanTile, n);
+    const bool vec = (reinterpret_cast<uintptr_t>(p.in) % 16) == 0;  // a paged pool is 16-byte aligned too
+    auto exponent = [](const uint32_t (&w)[4], uint32_t j) {
+        return BF16 ? (w[j >> 1] >> (7 + 16 * (j & 1))) & 0xFFu : (w[j >> 2] >> (8 * (j & 3) + 2)) & 0x1Fu;
+    };
+    uint64_t at = dst;
+    uint64_t resume = begin;  // first element not covered by the staged records
+    if (p.ws_cap > 0) {
+        // 3 ws_cap bytes (a multiple of 16) at a 16-byte aligned address.
+        const uint32_t nb = 3 * p.ws_cap;
+        const uint4* src = reinterpret_cast<const uint4*>(p.ws_rec + (uint64_t)st * nb);
+        for (uint32_t k = tid; k < nb / 16; k += kFinThreads) reinterpret_cast<uint4*>(buf)[k] = src[k];
+        __syncthreads();
+        const uint32_t last = (uint32_t)buf[nb - 3] | ((uint32_t)buf[nb - 2] << 8);
+        resume = (begin & ~(uint64_t)(kChunk - 1)) + last + 1;
+        copy_out(buf, nb, p.out, at, p.capacity, tid, kFinThreads);
+        at += nb;
+        __syncthreads();  // buf is reused below
+    }
+    for (uint64_t s0 = begin + (resume - begin) / kStep * kStep; s0 < end; s0 += kStep) {
+        uint32_t w[kU][4], m[kU];
+#pragma unroll
+        for (uint32_t u = 0; u < kU; u++) {
+            const uint64_t i0 = s0 + (uint64_t)(u * kFinThreads + tid) * kPer;
+            w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0;
+            m[u] = 0;
+            if (i0 < end && i0 + kPer > resume) {
+                const uint32_t valid = end - i0 >= kPer ? kPer : (uint32_t)(end - i0);
+                // Elements [skip, valid) of the piece are examined.
+                const uint32_t skip = resume > i0 ? (uint32_t)(resume - i0) : 0u;
+                m[u] = valid | (skip << 8);  // until the mask replaces it
+                if (vec && valid == kPer) {
+                    // A piece of 16 bytes never straddles a page (pages are a
+                    // power of two of at least 16 elements).
+                    const uint4 v = *reinterpret_cast<const uint4*>(p.in + elem_offset<PAGED>(p.pm, i0, kEsize, p.status));
+                    w[u][0] = v.x, w[u][1] = v.y, w[u][2] = v.z, w[u][3] = v.w;
+                } else {
+#pragma unroll
+                    for (uint32_t j = 0; j < kPer; j++) {
+                        if (j < valid) {
+                            const uint8_t* e = p.in + elem_offset<PAGED>(p.pm, i0 + j, kEsize, p.status);
+                            const uint32_t v = BF16 ? ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) : (uint32_t)e[0];
+                            w[u][j / (4 / kEsize)] |= v << (8 * kEsize * (j % (4 / kEsize)));
+                        }
+                    }
+                }
+            }
+        }
+        uint32_t c[kU], x[kU];
+#pragma unroll
+        for (uint32_t u = 0; u < kU; u++) {
+            const uint32_t valid = m[u] & 0xFFu, skip = m[u] >> 8;
+            m[u] = 0;
+#pragma unroll
+            for (uint32_t j = 0; j < kPer; j++)
+                if (j >= skip && j < valid && !s_member[exponent(w[u], j)]) m[u] |= 1u << j;
+            c[u] = __popc(m[u]);
+            x[u] = c[u];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, x[u], d);
+                if (lane >= (uint32_t)d) x[u] += a;
+            }
+            if (lane == 31) s_warp[u * kFinWarps + warp] = x[u];
+        }
+        __syncthreads();
+        uint32_t before = 0;  // records of the step before slice u
+#pragma unroll
+        for (uint32_t u = 0; u < kU; u++) {
+            uint32_t wbase = 0, total = 0;
+#pragma unroll
+            for (uint32_t v = 0; v < kFinWarps; v++) {
+                wbase += v < warp ? s_warp[u * kFinWarps + v] : 0u;
+                total += s_warp[u * kFinWarps + v];
+            }
+            uint32_t r = 3 * (before + wbase + x[u] - c[u]);
+            const uint32_t i0 = (uint32_t)(s0 + (uint64_t)(u * kFinThreads + tid) * kPer);
+#pragma unroll
+            for (uint32_t j = 0; j < kPer; j++) {
+                if ((m[u] >> j) & 1u) {
+                    const uint32_t pos = (i0 + j) & 0xFFFFu;
+                    buf[r] = (uint8_t)pos;
+                    buf[r + 1] = (uint8_t)(pos >> 8);
+                    buf[r + 2] = (uint8_t)exponent(w[u], j);
+                    r += 3;
+                }
+            }
+            before += total;
+        }
+        __syncthreads();
+        copy_out(buf, 3 * before, p.out, at, p.capacity, tid, kFinThreads);
+        at += 3ull * before;
+        __syncthreads();  // buf and s_warp are reused by the next step
+    }
 }
 
 }  // namespace
 
 template <bool BF16, bool PAGED>
-__global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams p) {
+__global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodeParams p) {
     __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 16];  // +16: realignment reads past the end
     __shared__ uint32_t s_sum[kFinWarps];
+    __shared__ uint32_t s_wsum[kRederiveU * kFinWarps];  // re-derivation: warp totals per slice
     __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
     __shared__ uint8_t s_member[256];  // exponent is in the codebook
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -122,7 +265,7 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
             }
         }
         __syncthreads();
-        // One warp per scan tile: copy the staged records, or re-derive them.
+        // One warp per scan tile with its records staged: copy them.
         const uint32_t batch = min(kFinThreads, t1 - c0);
         for (uint32_t j = warp; j < batch; j += kFinWarps) {
             const uint32_t st = c0 + j, c = s_count[j];
@@ -140,63 +283,15 @@ __global__ void __launch_bounds__(kFinThreads) finish_kernel(const EncodeParams 
                 for (uint32_t k = 0; k < kStageLoads; k++)
                     if (16 * lane + 512 * k < nbytes) reinterpret_cast<uint4*>(stage)[lane + 32 * k] = v[k];
                 __syncwarp();
-                // out + dst + head is 4-byte aligned; bytes before it, and the
-                // 0..3 bytes after the last whole word, go one at a time.
-                uint8_t* const o = p.out + dst;
-                const uint32_t head = min((uint32_t)((4u - (uint32_t)(reinterpret_cast<uintptr_t>(o) & 3u)) & 3u), nbytes);
-                const uint32_t words = (nbytes - head) / 4, tail = (nbytes - head) & 3u;
-                const uint32_t* sw = reinterpret_cast<const uint32_t*>(stage);
-                const uint32_t shift = 8u * (head & 3u);
-                for (uint32_t w = lane; w < words; w += 32) {
-                    const uint32_t off = head + 4 * w;
-                    const uint32_t val = __funnelshift_r(sw[off >> 2], sw[(off >> 2) + 1], shift);
-                    if (dst + off + 4 <= p.capacity) {
-                        *reinterpret_cast<uint32_t*>(o + off) = val;
-                    } else {
-#pragma unroll
-                        for (uint32_t b = 0; b < 4; b++)
-                            if (dst + off + b < p.capacity) o[off + b] = (uint8_t)(val >> (8 * b));
-                    }
-                }
-                if (lane < head + tail) {
-                    const uint32_t off = lane < head ? lane : head + 4 * words + (lane - head);
-                    if (dst + off < p.capacity) o[off] = stage[off];
-                }
+                copy_out(stage, nbytes, p.out, dst, p.capacity, lane, 32);
                 __syncwarp();  // the buffer is reused by the warp's next scan tile
-            } else {
-                // More escapes than staged: walk the tile in element order,
-                // 8 consecutive elements per lane, 256 per step.
-                const uint64_t n = p.L.n, end = min((uint64_t)(st + 1) * kScanTile, n);
-                uint64_t at = dst;
-                for (uint64_t s0 = (uint64_t)st * kScanTile; s0 < end; s0 += 256) {
-                    const uint64_t i0 = s0 + 8ull * lane;
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int jj = 0; jj < 8; jj++)
-                        if (i0 + jj < end && !s_member[exponent_at<BF16, PAGED>(p, i0 + jj)]) m |= 1u << jj;
-                    const uint32_t c8 = __popc(m);
-                    uint32_t x = c8;
-#pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {
-                        const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, x, d);
-                        if (lane >= (uint32_t)d) x += a;
-                    }
-                    uint64_t r = at + 3ull * (x - c8);
-                    while (m) {
-                        const uint32_t jj = __ffs(m) - 1;
-                        m &= m - 1;
-                        const uint32_t pos = (uint32_t)(i0 + jj) & 0xFFFFu;
-                        if (r + 3 <= p.capacity) {
-                            p.out[r] = (uint8_t)pos;
-                            p.out[r + 1] = (uint8_t)(pos >> 8);
-                            p.out[r + 2] = (uint8_t)exponent_at<BF16, PAGED>(p, i0 + jj);
-                        }
-                        r += 3;
-                    }
-                    at += 3ull * __shfl_sync(0xFFFFFFFFu, x, 31);
-                }
             }
         }
+        __syncthreads();
+        // Scan tiles with more escapes than staged: the whole block, one at a time.
+        for (uint32_t j = 0; j < batch; j++)
+            if (s_count[j] > p.ws_cap)
+                rederive_tile<BF16, PAGED>(p, c0 + j, p.L.rec_off + 3ull * s_prefix[j], s_member, &s_stage[0][0], s_wsum);
         base += total;
         __syncthreads();
     }

@@ -66,7 +66,7 @@ struct HistogramParams {
     uint64_t n;
     unsigned long long* hist;
     int bf16;
-    uint32_t stride;  // count the elements of every stride-th group of 8 (1: all)
+    uint32_t stride;  // sample one 128-byte line per run of `stride` lines (1: all)
 };
 
 // The codebook ablation's alternative BF16 codecs (sz_ablation.cu).

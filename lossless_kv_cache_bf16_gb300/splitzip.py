@@ -185,9 +185,9 @@ def sz_codebook_from_histogram_device(dt: int, hist: torch.Tensor, cb: torch.Ten
 
 def sz_calibrate_device(dt: int, x: torch.Tensor, hist: torch.Tensor, cb: torch.Tensor, sample_stride: int = 1,
                         stream=None, n: int | None = None) -> None:
-    """Online calibration on the device (histogram of every sample_stride-th
-    group of 8 elements, then top-16) into cb (16 uint8 on the device);
-    asynchronous, no host synchronisation."""
+    """Online calibration on the device (histogram of one 128-byte line per
+    run of sample_stride lines, at a hashed position in the run, then top-16)
+    into cb (16 uint8 on the device); asynchronous, no host synchronisation."""
     assert hist.numel() == sz_histogram_bins(dt) and hist.element_size() == 8
     assert cb.numel() * cb.element_size() >= SZ_CODEBOOK_SIZE
     n = _elements(dt, x) if n is None else n

@@ -69,10 +69,31 @@ def test_device_top16_matches_oracle(orc, kind):
         assert cb.cpu().tolist() == want, h
 
 
+def _lowbias32(x):
+    """C. Wellons' 32-bit integer hash, on uint64 arrays of 32-bit values."""
+    m = np.uint64(0xFFFFFFFF)
+    x = x.astype(np.uint64)
+    x ^= x >> np.uint64(16)
+    x = (x * np.uint64(0x7FEB352D)) & m
+    x ^= x >> np.uint64(15)
+    x = (x * np.uint64(0x846CA68B)) & m
+    x ^= x >> np.uint64(16)
+    return x
+
+
 def _sampled(xb, esize, n, stride):
-    """Elements of every stride-th group of 8, gathered on the host."""
-    idx = np.concatenate([np.arange(8 * g, min(8 * g + 8, n)) for g in range(0, (n + 7) // 8, stride)])
-    return xb.reshape(n, esize)[idx].reshape(-1)
+    """The sample, gathered on the host: 128-byte lines; run w of `stride`
+    lines (the last may be shorter, L lines) contributes line
+    w * stride + floor(lowbias32(w) * L / 2^32)."""
+    per = 128 // esize
+    lines = -(-n // per)
+    w = np.arange(-(-lines // stride), dtype=np.uint64)
+    first = w * np.uint64(stride)
+    length = np.minimum(np.uint64(lines) - first, np.uint64(stride))
+    sel = first + ((_lowbias32(w) * length) >> np.uint64(32))
+    keep = np.zeros(lines, dtype=bool)
+    keep[sel.astype(np.int64)] = True
+    return xb.reshape(n, esize)[keep[np.arange(n) // per]].reshape(-1)
 
 
 @pytest.mark.parametrize("kind", ["bf16", "e5m2"])
@@ -85,13 +106,16 @@ def test_calibrate_device_matches_oracle_on_the_sample(orc, kind, stride):
         x = W.kv_tiny("cuda", 2).reshape(-1)[: 300_001]
     else:
         x = W.fp8_e5m2_kv("cuda", 2, layers=1, tokens=64).reshape(-1)[: 300_001]
-    for xx in (x, x[1:]):  # aligned, then misaligned (scalar loads)
+    # aligned, misaligned (byte loads), then short tensors (one partial line)
+    for xx in (x, x[1:], x[:65], x[:1]):
         n = xx.numel()
         hist = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device="cuda")
         cb = torch.empty(16, dtype=torch.uint8, device="cuda")
         S.sz_calibrate_device(dt, xx, hist, cb, sample_stride=stride)
         xb = G.as_bytes(xx)
-        want = [int(v) for v in orc.calibrate(ODT[kind], _sampled(xb, 2 if kind == "bf16" else 1, n, stride))]
+        sample = _sampled(xb, 2 if kind == "bf16" else 1, n, stride)
+        assert hist.cpu().numpy().astype(np.uint64).tolist() == orc.histogram(ODT[kind], sample).tolist()
+        want = [int(v) for v in orc.calibrate(ODT[kind], sample)]
         assert cb.cpu().tolist() == want
 
 
