@@ -15,6 +15,7 @@
 #include "sz_device.cuh"
 #include "sz_params.h"
 #include "sz_pipeline.cuh"
+#include "sz_records.cuh"
 
 #include <algorithm>
 
@@ -408,7 +409,8 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
 // [bT/G, (b+1)T/G).  Because escape records are stored in element order, a
 // block's records also form one contiguous run of the stream: one block
 // search finds where the run starts (only when the range starts inside a
-// chunk), then a cursor walks the records through a shared-memory window.
+// chunk), then a cursor walks the records through shared-memory windows
+// that asynchronous copies fill ahead of the walk (RecordWindow).
 // Dense input (sign|mantissa bytes and nibbles) arrives through a 2-stage ring
 // of TMA bulk copies.  Per tile: nibble byte -> two exponents via a 256-entry
 // LUT, joined with the sm bytes; the tile's escapes, gathered into a bitmap
@@ -417,11 +419,12 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
 //
 // One block barrier per tile.  The escapes are gathered one tile ahead into
 // the other of two bitmap/table buffers: while tile t is decoded from buffer
-// t % 2, every thread takes one of the next (up to 256) records and, if it
-// lies below tile t+1's end, checks it and enters it into buffer (t+1) % 2.
-// The tile's closing barrier (__syncthreads_count) both publishes those
-// entries and counts them, which advances the cursor; only a tile with more
-// than 256 escapes takes further counted steps.  A bitmap word is read only
+// t % 2, every thread takes up to two of the next 512 records (cursor + tid
+// and cursor + 256 + tid) and, for each that lies below tile t+1's end,
+// checks it and enters it into buffer (t+1) % 2.  The tile's closing barrier
+// (count_taken_sync) both publishes those entries and counts them, which
+// advances the cursor; only a tile with more than 512 escapes takes further
+// counted steps.  A bitmap word is read only
 // by its owning thread, which clears it right after reading.  Chunk headers
 // are read two tiles ahead, also ahead of a closing barrier.
 //
@@ -435,7 +438,8 @@ namespace {
 
 constexpr uint32_t kDecStages = 2;
 constexpr uint32_t kDecThreads = kBf16Threads;  // 256
-constexpr uint32_t kWindowRecs = 1024;
+constexpr uint32_t kDecR = 2;                   // records a thread takes per step
+constexpr uint32_t kStepRecs = kDecR * kDecThreads;
 
 struct DecodeSmem {
     alignas(128) uint8_t sm[kDecStages][kBf16Tile];
@@ -444,12 +448,15 @@ struct DecodeSmem {
     uint32_t lut[256];
     uint32_t bits[2][kDecThreads];  // escape bitmaps: word tid belongs to thread tid
     uint8_t patch[2][kBf16Tile];    // escape exponents by position in the tile
-    uint8_t win[3 * kWindowRecs];
+    alignas(16) uint8_t win[3][kWinBytes];  // record windows (RecordWindow)
     uint32_t hdr[2][2];             // {offset, count} of a chunk, by chunk parity
     uint32_t scratch[8];
     int bad;
     int abort;
 };
+
+// Four blocks per SM: 4 x (this + 1 KB reserved) within 228 KB.
+static_assert(sizeof(DecodeSmem) <= 56 * 1024, "decode shared memory");
 
 }  // namespace
 
@@ -515,26 +522,16 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
     };
     auto last_of_chunk = [&](uint32_t t) { return t % kTilesPerChunk == kTilesPerChunk - 1 || t == T - 1; };
 
-    // Record window [win_lo, win_lo + win_len) and the walk state (the chunk
-    // of the tile whose escapes are gathered next).  All of it is
-    // block-uniform, so every thread reaches the same barriers.
-    uint32_t win_lo = 0, win_len = 0;
+    // Record windows and the walk state (the chunk of the tile whose escapes
+    // are gathered next).  All of it is block-uniform, so every thread
+    // reaches the same barriers.
+    RecordWindow<kDecThreads> W(S.win, rec, p.n_esc);
     uint32_t chunk_o = 0, chunk_end = 0, cursor = 0;
-    auto win_pos = [&](uint32_t j) {
-        const uint8_t* r = S.win + 3 * (j - win_lo);
-        return (uint32_t)r[0] | ((uint32_t)r[1] << 8);
-    };
-    auto refill = [&](uint32_t from) {  // block-wide; ends with a barrier
-        __syncthreads();
-        win_lo = from;
-        win_len = min(kWindowRecs, p.n_esc - from);
-        for (uint32_t b = tid; b < 3 * win_len; b += kDecThreads) S.win[b] = rec[3ull * from + b];
-        __syncthreads();
-    };
-    // The window must hold the next step's records [cursor, cursor + 256).
-    auto cover = [&]() {
-        const uint32_t nb = min(kDecThreads, chunk_end - cursor);
-        if (nb > 0 && (cursor < win_lo || cursor + nb > win_lo + win_len)) refill(cursor);
+    // The next step's records [cursor, cursor + kStepRecs), and record
+    // cursor - 1 when the step continues a tile, must be resident.
+    auto cover = [&](bool with_prev) {
+        const uint32_t nb = min(kStepRecs, chunk_end - cursor);
+        if (nb > 0) W.cover(with_prev ? cursor - 1 : cursor, cursor + nb);
     };
     // Chunk header {o, m} of chunk c into S.hdr[c & 1], after its checks;
     // prev_end is o + m of chunk c - 1 (used only at a chunk's first tile).
@@ -561,35 +558,41 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
             cursor = chunk_o;
         }
     };
-    // One gathering step for tile tw into buffer b: thread tid takes record
-    // cursor + tid.  Returns whether that record belongs to the tile (its
-    // position is below the tile's end); such a record is checked, and a good
-    // one is entered.  prev: position of the tile's record before the cursor,
-    // or ~0 at the tile's start.
+    // One gathering step for tile tw into buffer b: thread tid takes records
+    // cursor + tid + 256 k (k < kDecR) while they lie below the tile's end.
+    // Returns how many it took; each is checked, and a good one is entered.
+    // prev: position of the tile's record before the cursor, or ~0 at the
+    // tile's start.
     auto gather = [&](uint32_t tw, uint32_t b, uint32_t prev) {
-        const uint32_t r = cursor + tid;
-        if (r >= chunk_end) return false;
         const uint32_t p0 = tile_p0(tw);
-        const uint32_t pos = win_pos(r);
-        if (pos >= p0 + kBf16Tile) return false;
-        const uint32_t before = tid == 0 ? prev : win_pos(r - 1);
-        if (pos < p0 || pos - p0 >= tile_len_of(tw) || (before != 0xFFFFFFFFu && pos <= before)) {
-            S.bad = 1;
-            return true;
+        uint32_t took = 0;
+#pragma unroll
+        for (uint32_t k = 0; k < kDecR; k++) {
+            const uint32_t r = cursor + tid + k * kDecThreads;
+            if (r >= chunk_end) break;
+            const uint8_t* rp = W.at(r);
+            const uint32_t pos = (uint32_t)rp[0] | ((uint32_t)rp[1] << 8);
+            if (pos >= p0 + kBf16Tile) break;
+            took++;
+            const uint32_t before = (tid == 0 && k == 0) ? prev : W.pos(r - 1);
+            if (pos < p0 || pos - p0 >= tile_len_of(tw) || (before != 0xFFFFFFFFu && pos <= before)) {
+                S.bad = 1;
+                continue;
+            }
+            const uint32_t q = pos - p0;
+            S.patch[b][q] = rp[2];
+            atomicOr(&S.bits[b][(q >> 10) * 32u + ((q >> 3) & 31u)], 1u << (((q >> 8) & 3u) * 8u + (q & 7u)));
         }
-        const uint32_t q = pos - p0;
-        S.patch[b][q] = S.win[3 * (r - win_lo) + 2];
-        atomicOr(&S.bits[b][(q >> 10) * 32u + ((q >> 3) & 31u)], 1u << (((q >> 8) & 3u) * 8u + (q & 7u)));
-        return true;
+        return took;
     };
     // After a counted step that took k records: further steps while a step
     // was full, then the chunk-end and hand-off checks of tile tw.
     auto end_tile = [&](uint32_t tw, uint32_t b, uint32_t k) {
         cursor += k;
-        while (k == kDecThreads && cursor < chunk_end) {
-            const uint32_t prev = win_pos(cursor - 1);  // still in the window
-            cover();
-            k = (uint32_t)__syncthreads_count(gather(tw, b, prev));
+        while (k == kStepRecs && cursor < chunk_end) {
+            const uint32_t prev = W.pos(cursor - 1);  // still resident
+            cover(true);
+            k = count_taken_sync<kDecThreads>(gather(tw, b, prev));
             cursor += k;
         }
         if (last_of_chunk(tw) && cursor != chunk_end && tid == 0) S.bad = 1;
@@ -628,8 +631,8 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                 cursor = a;
             }
         }
-        cover();
-        end_tile(t_begin, 0, (uint32_t)__syncthreads_count(gather(t_begin, 0, 0xFFFFFFFFu)));
+        cover(false);
+        end_tile(t_begin, 0, count_taken_sync<kDecThreads>(gather(t_begin, 0, 0xFFFFFFFFu)));
     }
 
     bool aborted = false;
@@ -744,17 +747,17 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
         }
 
         // Tile t + 1: its first gathering step, into the other buffer.
-        bool mine = false;
+        uint32_t mine = 0;
         if (t + 1 < t_end) {
             begin_tile(t + 1);
-            cover();
+            cover(false);
             mine = gather(t + 1, buf ^ 1u, 0xFFFFFFFFu);
         }
         if (prefetch) store_header((t + 2) / kTilesPerChunk, next_o, next_m, true, chunk_end);
         if (failed_wait) S.abort = 1;
         // Closing barrier: stage slot and buffer buf free, buffer buf ^ 1 and
         // the next header published, the step counted.
-        const uint32_t k = (uint32_t)__syncthreads_count(mine);
+        const uint32_t k = count_taken_sync<kDecThreads>(mine);
         if (S.abort) {
             aborted = true;
             break;
@@ -767,6 +770,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
             mbar_wait(&S.full[k % kDecStages], (k / kDecStages) & 1u, p.wait_limit_ns);
         if (p.status) atomicMax(p.status, kStatusTimeout);
     }
+    W.drain();
     __syncthreads();
     if (tid == 0 && S.bad && p.status) atomicMax(p.status, kStatusCorrupt);
 }

@@ -21,6 +21,7 @@
 #include "sz_device.cuh"
 #include "sz_params.h"
 #include "sz_pipeline.cuh"
+#include "sz_records.cuh"
 
 namespace sz {
 
@@ -329,10 +330,11 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
 // A field becomes a byte by arithmetic when the codebook is 16 consecutive
 // exponents (exponent = cb0 + code), else through a 128-entry table.  The
 // tile's records are walked as in the BF16 decoder (block search only where
-// a range starts inside a chunk, then a cursor through a shared window, one
-// record per thread per step); after the step's counting barrier the holders
-// patch the exponent bits of their bytes in the output rows, and after a
-// second barrier the rows leave with coalesced 16-byte stores.  Validation is
+// a range starts inside a chunk, then a cursor through record windows filled
+// ahead by asynchronous copies, up to two records per thread per step); after
+// the step's counting barrier the holders patch the exponent bits of their
+// bytes in the output rows, and after a second barrier the rows leave with
+// coalesced 16-byte stores.  Validation is
 // the BF16 decoder's, plus exponents below 32 in the codebook and records.
 // ---------------------------------------------------------------------------
 namespace {
@@ -344,7 +346,8 @@ constexpr uint32_t kE5DecPer = kE5DecTile / kE5DecThreads;    // 64 elements = 8
 constexpr uint32_t kE5DecTileBytes = kE5DecTile / 8 * 7;      // 14336
 constexpr uint32_t kE5DecStages = 2;
 constexpr uint32_t kE5TilesPerChunk = kChunk / kE5DecTile;    // 4
-constexpr uint32_t kE5WindowRecs = 1024;
+constexpr uint32_t kE5R = 2;  // records a thread takes per step
+constexpr uint32_t kE5StepRecs = kE5R * kE5DecThreads;
 static_assert(kChunk % kE5DecTile == 0 && kE5DecTileBytes % 16 == 0, "tile layout");
 
 struct DecodeE5Smem {
@@ -352,13 +355,15 @@ struct DecodeE5Smem {
     alignas(16) uint4 out[kE5DecWarps][32 * 4];  // per warp: 32 rows of 4 swizzled pieces
     uint64_t full[kE5DecStages];
     uint8_t dec[128];                            // field -> byte
-    uint8_t win[3 * kE5WindowRecs];
+    alignas(16) uint8_t win[3][kWinBytes];       // record windows (RecordWindow)
     uint32_t hdr[2][2];                          // {offset, count} of a chunk, by chunk parity
     uint32_t scratch[8];
     int bad;
     int abort;
     int contig;
 };
+// Four blocks per SM: 4 x (this + 1 KB reserved) within 228 KB.
+static_assert(sizeof(DecodeE5Smem) <= 56 * 1024, "decode shared memory");
 
 // 16-byte slot of piece s (0..3) of row r in a 4-piece swizzled row set.
 __device__ __forceinline__ uint32_t swz4(uint32_t r, uint32_t s) { return r * 4u + (s ^ ((r >> 1) & 3u)); }
@@ -481,23 +486,12 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
     };
     auto last_of_chunk = [&](uint32_t t) { return t % kE5TilesPerChunk == kE5TilesPerChunk - 1 || t == T - 1; };
 
-    // Record window and walk state (block-uniform).
-    uint32_t win_lo = 0, win_len = 0;
+    // Record windows and walk state (block-uniform).
+    RecordWindow<kE5DecThreads> W(S.win, rec, p.n_esc);
     uint32_t chunk_o = 0, chunk_end = 0, cursor = 0;
-    auto win_pos = [&](uint32_t j) {
-        const uint8_t* r = S.win + 3 * (j - win_lo);
-        return (uint32_t)r[0] | ((uint32_t)r[1] << 8);
-    };
-    auto refill = [&](uint32_t from) {  // block-wide; ends with a barrier
-        __syncthreads();
-        win_lo = from;
-        win_len = min(kE5WindowRecs, p.n_esc - from);
-        for (uint32_t b = tid; b < 3 * win_len; b += kE5DecThreads) S.win[b] = rec[3ull * from + b];
-        __syncthreads();
-    };
-    auto cover = [&]() {
-        const uint32_t nb = min(kE5DecThreads, chunk_end - cursor);
-        if (nb > 0 && (cursor < win_lo || cursor + nb > win_lo + win_len)) refill(cursor);
+    auto cover = [&](bool with_prev) {
+        const uint32_t nb = min(kE5StepRecs, chunk_end - cursor);
+        if (nb > 0) W.cover(with_prev ? cursor - 1 : cursor, cursor + nb);
     };
     // Chunk header checks and store (thread 0), as in the BF16 decoder.
     auto store_header = [&](uint32_t c, uint32_t o, uint32_t m, bool at_chunk_start, uint64_t prev_end) {
@@ -512,25 +506,32 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
         S.hdr[c & 1][0] = o;
         S.hdr[c & 1][1] = bad ? 0u : m;
     };
-    // One step: thread tid takes record cursor + tid; returns whether it lies
-    // below the tile's end.  A good one leaves its byte position q in the tile
-    // and its exponent e for the patch.
-    auto gather = [&](uint32_t tw, uint32_t prev, bool& ok, uint32_t& q, uint32_t& e) {
-        ok = false;
-        const uint32_t r = cursor + tid;
-        if (r >= chunk_end) return false;
+    // One step: thread tid takes records cursor + tid + 256 k (k < kE5R)
+    // while they lie below the tile's end; returns how many it took.  Good
+    // ones leave their byte position q[k] in the tile and exponent e[k] for
+    // the patch, flagged in bit k of ok.
+    auto gather = [&](uint32_t tw, uint32_t prev, uint32_t& ok, uint32_t (&q)[kE5R], uint32_t (&e)[kE5R]) {
+        ok = 0;
         const uint32_t p0 = tile_p0(tw);
-        const uint32_t pos = win_pos(r);
-        if (pos >= p0 + kE5DecTile) return false;
-        const uint32_t before = tid == 0 ? prev : win_pos(r - 1);
-        e = S.win[3 * (r - win_lo) + 2];
-        if (pos < p0 || pos - p0 >= tile_len_of(tw) || (before != 0xFFFFFFFFu && pos <= before) || e >= 32) {
-            S.bad = 1;
-            return true;
+        uint32_t took = 0;
+#pragma unroll
+        for (uint32_t k = 0; k < kE5R; k++) {
+            const uint32_t r = cursor + tid + k * kE5DecThreads;
+            if (r >= chunk_end) break;
+            const uint8_t* rp = W.at(r);
+            const uint32_t pos = (uint32_t)rp[0] | ((uint32_t)rp[1] << 8);
+            if (pos >= p0 + kE5DecTile) break;
+            took++;
+            const uint32_t before = (tid == 0 && k == 0) ? prev : W.pos(r - 1);
+            e[k] = rp[2];
+            if (pos < p0 || pos - p0 >= tile_len_of(tw) || (before != 0xFFFFFFFFu && pos <= before) || e[k] >= 32) {
+                S.bad = 1;
+                continue;
+            }
+            ok |= 1u << k;
+            q[k] = pos - p0;
         }
-        ok = true;
-        q = pos - p0;
-        return true;
+        return took;
     };
     // Byte q of the tile lives in row q / 64 (warp q / 2048), byte q % 64.
     auto patch = [&](uint32_t q, uint32_t e) {
@@ -618,26 +619,29 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
 
         // This tile's records: one per thread, counted at the first barrier
         // (which also completes the rows); the holders then patch them.
-        bool ok = false;
-        uint32_t q = 0, e = 0;
-        cover();
-        const bool mine = gather(t, 0xFFFFFFFFu, ok, q, e);
+        uint32_t ok = 0, q[kE5R] = {0, 0}, e[kE5R] = {0, 0};
+        cover(false);
+        const uint32_t mine = gather(t, 0xFFFFFFFFu, ok, q, e);
         if (failed_wait) S.abort = 1;
-        uint32_t k = (uint32_t)__syncthreads_count(mine);
+        uint32_t k = count_taken_sync<kE5DecThreads>(mine);
         if (S.abort) {
             aborted = true;
             break;
         }
         // The dense pass has consumed the ring slot: refill it now.
         if (tid == 0 && t + kE5DecStages < t_end) issue(slot, t + kE5DecStages), issued++;
-        if (ok) patch(q, e);
+#pragma unroll
+        for (uint32_t j = 0; j < kE5R; j++)
+            if ((ok >> j) & 1u) patch(q[j], e[j]);
         cursor += k;
-        while (k == kE5DecThreads && cursor < chunk_end) {  // a full step: maybe more records
-            const uint32_t prev = win_pos(cursor - 1);
-            cover();
-            const bool more = gather(t, prev, ok, q, e);
-            k = (uint32_t)__syncthreads_count(more);
-            if (ok) patch(q, e);
+        while (k == kE5StepRecs && cursor < chunk_end) {  // a full step: maybe more records
+            const uint32_t prev = W.pos(cursor - 1);
+            cover(true);
+            const uint32_t more = gather(t, prev, ok, q, e);
+            k = count_taken_sync<kE5DecThreads>(more);
+#pragma unroll
+            for (uint32_t j = 0; j < kE5R; j++)
+                if ((ok >> j) & 1u) patch(q[j], e[j]);
             cursor += k;
         }
         if (last_of_chunk(t) && cursor != chunk_end && tid == 0) S.bad = 1;
@@ -671,6 +675,7 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
             mbar_wait(&S.full[k % kE5DecStages], (k / kE5DecStages) & 1u, p.wait_limit_ns);
         if (p.status) atomicMax(p.status, kStatusTimeout);
     }
+    W.drain();
     __syncthreads();
     if (tid == 0 && S.bad && p.status) atomicMax(p.status, kStatusCorrupt);
 }

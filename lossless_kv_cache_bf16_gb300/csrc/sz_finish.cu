@@ -12,12 +12,11 @@
 //    then aligned 4-byte stores (a funnel shift realigns the bytes) with at
 //    most 3 single bytes at either end;
 //  * a scan tile with more than ws_cap escapes has its ws_cap staged records
-//    copied by the whole block, which then walks the rest of the tile (after
-//    the last staged position) again, in element order, 4,096 (BF16) or
-//    8,192 (E5M2) elements per step: 16-byte loads (all of a step's in
-//    flight at once), a block scan of the escape counts, the step's records
-//    assembled in shared memory and written with the same aligned word
-//    stores;
+//    copied by its warp, which then walks the rest of the tile (after the
+//    last staged position) again, in element order, 512 (BF16) or 1,024
+//    (E5M2) elements per step: 16-byte loads (all of a step's in flight at once), a warp scan of
+//    the escape counts, the step's records assembled in the warp's staging
+//    buffer and written with the same aligned word stores;
 //  * a chunk's last scan tile writes the chunk's header (offset = escapes
 //    before the chunk, count = escapes in it); the last scan tile writes the
 //    stream size.
@@ -36,9 +35,6 @@ constexpr uint32_t kFinWarps = kFinThreads / 32;
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;
 constexpr uint32_t kStageBytes = 3 * kMaxStageRecs;      // staged records of one scan tile
 constexpr uint32_t kStageLoads = kStageBytes / 512;       // 16-byte loads per lane
-constexpr uint32_t kRederiveU = 2;  // 16-byte pieces per thread per re-derivation step
-static_assert(3 * kFinThreads * 16 * kRederiveU + 16 <= kFinWarps * (kStageBytes + 16),
-              "a step's records fit the staging space");
 static_assert(kStageBytes % 512 == 0, "whole warp-wide 16-byte loads");
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
 
@@ -72,22 +68,20 @@ __device__ __forceinline__ void copy_out(const uint8_t* src, uint32_t nbytes, ui
 }
 
 // The records of scan tile st, which has more escapes than the ws_cap it
-// staged, written by the whole block at byte offset dst of the stream
-// (element order): the staged records first (they are the tile's first
-// ws_cap escapes), then the ones after the last staged position, re-derived
-// from the input.  A step covers kU pieces of 16 bytes per thread (piece
-// u * 256 + tid of the step), all loaded before any is examined.  buf: shared
-// scratch of at least 3 * max(elements per step, ws_cap) + 16 bytes, 16-byte
-// aligned; s_warp: kU * 8 words.
+// staged, written by one warp at byte offset dst of the stream (element
+// order): the staged records first (they are the tile's first ws_cap
+// escapes), then the ones after the last staged position, re-derived from
+// the input.  A step covers kU pieces of 16 bytes per lane
+// (piece u * 32 + lane of the step), all loaded before any is examined.
+// buf: the warp's staging buffer (kStageBytes + 16 bytes, 16-byte aligned).
 template <bool BF16, bool PAGED>
-__device__ void rederive_tile(const EncodeParams& p, uint32_t st, uint64_t dst, const uint8_t* s_member, uint8_t* buf,
-                              uint32_t* s_warp) {
+__device__ void rederive_tile(const EncodeParams& p, uint32_t st, uint64_t dst, const uint8_t* s_member, uint8_t* buf) {
     constexpr uint32_t kPer = BF16 ? 8u : 16u;  // elements in 16 bytes
     constexpr uint32_t kEsize = BF16 ? 2u : 1u;
-    constexpr uint32_t kU = kRederiveU;
-    constexpr uint32_t kStep = kU * kFinThreads * kPer;  // elements per step (divides the scan tile)
-    static_assert(kScanTile % kStep == 0, "whole steps per scan tile");
-    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    constexpr uint32_t kU = 2;
+    constexpr uint32_t kStep = 32 * kU * kPer;  // 512 (BF16) or 1,024 (E5M2) elements
+    static_assert(3 * kStep <= kStageBytes && kScanTile % kStep == 0, "a step's records fit the staging buffer");
+    const uint32_t lane = threadIdx.x & 31u;
     const uint64_t n = p.L.n, begin = (uint64_t)st * kScanTile;
     const uint64_t end = min(begin + kScanTile, n);
     const bool vec = (reinterpret_cast<uintptr_t>(p.in) % 16) == 0;  // a paged pool is 16-byte aligned too
@@ -97,22 +91,23 @@ __device__ void rederive_tile(const EncodeParams& p, uint32_t st, uint64_t dst, 
     uint64_t at = dst;
     uint64_t resume = begin;  // first element not covered by the staged records
     if (p.ws_cap > 0) {
-        // 3 ws_cap bytes (a multiple of 16) at a 16-byte aligned address.
+        // 3 ws_cap bytes (a multiple of 16, at most kStageBytes) at a 16-byte
+        // aligned address.
         const uint32_t nb = 3 * p.ws_cap;
         const uint4* src = reinterpret_cast<const uint4*>(p.ws_rec + (uint64_t)st * nb);
-        for (uint32_t k = tid; k < nb / 16; k += kFinThreads) reinterpret_cast<uint4*>(buf)[k] = src[k];
-        __syncthreads();
+        for (uint32_t k = lane; k < nb / 16; k += 32) reinterpret_cast<uint4*>(buf)[k] = src[k];
+        __syncwarp();
         const uint32_t last = (uint32_t)buf[nb - 3] | ((uint32_t)buf[nb - 2] << 8);
         resume = (begin & ~(uint64_t)(kChunk - 1)) + last + 1;
-        copy_out(buf, nb, p.out, at, p.capacity, tid, kFinThreads);
+        copy_out(buf, nb, p.out, at, p.capacity, lane, 32);
         at += nb;
-        __syncthreads();  // buf is reused below
+        __syncwarp();  // buf is reused below
     }
     for (uint64_t s0 = begin + (resume - begin) / kStep * kStep; s0 < end; s0 += kStep) {
         uint32_t w[kU][4], m[kU];
 #pragma unroll
         for (uint32_t u = 0; u < kU; u++) {
-            const uint64_t i0 = s0 + (uint64_t)(u * kFinThreads + tid) * kPer;
+            const uint64_t i0 = s0 + (uint64_t)(u * 32 + lane) * kPer;
             w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0;
             m[u] = 0;
             if (i0 < end && i0 + kPer > resume) {
@@ -137,38 +132,26 @@ __device__ void rederive_tile(const EncodeParams& p, uint32_t st, uint64_t dst, 
                 }
             }
         }
-        uint32_t c[kU], x[kU];
-#pragma unroll
-        for (uint32_t u = 0; u < kU; u++) {
-            const uint32_t valid = m[u] & 0xFFu, skip = m[u] >> 8;
-            m[u] = 0;
-#pragma unroll
-            for (uint32_t j = 0; j < kPer; j++)
-                if (j >= skip && j < valid && !s_member[exponent(w[u], j)]) m[u] |= 1u << j;
-            c[u] = __popc(m[u]);
-            x[u] = c[u];
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, x[u], d);
-                if (lane >= (uint32_t)d) x[u] += a;
-            }
-            if (lane == 31) s_warp[u * kFinWarps + warp] = x[u];
-        }
-        __syncthreads();
         uint32_t before = 0;  // records of the step before slice u
 #pragma unroll
         for (uint32_t u = 0; u < kU; u++) {
-            uint32_t wbase = 0, total = 0;
+            const uint32_t valid = m[u] & 0xFFu, skip = m[u] >> 8;
+            uint32_t mask = 0;
 #pragma unroll
-            for (uint32_t v = 0; v < kFinWarps; v++) {
-                wbase += v < warp ? s_warp[u * kFinWarps + v] : 0u;
-                total += s_warp[u * kFinWarps + v];
+            for (uint32_t j = 0; j < kPer; j++)
+                if (j >= skip && j < valid && !s_member[exponent(w[u], j)]) mask |= 1u << j;
+            const uint32_t c = __popc(mask);
+            uint32_t x = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, x, d);
+                if (lane >= (uint32_t)d) x += a;
             }
-            uint32_t r = 3 * (before + wbase + x[u] - c[u]);
-            const uint32_t i0 = (uint32_t)(s0 + (uint64_t)(u * kFinThreads + tid) * kPer);
+            uint32_t r = 3 * (before + x - c);
+            const uint32_t i0 = (uint32_t)(s0 + (uint64_t)(u * 32 + lane) * kPer);
 #pragma unroll
             for (uint32_t j = 0; j < kPer; j++) {
-                if ((m[u] >> j) & 1u) {
+                if ((mask >> j) & 1u) {
                     const uint32_t pos = (i0 + j) & 0xFFFFu;
                     buf[r] = (uint8_t)pos;
                     buf[r + 1] = (uint8_t)(pos >> 8);
@@ -176,12 +159,12 @@ __device__ void rederive_tile(const EncodeParams& p, uint32_t st, uint64_t dst, 
                     r += 3;
                 }
             }
-            before += total;
+            before += __shfl_sync(0xFFFFFFFFu, x, 31);
         }
-        __syncthreads();
-        copy_out(buf, 3 * before, p.out, at, p.capacity, tid, kFinThreads);
+        __syncwarp();
+        copy_out(buf, 3 * before, p.out, at, p.capacity, lane, 32);
         at += 3ull * before;
-        __syncthreads();  // buf and s_warp are reused by the next step
+        __syncwarp();  // buf is reused by the next step
     }
 }
 
@@ -191,7 +174,6 @@ template <bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodeParams p) {
     __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 16];  // +16: realignment reads past the end
     __shared__ uint32_t s_sum[kFinWarps];
-    __shared__ uint32_t s_wsum[kRederiveU * kFinWarps];  // re-derivation: warp totals per slice
     __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
     __shared__ uint8_t s_member[256];  // exponent is in the codebook
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -265,7 +247,7 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
             }
         }
         __syncthreads();
-        // One warp per scan tile with its records staged: copy them.
+        // One warp per scan tile: copy its staged records, or re-derive them.
         const uint32_t batch = min(kFinThreads, t1 - c0);
         for (uint32_t j = warp; j < batch; j += kFinWarps) {
             const uint32_t st = c0 + j, c = s_count[j];
@@ -285,13 +267,10 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
                 __syncwarp();
                 copy_out(stage, nbytes, p.out, dst, p.capacity, lane, 32);
                 __syncwarp();  // the buffer is reused by the warp's next scan tile
+            } else {
+                rederive_tile<BF16, PAGED>(p, st, dst, s_member, stage);
             }
         }
-        __syncthreads();
-        // Scan tiles with more escapes than staged: the whole block, one at a time.
-        for (uint32_t j = 0; j < batch; j++)
-            if (s_count[j] > p.ws_cap)
-                rederive_tile<BF16, PAGED>(p, c0 + j, p.L.rec_off + 3ull * s_prefix[j], s_member, &s_stage[0][0], s_wsum);
         base += total;
         __syncthreads();
     }

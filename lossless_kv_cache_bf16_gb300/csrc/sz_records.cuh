@@ -1,0 +1,135 @@
+// sz_records.cuh -- the decoders' walk over escape records.
+//
+// Escape records are 3-byte (u16 position in the chunk, u8 exponent) pairs in
+// element order (SplitZip technical summary, gist.science/es, "Metodologia:
+// SplitZip" > "Flujo de Escape").  A decoder block consumes its records as
+// one contiguous run, a step of up to two records per thread at a time.
+// They are read from shared memory: three buffers of kWinRecs records each,
+// two resident (the records a step reads) and the one after them already in
+// flight as asynchronous copies (cp.async, 16 bytes each, zero-filled past
+// the end of the stream).  When a step no longer needs the older resident
+// window, the in-flight one is waited for and joins, and the freed buffer
+// starts loading the window after it; a long run of records then costs one
+// barrier per kWinRecs records instead of a full memory round trip.  Only a
+// jump outside the resident windows (the first step of a block, or a corrupt
+// header) reloads them synchronously.
+#pragma once
+
+#include <cstdint>
+
+#include "sz_pipeline.cuh"
+
+namespace sz {
+
+constexpr uint32_t kWinRecs = 1024;                // records per window
+constexpr uint32_t kWinBytes = 3 * kWinRecs + 32;  // + the 16-byte alignment offset, rounded up
+
+// 16-byte asynchronous copy global -> shared of which only the first
+// src_bytes (0..16) are read; the rest of the 16 bytes are zero-filled.  dst
+// and src must be 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits for all of this thread's asynchronous copies (they end by themselves).
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Block-uniform state: every thread holds the same values and calls the
+// members in the same order (their barriers are block-wide).
+template <uint32_t THREADS>
+struct RecordWindow {
+    uint8_t (*buf)[kWinBytes];  // 3 buffers in shared memory, 16-byte aligned
+    const uint8_t* rec;         // the stream's first record (global memory)
+    uint32_t n_esc;             // records in the stream
+    uint32_t lo = 0;            // first record of the older resident window
+    uint32_t slot = 0;          // its buffer; the newer one is in slot + 1
+    bool valid = false;
+    const uint8_t* base0 = nullptr;  // record lo in shared memory
+    const uint8_t* base1 = nullptr;  // record lo + kWinRecs
+
+    __device__ __forceinline__ RecordWindow(uint8_t (*b)[kWinBytes], const uint8_t* r, uint32_t n)
+        : buf(b), rec(r), n_esc(n) {}
+
+    __device__ __forceinline__ static uint32_t next(uint32_t s) { return s == 2 ? 0u : s + 1; }
+    // Where record `first` lands in buffer b: the copies start at the 16-byte
+    // boundary below it.
+    __device__ __forceinline__ const uint8_t* start(uint32_t first, uint32_t b) const {
+        return buf[b] + (reinterpret_cast<uintptr_t>(rec + 3ull * first) & 15u);
+    }
+    // Issues the copies of records [first, first + kWinRecs) (clipped to the
+    // stream) into buffer b; at most 194 pieces, one per thread.
+    __device__ __forceinline__ void issue(uint32_t first, uint32_t b) const {
+        if (first >= n_esc) return;
+        const uint32_t len = n_esc - first < kWinRecs ? n_esc - first : kWinRecs;
+        const uintptr_t s = reinterpret_cast<uintptr_t>(rec + 3ull * first), e = s + 3ull * len;
+        const uintptr_t as = s & ~(uintptr_t)15;
+        const uint32_t pieces = (uint32_t)((e - as + 15) / 16);
+        for (uint32_t i = threadIdx.x; i < pieces; i += THREADS) {
+            const uintptr_t src = as + 16ull * i;
+            cp_async16(buf[b] + 16 * i, reinterpret_cast<const void*>(src), e - src >= 16 ? 16u : (uint32_t)(e - src));
+        }
+    }
+    __device__ __forceinline__ void set_bases() {
+        base0 = start(lo, slot);
+        base1 = start(lo + kWinRecs, next(slot));
+    }
+    // Record j (resident): its 3 bytes.
+    __device__ __forceinline__ const uint8_t* at(uint32_t j) const {
+        const uint32_t d = j - lo;
+        return d < kWinRecs ? base0 + 3 * d : base1 + 3 * (d - kWinRecs);
+    }
+    __device__ __forceinline__ uint32_t pos(uint32_t j) const {
+        const uint8_t* r = at(j);
+        return (uint32_t)r[0] | ((uint32_t)r[1] << 8);
+    }
+    // Makes records [need_lo, need_hi) resident (need_hi - need_lo <=
+    // kWinRecs + 1; nothing when empty).  Block-wide.
+    __device__ __forceinline__ void cover(uint32_t need_lo, uint32_t need_hi) {
+        if (need_hi <= need_lo) return;
+        if (valid && need_lo >= lo + kWinRecs && need_hi <= lo + 3 * kWinRecs) {
+            // The older window is done with: the in-flight one joins, and
+            // the freed buffer loads the window after it.
+            cp_async_wait_all();
+            __syncthreads();
+            lo += kWinRecs;
+            slot = next(slot);
+            issue(lo + 2 * kWinRecs, next(next(slot)));
+            cp_async_commit();
+            set_bases();
+        }
+        if (!valid || need_lo < lo || need_hi > lo + 2 * kWinRecs) {
+            cp_async_wait_all();  // no copy may land in a buffer after this reload
+            __syncthreads();
+            lo = need_lo;
+            slot = 0;
+            valid = true;
+            issue(lo, 0);
+            issue(lo + kWinRecs, 1);
+            cp_async_wait_all();
+            __syncthreads();
+            issue(lo + 2 * kWinRecs, 2);
+            cp_async_commit();
+            set_bases();
+        }
+    }
+    // Before the block exits: no copy may still be writing its shared memory.
+    __device__ __forceinline__ void drain() const { cp_async_wait_all(); }
+};
+
+// Block-wide barrier that also counts the records a step took, when thread
+// t took records cursor + t + THREADS k for k < took (k = 0, 1; a second one
+// only after the first).  Records in order make the taken ones a prefix of
+// the step, so the count is the number of threads that took one, plus, when
+// all of them did, the number that took two (a second barrier, only in
+// steps that take more than THREADS records).  For records out of order
+// (a corrupt stream, which the checks report) the result still never
+// exceeds the records taken.
+template <uint32_t THREADS>
+__device__ __forceinline__ uint32_t count_taken_sync(uint32_t took) {
+    uint32_t k = (uint32_t)__syncthreads_count(took >= 1);
+    if (k == THREADS) k += (uint32_t)__syncthreads_count(took >= 2);
+    return k;
+}
+
+}  // namespace sz
