@@ -164,69 +164,43 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def e2e_segments(n: int, parts: int):
-    """[start, end) element ranges of at most `parts` segments of whole
-    65,536-element chunks (the last one may be partial) covering n elements."""
-    chunk = 65536
-    chunks = max(1, -(-n // chunk))
-    per = -(-chunks // max(1, parts))
-    out = []
-    for c0 in range(0, chunks, per):
-        a0, a1 = c0 * chunk, min(n, (c0 + per) * chunk)
-        if a1 > a0:
-            out.append((a0, a1))
-    return out or [(0, 0)]
-
-
-SWEEP_POINTS = (("p=0.001", 0.001), ("p=0.01", 0.01), ("p=0.05", 0.05), ("adversarial", None),
-                ("all_escape", None))
-
-
-def escape_sweep_leg(S, W, dt, cb, x, out, ob, est, ws, dst, dev, stream, peak, iters=20):
-    """Encode and decode throughput as the escape share grows: the sweep's
-    planted-escape tensors (same size and codebook as the p = 0 tensor x),
-    uniformly random non-NaN patterns, and a tensor with every exponent
-    outside the codebook.  Each point is checked bit-exact before it is
-    timed; the roofline fraction uses the point's own stream size."""
+def offload_leg(S, T, dt, cb, x, y, dev, parts, reps=5):
+    """The tensor to pinned host memory and back over this machine's host
+    link: raw copies against the pipelined codec (transfer.Pipeline), each
+    the median of `reps` host-timed runs; GB/s counts uncompressed bytes."""
     import torch
 
-    n = x.numel()
-    n_bytes = 2 * n
-    y = torch.empty_like(x)
-    res = {}
-    for name, p in SWEEP_POINTS:
-        if p is not None:
-            t = W.escape_sweep(p, cb, dev, n=n)
-        elif name == "adversarial":
-            t = W.adversarial(dev, n=n)
-        else:
-            t = W.all_escape(cb, dev, n=n)
-        S.sz_encode(dt, cb, t, out, ob, est, ws)
-        torch.cuda.synchronize()
-        size = int(ob.item())
-        S.sz_decode(dt, out, size, n, y, dst)
-        torch.cuda.synchronize()
-        assert int(est.item()) == 0 and int(dst.item()) == 0, name
-        assert torch.equal(y.view(torch.uint8), t.view(torch.uint8)), f"{name}: round trip is not bit-exact"
-        for _ in range(3):
-            S.sz_encode(dt, cb, t, out, ob, est, ws)
-            S.sz_decode(dt, out, size, n, y, dst)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        e[0].record(stream)
-        for _ in range(iters):
-            S.sz_encode(dt, cb, t, out, ob, est, ws)
-        e[1].record(stream)
-        for _ in range(iters):
-            S.sz_decode(dt, out, size, n, y, dst)
-        e[2].record(stream)
-        torch.cuda.synchronize()
-        te, td = e[0].elapsed_time(e[1]) / iters / 1e3, e[1].elapsed_time(e[2]) / iters / 1e3
-        res[name] = {"escape_rate": (size - S.sz_encoded_size(dt, n, 0)) / 3 / n, "ratio": n_bytes / size,
-                     "encode_gbs": n_bytes / te / 1e9, "decode_gbs": n_bytes / td / 1e9,
-                     "encode_frac_of_codec_roofline": (n_bytes + size) / te / 1e9 / peak,
-                     "decode_frac_of_codec_roofline": (n_bytes + size) / td / 1e9 / peak}
-        del t
-    return res
+    n_bytes = x.numel() * x.element_size()
+    xb = x.view(torch.uint8).reshape(-1)
+    yb = y.view(torch.uint8).reshape(-1)
+    raw = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
+    pipe = T.Pipeline(dt, cb, n_bytes // S.ELEMENT_BYTES[dt], dev, parts=parts)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+        return statistics.median(ts[1:])
+
+    t_raw_d2h = timed(lambda: raw.copy_(xb))
+    t_raw_h2d = timed(lambda: yb.copy_(raw))
+    held = {}
+    t_off = timed(lambda: held.__setitem__("hs", pipe.offload(x)))
+    y.fill_(0)
+    t_rel = timed(lambda: pipe.reload(held["hs"], y))
+    pipe.reload_status()
+    assert torch.equal(y.view(torch.uint8), x.view(torch.uint8)), "reloaded tensor is not bit-exact"
+    hs = held["hs"]
+    return {"segments": len(hs.segs), "raw_bytes": n_bytes, "host_bytes": hs.nbytes,
+            "raw_d2h_gbs": n_bytes / t_raw_d2h / 1e9, "raw_h2d_gbs": n_bytes / t_raw_h2d / 1e9,
+            "offload_gbs": n_bytes / t_off / 1e9, "reload_gbs": n_bytes / t_rel / 1e9,
+            "offload_speedup": t_raw_d2h / t_off, "reload_speedup": t_raw_h2d / t_rel,
+            "note": "offload = encode + D2H of the streams, reload = H2D + decode, pipelined over segments; "
+                    "raw = one pinned copy of the tensor"}
 
 
 # ---- the reference arm: the CPU oracle ------------------------------------------
@@ -324,6 +298,7 @@ def main():
 
     B.build()
     from lossless_kv_cache_bf16_gb300 import splitzip as S
+    from lossless_kv_cache_bf16_gb300 import transfer as T
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -534,7 +509,7 @@ def main():
         xh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
         xh.copy_(x.view(torch.uint8).reshape(-1))
         yh = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
-        segs = e2e_segments(n, args.e2e_segments)
+        segs = T.segments(n, args.e2e_segments)
         xf, yf = x.reshape(-1), y.reshape(-1)
         seg_cap = [S.sz_encoded_size(dt, a1 - a0, a1 - a0) for a0, a1 in segs]
         seg_at = [sum((c + 255) // 256 * 256 for c in seg_cap[:i]) for i in range(len(segs))]
@@ -612,6 +587,10 @@ def main():
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": n_bytes, "d2h_bytes_per_step": n_bytes,
                "steps": args.e2e_steps, "segments": len(segs), "streams": 3,
                "stream_bytes_per_step": sum(seg_size)}
+    offload = None
+    if not args.profile and args.e2e_steps > 0 and world == 1:
+        offload = offload_leg(S, T, dt, cb, x, y, dev, parts=args.e2e_segments)
+
     te, td = statistics.mean(t_enc), statistics.mean(t_dec)
     enc_gbs, dec_gbs = n_bytes / te / 1e9, n_bytes / td / 1e9
     peak, peak_src = measured_peaks()
@@ -659,7 +638,7 @@ def main():
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
                           "hardware": "not named on the pages"},
         "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online, "ablation": ablation, "paged": paged,
-        "escape_sweep": sweep, "e2e": e2e,
+        "escape_sweep": sweep, "offload": offload, "e2e": e2e,
         "gpu_launches": sum(len(OPS[op][0]) for op in ops) * K, "clocks": clocks,
     }
     print(json.dumps(line))

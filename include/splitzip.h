@@ -170,8 +170,12 @@ sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n,
  *                least sz_encoded_size(dt, n, 0) bytes.  When the escapes do
  *                not fit, *d_status becomes SZ_ERR_CAPACITY and the stream is
  *                incomplete; sz_encoded_size(dt, n, n) always suffices
- *  d_out_bytes   device u64, receives the stream size (also on
- *                SZ_ERR_CAPACITY, where it is the size that was needed)
+ *  d_out_bytes   u64 the device can write, receives the stream size (also
+ *                on SZ_ERR_CAPACITY, where it is the size that was needed):
+ *                device memory, or pinned host memory (mapped into the
+ *                device's address space under unified addressing), which a
+ *                host thread can read once the stream has passed the call
+ *                without a copy
  *  d_status      device int or NULL: SZ_OK, SZ_ERR_CAPACITY or SZ_ERR_TIMEOUT
  *                (sz_encode_dcb also SZ_ERR_INVALID_ARG for a bad codebook)
  *  d_ws          device workspace of ws_bytes >= sz_workspace_size(dt, n)

@@ -97,6 +97,16 @@ def _dev_ptr(t: torch.Tensor | None, what: str):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _written_ptr(t: torch.Tensor, what: str):
+    """A word the device writes: a CUDA tensor, or pinned host memory (mapped
+    into the device's address space under unified addressing)."""
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{what} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -201,7 +211,7 @@ def sz_encode_dcb(dt: int, cb: torch.Tensor, x: torch.Tensor, out: torch.Tensor,
     """sz_encode with the codebook in device memory (cb: 16 uint8 on the device)."""
     n = _elements(dt, x) if n is None else n
     _check("sz_encode_dcb", LIB.sz_encode_dcb(dt, _dev_ptr(cb, "cb"), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
-                                              out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                              out.numel() * out.element_size(), _written_ptr(out_bytes, "out_bytes"),
                                               _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
                                               ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -212,7 +222,7 @@ def sz_encode(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.
     c = _codebook(cb)
     n = _elements(dt, x) if n is None else n
     _check("sz_encode", LIB.sz_encode(dt, ctypes.byref(c), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
-                                      out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                      out.numel() * out.element_size(), _written_ptr(out_bytes, "out_bytes"),
                                       _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
                                       ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -244,7 +254,7 @@ def sz_encode_paged(dt: int, cb, pool: torch.Tensor, page_elems: int, block_ids:
     _check("sz_encode_paged",
            LIB.sz_encode_paged(dt, ctypes.byref(c), _dev_ptr(pool, "pool"), _pool_pages(dt, pool, page_elems),
                                page_elems, _dev_ptr(block_ids, "block_ids"), n, _dev_ptr(out, "out"),
-                               out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                               out.numel() * out.element_size(), _written_ptr(out_bytes, "out_bytes"),
                                _dev_ptr(status, "status"), _dev_ptr(ws, "ws"), ws.numel() * ws.element_size(),
                                _stream(stream)))
 
@@ -286,7 +296,7 @@ def sz_ablation_encode(variant: int, cb, x: torch.Tensor, out: torch.Tensor, out
     arr = (ctypes.c_uint8 * 16)(*vals)
     _check("sz_ablation_encode",
            LIB.sz_ablation_encode(variant, arr, _dev_ptr(x, "x"), _elements(SZ_BF16, x), _dev_ptr(out, "out"),
-                                  out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                  out.numel() * out.element_size(), _written_ptr(out_bytes, "out_bytes"),
                                   _dev_ptr(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 
@@ -308,7 +318,7 @@ def sz_encode_noalloc(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes
     n = _elements(dt, x) if n is None else n
     _check("sz_encode_noalloc", LIB.sz_encode_noalloc(dt, ctypes.byref(c), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
                                                       out.numel() * out.element_size(),
-                                                      _dev_ptr(out_bytes, "out_bytes"), _dev_ptr(status, "status"),
+                                                      _written_ptr(out_bytes, "out_bytes"), _dev_ptr(status, "status"),
                                                       _stream(stream)))
 
 
@@ -317,6 +327,6 @@ def sz_debug_encode_stalled(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out
     c = _codebook(cb)
     _check("sz_debug_encode_stalled",
            LIB.sz_debug_encode_stalled(dt, ctypes.byref(c), _dev_ptr(x, "x"), _elements(dt, x), _dev_ptr(out, "out"),
-                                       out.numel() * out.element_size(), _dev_ptr(out_bytes, "out_bytes"),
+                                       out.numel() * out.element_size(), _written_ptr(out_bytes, "out_bytes"),
                                        _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
                                        ws.numel() * ws.element_size(), wait_limit_ns, _stream(stream)))

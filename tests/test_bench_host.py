@@ -72,12 +72,3 @@ def test_two_rank_max_over_ranks():
         assert per_rank == [0.75, 0.5]
         assert t == 0.75
         assert value == pytest.approx(2 * 3 * 10 ** 9 / 0.75 / 1e9)
-
-
-def test_e2e_segments_cover_whole_chunks():
-    for n, parts in ((536870912, 8), (939524096, 8), (65537, 8), (100, 3), (0, 8), (131072 * 3, 2)):
-        segs = bench.e2e_segments(n, parts)
-        assert len(segs) <= max(1, parts)
-        assert segs[0][0] == 0 and segs[-1][1] == n
-        for (a0, a1), (b0, _) in zip(segs, segs[1:]):
-            assert a1 == b0 and a0 % 65536 == 0 and a1 % 65536 == 0
