@@ -164,6 +164,57 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+SWEEP_POINTS = (("p=0.001", 0.001), ("p=0.01", 0.01), ("p=0.05", 0.05), ("adversarial", None),
+                ("all_escape", None))
+
+
+def escape_sweep_leg(S, W, dt, cb, x, out, ob, est, ws, dst, dev, stream, peak, iters=20):
+    """Encode and decode throughput as the escape share grows: the sweep's
+    planted-escape tensors (same size and codebook as the p = 0 tensor x),
+    uniformly random non-NaN patterns, and a tensor with every exponent
+    outside the codebook.  Each point is checked bit-exact before it is
+    timed; the roofline fraction uses the point's own stream size."""
+    import torch
+
+    n = x.numel()
+    n_bytes = 2 * n
+    y = torch.empty_like(x)
+    res = {}
+    for name, p in SWEEP_POINTS:
+        if p is not None:
+            t = W.escape_sweep(p, cb, dev, n=n)
+        elif name == "adversarial":
+            t = W.adversarial(dev, n=n)
+        else:
+            t = W.all_escape(cb, dev, n=n)
+        S.sz_encode(dt, cb, t, out, ob, est, ws)
+        torch.cuda.synchronize()
+        size = int(ob.item())
+        S.sz_decode(dt, out, size, n, y, dst)
+        torch.cuda.synchronize()
+        assert int(est.item()) == 0 and int(dst.item()) == 0, name
+        assert torch.equal(y.view(torch.uint8), t.view(torch.uint8)), f"{name}: round trip is not bit-exact"
+        for _ in range(3):
+            S.sz_encode(dt, cb, t, out, ob, est, ws)
+            S.sz_decode(dt, out, size, n, y, dst)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        for _ in range(iters):
+            S.sz_encode(dt, cb, t, out, ob, est, ws)
+        e[1].record(stream)
+        for _ in range(iters):
+            S.sz_decode(dt, out, size, n, y, dst)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        te, td = e[0].elapsed_time(e[1]) / iters / 1e3, e[1].elapsed_time(e[2]) / iters / 1e3
+        res[name] = {"escape_rate": (size - S.sz_encoded_size(dt, n, 0)) / 3 / n, "ratio": n_bytes / size,
+                     "encode_gbs": n_bytes / te / 1e9, "decode_gbs": n_bytes / td / 1e9,
+                     "encode_frac_of_codec_roofline": (n_bytes + size) / te / 1e9 / peak,
+                     "decode_frac_of_codec_roofline": (n_bytes + size) / td / 1e9 / peak}
+        del t
+    return res
+
+
 def offload_leg(S, T, dt, cb, x, y, dev, parts, reps=5):
     """The tensor to pinned host memory and back over this machine's host
     link: raw copies against the pipelined codec (transfer.Pipeline), each

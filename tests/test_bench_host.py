@@ -72,3 +72,20 @@ def test_two_rank_max_over_ranks():
         assert per_rank == [0.75, 0.5]
         assert t == 0.75
         assert value == pytest.approx(2 * 3 * 10 ** 9 / 0.75 / 1e9)
+
+
+def test_bench_legs_are_defined():
+    # Every leg main() calls exists at module level (a missing one would only
+    # show on the GPU machine).
+    import ast
+
+    tree = ast.parse(open(bench.__file__).read())
+    defined = {n.name for n in tree.body if isinstance(n, (ast.FunctionDef, ast.ClassDef))}
+    main = next(n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name == "main")
+    called = {c.func.id for c in ast.walk(main) if isinstance(c, ast.Call) and isinstance(c.func, ast.Name)}
+    local = {n.name for n in ast.walk(main) if isinstance(n, ast.FunctionDef)}
+    local |= {n.id for n in ast.walk(main) if isinstance(n, ast.Name) and isinstance(n.ctx, ast.Store)}
+    import builtins
+
+    missing = {name for name in called - local - defined if not hasattr(builtins, name)}
+    assert not missing, missing
