@@ -1,8 +1,8 @@
 // sz_pipeline.cuh -- shared-memory mbarriers and TMA bulk copies (sm_90+ PTX),
-// with bounded waits.
+// with bounded waits, and 16-byte asynchronous copies (cp.async).
 //
-// Every wait here gives up after a time limit (globaltimer) instead of
-// spinning forever, so a broken producer can only end in an error status.
+// Every mbarrier wait here gives up after a time limit (globaltimer) instead
+// of spinning forever, so a broken producer can only end in an error status.
 #pragma once
 
 #include <cstdint>
@@ -62,6 +62,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                      smem_u32(dst)),
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (cp.async, sm_80+) of which only
+// the first src_bytes (0..16) are read; the rest of the 16 bytes are
+// zero-filled.  dst and src must be 16-byte aligned.  The copies end by
+// themselves; the waits below need no time limit.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits for all of this thread's asynchronous copies.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 }  // namespace sz

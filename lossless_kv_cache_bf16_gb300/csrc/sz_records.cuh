@@ -24,17 +24,6 @@ namespace sz {
 constexpr uint32_t kWinRecs = 1024;                // records per window
 constexpr uint32_t kWinBytes = 3 * kWinRecs + 32;  // + the 16-byte alignment offset, rounded up
 
-// 16-byte asynchronous copy global -> shared of which only the first
-// src_bytes (0..16) are read; the rest of the 16 bytes are zero-filled.  dst
-// and src must be 16-byte aligned.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Waits for all of this thread's asynchronous copies (they end by themselves).
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // Block-uniform state: every thread holds the same values and calls the
 // members in the same order (their barriers are block-wide).
 template <uint32_t THREADS>
