@@ -35,24 +35,43 @@ LINKS_GBS = (50.0, 100.0)   # inter-node links of the pages' transfer setting
 PAPER_ENCODE_GBS = 613.3    # pages' encode throughput (hardware not named): context only
 PAPER_DECODE_GBS = 2181.8
 
-# Each timed operation, the kernels it launches and the sources they are built from.
+# Each timed operation, the kernels it launches and the translation units they
+# are built from (their included headers count too, see kernel_source_hash).
 # sz_encode is two launches (the streaming encode kernel, then finish_kernel);
 # sz_decode is one.
 OPS = {
-    "encode_bf16": (["encode_bf16_kernel", "finish_kernel"],
-                    ["sz_bf16.cu", "sz_finish.cu", "sz_device.cuh", "sz_pipeline.cuh", "sz_params.h"]),
-    "decode_bf16": (["decode_bf16_kernel"], ["sz_bf16.cu", "sz_device.cuh", "sz_pipeline.cuh", "sz_params.h"]),
-    "encode_e5m2": (["encode_e5m2_kernel", "finish_kernel"],
-                    ["sz_e5m2.cu", "sz_finish.cu", "sz_device.cuh", "sz_params.h"]),
-    "decode_e5m2": (["decode_e5m2_kernel"], ["sz_e5m2.cu", "sz_device.cuh", "sz_params.h"]),
+    "encode_bf16": (["encode_bf16_kernel", "finish_kernel"], ["sz_bf16.cu", "sz_finish.cu"]),
+    "decode_bf16": (["decode_bf16_kernel"], ["sz_bf16.cu"]),
+    "encode_e5m2": (["encode_e5m2_kernel", "finish_kernel"], ["sz_e5m2.cu", "sz_finish.cu"]),
+    "decode_e5m2": (["decode_e5m2_kernel"], ["sz_e5m2.cu"]),
 }
 KERNEL_SOURCES = {op: srcs for op, (_, srcs) in OPS.items()}
 
 
+def _csrc() -> str:
+    return os.path.join(ROOT, "lossless_kv_cache_bf16_gb300", "csrc")
+
+
+def source_closure(names) -> list[str]:
+    """The given csrc files and every csrc header they include, transitively,
+    sorted."""
+    import re
+
+    seen, todo = set(), list(names)
+    while todo:
+        name = todo.pop()
+        if name in seen or not os.path.exists(os.path.join(_csrc(), name)):
+            continue
+        seen.add(name)
+        with open(os.path.join(_csrc(), name)) as f:
+            todo += re.findall(r'^#include "([A-Za-z0-9_.]+)"', f.read(), re.M)
+    return sorted(seen)
+
+
 def kernel_source_hash(op: str) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[op]:
-        with open(os.path.join(ROOT, "lossless_kv_cache_bf16_gb300", "csrc", name), "rb") as f:
+    for name in source_closure(KERNEL_SOURCES[op]):
+        with open(os.path.join(_csrc(), name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 

@@ -32,12 +32,21 @@ def test_traffic_is_null_without_matching_profile(tmp_path, monkeypatch):
     csrc = tmp_path / "lossless_kv_cache_bf16_gb300" / "csrc"
     os.makedirs(csrc)
     for name in bench.KERNEL_SOURCES["encode_bf16"]:
-        (csrc / name).write_text("v1")
-    h = bench.kernel_source_hash("encode_bf16")
-    (tmp_path / "profiles" / "encode_bf16_w.txt").write_text(
-        f"kernel_source_sha256_16: {h}\ndram_bytes_per_launch: 1234\n")
+        (csrc / name).write_text('#include "sz_hdr.cuh"\nv1')
+    (csrc / "sz_hdr.cuh").write_text("h1")
+    assert "sz_hdr.cuh" in bench.source_closure(bench.KERNEL_SOURCES["encode_bf16"])
+
+    def record():
+        h = bench.kernel_source_hash("encode_bf16")
+        (tmp_path / "profiles" / "encode_bf16_w.txt").write_text(
+            f"kernel_source_sha256_16: {h}\ndram_bytes_per_launch: 1234\n")
+
+    record()
     assert bench.profiled_traffic("encode_bf16", "w") == 1234
-    (csrc / "sz_bf16.cu").write_text("v2")   # kernel changed since the capture
+    (csrc / "sz_hdr.cuh").write_text("h2")   # an included header changed since the capture
+    assert bench.profiled_traffic("encode_bf16", "w") is None
+    record()
+    (csrc / "sz_bf16.cu").write_text('#include "sz_hdr.cuh"\nv2')   # the kernel itself changed
     assert bench.profiled_traffic("encode_bf16", "w") is None
 
 
