@@ -85,6 +85,34 @@ def test_fuzzed_metadata_e5m2(orc):
         _check_same_verdict(orc, O.E5M2, S.SZ_FP8_E5M2, t, n)
 
 
+@pytest.mark.parametrize("kind", ["bf16", "e5m2"])
+def test_fuzzed_metadata_dense_escapes_many_blocks(orc, kind):
+    # Uniformly random patterns (most of them escapes) over more tiles than
+    # the decoder has blocks, so that blocks start inside chunks and walk
+    # their records through several windows; corrupted headers and records
+    # make the walk jump.
+    rng = np.random.default_rng(36 if kind == "bf16" else 37)
+    if kind == "bf16":
+        n = 6_000_000 + 77
+        x = rng.integers(0, 1 << 16, n, dtype=np.uint16)
+        dt_o, dt_g, cb, dense = O.BF16, S.SZ_BF16, CB_MID, n + (n + 1) // 2
+    else:
+        n = 12_000_000 + 5
+        x = rng.integers(0, 256, n, dtype=np.uint8)
+        dt_o, dt_g, cb, dense = O.E5M2, S.SZ_FP8_E5M2, CB_E5_MID, 7 * ((n + 7) // 8)
+    s = orc.encode(dt_o, cb, x)
+    chunks = -(-n // 65536)
+    hdr, rec = dense + 16, dense + 16 + 8 * chunks
+    st, y, guard_ok = G.decode(dt_g, s, n)
+    assert st == 0 and guard_ok and np.array_equal(y, x.view(np.uint8))
+    for trial in range(12):
+        t = s.copy()
+        region = (hdr, rec) if trial % 2 == 0 else (rec, t.size)
+        for _ in range(rng.integers(1, 3)):
+            t[int(rng.integers(*region))] = rng.integers(0, 256)
+        _check_same_verdict(orc, dt_o, dt_g, t, n)
+
+
 def test_valid_stream_decodes_clean(orc):
     x, s = _stream(orc, seed=35)
     st, y, guard_ok = G.decode(S.SZ_BF16, s, x.size)
