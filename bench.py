@@ -34,6 +34,8 @@ UNIT = "GB/s"
 LINKS_GBS = (50.0, 100.0)   # inter-node links of the pages' transfer setting
 PAPER_ENCODE_GBS = 613.3    # pages' encode throughput (hardware not named): context only
 PAPER_DECODE_GBS = 2181.8
+PAPER_E5M2_RATIO = 1.14     # pages' E5M2 compression ratio (about 8/7)
+SPEC_HBM_GBS = 8000.0       # GB300 HBM3e, nominal
 
 # Each timed operation, the kernels it launches and the translation units they
 # are built from (their included headers count too, see kernel_source_hash).
@@ -674,6 +676,19 @@ def main():
                 "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": moved}
 
+    def dram_view(op, t):
+        """Achieved HBM GB/s of one call: its ncu DRAM bytes over this run's time."""
+        tr = profiled_traffic(op, args.config)
+        if tr is None:
+            return None
+        g = tr / t / 1e9
+        return {"dram_bytes_per_call": tr, "dram_gbs": g, "frac_of_spec": g / SPEC_HBM_GBS,
+                "frac_of_memcpy": g / memcpy_gbs if memcpy_gbs else None, "frac_of_measured_copy": g / peak}
+
+    hbm = {"encode": dram_view(f"encode_{suffix}", te), "decode": dram_view(f"decode_{suffix}", td),
+           "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per call (profiles/), over this run's "
+                     "CUDA-event time; null without a capture of the current kernels for this workload"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import oracle as O
@@ -703,10 +718,10 @@ def main():
         "decode_frac_of_codec_roofline": (n_bytes + size) / td / 1e9 / peak,
         "codec_roofline_gbs": peak * n_bytes / (n_bytes + size),
         "ratio": n_bytes / size, "escape_rate": n_esc / n, "stream_bytes": size,
-        "memcpy_d2d_gbs": memcpy_gbs, "spec_hbm_gbs": 8000.0,
+        "memcpy_d2d_gbs": memcpy_gbs, "spec_hbm_gbs": SPEC_HBM_GBS, "hbm_achieved": hbm,
         "link_model": link_model(n_bytes, size, te, td),
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
-                          "hardware": "not named on the pages"},
+                          "e5m2_ratio": PAPER_E5M2_RATIO, "hardware": "not named on the pages"},
         "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online, "ablation": ablation, "paged": paged,
         "escape_sweep": sweep, "offload": offload, "e2e": e2e,
         "gpu_launches": sum(len(OPS[op][0]) for op in ops) * K, "clocks": clocks,
