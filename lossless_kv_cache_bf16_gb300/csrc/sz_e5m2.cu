@@ -266,11 +266,23 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
     bool contig;
     bool ok;
     if (MODE == 2) {
+        // 16 consecutive exponents cb0..cb0+15 with cb0 <= 16 (valid and
+        // codable by arithmetic) are recognised word by word; anything else
+        // takes the full check.  Every block runs this, so it is kept short.
         const uint32_t w[4] = {cbv.x, cbv.y, cbv.z, cbv.w};
-        uint8_t dcb[16];
+        const uint32_t c0 = w[0] & 0xFFu, run = c0 * 0x01010101u + 0x03020100u;
+        if (c0 <= 16 && w[0] == run && w[1] == run + 0x04040404u && w[2] == run + 0x08080808u &&
+            w[3] == run + 0x0C0C0C0Cu) {
 #pragma unroll
-        for (int k = 0; k < 16; k++) dcb[k] = (uint8_t)(w[k >> 2] >> (8 * (k & 3)));
-        ok = load_codebook(dcb, nullptr, 32u, cb, contig);
+            for (int k = 0; k < 16; k++) cb[k] = (uint8_t)(c0 + k);
+            contig = true;
+            ok = true;
+        } else {
+            uint8_t dcb[16];
+#pragma unroll
+            for (int k = 0; k < 16; k++) dcb[k] = (uint8_t)(w[k >> 2] >> (8 * (k & 3)));
+            ok = load_codebook(dcb, nullptr, 32u, cb, contig);
+        }
     } else {
         ok = load_codebook(p.cb, nullptr, 32u, cb, contig);
     }
