@@ -101,14 +101,17 @@ __device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t 
         const uint32_t d1 = ((e1 & 0x7F7F7F7Fu) + b7) ^ (e1 & 0x80808080u) ^ b8;
         uint32_t c0 = d0, c1 = d1;
         if ((d0 | d1) & 0xF0F0F0F0u) {
-            // Escapes: bytes with d >= 16.  One flag bit per byte (bit 0),
-            // codes of escaped bytes zeroed, flags gathered into a mask.
-            uint32_t f0 = d0 & 0xF0F0F0F0u, f1 = d1 & 0xF0F0F0F0u;
-            f0 |= f0 >> 2, f1 |= f1 >> 2;
-            f0 |= f0 >> 1, f1 |= f1 >> 1;
-            f0 = (f0 >> 4) & 0x01010101u, f1 = (f1 >> 4) & 0x01010101u;
-            c0 &= ~(f0 * 0xFFu), c1 &= ~(f1 * 0xFFu);
-            m = ((f0 * 0x01020408u) >> 24) | (((f1 * 0x01020408u) >> 20) & 0xF0u);
+            // Escapes: bytes with d >= 16, flagged in their bit 7 (adding
+            // 0x70 to the low 7 bits carries into bit 7 from 16 up; a set
+            // bit 7 is an escape already).  Codes of escaped bytes are zeroed
+            // (g >> 7 as a high multiply, times 0xFF), and the flags gathered
+            // into the mask by one high multiply: bit 8j + 7 lands on bit j,
+            // every other partial product below bit 32 or above bit 35.
+            const uint32_t g0 = (((d0 & 0x7F7F7F7Fu) + 0x70707070u) | d0) & 0x80808080u;
+            const uint32_t g1 = (((d1 & 0x7F7F7F7Fu) + 0x70707070u) | d1) & 0x80808080u;
+            c0 &= ~(mul_hi<1u << 25>(g0) * 0xFFu);
+            c1 &= ~(mul_hi<1u << 25>(g1) * 0xFFu);
+            m = mad_lo<16u>(mul_hi<0x02040810u>(g1) & 0xFu, mul_hi<0x02040810u>(g0) & 0xFu);
         }
         // Bytes 0, 2: code pairs (every byte of c is < 16, so c + (c >> 4) = c | (c >> 4)).
         const uint32_t p0 = mad_hi<1u << 28>(c0, c0), p1 = mad_hi<1u << 28>(c1, c1);
