@@ -70,6 +70,7 @@ struct EncodeSmem {
 
 struct GroupOut {
     uint32_t sm_lo, sm_hi, nib, esc;
+    uint32_t ex0, ex1;  // the exponent bytes of elements 0..3 and 4..7
 };
 
 // Split and code one group of 8 elements (four 32-bit words of BF16 pairs).
@@ -132,6 +133,8 @@ __device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t 
         o.nib &= (uint32_t)((1ull << (4 * cnt)) - 1ull);
     }
     o.esc = m;
+    o.ex0 = e0;
+    o.ex1 = e1;
     return o;
 }
 
@@ -196,7 +199,7 @@ __device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64
 // starting at element `base`: record index first + off[k] + rank in group.
 // One loop over all of the lane's escape bits (group k = bit / 8), so the
 // warp iterates as often as its busiest lane has escapes, not once per group.
-__device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const uint32_t (&w)[4][4],
+__device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const uint32_t (&ex)[4][2],
                                              const uint32_t (&esc)[4], const uint32_t (&off)[4], uint64_t first,
                                              uint8_t* dst, uint64_t limit) {
     const uint32_t all = esc[0] | (esc[1] << 8) | (esc[2] << 16) | (esc[3] << 24);
@@ -208,15 +211,12 @@ __device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const
         const uint32_t k = b >> 3, jj = b & 7u;
         const uint32_t offk = k < 2 ? (k == 0 ? off[0] : off[1]) : (k == 2 ? off[2] : off[3]);
         const uint32_t before = __popc(all & ((1u << b) - 1u) & (0xFFu << (8 * k)));  // earlier in the group
-        // Exponent of element jj of group k: bits 7..14 of its 16-bit half.
-        const uint32_t q = jj >> 1;
-        uint32_t g0, g1, g2, g3;
-        g0 = q < 2 ? (q == 0 ? w[0][0] : w[0][1]) : (q == 2 ? w[0][2] : w[0][3]);
-        g1 = q < 2 ? (q == 0 ? w[1][0] : w[1][1]) : (q == 2 ? w[1][2] : w[1][3]);
-        g2 = q < 2 ? (q == 0 ? w[2][0] : w[2][1]) : (q == 2 ? w[2][2] : w[2][3]);
-        g3 = q < 2 ? (q == 0 ? w[3][0] : w[3][1]) : (q == 2 ? w[3][2] : w[3][3]);
-        const uint32_t word = k < 2 ? (k == 0 ? g0 : g1) : (k == 2 ? g2 : g3);
-        const uint32_t e = (word >> (7 + 16 * (jj & 1u))) & 0xFFu;
+        // Exponent of element jj of group k: byte jj & 3 of its exponent word.
+        const bool hi = jj >= 4;
+        const uint32_t w0 = hi ? ex[0][1] : ex[0][0], w1 = hi ? ex[1][1] : ex[1][0];
+        const uint32_t w2 = hi ? ex[2][1] : ex[2][0], w3 = hi ? ex[3][1] : ex[3][0];
+        const uint32_t word = k < 2 ? (k == 0 ? w0 : w1) : (k == 2 ? w2 : w3);
+        const uint32_t e = (word >> (8 * (jj & 3u))) & 0xFFu;
         const uint32_t pos = pos_base + k * 256u + jj;
         const uint64_t at = 3ull * (first + offk + before);
         if (at + 3 <= limit) {
@@ -302,7 +302,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
             // threads leave the loop together.
             const bool failed_wait = !mbar_wait(&S.full[slot], (i / kEncStages) & 1u, p.wait_limit_ns);
             if (!failed_wait) waited = i + 1;
-            uint32_t w[4][4], cnt[4], esc[4];
+            uint32_t w[4][4], cnt[4], esc[4], ex[4][2];
             if (full_sub(u)) {
                 // Whole sub-tile in range, buffers aligned: no bounds logic;
                 // lane's group k sits at constant offsets from its group 0.
@@ -315,6 +315,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
                     w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
                     const GroupOut o = code_group<CONTIG, true>(w[k], 8, lane_add, S.code);
                     esc[k] = o.esc;
+                    ex[k][0] = o.ex0, ex[k][1] = o.ex1;
                     st_stream_v2(o_sm + k * 256, make_uint2(o.sm_lo, o.sm_hi));
                     st_stream_u32(o_nib + k * 128, o.nib);
                 }
@@ -325,6 +326,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
                     const uint64_t i0 = wbase + k * 256u + lane * 8u;
                     const GroupOut o = code_group<CONTIG, false>(w[k], cnt[k], lane_add, S.code);
                     esc[k] = o.esc;
+                    ex[k][0] = o.ex0, ex[k][1] = o.ex1;
                     if (p.vec && cnt[k] == 8) {
                         st_stream_v2(p.out + i0, make_uint2(o.sm_lo, o.sm_hi));
                         st_stream_u32(p.out + p.L.nib_off + i0 / 2, o.nib);
@@ -361,7 +363,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
             // that scan tile's records from the input.  They are gathered in
             // shared memory and leave once per scan tile, in 16-byte stores.
             if (warp_total && run + warp_off < p.ws_cap)
-                emit_records(wbase, lane, w, esc, off, run + warp_off, S.rec, 3ull * p.ws_cap);
+                emit_records(wbase, lane, ex, esc, off, run + warp_off, S.rec, 3ull * p.ws_cap);
             run += sub_esc;
         }
         if (aborted) break;  // block-uniform
