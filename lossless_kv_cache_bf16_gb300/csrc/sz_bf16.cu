@@ -90,10 +90,11 @@ __device__ __forceinline__ GroupOut code_group(const uint32_t (&w)[4], uint32_t 
     const uint32_t L1 = __byte_perm(w[2], w[3], 0x6420), H1 = __byte_perm(w[2], w[3], 0x7531);
     o.sm_lo = (H0 & 0x80808080u) | (L0 & 0x7F7F7F7Fu);
     o.sm_hi = (H1 & 0x80808080u) | (L1 & 0x7F7F7F7Fu);
-    // Exponent byte = (high byte << 1) | (low byte >> 7): disjoint fields, so
-    // a multiply-add and a high multiply (FMA pipe; the coding is ALU-bound).
-    const uint32_t e0 = mad_lo<2u>(H0 & 0x7F7F7F7Fu, mul_hi<1u << 25>(L0 & 0x80808080u));  // exponents 0..3
-    const uint32_t e1 = mad_lo<2u>(H1 & 0x7F7F7F7Fu, mul_hi<1u << 25>(L1 & 0x80808080u));  // exponents 4..7
+    // Exponent byte = (high byte << 1) | (low byte >> 7): both shifts as
+    // multiplies (FMA pipe; the coding is ALU-bound), then one 3-input op
+    // keeps bits 1..7 of the first and bit 0 of the second in every byte.
+    const uint32_t e0 = (mad_lo<2u>(H0, 0u) & 0xFEFEFEFEu) | (mul_hi<1u << 25>(L0) & 0x01010101u);  // exponents 0..3
+    const uint32_t e1 = (mad_lo<2u>(H1, 0u) & 0xFEFEFEFEu) | (mul_hi<1u << 25>(L1) & 0x01010101u);  // exponents 4..7
     uint32_t m = 0;
     if (CONTIG) {
         // sub_lo = (256 - cb0) mod 256 in every byte.
