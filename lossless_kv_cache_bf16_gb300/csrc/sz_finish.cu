@@ -14,9 +14,10 @@
 //  * a scan tile with more than ws_cap escapes has its ws_cap staged records
 //    copied by its warp, which then walks the rest of the tile (after the
 //    last staged position) again, in element order, 512 (BF16) or 1,024
-//    (E5M2) elements per step: 16-byte loads (all of a step's in flight at once), a warp scan of
-//    the escape counts, the step's records assembled in the warp's staging
-//    buffer and written with the same aligned word stores;
+//    (E5M2) elements per step: 16-byte loads (all of a step's in flight at
+//    once), a warp scan of the escape counts, the step's records assembled
+//    in the warp's staging buffer and written with the same aligned word
+//    stores;
 //  * a chunk's last scan tile writes the chunk's header (offset = escapes
 //    before the chunk, count = escapes in it); the last scan tile writes the
 //    stream size.
