@@ -381,12 +381,8 @@ __global__ void __launch_bounds__(kAblThreads, 4) decode_sentinel_kernel(const D
 cudaError_t launch_decode_sentinel(const DecodeParams& p, cudaStream_t s) {
     if (p.L.num_chunks == 0) return cudaSuccess;
     const size_t smem = sizeof(SentinelSmem);
-    cudaError_t err = cudaFuncSetAttribute(decode_sentinel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    int dev = 0, sms = 0, per_sm = 0;
-    if (err == cudaSuccess) err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess)
-        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_sentinel_kernel, kAblThreads, smem);
+    int sms = 0, per_sm = 0;
+    const cudaError_t err = kernel_fit((const void*)decode_sentinel_kernel, kAblThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(p.L.num_chunks, (uint64_t)std::max(per_sm, 1) * sms);
     decode_sentinel_kernel<<<grid, kAblThreads, smem, s>>>(p);

@@ -171,6 +171,51 @@ sz_status noalloc_scratch_for_current_device(void** out) {
 
 }  // namespace
 
+namespace sz {
+
+namespace {
+struct FitEntry {
+    int dev;
+    const void* kern;
+    int threads;
+    size_t smem;
+    int sms, per_sm;
+};
+constexpr int kMaxFits = 128;
+std::mutex g_fit_mu;
+FitEntry g_fit[kMaxFits];
+int g_fit_n = 0;
+}  // namespace
+
+cudaError_t kernel_fit(const void* kern, int threads, size_t smem, int* sms, int* per_sm) {
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    {
+        std::lock_guard<std::mutex> lock(g_fit_mu);
+        for (int k = 0; k < g_fit_n; k++) {
+            const FitEntry& f = g_fit[k];
+            if (f.dev == dev && f.kern == kern && f.threads == threads && f.smem == smem) {
+                *sms = f.sms;
+                *per_sm = f.per_sm;
+                return cudaSuccess;
+            }
+        }
+    }
+    FitEntry f{dev, kern, threads, smem, 0, 0};
+    if (smem > 0) err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm, kern, threads, smem);
+    if (err != cudaSuccess) return err;
+    *sms = f.sms;
+    *per_sm = f.per_sm;
+    std::lock_guard<std::mutex> lock(g_fit_mu);
+    if (g_fit_n < kMaxFits) g_fit[g_fit_n++] = f;  // a full table only costs the queries again
+    return cudaSuccess;
+}
+
+}  // namespace sz
+
 extern "C" {
 
 size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes) {

@@ -787,11 +787,8 @@ cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
     const void* kern = p.cb_dev   ? (const void*)encode_bf16_kernel<2>
                        : p.contig ? (paged ? (const void*)encode_bf16_kernel<1, true> : (const void*)encode_bf16_kernel<1>)
                                   : (paged ? (const void*)encode_bf16_kernel<0, true> : (const void*)encode_bf16_kernel<0>);
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    int dev = 0, sms = 0, per_sm = 0;
-    if (err == cudaSuccess) err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kComputeThreads, smem);
+    int sms = 0, per_sm = 0;
+    cudaError_t err = kernel_fit(kern, kComputeThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     EncodeParams q = p;
     q.grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
@@ -804,11 +801,8 @@ cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8) {
     const size_t smem = sizeof(DecodeSmem);
     auto kern = top8 ? decode_bf16_kernel<false, true> : p.pm.ids ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    int dev = 0, sms = 0, per_sm = 0;
-    if (err == cudaSuccess) err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem);
+    int sms = 0, per_sm = 0;
+    cudaError_t err = kernel_fit((const void*)kern, kDecThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
     kern<<<grid, kDecThreads, smem, s>>>(p);

@@ -698,7 +698,8 @@ cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
     auto kern = p.cb_dev   ? encode_e5m2_kernel<2>
                 : p.contig ? (paged ? encode_e5m2_kernel<1, true> : encode_e5m2_kernel<1>)
                            : (paged ? encode_e5m2_kernel<0, true> : encode_e5m2_kernel<0>);
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int sms = 0, per_sm = 0;  // one block per scan tile; only the shared memory limit matters
+    cudaError_t err = kernel_fit((const void*)kern, kEncThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     kern<<<p.num_tiles, kEncThreads, smem, s>>>(p);
     err = cudaGetLastError();
@@ -709,11 +710,8 @@ cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {
     const size_t smem = sizeof(DecodeE5Smem);
     auto kern = p.pm.ids ? decode_e5m2_kernel<true> : decode_e5m2_kernel<false>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    int dev = 0, sms = 0, per_sm = 0;
-    if (err == cudaSuccess) err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err == cudaSuccess) err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kE5DecThreads, smem);
+    int sms = 0, per_sm = 0;
+    cudaError_t err = kernel_fit((const void*)kern, kE5DecThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
     kern<<<grid, kE5DecThreads, smem, s>>>(p);

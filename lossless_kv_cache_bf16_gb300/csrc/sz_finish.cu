@@ -278,9 +278,8 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
 }
 
 cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s) {
-    int dev = 0, sms = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 0, per_sm = 0;
+    cudaError_t err = kernel_fit((const void*)finish_kernel<true, false>, kFinThreads, 0, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     // Several blocks per SM: the record copies are latency bound.
     const uint64_t want = (uint64_t)4 * sms;

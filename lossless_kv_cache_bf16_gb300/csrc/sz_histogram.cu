@@ -175,18 +175,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const unsigned long
 }
 
 cudaError_t launch_histogram(const HistogramParams& p, cudaStream_t s) {
-    int dev = 0, sms = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (err != cudaSuccess) return err;
+
     // Every line (stride 1): coalesced already; sparse samples load four
     // pieces at a time.
     const bool dense = p.stride == 1;
     const uint32_t U = dense ? 1u : 4u;
     const void* kern = p.bf16 ? (dense ? (const void*)histogram_kernel<true, 1> : (const void*)histogram_kernel<true, 4>)
                               : (dense ? (const void*)histogram_kernel<false, 1> : (const void*)histogram_kernel<false, 4>);
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kHistThreads, 0);
+    int sms = 0, per_sm = 0;
+    const cudaError_t err = kernel_fit(kern, kHistThreads, 0, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     const uint64_t lines = (p.n * (p.bf16 ? 2 : 1) + kLineBytes - 1) / kLineBytes;
     const uint64_t pieces = (lines + p.stride - 1) / p.stride * kPieces;

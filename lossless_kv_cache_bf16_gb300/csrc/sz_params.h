@@ -96,6 +96,13 @@ constexpr uint32_t kScanTile = 32768;
 // multiple of 16 so that every tile's staged run starts 16-byte aligned).
 constexpr uint32_t kMaxStageRecs = 1024;
 
+// Launch shape of kernel `kern` with `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device: the SM count and how many
+// blocks fit per SM.  The first query per device and kernel also raises the
+// kernel's dynamic shared memory limit to `smem`; the answers are cached, so
+// a call after that costs one cudaGetDevice and a table lookup.
+cudaError_t kernel_fit(const void* kern, int threads, size_t smem, int* sms, int* per_sm);
+
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s);
 // top8: the Top-8 layout of the codebook ablation (see sz_ablation_decode).
 cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8 = false);
