@@ -689,6 +689,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
             };
             if (full_tile(t)) {
                 // Whole tile in the stage slot: no bounds to check.
+                const RunOffset<PAGED> tile_off(p.pm, base, 13, 2, p.status);  // 8,192-element tile
                 const uint8_t* ssm = S.sm[slot] + qt;
                 const uint8_t* snb = S.nib[slot] + qt / 2;
                 const uint32_t* scw = reinterpret_cast<const uint32_t*>(S.nib[slot]);
@@ -705,8 +706,9 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                         codes = *reinterpret_cast<const uint32_t*>(snb + k * 128);
                     }
                     decode_group(k, *reinterpret_cast<const uint2*>(ssm + k * 256), codes, y);
-                    // A group of 8 never straddles a page.
-                    uint8_t* dst = PAGED ? p.out + elem_offset<true>(p.pm, base + qt + k * 256u, 2, p.status) : o + k * 512;
+                    // A group of 8 never straddles a page; a tile in one page
+                    // takes one lookup.
+                    uint8_t* dst = PAGED ? p.out + tile_off.at(p.pm, base, qt + k * 256u, 2, p.status) : o + k * 512;
                     st_stream_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
                 }
             } else {

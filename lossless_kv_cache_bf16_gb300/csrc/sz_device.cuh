@@ -181,6 +181,23 @@ __device__ __forceinline__ uint64_t elem_offset(const PageMap& m, uint64_t e, ui
     return off;
 }
 
+// Byte offset of element first + i (0 <= i < 2^lg_run) of a run that starts
+// at `first`, aligned to 2^lg_run elements: when the run lies in one page
+// (pages of at least 2^lg_run elements) one page lookup serves the whole run.
+template <bool PAGED>
+struct RunOffset {
+    uint64_t base;
+    bool one_page;
+    __device__ __forceinline__ RunOffset(const PageMap& m, uint64_t first, uint32_t lg_run, uint32_t esize, int* status) {
+        one_page = !PAGED || m.lg >= lg_run;
+        base = one_page ? elem_offset<PAGED>(m, first, esize, status) : 0ull;
+    }
+    __device__ __forceinline__ uint64_t at(const PageMap& m, uint64_t first, uint32_t i, uint32_t esize,
+                                           int* status) const {
+        return one_page ? base + (uint64_t)i * esize : elem_offset<PAGED>(m, first + i, esize, status);
+    }
+};
+
 // Integer multiply-adds with a constant multiplier (IMAD, on the FMA pipe).
 // A right shift by k of a word whose low k bits are masked off is a high
 // multiply by 2^(32-k), and adding disjoint bit fields equals OR-ing them, so

@@ -254,12 +254,13 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
 
     // Input bytes into this thread's row.
     if (warp_full) {
+        // A 16-element piece never straddles a page; the warp's 4,096
+        // elements in one page take one lookup.
+        const RunOffset<PAGED> run(p.pm, warp_base, 12, 1, p.status);
 #pragma unroll
         for (uint32_t i = 0; i < 8; i++) {
             const uint32_t piece = lane + 32 * i;
-            // A 16-element piece never straddles a page.
-            s_in[warp][swz8(piece >> 3, piece & 7u)] =
-                ld_stream_v4(p.in + elem_offset<PAGED>(p.pm, warp_base + 16 * piece, 1, p.status));
+            s_in[warp][swz8(piece >> 3, piece & 7u)] = ld_stream_v4(p.in + run.at(p.pm, warp_base, 16 * piece, 1, p.status));
         }
     }
     uint8_t cb[16];
@@ -669,11 +670,13 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
         // The warp's rows -> global memory.
         const uint64_t wbase = base + warp * (32u * kE5DecPer);
         if (p.vec && wbase + 32u * kE5DecPer <= n) {
+            // 16 elements never straddle a page; the warp's 2,048 elements in
+            // one page take one lookup.
+            const RunOffset<PAGED> run(p.pm, wbase, 11, 1, p.status);
 #pragma unroll
             for (uint32_t r = 0; r < 4; r++) {
-                const uint32_t piece = lane + 32 * r;  // 16 elements: never straddles a page
-                st_stream_v4(p.out + elem_offset<PAGED>(p.pm, wbase + 16 * piece, 1, p.status),
-                             rows[swz4(piece >> 2, piece & 3u)]);
+                const uint32_t piece = lane + 32 * r;
+                st_stream_v4(p.out + run.at(p.pm, wbase, 16 * piece, 1, p.status), rows[swz4(piece >> 2, piece & 3u)]);
             }
         } else {
             const uint8_t* row = reinterpret_cast<const uint8_t*>(rows);
