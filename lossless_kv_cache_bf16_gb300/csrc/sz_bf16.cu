@@ -574,8 +574,10 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
         uint32_t took = 0;
 #pragma unroll
         for (uint32_t k = 0; k < kDecR; k++) {
-            const uint32_t r = cursor + tid + k * kDecThreads;
-            if (r >= chunk_end) break;
+            // 64-bit: cursor + 511 may pass 2^32 near the end of 2^32 records.
+            const uint64_t r64 = (uint64_t)cursor + tid + k * kDecThreads;
+            if (r64 >= chunk_end) break;
+            const uint32_t r = (uint32_t)r64;
             const uint8_t* rp = W.at(r);
             const uint32_t pos = (uint32_t)rp[0] | ((uint32_t)rp[1] << 8);
             if (pos >= p0 + kBf16Tile) break;

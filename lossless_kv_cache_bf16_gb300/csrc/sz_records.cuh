@@ -43,14 +43,14 @@ struct RecordWindow {
     __device__ __forceinline__ static uint32_t next(uint32_t s) { return s == 2 ? 0u : s + 1; }
     // Where record `first` lands in buffer b: the copies start at the 16-byte
     // boundary below it.
-    __device__ __forceinline__ const uint8_t* start(uint32_t first, uint32_t b) const {
+    __device__ __forceinline__ const uint8_t* start(uint64_t first, uint32_t b) const {
         return buf[b] + (reinterpret_cast<uintptr_t>(rec + 3ull * first) & 15u);
     }
     // Issues the copies of records [first, first + kWinRecs) (clipped to the
     // stream) into buffer b; at most 194 pieces, one per thread.
-    __device__ __forceinline__ void issue(uint32_t first, uint32_t b) const {
+    __device__ __forceinline__ void issue(uint64_t first, uint32_t b) const {
         if (first >= n_esc) return;
-        const uint32_t len = n_esc - first < kWinRecs ? n_esc - first : kWinRecs;
+        const uint32_t len = n_esc - first < kWinRecs ? (uint32_t)(n_esc - first) : kWinRecs;
         const uintptr_t s = reinterpret_cast<uintptr_t>(rec + 3ull * first), e = s + 3ull * len;
         const uintptr_t as = s & ~(uintptr_t)15;
         const uint32_t pieces = (uint32_t)((e - as + 15) / 16);
@@ -61,7 +61,7 @@ struct RecordWindow {
     }
     __device__ __forceinline__ void set_bases() {
         base0 = start(lo, slot);
-        base1 = start(lo + kWinRecs, next(slot));
+        base1 = start((uint64_t)lo + kWinRecs, next(slot));
     }
     // Record j (resident): its 3 bytes.
     __device__ __forceinline__ const uint8_t* at(uint32_t j) const {
@@ -73,31 +73,33 @@ struct RecordWindow {
         return (uint32_t)r[0] | ((uint32_t)r[1] << 8);
     }
     // Makes records [need_lo, need_hi) resident (need_hi - need_lo <=
-    // kWinRecs + 1; nothing when empty).  Block-wide.
+    // kWinRecs + 1; nothing when empty).  Block-wide.  Window bounds are
+    // 64-bit: lo + 3 kWinRecs may pass 2^32 near the end of 2^32 records.
     __device__ __forceinline__ void cover(uint32_t need_lo, uint32_t need_hi) {
         if (need_hi <= need_lo) return;
-        if (valid && need_lo >= lo + kWinRecs && need_hi <= lo + 3 * kWinRecs) {
+        const uint64_t lo64 = lo;
+        if (valid && need_lo >= lo64 + kWinRecs && need_hi <= lo64 + 3 * kWinRecs) {
             // The older window is done with: the in-flight one joins, and
             // the freed buffer loads the window after it.
             cp_async_wait_all();
             __syncthreads();
             lo += kWinRecs;
             slot = next(slot);
-            issue(lo + 2 * kWinRecs, next(next(slot)));
+            issue((uint64_t)lo + 2 * kWinRecs, next(next(slot)));
             cp_async_commit();
             set_bases();
         }
-        if (!valid || need_lo < lo || need_hi > lo + 2 * kWinRecs) {
+        if (!valid || need_lo < lo || need_hi > (uint64_t)lo + 2 * kWinRecs) {
             cp_async_wait_all();  // no copy may land in a buffer after this reload
             __syncthreads();
             lo = need_lo;
             slot = 0;
             valid = true;
             issue(lo, 0);
-            issue(lo + kWinRecs, 1);
+            issue((uint64_t)lo + kWinRecs, 1);
             cp_async_wait_all();
             __syncthreads();
-            issue(lo + 2 * kWinRecs, 2);
+            issue((uint64_t)lo + 2 * kWinRecs, 2);
             cp_async_commit();
             set_bases();
         }
