@@ -68,18 +68,21 @@ class Pipeline:
     """Offload/reload of tensors of n elements of type dt with codebook cb,
     on `device`, cut into `parts` segments.  Buffers are allocated once:
     two device staging buffers and a workspace for the largest segment, and a
-    pinned host buffer for the worst-case streams of all segments."""
+    pinned host buffer of host_bytes (default: the worst case of all
+    segments, every element an escape).  The streams are packed one after
+    the other in the host buffer; an offload whose streams do not fit raises
+    SplitZipError with SZ_ERR_CAPACITY."""
 
-    def __init__(self, dt: int, cb, n: int, device, parts: int = 8):
+    def __init__(self, dt: int, cb, n: int, device, parts: int = 8, host_bytes: int | None = None):
         self.dt, self.cb, self.n = dt, [int(v) for v in cb], n
         self.device = torch.device(device)
         self.segs = segments(n, parts)
         self.caps = [S.sz_encoded_size(dt, a1 - a0, a1 - a0) for a0, a1 in self.segs]
-        self.offsets = [sum(self.caps[:i]) for i in range(len(self.segs))]
         big = max(a1 - a0 for a0, a1 in self.segs)
         self.dev = [torch.empty(max(self.caps), dtype=torch.uint8, device=self.device) for _ in range(2)]
         self.ws = torch.empty(S.sz_workspace_size(dt, big), dtype=torch.uint8, device=self.device)
-        self.host = torch.empty(sum(self.caps), dtype=torch.uint8, pin_memory=True)
+        self.host = torch.empty(sum(self.caps) if host_bytes is None else host_bytes, dtype=torch.uint8,
+                                pin_memory=True)
         k = len(self.segs)
         self.sizes_h = torch.zeros(k, dtype=torch.int64, pin_memory=True)
         self.status = torch.zeros(k, dtype=torch.int32, device=self.device)
@@ -120,22 +123,27 @@ class Pipeline:
                             self.status[i:i + 1], self.ws, n=a1 - a0)
                 enc[i].record(self.codec)
 
-        sizes = []
+        sizes, offsets, o = [], [], 0
         encode(0)
         for i in range(k):
             if i + 1 < k:
                 encode(i + 1)
             enc[i].synchronize()  # host learns segment i's size; the GPU runs on
             size = int(self.sizes_h[i])
+            if o + size > self.host.numel():
+                self.codec.synchronize()
+                self.copy.synchronize()
+                raise S.SplitZipError("offload", S.SZ_ERR_CAPACITY)
             sizes.append(size)
-            o = self.offsets[i]
+            offsets.append(o)
             with torch.cuda.stream(self.copy):
                 self.copy.wait_event(enc[i])
                 self.host[o:o + size].copy_(self.dev[i % 2][:size], non_blocking=True)
                 freed[i % 2].record(self.copy)
+            o += size
         self.copy.synchronize()
         self._check_status("offload")
-        return HostStreams(dt, self.n, list(self.segs), list(self.offsets), sizes, self.host)
+        return HostStreams(dt, self.n, list(self.segs), offsets, sizes, self.host)
 
     def reload(self, hs: HostStreams, y: torch.Tensor) -> None:
         """Decodes hs into y on the device; y is ready on the current stream

@@ -79,3 +79,23 @@ def test_encode_writes_its_size_to_pinned_host_memory():
     assert int(host_size[0]) == int(dev_size.item()) > 0
     with pytest.raises(ValueError):
         S.sz_encode(S.SZ_BF16, CB_MID, x, out, torch.zeros(1, dtype=torch.int64), None, ws)
+
+
+def test_packed_host_buffer_and_capacity():
+    from lossless_kv_cache_bf16_gb300 import splitzip as S
+    from lossless_kv_cache_bf16_gb300 import transfer as T
+
+    n = 5 * 65_536 + 3
+    x = _tensor("bf16", n, 8)
+    need = T.Pipeline(G.DT["bf16"], CB_MID, n, "cuda", parts=3).offload(x).nbytes
+    pipe = T.Pipeline(G.DT["bf16"], CB_MID, n, "cuda", parts=3, host_bytes=need)
+    hs = pipe.offload(x)
+    assert hs.nbytes == need and hs.offsets == [sum(hs.sizes[:i]) for i in range(len(hs.sizes))]
+    y = torch.empty_like(x)
+    pipe.reload(hs, y)
+    pipe.reload_status()
+    assert torch.equal(y.view(torch.uint8), x.view(torch.uint8))
+    small = T.Pipeline(G.DT["bf16"], CB_MID, n, "cuda", parts=3, host_bytes=need - 1)
+    with pytest.raises(S.SplitZipError) as e:
+        small.offload(x)
+    assert e.value.status == S.SZ_ERR_CAPACITY
