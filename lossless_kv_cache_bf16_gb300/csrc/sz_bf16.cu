@@ -349,16 +349,20 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
                 break;
             }
             if (tid == 0 && issued < my_subs) issue(issued++);
-            uint32_t warp_off = 0, sub_esc = 0;
+            uint32_t warp_off, sub_esc;
             {
+                // Inclusive prefix sums of the 8 warp totals; this warp's
+                // offset is the one before it, picked by the warp index bits
+                // (fixed per thread, so the tests leave the loop).
+                static_assert(kWarps == 8, "eight warp totals");
                 const uint4 a = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][0]);
                 const uint4 b = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][4]);
-                const uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-                for (uint32_t v = 0; v < kWarps; v++) {
-                    warp_off += v < warp ? c[v] : 0u;
-                    sub_esc += c[v];
-                }
+                const uint32_t p0 = a.x, p1 = p0 + a.y, p2 = p1 + a.z, p3 = p2 + a.w;
+                const uint32_t p4 = p3 + b.x, p5 = p4 + b.y, p6 = p5 + b.z, p7 = p6 + b.w;
+                const uint32_t lo = (warp & 2u) ? ((warp & 1u) ? p2 : p1) : ((warp & 1u) ? p0 : 0u);
+                const uint32_t hi = (warp & 2u) ? ((warp & 1u) ? p6 : p5) : ((warp & 1u) ? p4 : p3);
+                warp_off = (warp & 4u) ? hi : lo;
+                sub_esc = p7;
             }
             // Records beyond ws_cap are not staged; the finish kernel re-derives
             // that scan tile's records from the input.  They are gathered in
