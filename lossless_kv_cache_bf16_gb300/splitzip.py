@@ -120,13 +120,25 @@ def _elements(dt: int, t: torch.Tensor) -> int:
     return nbytes // ELEMENT_BYTES[dt]
 
 
+_CODEBOOKS: dict = {}  # codebook values -> its C struct (read by the library during a call only)
+
+
 def _codebook(cb) -> sz_codebook:
-    vals = [int(v) for v in (cb.tolist() if hasattr(cb, "tolist") else cb)]
-    if len(vals) != SZ_CODEBOOK_SIZE:
-        raise ValueError("a codebook has 16 exponents")
-    c = sz_codebook()
-    for k, v in enumerate(vals):
-        c.exp[k] = v
+    if isinstance(cb, sz_codebook):
+        return cb
+    key = tuple(cb.tolist() if hasattr(cb, "tolist") else cb)
+    c = _CODEBOOKS.get(key)
+    if c is None:
+        vals = [int(v) for v in key]
+        if len(vals) != SZ_CODEBOOK_SIZE:
+            raise ValueError("a codebook has 16 exponents")
+        if any(v < 0 or v > 255 for v in vals):
+            raise ValueError("codebook exponents are bytes (0..255)")
+        c = sz_codebook()
+        for k, v in enumerate(vals):
+            c.exp[k] = v
+        if len(_CODEBOOKS) < 1024:
+            _CODEBOOKS[key] = c
     return c
 
 

@@ -131,3 +131,16 @@ def test_ablation_codebook_and_sizes_match_oracle(S, orc):
             assert S.sz_ablation_codebook(variant, h) == [int(v) for v in orc.abl_codebook(ov, h)]
         for n, e in ((0, 0), (1, 1), (65536, 9), (65537, 65537), (10 ** 6, 123)):
             assert S.sz_ablation_encoded_size(variant, n, e) == orc.abl_size(ov, n, e)
+
+
+def test_codebook_marshalling(S):
+    import numpy as np
+
+    cb = list(range(120, 136))
+    c = S._codebook(cb)
+    assert list(c.exp) == cb
+    assert S._codebook(np.arange(120, 136, dtype=np.uint8)) is c   # cached by value
+    assert S._codebook(c) is c
+    for bad in ([1, 2, 3], [300] + list(range(15)), [-1] + list(range(15))):
+        with pytest.raises(ValueError):
+            S._codebook(bad)
