@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
         for (int k = 0; k < kCodes; k++) member |= cb[k] == tid;
         s_member[tid] = (uint8_t)member;
     }
+    // The kernel is launched as a programmatic dependent of the encode
+    // kernel, so the lines above overlap its tail; everything below reads
+    // what it wrote, once it has finished (no wait without that launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Escapes in all scan tiles before this block's range.  ws_count is
     // 16-byte aligned.
     uint32_t part = 0;
@@ -285,13 +289,22 @@ cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s) {
     const uint64_t want = (uint64_t)4 * sms;
     const uint32_t grid = (uint32_t)(p.num_tiles < want ? p.num_tiles : want);
     const bool paged = p.pm.ids != nullptr;
-    if (bf16)
-        paged ? finish_kernel<true, true><<<grid, kFinThreads, 0, s>>>(p)
-              : finish_kernel<true, false><<<grid, kFinThreads, 0, s>>>(p);
-    else
-        paged ? finish_kernel<false, true><<<grid, kFinThreads, 0, s>>>(p)
-              : finish_kernel<false, false><<<grid, kFinThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    auto kern = bf16 ? (paged ? finish_kernel<true, true> : finish_kernel<true, false>)
+                     : (paged ? finish_kernel<false, true> : finish_kernel<false, false>);
+    // A programmatic dependent launch: the kernel may start before the encode
+    // kernel ahead of it in the stream has finished, and waits for it at
+    // griddepcontrol.wait, which hides the launch gap.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace sz
