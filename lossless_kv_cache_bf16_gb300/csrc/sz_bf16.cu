@@ -477,6 +477,7 @@ template <bool PAGED, bool TOP8 = false>
 __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const DecodeParams p) {
     constexpr uint32_t kCodeBytes = TOP8 ? kBf16Tile / 8 * 3 : kBf16Tile / 2;  // code bytes per tile
     constexpr int kEntries = TOP8 ? 8 : kCodes;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // launched as a programmatic dependent
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem& S = *reinterpret_cast<DecodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -813,8 +814,9 @@ cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8)
     cudaError_t err = kernel_fit((const void*)kern, kDecThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
-    kern<<<grid, kDecThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    // A programmatic dependent of whatever kernel precedes it (the stream's
+    // producer): only the launch overlaps, the kernel waits first thing.
+    return launch_dependent(kern, dim3(grid), dim3(kDecThreads), smem, s, p);
 }
 
 }  // namespace sz

@@ -445,6 +445,7 @@ __device__ __forceinline__ void decode_rows(const uint32_t (&pw)[14], uint32_t c
 // PAGED: the output is a paged tensor (DecodeParams::pm).
 template <bool PAGED>
 __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const DecodeParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // launched as a programmatic dependent
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeE5Smem& S = *reinterpret_cast<DecodeE5Smem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -719,8 +720,9 @@ cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {
     cudaError_t err = kernel_fit((const void*)kern, kE5DecThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(p.num_tiles, (uint64_t)std::max(per_sm, 1) * sms);
-    kern<<<grid, kE5DecThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    // A programmatic dependent of whatever kernel precedes it (the stream's
+    // producer): only the launch overlaps, the kernel waits first thing.
+    return launch_dependent(kern, dim3(grid), dim3(kE5DecThreads), smem, s, p);
 }
 
 }  // namespace sz

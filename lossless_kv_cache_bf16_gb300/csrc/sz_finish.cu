@@ -291,20 +291,8 @@ cudaError_t launch_finish(const EncodeParams& p, bool bf16, cudaStream_t s) {
     const bool paged = p.pm.ids != nullptr;
     auto kern = bf16 ? (paged ? finish_kernel<true, true> : finish_kernel<true, false>)
                      : (paged ? finish_kernel<false, true> : finish_kernel<false, false>);
-    // A programmatic dependent launch: the kernel may start before the encode
-    // kernel ahead of it in the stream has finished, and waits for it at
-    // griddepcontrol.wait, which hides the launch gap.
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kFinThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    // A programmatic dependent of the encode kernel ahead of it.
+    return launch_dependent(kern, dim3(grid), dim3(kFinThreads), 0, s, p);
 }
 
 }  // namespace sz

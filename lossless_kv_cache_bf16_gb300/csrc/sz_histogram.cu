@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const unsigned long
     __shared__ unsigned long long s_key[kSelThreads / 32];
     __shared__ uint32_t s_win, s_rank[kSelThreads / 32];
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the counts are complete
     const unsigned long long count = tid < bins ? hist[tid] : 0ull;
     bool taken = false;
     for (int round = 0; round < kCodes; round++) {
@@ -195,8 +196,8 @@ cudaError_t launch_histogram(const HistogramParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_select(const unsigned long long* hist, uint32_t bins, uint8_t* cb_out, cudaStream_t s) {
-    select_kernel<<<1, kSelThreads, 0, s>>>(hist, bins, cb_out);
-    return cudaGetLastError();
+    // A programmatic dependent of the histogram kernel ahead of it.
+    return launch_dependent(select_kernel, dim3(1), dim3(kSelThreads), 0, s, hist, bins, cb_out);
 }
 
 }  // namespace sz

@@ -96,6 +96,26 @@ constexpr uint32_t kScanTile = 32768;
 // multiple of 16 so that every tile's staged run starts 16-byte aligned).
 constexpr uint32_t kMaxStageRecs = 1024;
 
+// Launches kern as a programmatic dependent of the kernel before it in the
+// stream: its blocks may be scheduled while that kernel finishes, and must
+// execute griddepcontrol.wait before reading anything it wrote (the wait
+// returns at once when there is no such kernel).  This hides launch gaps.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Launch shape of kernel `kern` with `threads` threads and `smem` bytes of
 // dynamic shared memory on the current device: the SM count and how many
 // blocks fit per SM.  The first query per device and kernel also raises the
