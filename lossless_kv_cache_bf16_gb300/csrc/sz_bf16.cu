@@ -716,7 +716,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     // A group of 8 never straddles a page; a tile in one page
                     // takes one lookup.
                     uint8_t* dst = PAGED ? p.out + tile_off.at(p.pm, base, qt + k * 256u, 2, p.status) : o + k * 512;
-                    st_stream_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
+                    st_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
                 }
             } else {
 #pragma unroll
@@ -746,7 +746,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     decode_group(k, smv, nibv, y);
                     uint8_t* dst = p.out + (cnt ? elem_offset<PAGED>(p.pm, i0, 2, p.status) : 2 * i0);
                     if (p.vec && cnt == 8) {
-                        st_stream_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
+                        st_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
                     } else {
 #pragma unroll
                         for (uint32_t jj = 0; jj < 8; jj++) {

@@ -222,7 +222,7 @@ __device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5
 #pragma unroll
         for (uint32_t i = 0; i < 7; i++) {
             const uint32_t piece = lane + 32 * i;
-            st_stream_v4(p.out + out_base + 16 * piece, s_out[warp][piece]);
+            st_v4(p.out + out_base + 16 * piece, s_out[warp][piece]);
         }
     } else if (cnt > 0) {
         const uint32_t nbytes = 7 * ((cnt + 7) / 8);
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kE5DecThreads, 4) decode_e5m2_kernel(const Dec
 #pragma unroll
             for (uint32_t r = 0; r < 4; r++) {
                 const uint32_t piece = lane + 32 * r;
-                st_stream_v4(p.out + run.at(p.pm, wbase, 16 * piece, 1, p.status), rows[swz4(piece >> 2, piece & 3u)]);
+                st_v4(p.out + run.at(p.pm, wbase, 16 * piece, 1, p.status), rows[swz4(piece >> 2, piece & 3u)]);
             }
         } else {
             const uint8_t* row = reinterpret_cast<const uint8_t*>(rows);
