@@ -7,15 +7,15 @@
 // a 56-bit little-endian word stored as 7 bytes; escapes use the same
 // (u16 position, u8 exponent) stream as BF16.
 //
-// Work layout.  Thread t of a block owns 128 contiguous elements = 16 groups
-// = 128 input bytes and 112 packed bytes.  A warp's 4 KB of elements and
-// 3.5 KB of packed bytes move between global memory and registers through a
-// per-warp shared-memory transpose, so every global access is a fully
-// coalesced 16 B/lane instruction and every shared access is free of bank
-// conflicts (XOR swizzle for 8-piece rows; the 7-piece rows need none
-// because 7 is odd).  The encoder's block of 256 threads owns one
-// 32,768-element scan tile; the decoder's block of 128 threads owns a
-// 16,384-element tile.
+// Work layout.  Encoder: a block of 256 threads owns one 32,768-element scan
+// tile, and thread t codes 128 contiguous elements of it (16 groups: 128
+// input bytes, 112 packed bytes).  A warp's 4 KB of elements and 3.5 KB of
+// packed bytes move between global memory and registers through a per-warp
+// shared-memory transpose, so every global access is a fully coalesced
+// 16 B/lane instruction and every shared access is free of bank conflicts
+// (XOR swizzle for 8-piece rows; the 7-piece rows need none because 7 is
+// odd).  Decoder: persistent blocks of 256 threads work through 16,384-element
+// tiles, thread t decoding elements 64t..64t+63 of a tile (see below).
 #include <algorithm>
 
 #include "sz_device.cuh"
