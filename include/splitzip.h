@@ -36,8 +36,10 @@
  * Conventions for every call:
  *  - Pointers named d_* are device pointers, h_* host pointers.  The caller
  *    owns every buffer; the library allocates no memory and keeps no state
- *    between calls, so calls on different streams with different buffers may
- *    run concurrently.
+ *    between calls other than a per-device cache of kernel launch shapes
+ *    (filled under a lock on first use), so calls on different streams with
+ *    different buffers, from any host threads, may run concurrently.  The one
+ *    exception is sz_encode_noalloc's static scratch, below.
  *  - Element data needs only its natural alignment (2 bytes for BF16); the
  *    kernels take a vectorised path when the buffers are 16-byte aligned and
  *    N is a multiple of 32, and a byte-exact slower path otherwise.
@@ -204,9 +206,11 @@ sz_status sz_encode_dcb(sz_dtype dt, const uint8_t* d_cb, const void* d_in, size
  *  d_out           n elements of dtype dt (device)
  *  d_status        device int or NULL: SZ_OK or SZ_ERR_CORRUPT (bad codebook,
  *                  headers that are not a running sum, a position outside its
- *                  chunk or out of order, an E5M2 exponent above 31).  On
- *                  SZ_ERR_CORRUPT the contents of d_out are unspecified, but
- *                  nothing outside d_out[0, n) is written.
+ *                  chunk or out of order, an E5M2 exponent above 31), or
+ *                  SZ_ERR_TIMEOUT if an in-kernel copy did not land within
+ *                  the bounded wait (about 1 s).  On an error the contents of
+ *                  d_out are unspecified, but nothing outside d_out[0, n) is
+ *                  written.
  * Asynchronous. */
 sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n,
                     void* d_out, int* d_status, cudaStream_t stream);
