@@ -240,6 +240,35 @@ sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t
                           void* d_pool, size_t pool_pages, size_t page_elems,
                           const int32_t* d_block_ids, int* d_status, cudaStream_t stream);
 
+/* Concatenation of shard streams into the stream of the whole tensor.  The
+ * chunk headers make every 65,536-element chunk addressable on its own
+ * ([MET] "Flujo de Escape": positions are 16-bit, so escapes are grouped per
+ * chunk), so a tensor cut into shards of whole chunks can be encoded shard by
+ * shard (on one GPU each, or as pipeline segments) and joined afterwards:
+ * the dense parts and the escape records are copied to their places, the
+ * codebook once, and each shard's header offsets are shifted by the escapes
+ * of the shards before it (an exclusive scan of the shard escape counts, on
+ * the host from the stream sizes).  The result is byte-for-byte the stream
+ * sz_encode gives for the whole tensor with the same codebook.
+ *  count           number of shards (>= 1), in tensor order
+ *  h_streams       host array of count device pointers to the shard streams
+ *  h_bytes, h_n    host arrays: each shard's stream size and element count;
+ *                  every shard but the last must hold whole chunks
+ *                  (h_n[k] % 65536 == 0, 0 allowed), and each size must be
+ *                  the closed form for h_n[k] and some escape count, else
+ *                  SZ_ERR_INVALID_ARG / SZ_ERR_CORRUPT is returned at once
+ *  d_out           device buffer of out_capacity bytes, not overlapping any
+ *                  shard stream; receives sz_encoded_size(dt, sum n, sum E)
+ *                  bytes, the size also written to *h_out_bytes (nullable)
+ *  d_status        device int or NULL: SZ_OK, or SZ_ERR_INVALID_ARG when a
+ *                  shard's codebook differs from the first shard's
+ * Asynchronous (device-to-device copies and one header kernel per 64
+ * shards).  The shards' own headers are not checked here; a decode of the
+ * result checks them all. */
+sz_status sz_concat(sz_dtype dt, size_t count, const void* const* h_streams, const size_t* h_bytes,
+                    const size_t* h_n, void* d_out, size_t out_capacity, size_t* h_out_bytes,
+                    int* d_status, cudaStream_t stream);
+
 /* The codebook ablation's two alternative designs as working BF16 codecs,
  * for measuring their decode speed against this format ([RES] "Estudios de
  * Ablacion": Top-8 is reported to decode 3x slower, a Top-15 sentinel 3.5x

@@ -74,6 +74,8 @@ def _load() -> ctypes.CDLL:
         "sz_ablation_encode": (i32, [i32, vp, vp, sz, vp, sz, vp, vp, sz, vp]),
         "sz_ablation_decode": (i32, [i32, vp, sz, sz, vp, vp, vp]),
         "sz_decode_paged": (i32, [i32, vp, sz, sz, vp, sz, sz, vp, vp, vp]),
+        "sz_concat": (i32, [i32, sz, ctypes.POINTER(vp), ctypes.POINTER(sz), ctypes.POINTER(sz), vp, sz,
+                            ctypes.POINTER(sz), vp, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -293,6 +295,27 @@ def sz_decode_paged(dt: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, 
            LIB.sz_decode_paged(dt, _dev_ptr(stream_bytes, "stream"), in_bytes, n, _dev_ptr(pool, "pool"),
                                _pool_pages(dt, pool, page_elems), page_elems, _dev_ptr(block_ids, "block_ids"),
                                _dev_ptr(status, "status"), _stream(stream)))
+
+
+def sz_concat(dt: int, streams, sizes, ns, out: torch.Tensor, status: torch.Tensor | None = None,
+              stream=None) -> int:
+    """Join shard streams (device tensors in tensor order; sizes[k] bytes of
+    streams[k] encode ns[k] elements) into the stream of the whole tensor in
+    `out`.  Returns the joined stream's size (known on the host at once)."""
+    k = len(streams)
+    if len(sizes) != k or len(ns) != k:
+        raise ValueError("streams, sizes and ns must have the same length")
+    for t, b in zip(streams, sizes):
+        if b > t.numel() * t.element_size():
+            raise ValueError("a shard size exceeds its buffer")
+    ptrs = (ctypes.c_void_p * k)(*[_dev_ptr(t, "stream") for t in streams])
+    nbytes = (ctypes.c_size_t * k)(*sizes)
+    counts = (ctypes.c_size_t * k)(*ns)
+    total = ctypes.c_size_t(0)
+    _check("sz_concat", LIB.sz_concat(dt, k, ptrs, nbytes, counts, _dev_ptr(out, "out"),
+                                      out.numel() * out.element_size(), ctypes.byref(total),
+                                      _dev_ptr(status, "status"), _stream(stream)))
+    return total.value
 
 
 def sz_ablation_encoded_size(variant: int, n: int, n_escapes: int) -> int:

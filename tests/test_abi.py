@@ -92,6 +92,33 @@ def test_host_argument_checks_return_before_launching(S):
     assert lib.sz_debug_encode_stalled(0, ctypes.byref(cb), fake, n, fake, cap, fake, None, fake, ws, 1000, None) == S.SZ_ERR_INVALID_ARG
 
 
+def test_concat_host_checks_return_before_launching(S):
+    """sz_concat refuses bad shard lists before it touches a device pointer."""
+    lib = S.LIB
+    fake = 0x10000
+    C = S.SZ_CHUNK_ELEMS
+
+    def call(dt, ns, sizes, cap=1 << 40, out=fake, ptr=fake):
+        k = len(ns)
+        ptrs = (ctypes.c_void_p * k)(*([ptr] * k))
+        b = (ctypes.c_size_t * k)(*sizes)
+        n = (ctypes.c_size_t * k)(*ns)
+        total = ctypes.c_size_t(0)
+        return lib.sz_concat(dt, k, ptrs, b, n, out, cap, ctypes.byref(total), None, None), total.value
+
+    size = lambda n, e=0: S.sz_encoded_size(0, n, e)
+    assert call(0, [], [])[0] == S.SZ_ERR_INVALID_ARG                       # no shards
+    assert call(5, [C], [size(C)])[0] == S.SZ_ERR_INVALID_ARG               # unknown dtype
+    assert call(0, [C + 1, C], [size(C + 1), size(C)])[0] == S.SZ_ERR_INVALID_ARG  # not whole chunks
+    assert call(0, [C], [size(C)], out=None)[0] == S.SZ_ERR_INVALID_ARG
+    assert call(0, [C], [size(C)], ptr=None)[0] == S.SZ_ERR_INVALID_ARG
+    assert call(0, [C, 7], [size(C) + 1, size(7)])[0] == S.SZ_ERR_CORRUPT   # not the closed form
+    assert call(0, [C, 7], [size(C), size(7, 8)])[0] == S.SZ_ERR_CORRUPT    # more escapes than elements
+    want = size(2 * C + 7, 5)
+    assert call(0, [C, C, 7], [size(C, 2), size(C), size(7, 3)], cap=want - 1) == (S.SZ_ERR_CAPACITY, 0)
+    assert call(1, [1 << 31, 1 << 31], [S.sz_encoded_size(1, 1 << 31, 0)] * 2)[0] == S.SZ_ERR_INVALID_ARG  # n >= 2^32
+
+
 def test_status_strings(S):
     assert S.sz_status_string(0) == "SZ_OK"
     assert S.sz_status_string(5) == "SZ_ERR_TIMEOUT"
