@@ -253,10 +253,11 @@ sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t
  *  count           number of shards (>= 1), in tensor order
  *  h_streams       host array of count device pointers to the shard streams
  *  h_bytes, h_n    host arrays: each shard's stream size and element count;
- *                  every shard but the last must hold whole chunks
- *                  (h_n[k] % 65536 == 0, 0 allowed), and each size must be
- *                  the closed form for h_n[k] and some escape count, else
- *                  SZ_ERR_INVALID_ARG / SZ_ERR_CORRUPT is returned at once
+ *                  only the last non-empty shard may end inside a chunk
+ *                  (h_n[k] % 65536 != 0; empty shards are allowed anywhere),
+ *                  and each size must be the closed form for h_n[k] and some
+ *                  escape count, else SZ_ERR_INVALID_ARG / SZ_ERR_CORRUPT is
+ *                  returned at once
  *  d_out           device buffer of out_capacity bytes, not overlapping any
  *                  shard stream; receives sz_encoded_size(dt, sum n, sum E)
  *                  bytes, the size also written to *h_out_bytes (nullable)

@@ -80,12 +80,15 @@ extern "C" sz_status sz_concat(sz_dtype dt, size_t count, const void* const* h_s
     if ((dt != SZ_BF16 && dt != SZ_FP8_E5M2) || count == 0 || !h_streams || !h_bytes || !h_n || !d_out)
         return SZ_ERR_INVALID_ARG;
     if (d_status && reinterpret_cast<uintptr_t>(d_status) % 4 != 0) return SZ_ERR_INVALID_ARG;
-    // Shard sizes -> escape counts; totals; every shard but the last whole chunks.
+    // Shard sizes -> escape counts; totals.  Only the last non-empty shard
+    // may end inside a chunk.
     std::vector<uint64_t> esc(count);
     uint64_t n_all = 0, e_all = 0;
+    bool partial = false;
     for (size_t k = 0; k < count; k++) {
         if (!h_streams[k]) return SZ_ERR_INVALID_ARG;
-        if (k + 1 < count && h_n[k] % SZ_CHUNK_ELEMS != 0) return SZ_ERR_INVALID_ARG;
+        if (partial && h_n[k] > 0) return SZ_ERR_INVALID_ARG;
+        partial = partial || h_n[k] % SZ_CHUNK_ELEMS != 0;
         if ((uint64_t)h_n[k] >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
         const uint64_t fixed = sz_encoded_size(dt, h_n[k], 0);
         if (h_bytes[k] < fixed || (h_bytes[k] - fixed) % 3 != 0) return SZ_ERR_CORRUPT;

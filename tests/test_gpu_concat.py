@@ -46,6 +46,7 @@ SPLITS = [
     [4 * C + 1],                     # one shard: a copy
     [C] * 70 + [77],                 # more shards than one header launch takes
     [2 * C, 0, C, 0],                # empty shards in the middle and at the end
+    [2 * C + 5, 0, 0],               # a ragged shard followed by empty ones
 ]
 
 
