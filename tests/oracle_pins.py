@@ -414,6 +414,52 @@ def check_ablation_codecs_reject_corruption(orc):
         assert orc.abl_decode(variant, bad, x.size)[0] == O.CORRUPT
 
 
+def _join_streams(dt, parts, ns):
+    """The stream of the concatenated tensor assembled from shard streams by
+    the layout alone (R9, R7): dense parts in order, the codebook once, each
+    shard's headers with offsets shifted by the escapes before it, records
+    in order.  Every shard but the last holds whole chunks."""
+    dense_parts, nibs, hdrs, recs, e_before, cb = [], [], [], [], 0, None
+    for s, n in zip(parts, ns):
+        dense = n + (n + 1) // 2 if dt == O.BF16 else 7 * (-(-n // 8))
+        C = -(-n // 65536)
+        if dt == O.BF16:
+            dense_parts.append(s[:n])
+            nibs.append(s[n:dense])
+        else:
+            dense_parts.append(s[:dense])
+        cb = s[dense:dense + 16] if cb is None else cb
+        h = s[dense + 16:dense + 16 + 8 * C].copy().view(np.uint32).reshape(C, 2).copy()
+        h[:, 0] += e_before
+        hdrs.append(h.reshape(-1).view(np.uint8))
+        rec = s[dense + 16 + 8 * C:]
+        recs.append(rec)
+        e_before += rec.size // 3
+    return np.concatenate(dense_parts + nibs + [cb] + hdrs + recs)
+
+
+def check_shard_join(orc):
+    # Chunks are independent apart from the header offsets: shards of whole
+    # chunks, encoded on their own and joined by the layout alone, give the
+    # whole tensor's stream (positions are chunk-relative, offsets running sums).
+    rng = np.random.default_rng(14)
+    C = 65536
+    for dt, cb in ((O.BF16, CB_MID), (O.E5M2, CB_E5_MID)):
+        for ns in ([C, 2 * C + 77], [0, C, 0, C + 1], [3 * C], [C, C, 5]):
+            n = sum(ns)
+            if dt == O.BF16:
+                x = _gaussian_bf16(rng, n, scale=np.exp(2 * rng.standard_normal(n))).view(np.uint8)
+            else:
+                x = rng.integers(0, 256, n, dtype=np.uint8)
+            esize = 2 if dt == O.BF16 else 1
+            parts, at = [], 0
+            for m in ns:
+                parts.append(orc.encode(dt, cb, x[at * esize:(at + m) * esize]))
+                at += m
+            whole = orc.encode(dt, cb, x)
+            assert np.array_equal(_join_streams(dt, parts, ns), whole)
+
+
 CHECKS = [
     check_hand_bf16,
     check_hand_e5m2,
@@ -434,4 +480,5 @@ CHECKS = [
     check_ablation_codecs_hand,
     check_ablation_codecs_bruteforce,
     check_ablation_codecs_reject_corruption,
+    check_shard_join,
 ]
