@@ -70,7 +70,7 @@ typedef enum sz_status {
     SZ_ERR_UNSUPPORTED = 2, /* no usable CUDA device for this build (needs sm_103) */
     SZ_ERR_CAPACITY = 3,    /* output or workspace too small */
     SZ_ERR_CORRUPT = 4,     /* encoded stream fails validation */
-    SZ_ERR_TIMEOUT = 5,     /* a bounded inter-block wait in encode gave up */
+    SZ_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait for an asynchronous copy gave up (about 1 s) */
     SZ_ERR_CUDA = 6         /* a CUDA runtime call failed */
 } sz_status;
 

@@ -15,7 +15,7 @@ namespace {
 
 using namespace sz;
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded inter-block waits: 1 s
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded in-kernel waits for asynchronous copies: 1 s
 
 // An NVTX range around a public call, so that profilers can attribute the
 // kernels it launches (free when no tool is attached).
