@@ -35,6 +35,18 @@ def test_shards_cover_the_tensor_in_whole_chunks(n, world):
         assert a0 % C == 0 and a1 % C == 0
 
 
+@pytest.mark.parametrize("n", [1, C, 3 * C + 7, 10 * C, 17 * C + 1])
+@pytest.mark.parametrize("parts", [1, 2, 3, 8])
+def test_shards_are_the_transfer_segments(n, parts):
+    # The offload pipeline's segments and the ranks' shards cut alike, so a
+    # rank's offloaded segments join exactly like its shards.
+    from lossless_kv_cache_bf16_gb300 import transfer as T
+
+    sh = _shards()
+    ranges = [sh.shard(n, parts, r) for r in range(parts)]
+    assert [r for r in ranges if r[1] > r[0]] == T.segments(n, parts)
+
+
 def _bf16_bytes(n, seed):
     rng = np.random.default_rng(seed)
     x = (rng.standard_normal(n) * 30).astype(np.float32)
