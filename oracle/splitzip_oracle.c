@@ -4,9 +4,9 @@
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the parity reference that the CUDA
  * path is checked against.  Only the test suite, the smoke check and the
- * bench's CPU-baseline leg may load it.  It shares no code, header, table or
- * constant generator with the CUDA library; it includes only the C standard
- * library.
+ * bench's CPU-baseline and reference legs may load it.  It shares no code,
+ * header, table or constant generator with the CUDA library; it includes
+ * only the C standard library.
  *
  * Sources (the method is described in prose only; no listing is followed):
  *  [ABS]  SplitZip: Ultra Fast Lossless KV Compression for Disaggregated LLM
@@ -19,7 +19,7 @@
  *  [CAL]  same summary, "Resultados" > "Estudios de Ablacion" > "Calibracion"
  *         (one offline codebook).
  *
- * Readings of points the pages leave open (each one is listed in the design doc):
+ * Readings of points the pages leave open:
  *  R1  sign|mantissa byte = sign << 7 | mantissa (BF16); 3-bit field
  *      sign << 2 | mantissa (E5M2).
  *  R2  two 4-bit codes per byte, the even element in the low nibble.

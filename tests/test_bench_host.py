@@ -85,7 +85,7 @@ def test_two_rank_max_over_ranks():
 
 def test_bench_legs_are_defined():
     # Every leg main() calls exists at module level (a missing one would only
-    # show on the GPU machine).
+    # show where a GPU runs the bench).
     import ast
 
     tree = ast.parse(open(bench.__file__).read())
