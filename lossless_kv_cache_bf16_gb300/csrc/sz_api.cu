@@ -34,14 +34,19 @@ uint64_t dense_bytes(sz_dtype dt, uint64_t n) { return dt == SZ_BF16 ? n + cdiv(
 uint64_t scan_tiles_for(uint64_t n) { return std::max<uint64_t>(1, cdiv(n, kScanTile)); }
 
 // The encoders stage up to this many escape records per scan tile in the
-// workspace; scan tiles with more are re-derived by the finish kernel.
-constexpr uint32_t kStageRecs = kMaxStageRecs;
-static_assert(kStageRecs <= kMaxStageRecs && kStageRecs % 16 == 0, "finish kernel staging limits");
+// workspace; the records of scan tiles with more are re-derived by the
+// finish kernel.
+uint32_t stage_recs_for(sz_dtype dt) { return dt == SZ_BF16 ? kStageRecsBf16 : kStageRecsE5; }
+static_assert(kStageRecsBf16 % 16 == 0 && kStageRecsE5 % 16 == 0, "staged runs start 16-byte aligned");
 uint64_t align16(uint64_t x) { return (x + 15) & ~15ull; }
-// Workspace: [u32 count per scan tile][3 * cap bytes of records per scan tile].
-uint64_t workspace_bytes(uint64_t n, uint32_t cap = kStageRecs) {
+// Workspace: [u32 count per scan tile][u16 count per 1,024-element unit,
+// 32 per scan tile][3 * cap bytes of records per scan tile].  Each section
+// starts 16-byte aligned.
+uint64_t unit_counts_offset(uint64_t tiles) { return align16(4 * tiles); }
+uint64_t staged_records_offset(uint64_t tiles) { return unit_counts_offset(tiles) + 2ull * kUnitsPerScan * tiles; }
+uint64_t workspace_bytes(uint64_t n, uint32_t cap) {
     const uint64_t tiles = scan_tiles_for(n);
-    return align16(4 * tiles) + 3ull * cap * tiles;
+    return staged_records_offset(tiles) + 3ull * cap * tiles;
 }
 // Tiles of the decoder (independent of the encoder's scan tiles).
 uint64_t decode_tiles_for(sz_dtype dt, uint64_t n) {
@@ -90,7 +95,7 @@ bool codebook_ok(sz_dtype dt, const uint8_t* cb) {
 sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
                       size_t out_capacity, unsigned long long* d_out_bytes, int* d_status, void* d_ws,
                       size_t ws_bytes, uint32_t skip_first, uint64_t wait_ns, cudaStream_t stream,
-                      uint32_t stage_recs = kStageRecs, const uint8_t* d_cb = nullptr, PageMap pm = PageMap{}) {
+                      uint32_t stage_recs = 0, const uint8_t* d_cb = nullptr, PageMap pm = PageMap{}) {
     if (!dtype_ok(dt) || (!h_cb == !d_cb) || !d_out || !d_out_bytes || !d_ws) return SZ_ERR_INVALID_ARG;
     if ((n > 0 && !d_in) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
     if (dt == SZ_BF16 && !aligned(d_in, 2)) return SZ_ERR_INVALID_ARG;
@@ -98,6 +103,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     if (h_cb && !codebook_ok(dt, h_cb->exp)) return SZ_ERR_INVALID_ARG;
     if (d_cb && !aligned(d_cb, 16)) return SZ_ERR_INVALID_ARG;
     if (out_capacity < sz_encoded_size(dt, n, 0)) return SZ_ERR_CAPACITY;
+    if (stage_recs == 0) stage_recs = stage_recs_for(dt);
     const uint64_t ws_need = workspace_bytes(n, stage_recs);
     if (ws_bytes < ws_need) return SZ_ERR_CAPACITY;
 
@@ -108,7 +114,8 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     p.capacity = out_capacity;
     p.num_tiles = (uint32_t)scan_tiles_for(n);
     p.ws_count = static_cast<uint32_t*>(d_ws);
-    p.ws_rec = static_cast<uint8_t*>(d_ws) + align16(4 * (uint64_t)p.num_tiles);
+    p.ws_unit = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(d_ws) + unit_counts_offset(p.num_tiles));
+    p.ws_rec = static_cast<uint8_t*>(d_ws) + staged_records_offset(p.num_tiles);
     p.ws_cap = stage_recs;
     p.out_bytes = d_out_bytes;
     p.status = d_status;
@@ -142,8 +149,9 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
 // rest are re-derived): 6.1 MiB.
 constexpr uint64_t kNoAllocMaxElems = 1ull << 28;
 constexpr uint32_t kNoAllocStageRecs = 256;
-static_assert(kNoAllocStageRecs <= kMaxStageRecs && kNoAllocStageRecs % 16 == 0, "finish kernel staging limits");
-constexpr uint64_t kNoAllocScratchBytes = (kNoAllocMaxElems / kScanTile) * (4 + 3ull * kNoAllocStageRecs);
+static_assert(kNoAllocStageRecs <= kStageRecsE5 && kNoAllocStageRecs % 16 == 0, "within both encoders' staging");
+constexpr uint64_t kNoAllocScratchBytes =
+    (kNoAllocMaxElems / kScanTile) * (4 + 2ull * kUnitsPerScan + 3ull * kNoAllocStageRecs);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Host code cannot use g_noalloc_scratch as a device address (in host code the
@@ -225,7 +233,7 @@ size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes) {
 
 size_t sz_workspace_size(sz_dtype dt, size_t n) {
     if (!dtype_ok(dt)) return 0;
-    return workspace_bytes(n);
+    return workspace_bytes(n, stage_recs_for(dt));
 }
 
 size_t sz_histogram_bins(sz_dtype dt) {
@@ -328,7 +336,7 @@ sz_status sz_encode_dcb(sz_dtype dt, const uint8_t* d_cb, const void* d_in, size
     const NvtxRange range("sz_encode_dcb");
     if (!d_cb) return SZ_ERR_INVALID_ARG;
     return encode_impl(dt, nullptr, d_in, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
-                       kWaitLimitNs, stream, kStageRecs, d_cb);
+                       kWaitLimitNs, stream, 0, d_cb);
 }
 
 sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n, void* d_out,
@@ -416,7 +424,7 @@ sz_status sz_encode_paged(sz_dtype dt, const sz_codebook* h_cb, const void* d_po
     if (!page_map_for(d_pool, pool_pages, page_elems, d_block_ids, n, &pm)) return SZ_ERR_INVALID_ARG;
     if (n > 0 && cdiv(n, page_elems) > (1ull << 31)) return SZ_ERR_INVALID_ARG;
     return encode_impl(dt, h_cb, d_pool, n, d_out, out_capacity, d_out_bytes, d_status, d_ws, ws_bytes, 0,
-                       kWaitLimitNs, stream, kStageRecs, nullptr, pm);
+                       kWaitLimitNs, stream, 0, nullptr, pm);
 }
 
 sz_status sz_decode_paged(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_pool, size_t pool_pages,

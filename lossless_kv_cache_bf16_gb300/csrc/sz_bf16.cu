@@ -37,12 +37,14 @@ constexpr uint32_t kWarps = kBf16Threads / 32;
 //    round-robin order.  Sub-tiles arrive through a 2-stage ring of TMA bulk
 //    copies; per sub-tile the block splits, codes and packs, stores the dense
 //    streams, and ranks the escapes (ballot/popc warp scans, then a block
-//    scan).  Each scan tile's escape count and its first ws_cap records, in
-//    element order, go to the workspace.  Blocks never wait for each other.
+//    scan).  Each scan tile's escape count, the count of each of its
+//    1,024-element units (one per warp and sub-tile) and its first ws_cap
+//    records, in element order, go to the workspace.  Blocks never wait for
+//    each other.
 // 2. finish_kernel (sz_finish.cu) turns the counts into escape offsets,
 //    copies the staged records into the stream, writes the chunk headers and
-//    the stream size, and re-derives the records of any scan tile with more
-//    than ws_cap escapes from the input.
+//    the stream size, and re-derives the records of any scan tile beyond its
+//    first ws_cap from the input, unit by unit.
 // The records cost 6 extra bytes of traffic per escape (staged, read back),
 // a small price for a streaming pass without inter-block waits.
 // ---------------------------------------------------------------------------
@@ -59,12 +61,13 @@ constexpr uint32_t kSubsPerScan = 4;
 constexpr uint32_t kComputeThreads = kBf16Threads;           // 256
 constexpr uint32_t kTileBytes = kBf16Tile * 2;               // 16 KB of BF16 per sub-tile
 static_assert(kBf16Tile * kSubsPerScan == kScanTile, "four sub-tiles per scan tile");
+static_assert(kBf16Tile / kWarps == kUnitElems, "a unit is one warp's share of a sub-tile");
 
 struct EncodeSmem {
     alignas(128) uint8_t in[kEncStages][kTileBytes];
     uint64_t full[kEncStages];        // TMA -> compute: sub-tile landed
     alignas(16) uint32_t warp_esc[2][kWarps];
-    alignas(16) uint8_t rec[3 * kMaxStageRecs];  // the scan tile's staged records
+    alignas(16) uint8_t rec[3 * kStageRecsBf16];  // the scan tile's staged records
     uint8_t code[256];                // exponent -> code; 0x10 marks an escape
 };
 
@@ -341,7 +344,11 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
             }
             uint32_t off[4];
             const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
-            if (lane == 0) S.warp_esc[i & 1][warp] = warp_total;
+            if (lane == 0) {
+                S.warp_esc[i & 1][warp] = warp_total;
+                // The warp's 1,024 elements are unit part * 8 + warp of the scan tile.
+                p.ws_unit[(uint64_t)st * kUnitsPerScan + part * kWarps + warp] = (uint16_t)warp_total;
+            }
             // Block barrier: warp totals visible, the ring slot consumed by
             // every thread (its words were used by the stores above).
             if (__syncthreads_or(failed_wait)) {

@@ -28,6 +28,7 @@ namespace sz {
 namespace {
 
 static_assert(kChunk % kE5Tile == 0, "tiles must not straddle chunks");
+static_assert(8 * kE5PerThread == kUnitElems, "a unit is eight encoder threads' elements");
 constexpr uint32_t kWarpElems = 32 * kE5PerThread;     // 4096
 constexpr uint32_t kEncThreads = kScanTile / kE5PerThread;  // 256: one scan tile per encode block
 constexpr uint32_t kEncWarps = kEncThreads / 32;
@@ -105,13 +106,14 @@ __device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t add,
 // loads stay coalesced while each thread codes its own 128 contiguous bytes.
 // The packed bytes (7 pieces of 16 bytes per thread) reuse the same buffer
 // once the whole warp has read its rows, and leave with coalesced stores.
-// Before that, the tile's escape count and its first ws_cap records (element
-// order: thread, then element; exponents read back from the rows) go to the
-// workspace; finish_kernel (sz_finish.cu) places the records.
+// Before that, the tile's escape count, the counts of its 1,024-element
+// units and its first ws_cap records (element order: thread, then element;
+// exponents read back from the rows) go to the workspace; finish_kernel
+// (sz_finish.cu) places the records.
 // ---------------------------------------------------------------------------
 struct EncodeE5Smem {
     uint4 buf[kEncWarps][256];  // input: 8 swizzled pieces per thread; then output: 7 pieces per thread
-    alignas(16) uint8_t rec[3 * kMaxStageRecs];  // the scan tile's staged records
+    alignas(16) uint8_t rec[3 * kStageRecsE5];  // the scan tile's staged records
     uint32_t warp_esc[kEncWarps];
     uint8_t field[256];         // byte -> field; 0x80 marks an escape
 };
@@ -166,6 +168,13 @@ __device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5
         if (lane >= (uint32_t)d) incl += a;
     }
     if (lane == 31) s_warp_esc[warp] = incl;
+    {
+        // Escapes of each 1,024-element unit (8 lanes of 128 elements):
+        // unit warp * 4 + lane / 8 of the scan tile.
+        const uint32_t prev8 = __shfl_up_sync(0xFFFFFFFFu, incl, 8);
+        if ((lane & 7u) == 7u)
+            p.ws_unit[(uint64_t)st * kUnitsPerScan + warp * 4u + (lane >> 3)] = (uint16_t)(incl - (lane >= 8 ? prev8 : 0u));
+    }
     __syncthreads();
     uint32_t rank = incl - mine, tile_esc = 0;
 #pragma unroll

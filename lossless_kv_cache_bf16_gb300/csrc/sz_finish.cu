@@ -12,12 +12,13 @@
 //    then aligned 4-byte stores (a funnel shift realigns the bytes) with at
 //    most 3 single bytes at either end;
 //  * a scan tile with more than ws_cap escapes has its ws_cap staged records
-//    copied by its warp, which then walks the rest of the tile (after the
-//    last staged position) again, in element order, 512 (BF16) or 1,024
-//    (E5M2) elements per step: 16-byte loads (all of a step's in flight at
-//    once), a warp scan of the escape counts, the step's records assembled
-//    in the warp's staging buffer and written with the same aligned word
-//    stores;
+//    copied the same way; the rest are re-derived from the input unit by
+//    unit (1,024 elements each, whose escape counts the encoders also left
+//    in the workspace, so every unit's first record index is known).  The
+//    units holding unstaged records are spread over all warps of the block:
+//    a warp loads its unit with all 16-byte loads in flight, finds and ranks
+//    the escapes (a warp scan), assembles their records in its staging
+//    buffer and writes them with the same aligned word stores;
 //  * a chunk's last scan tile writes the chunk's header (offset = escapes
 //    before the chunk, count = escapes in it); the last scan tile writes the
 //    stream size.
@@ -34,139 +35,173 @@ namespace {
 constexpr uint32_t kFinThreads = 256;
 constexpr uint32_t kFinWarps = kFinThreads / 32;
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;
-constexpr uint32_t kStageBytes = 3 * kMaxStageRecs;      // staged records of one scan tile
+constexpr uint32_t kPieceRecs = 1024;                     // records a warp moves at a time
+constexpr uint32_t kStageBytes = 3 * kPieceRecs;          // a warp's staging buffer
 constexpr uint32_t kStageLoads = kStageBytes / 512;       // 16-byte loads per lane
 static_assert(kStageBytes % 512 == 0, "whole warp-wide 16-byte loads");
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
 
 // Copy nbytes from shared memory (src, 4-byte aligned, readable up to 4 bytes
-// past the end) to out + dst with aligned 4-byte stores; the 0..3 bytes
-// before the first aligned word and after the last go one at a time.  Bytes
-// at or beyond `capacity` are not written.  Threads tid = 0, step, 2 step, ...
-// share the work.
+// past the end) to out + dst with aligned 16-byte stores (funnel shifts
+// realign the bytes); the 0..15 bytes before the first aligned piece and
+// after the last go one at a time.  Bytes at or beyond `capacity` are not
+// written.  Threads tid = 0, step, 2 step, ... share the work.
 __device__ __forceinline__ void copy_out(const uint8_t* src, uint32_t nbytes, uint8_t* out, uint64_t dst,
                                          uint64_t capacity, uint32_t tid, uint32_t step) {
     uint8_t* const o = out + dst;
-    const uint32_t head = min((uint32_t)((4u - (uint32_t)(reinterpret_cast<uintptr_t>(o) & 3u)) & 3u), nbytes);
-    const uint32_t words = (nbytes - head) / 4, tail = (nbytes - head) & 3u;
+    const uint32_t head = min((uint32_t)((16u - (uint32_t)(reinterpret_cast<uintptr_t>(o) & 15u)) & 15u), nbytes);
+    const uint32_t pieces = (nbytes - head) / 16, tail = (nbytes - head) & 15u;
     const uint32_t* sw = reinterpret_cast<const uint32_t*>(src);
     const uint32_t shift = 8u * (head & 3u);
-    for (uint32_t w = tid; w < words; w += step) {
-        const uint32_t off = head + 4 * w;
-        const uint32_t val = __funnelshift_r(sw[off >> 2], sw[(off >> 2) + 1], shift);
-        if (dst + off + 4 <= capacity) {
-            *reinterpret_cast<uint32_t*>(o + off) = val;
+    for (uint32_t c = tid; c < pieces; c += step) {
+        const uint32_t off = head + 16 * c, i = off >> 2;
+        const uint4 v = make_uint4(__funnelshift_r(sw[i], sw[i + 1], shift), __funnelshift_r(sw[i + 1], sw[i + 2], shift),
+                                   __funnelshift_r(sw[i + 2], sw[i + 3], shift), __funnelshift_r(sw[i + 3], sw[i + 4], shift));
+        if (dst + off + 16 <= capacity) {
+            *reinterpret_cast<uint4*>(o + off) = v;
         } else {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (uint32_t b = 0; b < 4; b++)
-                if (dst + off + b < capacity) o[off + b] = (uint8_t)(val >> (8 * b));
+            for (uint32_t b = 0; b < 16; b++)
+                if (dst + off + b < capacity) o[off + b] = (uint8_t)(w[b >> 2] >> (8 * (b & 3)));
         }
     }
-    if (tid < head + tail) {
-        const uint32_t off = tid < head ? tid : head + 4 * words + (tid - head);
+    for (uint32_t e = tid; e < head + tail; e += step) {
+        const uint32_t off = e < head ? e : head + 16 * pieces + (e - head);
         if (dst + off < capacity) o[off] = src[off];
     }
 }
 
-// The records of scan tile st, which has more escapes than the ws_cap it
-// staged, written by one warp at byte offset dst of the stream (element
-// order): the staged records first (they are the tile's first ws_cap
-// escapes), then the ones after the last staged position, re-derived from
-// the input.  A step covers kU pieces of 16 bytes per lane
-// (piece u * 32 + lane of the step), all loaded before any is examined.
-// buf: the warp's staging buffer (kStageBytes + 16 bytes, 16-byte aligned).
+// The 8 records of a group of 8 consecutive escaped elements, 24 bytes, at
+// byte offset a of the staging buffer: record j is (pos0 + j as u16, the
+// exponent in byte j & 3 of ex[j >> 2]).  pos0 is a multiple of 8, so the
+// eight positions share their high byte and the low bytes do not carry.
+// The words are assembled with byte permutes from two position pairs and
+// the exponent words; a start that is not word aligned takes funnel shifts
+// for the middle words and single bytes at both ends (those words are
+// shared with the neighbouring records).
+__device__ __forceinline__ void put_full_group(uint8_t* buf, uint32_t a, uint32_t pos0, uint32_t ex0, uint32_t ex1) {
+    const uint32_t A = pos0 * 0x10001u + 0x10000u;  // pos0 | (pos0 + 1) << 16
+    const uint32_t B = A + 0x20002u, C = A + 0x40004u, D = A + 0x60006u;
+    const uint32_t w[6] = {__byte_perm(A, ex0, 0x2410), __byte_perm(B, ex0, 0x1051), __byte_perm(B, ex0, 0x7326),
+                           __byte_perm(C, ex1, 0x2410), __byte_perm(D, ex1, 0x1051), __byte_perm(D, ex1, 0x7326)};
+    uint32_t* bw = reinterpret_cast<uint32_t*>(buf) + (a >> 2);
+    const uint32_t s = a & 3u;
+    if (s == 0) {
+#pragma unroll
+        for (int k = 0; k < 6; k++) bw[k] = w[k];
+    } else {
+        const uint32_t sh = 8 * s;
+#pragma unroll
+        for (int k = 1; k < 6; k++) bw[k] = __funnelshift_l(w[k - 1], w[k], sh);
+        for (uint32_t b = 0; b < 4 - s; b++) buf[a + b] = (uint8_t)(w[0] >> (8 * b));
+        for (uint32_t b = 0; b < s; b++) buf[a + 24 - s + b] = (uint8_t)(w[5] >> (8 * (4 - s + b)));
+    }
+}
+
+// The records of one 1,024-element unit of a scan tile that did not fit the
+// staged ones, re-derived from the input and written by one warp at byte
+// offset dst of the stream, in element order: the unit's records of
+// unit-local rank >= skip (those below are among the staged records).  The
+// unit is kU pieces of 16 bytes per lane (piece u * 32 + lane), all loaded
+// before any is examined.  buf: the warp's staging buffer (kStageBytes + 16
+// bytes, 16-byte aligned), which holds the 1,024 records a unit can have.
 template <bool BF16, bool PAGED>
-__device__ void rederive_tile(const EncodeParams& p, uint32_t st, uint64_t dst, const uint8_t* s_member, uint8_t* buf) {
+__device__ void rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
+                              const uint8_t* s_member, uint8_t* buf) {
     constexpr uint32_t kPer = BF16 ? 8u : 16u;  // elements in 16 bytes
     constexpr uint32_t kEsize = BF16 ? 2u : 1u;
-    constexpr uint32_t kU = 2;
-    constexpr uint32_t kStep = 32 * kU * kPer;  // 512 (BF16) or 1,024 (E5M2) elements
-    static_assert(3 * kStep <= kStageBytes && kScanTile % kStep == 0, "a step's records fit the staging buffer");
+    constexpr uint32_t kU = kUnitElems / (32 * kPer);  // 4 (BF16) or 2 (E5M2)
+    static_assert(3 * kUnitElems <= kStageBytes, "a unit's records fit the staging buffer");
     const uint32_t lane = threadIdx.x & 31u;
-    const uint64_t n = p.L.n, begin = (uint64_t)st * kScanTile;
-    const uint64_t end = min(begin + kScanTile, n);
+    const uint64_t n = p.L.n;
+    const uint64_t end = min(ubase + kUnitElems, n);
     const bool vec = (reinterpret_cast<uintptr_t>(p.in) % 16) == 0;  // a paged pool is 16-byte aligned too
-    auto exponent = [](const uint32_t (&w)[4], uint32_t j) {
-        return BF16 ? (w[j >> 1] >> (7 + 16 * (j & 1))) & 0xFFu : (w[j >> 2] >> (8 * (j & 3) + 2)) & 0x1Fu;
-    };
-    uint64_t at = dst;
-    uint64_t resume = begin;  // first element not covered by the staged records
-    if (p.ws_cap > 0) {
-        // 3 ws_cap bytes (a multiple of 16, at most kStageBytes) at a 16-byte
-        // aligned address.
-        const uint32_t nb = 3 * p.ws_cap;
-        const uint4* src = reinterpret_cast<const uint4*>(p.ws_rec + (uint64_t)st * nb);
-        for (uint32_t k = lane; k < nb / 16; k += 32) reinterpret_cast<uint4*>(buf)[k] = src[k];
-        __syncwarp();
-        const uint32_t last = (uint32_t)buf[nb - 3] | ((uint32_t)buf[nb - 2] << 8);
-        resume = (begin & ~(uint64_t)(kChunk - 1)) + last + 1;
-        copy_out(buf, nb, p.out, at, p.capacity, lane, 32);
-        at += nb;
-        __syncwarp();  // buf is reused below
+    uint32_t w[kU][4], valid[kU];
+#pragma unroll
+    for (uint32_t u = 0; u < kU; u++) {
+        const uint64_t i0 = ubase + (uint64_t)(u * 32 + lane) * kPer;
+        w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0;
+        valid[u] = i0 >= end ? 0u : (end - i0 >= kPer ? kPer : (uint32_t)(end - i0));
+        if (vec && valid[u] == kPer) {
+            // A piece of 16 bytes never straddles a page (pages are a power
+            // of two of at least 16 elements).
+            const uint4 v = ld_stream_v4(p.in + elem_offset<PAGED>(p.pm, i0, kEsize, p.status));
+            w[u][0] = v.x, w[u][1] = v.y, w[u][2] = v.z, w[u][3] = v.w;
+        } else {
+#pragma unroll
+            for (uint32_t j = 0; j < kPer; j++) {
+                if (j < valid[u]) {
+                    const uint8_t* e = p.in + elem_offset<PAGED>(p.pm, i0 + j, kEsize, p.status);
+                    const uint32_t v = BF16 ? ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) : (uint32_t)e[0];
+                    w[u][j / (4 / kEsize)] |= v << (8 * kEsize * (j % (4 / kEsize)));
+                }
+            }
+        }
     }
-    for (uint64_t s0 = begin + (resume - begin) / kStep * kStep; s0 < end; s0 += kStep) {
-        uint32_t w[kU][4], m[kU];
+    uint32_t before = 0;  // records of the unit before piece row u
 #pragma unroll
-        for (uint32_t u = 0; u < kU; u++) {
-            const uint64_t i0 = s0 + (uint64_t)(u * 32 + lane) * kPer;
-            w[u][0] = w[u][1] = w[u][2] = w[u][3] = 0;
-            m[u] = 0;
-            if (i0 < end && i0 + kPer > resume) {
-                const uint32_t valid = end - i0 >= kPer ? kPer : (uint32_t)(end - i0);
-                // Elements [skip, valid) of the piece are examined.
-                const uint32_t skip = resume > i0 ? (uint32_t)(resume - i0) : 0u;
-                m[u] = valid | (skip << 8);  // until the mask replaces it
-                if (vec && valid == kPer) {
-                    // A piece of 16 bytes never straddles a page (pages are a
-                    // power of two of at least 16 elements).
-                    const uint4 v = *reinterpret_cast<const uint4*>(p.in + elem_offset<PAGED>(p.pm, i0, kEsize, p.status));
-                    w[u][0] = v.x, w[u][1] = v.y, w[u][2] = v.z, w[u][3] = v.w;
-                } else {
+    for (uint32_t u = 0; u < kU; u++) {
+        // The exponent bytes of the piece, four elements per word.
+        uint32_t ex[kPer / 4];
+        if (BF16) {
+            // Element pairs: low byte = exponent bit 0 | mantissa, high byte
+            // = sign | exponent bits 7..1.
 #pragma unroll
-                    for (uint32_t j = 0; j < kPer; j++) {
-                        if (j < valid) {
-                            const uint8_t* e = p.in + elem_offset<PAGED>(p.pm, i0 + j, kEsize, p.status);
-                            const uint32_t v = BF16 ? ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) : (uint32_t)e[0];
-                            w[u][j / (4 / kEsize)] |= v << (8 * kEsize * (j % (4 / kEsize)));
+            for (uint32_t g = 0; g < 2; g++) {
+                const uint32_t lo = __byte_perm(w[u][2 * g], w[u][2 * g + 1], 0x6420);
+                const uint32_t hi = __byte_perm(w[u][2 * g], w[u][2 * g + 1], 0x7531);
+                ex[g] = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
+            }
+        } else {
+#pragma unroll
+            for (uint32_t g = 0; g < 4; g++) ex[g] = (w[u][g] >> 2) & 0x1F1F1F1Fu;
+        }
+        uint32_t mask = 0;
+#pragma unroll
+        for (uint32_t j = 0; j < kPer; j++)
+            if (j < valid[u] && !s_member[(ex[j >> 2] >> (8 * (j & 3))) & 0xFFu]) mask |= 1u << j;
+        const uint32_t c = __popc(mask);
+        uint32_t x = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, x, d);
+            if (lane >= (uint32_t)d) x += a;
+        }
+        uint32_t r = before + x - c;  // unit-local rank of this piece's first record
+        const uint32_t pos0 = (uint32_t)(ubase + (uint64_t)(u * 32 + lane) * kPer) & 0xFFFFu;
+        // Groups of 8 elements: when the group of every lane is 8 escapes
+        // (all-escape data), each lane writes its 24 bytes as six words;
+        // otherwise record by record.
+#pragma unroll
+        for (uint32_t g = 0; g < kPer / 8; g++) {
+            const uint32_t m8 = (mask >> (8 * g)) & 0xFFu;
+            // Only when every lane of the warp takes this path: lanes that
+            // diverge would pay for both.
+            if (__all_sync(0xFFFFFFFFu, m8 == 0xFFu && r >= skip)) {
+                put_full_group(buf, 3 * (r - skip), pos0 + 8 * g, ex[2 * g], ex[2 * g + 1]);
+                r += 8;
+            } else {
+#pragma unroll
+                for (uint32_t j = 0; j < 8; j++) {
+                    if ((m8 >> j) & 1u) {
+                        if (r >= skip) {
+                            const uint32_t pos = pos0 + 8 * g + j;
+                            uint8_t* b = buf + 3 * (r - skip);
+                            b[0] = (uint8_t)pos;
+                            b[1] = (uint8_t)(pos >> 8);
+                            b[2] = (uint8_t)(ex[2 * g + (j >> 2)] >> (8 * (j & 3)));
                         }
+                        r++;
                     }
                 }
             }
         }
-        uint32_t before = 0;  // records of the step before slice u
-#pragma unroll
-        for (uint32_t u = 0; u < kU; u++) {
-            const uint32_t valid = m[u] & 0xFFu, skip = m[u] >> 8;
-            uint32_t mask = 0;
-#pragma unroll
-            for (uint32_t j = 0; j < kPer; j++)
-                if (j >= skip && j < valid && !s_member[exponent(w[u], j)]) mask |= 1u << j;
-            const uint32_t c = __popc(mask);
-            uint32_t x = c;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, x, d);
-                if (lane >= (uint32_t)d) x += a;
-            }
-            uint32_t r = 3 * (before + x - c);
-            const uint32_t i0 = (uint32_t)(s0 + (uint64_t)(u * 32 + lane) * kPer);
-#pragma unroll
-            for (uint32_t j = 0; j < kPer; j++) {
-                if ((mask >> j) & 1u) {
-                    const uint32_t pos = (i0 + j) & 0xFFFFu;
-                    buf[r] = (uint8_t)pos;
-                    buf[r + 1] = (uint8_t)(pos >> 8);
-                    buf[r + 2] = (uint8_t)exponent(w[u], j);
-                    r += 3;
-                }
-            }
-            before += __shfl_sync(0xFFFFFFFFu, x, 31);
-        }
-        __syncwarp();
-        copy_out(buf, 3 * before, p.out, at, p.capacity, lane, 32);
-        at += 3ull * before;
-        __syncwarp();  // buf is reused by the next step
+        before += __shfl_sync(0xFFFFFFFFu, x, 31);
     }
+    __syncwarp();
+    copy_out(buf, before > skip ? 3 * (before - skip) : 0u, p.out, dst, p.capacity, lane, 32);
+    __syncwarp();  // buf is reused by the warp's next unit
 }
 
 }  // namespace
@@ -176,6 +211,9 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
     __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 16];  // +16: realignment reads past the end
     __shared__ uint32_t s_sum[kFinWarps];
     __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
+    __shared__ uint16_t s_units[kFinThreads][kUnitsPerScan];  // unit escape counts of the heavy tiles
+    __shared__ uint8_t s_heavy[kFinThreads];                 // the batch's heavy tiles, in order
+    __shared__ uint32_t s_nheavy[kFinWarps];
     __shared__ uint8_t s_member[256];  // exponent is in the codebook
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint32_t T = p.num_tiles, F = gridDim.x;
@@ -252,16 +290,37 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
             }
         }
         __syncthreads();
-        // One warp per scan tile: copy its staged records, or re-derive them.
+        // The batch's heavy tiles (more escapes than staged), in order, and
+        // the escape counts of their units (units past n were never
+        // written: 0), loaded once for all warps.
         const uint32_t batch = min(kFinThreads, t1 - c0);
+        const bool is_heavy = tid < batch && cnt > p.ws_cap;
+        const uint32_t hb = __ballot_sync(0xFFFFFFFFu, is_heavy);
+        if (lane == 0) s_nheavy[warp] = __popc(hb);
+        __syncthreads();
+        uint32_t nheavy = 0, hbefore = 0;
+#pragma unroll
+        for (uint32_t v = 0; v < kFinWarps; v++) {
+            hbefore += v < warp ? s_nheavy[v] : 0u;
+            nheavy += s_nheavy[v];
+        }
+        if (is_heavy) s_heavy[hbefore + __popc(hb & ((1u << lane) - 1u))] = (uint8_t)tid;
+        __syncthreads();
+        for (uint32_t i = tid; i < nheavy * kUnitsPerScan; i += kFinThreads) {
+            const uint32_t h = i / kUnitsPerScan, u = i % kUnitsPerScan, st = c0 + s_heavy[h];
+            const bool in_range = (uint64_t)st * kScanTile + (uint64_t)u * kUnitElems < p.L.n;
+            s_units[h][u] = in_range ? p.ws_unit[(uint64_t)st * kUnitsPerScan + u] : (uint16_t)0;
+        }
+        // One warp per scan tile: copy its staged records (all of them, or
+        // the first ws_cap of a heavier tile), 1,024 records at a time.
         for (uint32_t j = warp; j < batch; j += kFinWarps) {
-            const uint32_t st = c0 + j, c = s_count[j];
-            const uint64_t dst = p.L.rec_off + 3ull * s_prefix[j];
-            if (c <= p.ws_cap) {
-                // Staged run: 3c bytes at a 16-byte aligned address, inside a
-                // region of 3 * ws_cap bytes (a multiple of 16).
-                const uint32_t nbytes = 3 * c;
-                const uint4* src = reinterpret_cast<const uint4*>(p.ws_rec + (uint64_t)st * 3 * p.ws_cap);
+            const uint32_t st = c0 + j, c = min(s_count[j], p.ws_cap);
+            // The staged run starts 16-byte aligned inside a region of
+            // 3 * ws_cap bytes (a multiple of 16); so does every piece.
+            const uint8_t* run = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
+            for (uint32_t q = 0; q < c; q += kPieceRecs) {
+                const uint32_t nbytes = 3 * min(kPieceRecs, c - q);
+                const uint4* src = reinterpret_cast<const uint4*>(run + 3 * q);
                 uint4 v[kStageLoads];
 #pragma unroll
                 for (uint32_t k = 0; k < kStageLoads; k++)
@@ -270,10 +329,43 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
                 for (uint32_t k = 0; k < kStageLoads; k++)
                     if (16 * lane + 512 * k < nbytes) reinterpret_cast<uint4*>(stage)[lane + 32 * k] = v[k];
                 __syncwarp();
-                copy_out(stage, nbytes, p.out, dst, p.capacity, lane, 32);
-                __syncwarp();  // the buffer is reused by the warp's next scan tile
-            } else {
-                rederive_tile<BF16, PAGED>(p, st, dst, s_member, stage);
+                copy_out(stage, nbytes, p.out, p.L.rec_off + 3ull * ((uint64_t)s_prefix[j] + q), p.capacity, lane, 32);
+                __syncwarp();  // the buffer is reused next
+            }
+        }
+        __syncthreads();  // s_units complete
+        // The units that hold the heavy tiles' remaining records are
+        // re-derived, spread over all warps of the block.  Every warp walks
+        // the same list of such units in the same order (heavy tiles in tile
+        // order, units in element order) and takes every kFinWarps-th one, so
+        // the units of one tile run side by side.
+        uint32_t k = 0;  // running index of the units walked so far
+        for (uint32_t h = 0; h < nheavy; h++) {
+            const uint32_t j = s_heavy[h];
+            const uint64_t tbase = (uint64_t)(c0 + j) * kScanTile;
+            const uint32_t uc = s_units[h][lane];
+            uint32_t incl = uc;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= (uint32_t)d) incl += a;
+            }
+            const uint32_t ufirst = incl - uc;  // escapes of the tile before this unit
+            uint32_t units = __ballot_sync(0xFFFFFFFFu, uc > 0 && incl > p.ws_cap);
+            // This warp's units of the tile: running index = warp mod kFinWarps.
+            uint32_t skip_units = (warp - k % kFinWarps + kFinWarps) % kFinWarps;
+            k += __popc(units);
+            while (units && skip_units) {
+                units &= units - 1;
+                skip_units--;
+            }
+            while (units) {
+                const uint32_t u = __ffs(units) - 1;
+                for (uint32_t q = 0; q < kFinWarps && units; q++) units &= units - 1;  // the next one is 8 on
+                const uint32_t f = __shfl_sync(0xFFFFFFFFu, ufirst, u);
+                const uint32_t skip = p.ws_cap > f ? p.ws_cap - f : 0u;
+                const uint64_t dst = p.L.rec_off + 3ull * ((uint64_t)s_prefix[j] + f + skip);
+                rederive_unit<BF16, PAGED>(p, tbase + (uint64_t)u * kUnitElems, skip, dst, s_member, stage);
             }
         }
         base += total;

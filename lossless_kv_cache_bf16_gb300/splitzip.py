@@ -133,6 +133,32 @@ def _elements(dt: int, t: torch.Tensor) -> int:
     return nbytes // ELEMENT_BYTES[dt]
 
 
+def _count(dt: int, x: torch.Tensor, n: int | None) -> int:
+    """Elements to encode: all of x, or the first n of them.  An n beyond x
+    would make the kernels read past x's allocation, so it is refused here,
+    before anything is launched."""
+    have = _elements(dt, x)
+    if n is None:
+        return have
+    if n < 0 or n > have:
+        raise ValueError(f"n = {n} is outside the tensor's {have} elements")
+    return n
+
+
+def _block_table(block_ids: torch.Tensor, n: int, page_elems: int) -> None:
+    """The block table must name a page for every element of the logical
+    tensor: ceil(n / page_elems) int32 ids.  The kernels index it without a
+    bound, so a shorter table is refused before anything is launched."""
+    if block_ids.dtype != torch.int32:
+        raise ValueError("block_ids must be int32")
+    if page_elems < 16 or page_elems & (page_elems - 1):
+        return  # not a page size the library accepts: it refuses the call itself
+    need = -(-n // page_elems)
+    if block_ids.numel() < need:
+        raise ValueError(f"block_ids holds {block_ids.numel()} ids; {n} elements in pages of "
+                         f"{page_elems} need {need}")
+
+
 _CODEBOOKS: dict = {}  # codebook values -> its C struct (read by the library during a call only)
 
 
@@ -225,7 +251,7 @@ def sz_calibrate_device(dt: int, x: torch.Tensor, hist: torch.Tensor, cb: torch.
     into cb (16 uint8 on the device); asynchronous, no host synchronisation."""
     assert hist.numel() == sz_histogram_bins(dt) and hist.element_size() == 8
     assert cb.numel() * cb.element_size() >= SZ_CODEBOOK_SIZE
-    n = _elements(dt, x) if n is None else n
+    n = _count(dt, x, n)
     _check("sz_calibrate_device",
            LIB.sz_calibrate_device(dt, _dev_ptr(x, "x"), n, sample_stride, _dev_ptr(hist, "hist"),
                                    _dev_ptr(cb, "cb"), _stream(stream)))
@@ -234,7 +260,7 @@ def sz_calibrate_device(dt: int, x: torch.Tensor, hist: torch.Tensor, cb: torch.
 def sz_encode_dcb(dt: int, cb: torch.Tensor, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.Tensor,
                   status: torch.Tensor | None, ws: torch.Tensor, stream=None, n: int | None = None) -> None:
     """sz_encode with the codebook in device memory (cb: 16 uint8 on the device)."""
-    n = _elements(dt, x) if n is None else n
+    n = _count(dt, x, n)
     _check("sz_encode_dcb", LIB.sz_encode_dcb(dt, _dev_ptr(cb, "cb"), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
                                               out.numel() * out.element_size(), _written_ptr(out_bytes, "out_bytes"),
                                               _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
@@ -245,7 +271,7 @@ def sz_encode(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes: torch.
               status: torch.Tensor | None, ws: torch.Tensor, stream=None, n: int | None = None) -> None:
     """Asynchronous encode of x (n elements, default all of x) into out."""
     c = _codebook(cb)
-    n = _elements(dt, x) if n is None else n
+    n = _count(dt, x, n)
     _check("sz_encode", LIB.sz_encode(dt, ctypes.byref(c), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
                                       out.numel() * out.element_size(), _written_ptr(out_bytes, "out_bytes"),
                                       _dev_ptr(status, "status"), _dev_ptr(ws, "ws"),
@@ -273,8 +299,7 @@ def sz_encode_paged(dt: int, cb, pool: torch.Tensor, page_elems: int, block_ids:
                     stream=None) -> None:
     """Encode the n-element tensor whose element e is element e % page_elems
     of page block_ids[e // page_elems] of `pool` (pages of page_elems)."""
-    if block_ids.dtype != torch.int32:
-        raise ValueError("block_ids must be int32")
+    _block_table(block_ids, n, page_elems)
     c = _codebook(cb)
     _check("sz_encode_paged",
            LIB.sz_encode_paged(dt, ctypes.byref(c), _dev_ptr(pool, "pool"), _pool_pages(dt, pool, page_elems),
@@ -287,8 +312,7 @@ def sz_encode_paged(dt: int, cb, pool: torch.Tensor, page_elems: int, block_ids:
 def sz_decode_paged(dt: int, stream_bytes: torch.Tensor, in_bytes: int, n: int, pool: torch.Tensor, page_elems: int,
                     block_ids: torch.Tensor, status: torch.Tensor | None, stream=None) -> None:
     """Decode into the pages of `pool` that block_ids names (see sz_encode_paged)."""
-    if block_ids.dtype != torch.int32:
-        raise ValueError("block_ids must be int32")
+    _block_table(block_ids, n, page_elems)
     if in_bytes > stream_bytes.numel() * stream_bytes.element_size():
         raise ValueError("in_bytes exceeds the stream buffer")
     _check("sz_decode_paged",
@@ -361,7 +385,7 @@ def sz_encode_noalloc(dt: int, cb, x: torch.Tensor, out: torch.Tensor, out_bytes
     """sz_encode without a caller workspace (the library's static scratch is
     used instead), for callers that cannot allocate device memory."""
     c = _codebook(cb)
-    n = _elements(dt, x) if n is None else n
+    n = _count(dt, x, n)
     _check("sz_encode_noalloc", LIB.sz_encode_noalloc(dt, ctypes.byref(c), _dev_ptr(x, "x"), n, _dev_ptr(out, "out"),
                                                       out.numel() * out.element_size(),
                                                       _written_ptr(out_bytes, "out_bytes"), _dev_ptr(status, "status"),

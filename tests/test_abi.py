@@ -45,10 +45,11 @@ def test_encoded_size_matches_oracle(S, orc):
 
 
 def test_workspace_size(S):
-    # A u32 count (16-byte aligned block) and 1,024 staged 3-byte records per
-    # 32,768-element scan tile, for either dtype.
-    ws = lambda tiles: ((4 * tiles + 15) // 16) * 16 + 3072 * tiles
-    for dt in (S.SZ_BF16, S.SZ_FP8_E5M2):
+    # Per 32,768-element scan tile: a u32 count (a 16-byte aligned block of
+    # them), 32 u16 counts of its 1,024-element units, and 2,048 (BF16) or
+    # 1,024 (E5M2) staged 3-byte records.
+    for dt, staged in ((S.SZ_BF16, 2048), (S.SZ_FP8_E5M2, 1024)):
+        ws = lambda tiles: ((4 * tiles + 15) // 16) * 16 + 64 * tiles + 3 * staged * tiles
         assert S.sz_workspace_size(dt, 0) == ws(1)
         assert S.sz_workspace_size(dt, 32768) == ws(1)
         assert S.sz_workspace_size(dt, 32769) == ws(2)
@@ -171,3 +172,60 @@ def test_codebook_marshalling(S):
     for bad in ([1, 2, 3], [300] + list(range(15)), [-1] + list(range(15))):
         with pytest.raises(ValueError):
             S._codebook(bad)
+
+
+def test_binding_refuses_out_of_range_counts_before_any_call(S, monkeypatch):
+    """An n above the tensor's element count, or a block table shorter than
+    ceil(n / page_elems), would make the kernels read (or write) past a
+    caller's buffer.  The binding refuses both before it calls the library:
+    the fake library below records every call, and none may happen."""
+    import torch
+
+    calls = []
+    real = S.LIB
+    host_only = {"sz_histogram_bins", "sz_encoded_size", "sz_workspace_size", "sz_status_string"}
+
+    class Recorder:
+        def __getattr__(self, name):
+            if name in host_only:
+                return getattr(real, name)
+
+            def fn(*args):
+                calls.append(name)
+                return S.SZ_OK
+            return fn
+
+    monkeypatch.setattr(S, "LIB", Recorder())
+    cb = list(range(120, 136))
+    x = torch.zeros(1000, dtype=torch.bfloat16)
+    x8 = torch.zeros(1000, dtype=torch.uint8)
+    out = torch.zeros(8, dtype=torch.uint8)
+    ob = torch.zeros(1, dtype=torch.int64)
+    hist = torch.zeros(256, dtype=torch.int64)
+    dcb = torch.zeros(16, dtype=torch.uint8)
+    for dt, t in ((S.SZ_BF16, x), (S.SZ_FP8_E5M2, x8)):
+        for bad in (1001, 5000, -1):
+            with pytest.raises(ValueError, match="outside the tensor"):
+                S.sz_encode(dt, cb, t, out, ob, None, out, n=bad)
+            with pytest.raises(ValueError, match="outside the tensor"):
+                S.sz_encode_dcb(dt, dcb, t, out, ob, None, out, n=bad)
+            with pytest.raises(ValueError, match="outside the tensor"):
+                S.sz_encode_noalloc(dt, cb, t, out, ob, None, n=bad)
+            with pytest.raises(ValueError, match="outside the tensor"):
+                S.sz_calibrate_device(dt, t, hist[: 256 if dt == S.SZ_BF16 else 32], dcb, n=bad)
+    page = 16
+    for n, ids in ((1000, 62), (1000, 0), (17, 1), (16 * 9 + 1, 9)):
+        table = torch.zeros(ids, dtype=torch.int32)
+        with pytest.raises(ValueError, match="block_ids holds"):
+            S.sz_encode_paged(S.SZ_BF16, cb, x, page, table, n, out, ob, None, out)
+        with pytest.raises(ValueError, match="block_ids holds"):
+            S.sz_decode_paged(S.SZ_BF16, out, 8, n, x, page, table, None)
+    with pytest.raises(ValueError, match="int32"):
+        S.sz_encode_paged(S.SZ_BF16, cb, x, page, torch.zeros(63, dtype=torch.int64), 1000, out, ob, None, out)
+    assert calls == []
+    # A count inside the tensor and a table of exactly ceil(n / page) ids pass
+    # the binding's checks and reach the library (here: the recorder, which
+    # only sees host-side arguments).
+    assert S._count(S.SZ_BF16, x, 1000) == 1000 and S._count(S.SZ_BF16, x, 0) == 0
+    S._block_table(torch.zeros(63, dtype=torch.int32), 1000, 16)
+    S._block_table(torch.zeros(0, dtype=torch.int32), 0, 16)

@@ -159,3 +159,47 @@ def test_capacity_overflow_reported(orc):
     got, st, size = G.encode(S.SZ_BF16, CB_MID, x, capacity=cap)
     assert st == S.SZ_ERR_CAPACITY and size == want.size
     assert np.array_equal(got[:cap], want[:cap])  # everything that fits is right
+
+
+def _unit_density_tensor(kind, n, seed, densities):
+    """A tensor whose 1,024-element units each have their own escape density
+    (drawn per unit from `densities`), so that scan tiles hold anywhere from
+    no escapes to all escapes, with the staged-record limit falling inside
+    units at varying places.  Escaped elements get an exponent outside CB_MID
+    (BF16) or CB_E5_MID (E5M2), the others one inside it."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    units = (n + 1023) // 1024
+    d = torch.tensor(densities, dtype=torch.float32, device="cuda")
+    per_unit = d[torch.randint(0, len(densities), (units,), generator=g, device="cuda")]
+    p = per_unit.repeat_interleave(1024)[:n]
+    esc = torch.rand(n, generator=g, device="cuda") < p
+    r = torch.randint(0, 1 << 16, (n,), generator=g, device="cuda", dtype=torch.int32)
+    if kind == "bf16":
+        inside = torch.randint(120, 136, (n,), generator=g, device="cuda", dtype=torch.int32)
+        outside = torch.randint(0, 120, (n,), generator=g, device="cuda", dtype=torch.int32)
+        outside = torch.where(outside >= 110, outside + 26, outside)  # 0..109 and 136..145
+        e = torch.where(esc, outside, inside)
+        return ((r & 0x807F) | (e << 7)).to(torch.int16).view(torch.bfloat16)
+    inside = torch.randint(14, 30, (n,), generator=g, device="cuda", dtype=torch.int32)
+    outside = torch.randint(0, 16, (n,), generator=g, device="cuda", dtype=torch.int32)
+    outside = torch.where(outside >= 14, outside + 16, outside)  # 0..13, 30, 31
+    e = torch.where(esc, outside, inside)
+    return ((r & 0x83) | (e << 2)).to(torch.uint8)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e5m2"])
+@pytest.mark.parametrize("seed,densities", [
+    (31, (0.0, 0.002, 0.05, 0.3, 0.9, 1.0)),
+    (32, (0.0, 1.0)),
+    (33, (0.025, 0.035, 0.055, 0.065)),  # tiles around the staging limits (1,024 and 2,048 records)
+    (34, (0.5,)),
+])
+def test_scan_tiles_beyond_staging(orc, kind, seed, densities):
+    """Scan tiles with more escapes than the encoder stages have their
+    remaining records re-derived unit by unit; the stream must still be the
+    oracle's byte for byte, for tiles of every density mix and a ragged end."""
+    n = 7 * 32768 + 1234
+    cb = CB_MID if kind == "bf16" else CB_E5_MID
+    x = _unit_density_tensor(kind, n, seed, densities)
+    roundtrip_vs_oracle(orc, kind, cb, x)
