@@ -3,10 +3,15 @@
 
 One step = one pass of the whole hot path over one batch: sz_encode of the
 workload tensor (split, code, pack, ordered escape compaction), then
-sz_decode of the stream (dense LUT pass + escape overwrite).  The default
-workload is the Llama-3-8B-shaped BF16 prefill KV cache [32, 2, 8192, 8, 128]
-(1.07 GB).  Throughput is uncompressed bytes / time.  Inputs (1.07 GB) are
-larger than L2 (129 MB), so no L2 flush is needed between steps.
+sz_decode of the stream (dense LUT pass + escape overwrite).  The headline
+workload is the long-context GQA BF16 KV cache [28, 2, 32768, 4, 128]
+(1.88 GB), the largest configuration; throughput is uncompressed bytes /
+time.  Inputs are larger than L2 (129 MB), so no L2 flush is needed between
+steps.  The same run also measures the other graded workloads -- the
+Llama-3-8B-shaped BF16 prefill KV cache (1.07 GB), the FP8 E5M2 KV cache
+(1 GiB) and the escape-rate sweep (256 MB, L2 flushed before every call) --
+and encode + decode pairs on small tensors (one layer, 1M elements), all in
+the one JSON line.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
 the host instead.  For N > 1 (torchrun), every rank runs its own copy of the
@@ -188,60 +193,255 @@ class ClockSampler:
 SWEEP_POINTS = (("p=0", 0.0), ("p=0.001", 0.001), ("p=0.01", 0.01), ("p=0.05", 0.05), ("adversarial", None),
                 ("all_escape", None))
 L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+GRADED = ("long_ctx_gqa", "llama8b_prefill", "fp8_e5m2")  # the >= 1 GB workloads
 
 
-def escape_sweep_leg(S, W, dt, cb, x, out, ob, est, ws, dst, dev, stream, peak, iters=20):
-    """Encode and decode throughput as the escape share grows: the sweep's
-    planted-escape tensors (same size and codebook as the p = 0 tensor x),
-    uniformly random non-NaN patterns, and a tensor with every exponent
-    outside the codebook.  Each point is checked bit-exact before it is
-    timed; the roofline fraction uses the point's own stream size.  The
-    tensors are only twice the L2, so repeated calls on the same buffers would
-    find part of their input still in L2: every timed call is preceded by a
-    write of a buffer twice the L2 and timed on its own."""
+class Codec:
+    """One workload on the device: its tensor, codebook (calibrated offline
+    on the workload's calibration sample) and the caller-owned buffers of an
+    encode and a decode."""
+
+    def __init__(self, S, W, name, dev, layers=None, x=None, cb=None):
+        import torch
+
+        self.S, self.name = S, name
+        cfg = W.CONFIGS[name]
+        self.dt = S.SZ_BF16 if cfg.dtype == "bf16" else S.SZ_FP8_E5M2
+        if x is None:
+            x = W.workload(name, dev)
+        if cb is None:
+            sample = W.calibration_sample(name, dev, full=x)
+            hist = torch.empty(S.sz_histogram_bins(self.dt), dtype=torch.int64, device=dev)
+            cb = S.sz_calibrate(self.dt, sample, hist)
+            del sample
+        if layers is not None:
+            assert x.dim() == 5 and 0 < layers <= x.shape[0], "--layers needs a layered workload"
+            x = x[:layers].contiguous()
+        self.x, self.cb = x, cb
+        self.n = x.numel()
+        self.n_bytes = self.n * x.element_size()
+        self.out = torch.empty(S.sz_encoded_size(self.dt, self.n, self.n), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(S.sz_workspace_size(self.dt, self.n), dtype=torch.uint8, device=dev)
+        self.ob = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.est = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.dst = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.y = torch.empty_like(x)
+        self.size = None
+
+    def encode(self, x=None):
+        self.S.sz_encode(self.dt, self.cb, self.x if x is None else x, self.out, self.ob, self.est, self.ws)
+
+    def decode(self, size=None):
+        self.S.sz_decode(self.dt, self.out, self.size if size is None else size, self.n, self.y, self.dst)
+
+    def check_round_trip(self, x=None):
+        """Encode and decode once; the stream size, after checking the round
+        trip bit for bit and both status words."""
+        import torch
+
+        x = self.x if x is None else x
+        self.encode(x)
+        torch.cuda.synchronize()
+        size = int(self.ob.item())
+        self.decode(size)
+        torch.cuda.synchronize()
+        assert int(self.est.item()) == 0 and int(self.dst.item()) == 0, f"{self.name}: codec reported an error"
+        assert torch.equal(self.y.view(torch.uint8), x.view(torch.uint8)), f"{self.name}: round trip is not bit-exact"
+        return size
+
+    def escapes(self, size):
+        return (size - self.S.sz_encoded_size(self.dt, self.n, 0)) // 3
+
+    def release(self):
+        for k in ("x", "out", "ws", "y"):
+            setattr(self, k, None)
+
+
+def timed_steps(c, K, warmup, stream):
+    """K encode + decode steps back to back, each call bracketed by CUDA
+    events on the launching stream: (per-call encode times, decode times,
+    elapsed time of all K steps), in seconds."""
     import torch
 
-    n = x.numel()
-    n_bytes = 2 * n
-    y = torch.empty_like(x)
+    for _ in range(warmup):
+        c.encode()
+        c.decode()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        c.encode()
+        e1.record(stream)
+        c.decode()
+        e2.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    t_enc = [a.elapsed_time(b) / 1e3 for a, b, _ in ev]
+    t_dec = [b.elapsed_time(d) / 1e3 for _, b, d in ev]
+    return t_enc, t_dec, t0.elapsed_time(t1) / 1e3
+
+
+def rates(n_bytes, size, te, td, peak):
+    """Uncompressed GB/s of an encode and a decode of te and td seconds, and
+    each one's fraction of the codec roofline: (input + stream bytes) / time
+    over the measured copy bandwidth."""
+    moved = n_bytes + size
+    return {"encode_gbs": n_bytes / te / 1e9, "decode_gbs": n_bytes / td / 1e9,
+            "encode_frac_of_codec_roofline": moved / te / 1e9 / peak,
+            "decode_frac_of_codec_roofline": moved / td / 1e9 / peak,
+            "codec_roofline_gbs": peak * n_bytes / moved}
+
+
+def dram_view(op, workload, t, peak, memcpy_gbs):
+    """Achieved HBM GB/s of one call: its ncu DRAM bytes (profiles/) over this
+    run's CUDA-event time; None without a capture of the current kernels."""
+    tr = profiled_traffic(op, workload)
+    if tr is None:
+        return None
+    g = tr / t / 1e9
+    return {"dram_bytes_per_call": tr, "dram_gbs": g, "frac_of_spec": g / SPEC_HBM_GBS,
+            "frac_of_memcpy": g / memcpy_gbs if memcpy_gbs else None, "frac_of_measured_copy": g / peak}
+
+
+def per_config_leg(S, W, name, dev, stream, K, warmup, peak, memcpy_gbs):
+    """One graded workload, measured the way the headline is: K encode +
+    decode steps after the round trip is checked bit for bit."""
+    import torch
+
+    c = Codec(S, W, name, dev)
+    size = c.size = c.check_round_trip()
+    t_enc, t_dec, elapsed = timed_steps(c, K, warmup, stream)
+    te, td = statistics.mean(t_enc), statistics.mean(t_dec)
+    assert int(c.est.item()) == 0 and int(c.dst.item()) == 0
+    suffix = "bf16" if c.dt == S.SZ_BF16 else "e5m2"
+    out = {"workload": name, "elements": c.n, "input_bytes": c.n_bytes, "steps": K,
+           "roundtrip_gbs": K * c.n_bytes / elapsed / 1e9, **rates(c.n_bytes, size, te, td, peak),
+           "ratio": c.n_bytes / size, "escape_rate": c.escapes(size) / c.n, "stream_bytes": size,
+           "hbm_achieved": {"encode": dram_view(f"encode_{suffix}", name, te, peak, memcpy_gbs),
+                            "decode": dram_view(f"decode_{suffix}", name, td, peak, memcpy_gbs)},
+           "link_model": link_model(c.n_bytes, size, te, td)}
+    c.release()
+    del c
+    torch.cuda.empty_cache()
+    return out
+
+
+def escape_sweep_leg(S, W, dev, stream, peak, iters=20):
+    """Encode and decode throughput as the escape share grows: the sweep's
+    planted-escape tensors (128M BF16 elements, the codebook of the p = 0
+    recipe's calibration sample), uniformly random non-NaN patterns, and a
+    tensor with every exponent outside the codebook.  Each point is checked
+    bit-exact before it is timed; the roofline fraction uses the point's own
+    stream size.  The tensors are only twice the L2, so repeated calls on
+    the same buffers would find part of their input still in L2: every timed
+    call is preceded by a write of a buffer twice the L2 and timed on its
+    own."""
+    import torch
+
+    c = Codec(S, W, "escape_sweep", dev)
+    n, n_bytes = c.n, c.n_bytes
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     e = [torch.cuda.Event(enable_timing=True) for _ in range(4 * iters)]
     res = {}
     for name, p in SWEEP_POINTS:
         if p is not None:
-            t = W.escape_sweep(p, cb, dev, n=n)
+            t = W.escape_sweep(p, c.cb, dev, n=n)
         elif name == "adversarial":
             t = W.adversarial(dev, n=n)
         else:
-            t = W.all_escape(cb, dev, n=n)
-        S.sz_encode(dt, cb, t, out, ob, est, ws)
-        torch.cuda.synchronize()
-        size = int(ob.item())
-        S.sz_decode(dt, out, size, n, y, dst)
-        torch.cuda.synchronize()
-        assert int(est.item()) == 0 and int(dst.item()) == 0, name
-        assert torch.equal(y.view(torch.uint8), t.view(torch.uint8)), f"{name}: round trip is not bit-exact"
+            t = W.all_escape(c.cb, dev, n=n)
+        size = c.check_round_trip(t)
         for _ in range(3):
-            S.sz_encode(dt, cb, t, out, ob, est, ws)
-            S.sz_decode(dt, out, size, n, y, dst)
+            c.encode(t)
+            c.decode(size)
         for i in range(iters):
             flush.fill_(i & 0xFF)
             e[4 * i].record(stream)
-            S.sz_encode(dt, cb, t, out, ob, est, ws)
+            c.encode(t)
             e[4 * i + 1].record(stream)
             flush.fill_((i + 1) & 0xFF)
             e[4 * i + 2].record(stream)
-            S.sz_decode(dt, out, size, n, y, dst)
+            c.decode(size)
             e[4 * i + 3].record(stream)
         torch.cuda.synchronize()
         te = sum(e[4 * i].elapsed_time(e[4 * i + 1]) for i in range(iters)) / iters / 1e3
         td = sum(e[4 * i + 2].elapsed_time(e[4 * i + 3]) for i in range(iters)) / iters / 1e3
-        res[name] = {"escape_rate": (size - S.sz_encoded_size(dt, n, 0)) / 3 / n, "ratio": n_bytes / size,
-                     "encode_gbs": n_bytes / te / 1e9, "decode_gbs": n_bytes / td / 1e9,
-                     "encode_frac_of_codec_roofline": (n_bytes + size) / te / 1e9 / peak,
-                     "decode_frac_of_codec_roofline": (n_bytes + size) / td / 1e9 / peak}
+        res[name] = {"escape_rate": c.escapes(size) / n, "ratio": n_bytes / size, **rates(n_bytes, size, te, td, peak)}
         del t
+    c.release()
+    del c, flush
+    torch.cuda.empty_cache()
     return res
+
+
+def small_tensor_leg(S, W, dev, stream, reps=50):
+    """Encode + decode pairs on small tensors, where fixed costs per call
+    weigh most: one layer of the Llama-3-8B-shaped KV cache (16.8M elements)
+    and the tiny K tensor (1M elements).  Per pair: the GPU time (the pairs
+    are queued behind a sleeping kernel, so the host runs ahead and only the
+    GPU's own time shows), the host time to issue one pair through the
+    binding, and the time per pair when a CUDA graph of one pair is
+    replayed."""
+    import torch
+
+    out = {}
+    for label, x, sample in (("llama8b_one_layer", W.llama8b_prefill(dev, 0, layers=1),
+                              W.llama8b_prefill(dev, 1, layers=1)),
+                             ("tiny_1m", W.kv_tiny(dev, 0), W.kv_tiny(dev, 1))):
+        c = Codec(S, W, "tiny", dev, x=x, cb=S.sz_calibrate(S.SZ_BF16, sample,
+                                                           torch.empty(256, dtype=torch.int64, device=dev)))
+        c.size = c.check_round_trip()
+        for _ in range(5):
+            c.encode()
+            c.decode()
+        torch.cuda.synchronize()
+        # GPU time: the pairs wait behind a sleep while the host queues them.
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200_000_000)
+        e0.record(stream)
+        h0 = time.perf_counter()
+        for _ in range(reps):
+            c.encode()
+            c.decode()
+        h1 = time.perf_counter()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        gpu_us = e0.elapsed_time(e1) / reps * 1e3
+        host_us = (h1 - h0) / reps * 1e6
+        # A CUDA graph of one pair, replayed.
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            c.encode()
+            c.decode()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            c.encode()
+            c.decode()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(c.est.item()) == 0 and int(c.dst.item()) == 0
+        assert torch.equal(c.y.view(torch.uint8), c.x.view(torch.uint8)), f"{label}: graph round trip"
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = e0.elapsed_time(e1) / reps * 1e3
+        out[label] = {"elements": c.n, "input_bytes": c.n_bytes, "gpu_us_per_pair": gpu_us,
+                      "host_us_per_pair": host_us, "graph_us_per_pair": graph_us,
+                      "pair_gbs_gpu": c.n_bytes / (gpu_us / 1e6) / 1e9,
+                      "pair_gbs_graph": c.n_bytes / (graph_us / 1e6) / 1e9}
+        del g
+        c.release()
+        del c
+    torch.cuda.empty_cache()
+    return out
 
 
 def offload_leg(S, T, dt, cb, x, y, dev, parts, reps=5):
@@ -303,8 +503,12 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["splitzip", "reference"], default="splitzip")
-    ap.add_argument("--config", default="llama8b_prefill",
-                    choices=["llama8b_prefill", "long_ctx_gqa", "fp8_e5m2", "escape_sweep", "tiny"])
+    ap.add_argument("--config", default="long_ctx_gqa",
+                    choices=["long_ctx_gqa", "llama8b_prefill", "fp8_e5m2", "escape_sweep", "tiny"])
+    ap.add_argument("--config-steps", type=int, default=100,
+                    help="timed steps of each other graded workload measured in the same run")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the --config workload only (no other workloads, sweep or small tensors)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-segments", type=int, default=8,
@@ -312,11 +516,13 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first L layers of a layered workload (smaller captures for ncu)")
     ap.add_argument("--profile", action="store_true",
-                    help="only the timed encode/decode steps: no clock warm-up, e2e, memcpy or CPU baseline")
+                    help="only the timed encode/decode steps: no clock warm-up, e2e, memcpy, CPU baseline "
+                         "or other workloads")
     args = ap.parse_args()
     if args.profile:
         args.no_cpu_baseline = True
         args.e2e_steps = 0
+        args.no_per_config = True
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
@@ -382,79 +588,37 @@ def main():
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    dt = S.SZ_BF16 if is_bf16 else S.SZ_FP8_E5M2
     stream = torch.cuda.current_stream()
+    peak, peak_src = measured_peaks()
 
-    x = W.workload(args.config, dev)
-    sample = W.calibration_sample(args.config, dev, full=x)
-    if args.layers is not None:
-        assert x.dim() == 5 and 0 < args.layers <= x.shape[0], "--layers needs a layered workload"
-        x = x[: args.layers].contiguous()
-    hist = torch.empty(S.sz_histogram_bins(dt), dtype=torch.int64, device=dev)
-    cb = S.sz_calibrate(dt, sample, hist)
-    del sample
-    n = x.numel()
-    n_bytes = n * elem_bytes
-    cap = S.sz_encoded_size(dt, n, n)
-    out = torch.empty(cap, dtype=torch.uint8, device=dev)
-    ws = torch.empty(S.sz_workspace_size(dt, n), dtype=torch.uint8, device=dev)
-    ob = torch.zeros(1, dtype=torch.int64, device=dev)
-    est = torch.zeros(1, dtype=torch.int32, device=dev)
-    dst = torch.zeros(1, dtype=torch.int32, device=dev)
-    y = torch.empty_like(x)
-
-    def encode():
-        S.sz_encode(dt, cb, x, out, ob, est, ws)
-
-    def decode(size):
-        S.sz_decode(dt, out, size, n, y, dst)
-
-    # Size of the stream (fixed for a given input), then check the round trip.
-    encode()
-    torch.cuda.synchronize()
-    size = int(ob.item())
-    decode(size)
-    torch.cuda.synchronize()
-    assert int(est.item()) == 0 and int(dst.item()) == 0, "codec reported an error"
-    assert torch.equal(y.view(torch.uint8), x.view(torch.uint8)), "round trip is not bit-exact"
-    n_esc = (size - S.sz_encoded_size(dt, n, 0)) // 3
+    c = Codec(S, W, args.config, dev, layers=args.layers)
+    dt, cb, x, y, n, n_bytes = c.dt, c.cb, c.x, c.y, c.n, c.n_bytes
+    out, ob, est, dst, ws = c.out, c.ob, c.est, c.dst, c.ws
+    # Size of the stream (fixed for a given input), after checking the round trip.
+    size = c.size = c.check_round_trip()
+    n_esc = c.escapes(size)
 
     for _ in range(args.warmup):
-        encode()
-        decode(size)
+        c.encode()
+        c.decode()
     # Keep the GPU busy for a moment so the clock sampler sees it under load.
     sampler = ClockSampler(local_rank)
     if not args.profile:
         sampler.start()
         t_end = time.time() + 0.6
         while time.time() < t_end:
-            encode()
-            decode(size)
+            c.encode()
+            c.decode()
             torch.cuda.synchronize()
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for e0, e1, e2 in ev:
-        e0.record(stream)
-        encode()
-        e1.record(stream)
-        decode(size)
-        e2.record(stream)
-    t_stop.record(stream)
-    torch.cuda.synchronize()
+    t_enc, t_dec, elapsed = timed_steps(c, K, 0, stream)
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed = t_start.elapsed_time(t_stop) / 1e3
-    t_enc = [a.elapsed_time(b) / 1e3 for a, b, _ in ev]
-    t_dec = [b.elapsed_time(c) / 1e3 for _, b, c in ev]
     assert int(est.item()) == 0 and int(dst.item()) == 0
 
     value, t_max = aggregate(K * n_bytes, gather_elapsed(dist, elapsed, dev))
@@ -492,6 +656,7 @@ def main():
                        "encode_dcb_gbs": n_bytes / (c0.elapsed_time(c1) / 20 / 1e3) / 1e9,
                        "codebook": dcb.cpu().tolist(), "offline_codebook": [int(v) for v in cb],
                        "ratio": n_bytes / online_size, "ratio_offline": n_bytes / size})
+        c.encode()  # the stream of the offline codebook again, for what follows
 
     paged = None
     if not args.profile:
@@ -526,8 +691,9 @@ def main():
                      "encode_gbs": n_bytes / (ev3[0].elapsed_time(ev3[1]) / 20 / 1e3) / 1e9,
                      "decode_gbs": n_bytes / (ev3[1].elapsed_time(ev3[2]) / 20 / 1e3) / 1e9,
                      "stream_bytes": psize}
+            del pout
             # Restore y as the plain decode of the contiguous stream for what follows.
-            S.sz_decode(dt, out, size, n, y, dst)
+            c.decode()
 
     ablation = None
     if not args.profile:
@@ -569,13 +735,7 @@ def main():
                 del aout, aws
             ablation["decode_gbs"] = speeds
             ablation["decode_slowdown_vs_top16"] = {k: speeds["top16"] / v for k, v in speeds.items()}
-            S.sz_decode(dt, out, size, n, y, dst)
-
-    sweep = None
-    if not args.profile and args.config == "escape_sweep":
-        sweep = escape_sweep_leg(S, W, dt, cb, x, out, ob, est, ws, dst, dev, stream, peak=measured_peaks()[0])
-        S.sz_encode(dt, cb, x, out, ob, est, ws)
-        S.sz_decode(dt, out, size, n, y, dst)
+            c.decode()
 
     e2e = None
     memcpy_gbs = None
@@ -592,9 +752,9 @@ def main():
         segs = T.segments(n, args.e2e_segments)
         xf, yf = x.reshape(-1), y.reshape(-1)
         seg_cap = [S.sz_encoded_size(dt, a1 - a0, a1 - a0) for a0, a1 in segs]
-        seg_at = [sum((c + 255) // 256 * 256 for c in seg_cap[:i]) for i in range(len(segs))]
+        seg_at = [sum((cp + 255) // 256 * 256 for cp in seg_cap[:i]) for i in range(len(segs))]
         seg_buf = torch.empty(seg_at[-1] + seg_cap[-1], dtype=torch.uint8, device=dev)
-        seg_out = [seg_buf[o:o + c] for o, c in zip(seg_at, seg_cap)]
+        seg_out = [seg_buf[o:o + cp] for o, cp in zip(seg_at, seg_cap)]
         seg_size = []  # per-segment stream sizes (fixed for this input)
         for (a0, a1), o in zip(segs, seg_out):
             S.sz_encode(dt, cb, xf[a0:a1], o, ob, est, ws)
@@ -649,6 +809,7 @@ def main():
         e2e_value, _ = aggregate(args.e2e_steps * n_bytes, gather_elapsed(dist, e2e_t, dev))
         assert int(est.item()) == 0 and int(dst.item()) == 0, "codec reported an error"
         assert torch.equal(yh, xh), "end-to-end round trip is not bit-exact"
+        del seg_buf, seg_out
 
         # Device-to-device copy bandwidth in the same run (bytes = read + write).
         a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
@@ -672,8 +833,7 @@ def main():
         offload = offload_leg(S, T, dt, cb, x, y, dev, parts=args.e2e_segments)
 
     te, td = statistics.mean(t_enc), statistics.mean(t_dec)
-    enc_gbs, dec_gbs = n_bytes / te / 1e9, n_bytes / td / 1e9
-    peak, peak_src = measured_peaks()
+    head = rates(n_bytes, size, te, td, peak)
     moved = n_bytes + size
     suffix = "bf16" if is_bf16 else "e5m2"
     ops = {f"encode_{suffix}": te, f"decode_{suffix}": td}
@@ -682,18 +842,11 @@ def main():
     traffic = profiled_traffic(dominant, args.config)
     roofline = {"bound": "hbm", "kernel": " + ".join(OPS[dominant][0]), "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} hbm_gbs (copy)",
-                "algorithmic_bytes_per_launch": moved}
-
-    def dram_view(op, t):
-        """Achieved HBM GB/s of one call: its ncu DRAM bytes over this run's time."""
-        tr = profiled_traffic(op, args.config)
-        if tr is None:
-            return None
-        g = tr / t / 1e9
-        return {"dram_bytes_per_call": tr, "dram_gbs": g, "frac_of_spec": g / SPEC_HBM_GBS,
-                "frac_of_memcpy": g / memcpy_gbs if memcpy_gbs else None, "frac_of_measured_copy": g / peak}
-
-    hbm = {"encode": dram_view(f"encode_{suffix}", te), "decode": dram_view(f"decode_{suffix}", td),
+                "algorithmic_bytes_per_launch": moved,
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per call from profiles/ "
+                                  "(a 2-layer capture scaled by elements to the full tensor)"}
+    hbm = {"encode": dram_view(f"encode_{suffix}", args.config, te, peak, memcpy_gbs),
+           "decode": dram_view(f"decode_{suffix}", args.config, td, peak, memcpy_gbs),
            "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per call (profiles/), over this run's "
                      "CUDA-event time; null without a capture of the current kernels for this workload"}
 
@@ -709,6 +862,25 @@ def main():
         cpu = {"value": n_bytes / (tenc + tdec) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"the whole {args.config} tensor ({n_bytes} bytes), one encode + one decode",
                "encode_gbs": n_bytes / tenc / 1e9, "decode_gbs": n_bytes / tdec / 1e9}
+        del xb
+
+    # The other graded workloads, the escape sweep and small tensors, each
+    # measured after the headline's tensors are freed.
+    per_config, sweep, small = None, None, None
+    headline_launches = sum(len(OPS[op][0]) for op in ops) * K
+    if not args.no_per_config:
+        c.release()
+        del x, y, out, ws
+        torch.cuda.empty_cache()
+        per_config = {}
+        for name in GRADED:
+            if name != args.config:
+                per_config[name] = per_config_leg(S, W, name, dev, stream, args.config_steps, args.warmup, peak,
+                                                  memcpy_gbs)
+        sweep = escape_sweep_leg(S, W, dev, stream, peak)
+        small = small_tensor_leg(S, W, dev, stream)
+    elif args.config == "escape_sweep" and not args.profile:
+        sweep = escape_sweep_leg(S, W, dev, stream, peak)
 
     if rank != 0:
         if dist:
@@ -718,23 +890,21 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": t_max / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u8" if not is_bf16 else "u16", "data": "synthetic",
-        "config": {"workload": args.config + (f"[:{args.layers} layers]" if args.layers else ""), "elements": n, "input_bytes": n_bytes,
-                   "step": "one sz_encode + one sz_decode of the whole tensor",
+        "config": {"workload": args.config + (f"[:{args.layers} layers]" if args.layers else ""), "elements": n,
+                   "input_bytes": n_bytes, "step": "one sz_encode + one sz_decode of the whole tensor",
                    "l2": "inputs larger than L2 (129 MB); no flush", "parallelism": f"{world} independent shards"},
-        "encode_gbs": enc_gbs, "decode_gbs": dec_gbs,
-        "encode_frac_of_codec_roofline": (n_bytes + size) / te / 1e9 / peak,
-        "decode_frac_of_codec_roofline": (n_bytes + size) / td / 1e9 / peak,
-        "codec_roofline_gbs": peak * n_bytes / (n_bytes + size),
+        **head,
         "ratio": n_bytes / size, "escape_rate": n_esc / n, "stream_bytes": size,
         "memcpy_d2d_gbs": memcpy_gbs, "spec_hbm_gbs": SPEC_HBM_GBS, "hbm_achieved": hbm,
         "link_model": link_model(n_bytes, size, te, td),
         "paper_context": {"encode_gbs": PAPER_ENCODE_GBS, "decode_gbs": PAPER_DECODE_GBS,
                           "e5m2_ratio": PAPER_E5M2_RATIO, "hardware": "not named on the pages"},
-        "roofline": roofline, "cpu_baseline": cpu, "online_calibration": online, "ablation": ablation, "paged": paged,
+        "roofline": roofline, "cpu_baseline": cpu, "per_config": per_config,
         "escape_sweep": sweep,
         "escape_sweep_timing": sweep and "each call timed on its own after a 256 MiB write that flushes L2",
+        "small_tensors": small, "online_calibration": online, "ablation": ablation, "paged": paged,
         "offload": offload, "e2e": e2e,
-        "gpu_launches": sum(len(OPS[op][0]) for op in ops) * K, "clocks": clocks,
+        "gpu_launches": headline_launches, "clocks": clocks,
     }
     print(json.dumps(line))
     if dist:

@@ -94,12 +94,15 @@ typedef struct sz_codebook {
  * Host only; returns 0 for an unknown dtype. */
 size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes);
 
-/* Bytes of device workspace that sz_encode needs for n elements: the escape
- * count of every 32,768-element scan tile and up to 1,024 staged escape
- * records (3 bytes each) per scan tile -- about 4.7% of a BF16 input, 9.4%
- * of an E5M2 input.  The workspace is scratch: its contents on entry do not
- * matter, and it must not be shared by encodes that can run at the same
- * time.  Host only; returns 0 for an unknown dtype. */
+/* Bytes of device workspace that sz_encode needs for n elements: for every
+ * 32,768-element scan tile its escape count, the escape counts of its 32
+ * units of 1,024 elements, and up to 2,048 (BF16) or 1,024 (E5M2) staged
+ * escape records of 3 bytes -- about 9.6% of the input bytes for either
+ * dtype.  A scan tile with more escapes than it stages has the rest of its
+ * records re-derived from the input (same stream, more time).  The
+ * workspace is scratch: its contents on entry do not matter (every count is
+ * written before it is read), and it must not be shared by encodes that can
+ * run at the same time.  Host only; returns 0 for an unknown dtype. */
 size_t sz_workspace_size(sz_dtype dt, size_t n);
 
 /* Number of exponent bins: 256 (BF16) or 32 (E5M2); 0 for an unknown dtype. */
@@ -226,10 +229,13 @@ sz_status sz_decode(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n,
  *  page_elems    a power of two, 16 <= page_elems <= 2^30
  *  d_block_ids   device int32[ceil(n / page_elems)]: element e of the logical
  *                tensor is element e % page_elems of page d_block_ids[e /
- *                page_elems].  An id outside [0, pool_pages) is never
- *                dereferenced: *d_status becomes SZ_ERR_INVALID_ARG and the
- *                result is meaningless.  Decode writes only the pages the
- *                table names (ids must not repeat for decode).
+ *                page_elems].  The kernels read the first ceil(n /
+ *                page_elems) entries without a bound, so the table must hold
+ *                at least that many (the library cannot see its length; the
+ *                Python binding checks it).  An id outside [0, pool_pages)
+ *                is never dereferenced: *d_status becomes SZ_ERR_INVALID_ARG
+ *                and the result is meaningless.  Decode writes only the
+ *                pages the table names (ids must not repeat for decode).
  * The stream is byte for byte the sz_encode stream of the logical tensor;
  * other arguments and errors as for sz_encode / sz_decode. */
 sz_status sz_encode_paged(sz_dtype dt, const sz_codebook* h_cb, const void* d_pool, size_t pool_pages,
@@ -310,22 +316,29 @@ const char* sz_status_string(int status);
  * almost all device memory to its KV-cache pool and forbids further
  * allocations, or a latency-critical path that must not take cudaMalloc's
  * implicit device synchronisation -- and so cannot provide the workspace
- * that sz_encode takes.  This call uses a workspace of about 6.1 MiB held
- * in a static device array inside the library instead, and otherwise behaves
- * exactly like sz_encode (same arguments, stream bytes, d_out_bytes and
- * d_status semantics).  It allocates nothing and calls no allocating routine.
+ * that sz_encode takes.  This call uses a workspace of 6,848,512 bytes
+ * (6.53 MiB) held in a static device array inside the library instead, and
+ * otherwise behaves exactly like sz_encode (same arguments, stream bytes,
+ * d_out_bytes and d_status semantics).  It allocates nothing and calls no
+ * allocating routine.
  *  - Limit: n up to 2^28 elements of either dtype; larger n returns
  *    SZ_ERR_CAPACITY at once and launches nothing.  Its smaller staging area
- *    (256 escape records per BF16 scan tile) makes scan tiles with more
- *    escapes take a slower re-derivation path; the output is the same.
- *  - Every GPU that loads the library holds the 6.1 MiB array until the
- *    process exits.
+ *    (256 escape records per scan tile, of either dtype) makes scan tiles
+ *    with more escapes re-derive the rest of their records from the input;
+ *    the output is the same.
+ *  - Every GPU that loads the library holds the array until the process
+ *    exits.
  *  - The first call on each device looks up the array's device address with
- *    that device current; make that first call before any stream capture.
- *  - All calls on a device share the one array (each call clears what it
- *    uses first), so calls that can overlap on the GPU -- on different
- *    streams without ordering between them -- race and corrupt each other's
- *    output.  Serialise them, e.g. by issuing them on one stream. */
+ *    that device current and keeps it; make that first call before any
+ *    stream capture.  The address belongs to the device's primary context:
+ *    do not use this call after a cudaDeviceReset in the same process.
+ *  - Nothing in the array is cleared: each call writes every count it later
+ *    reads, so what an earlier call left there does not matter.  The output
+ *    of a call that reported an error is undefined.
+ *  - All calls on a device share the one array, so calls that can overlap
+ *    on the GPU -- on different streams without ordering between them --
+ *    race and corrupt each other's output.  Serialise them, e.g. by issuing
+ *    them on one stream. */
 sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n,
                             void* d_out, size_t out_capacity, unsigned long long* d_out_bytes,
                             int* d_status, cudaStream_t stream);

@@ -145,18 +145,21 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
 // sz_encode_noalloc keeps its workspace in this file-scope device array
 // instead of taking one from the caller.  Every GPU that loads the library
 // holds the array until the process exits.  Sized for n up to 2^28 elements
-// of either dtype, staging up to 256 escape records per BF16 scan tile (the
-// rest are re-derived): 6.1 MiB.
+// of either dtype, staging up to 256 escape records per scan tile (the rest
+// are re-derived): 8,192 scan tiles x (4 + 64 + 768) bytes = 6,848,512 bytes.
 constexpr uint64_t kNoAllocMaxElems = 1ull << 28;
 constexpr uint32_t kNoAllocStageRecs = 256;
 static_assert(kNoAllocStageRecs <= kStageRecsE5 && kNoAllocStageRecs % 16 == 0, "within both encoders' staging");
 constexpr uint64_t kNoAllocScratchBytes =
     (kNoAllocMaxElems / kScanTile) * (4 + 2ull * kUnitsPerScan + 3ull * kNoAllocStageRecs);
+static_assert(kNoAllocScratchBytes == 6848512, "the size the header states");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Host code cannot use g_noalloc_scratch as a device address (in host code the
 // name is a host-side stand-in), so its device address is looked up once per
-// device, with that device current, and cached.
+// device, with that device current, and cached.  The address belongs to the
+// device's primary context; a cudaDeviceReset would make it stale, which the
+// header rules out.
 constexpr int kMaxDevices = 128;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
@@ -348,7 +351,8 @@ sz_status sz_encode_noalloc(sz_dtype dt, const sz_codebook* h_cb, const void* d_
     void* ws = nullptr;
     const sz_status st = noalloc_scratch_for_current_device(&ws);
     if (st != SZ_OK) return st;
-    // The two-phase encode needs no cleared workspace.
+    // Nothing needs clearing: the encoders write every count that the finish
+    // kernel reads.
     return encode_impl(dt, h_cb, d_in, n, d_out, out_capacity, d_out_bytes, d_status, ws, kNoAllocScratchBytes, 0,
                        kWaitLimitNs, stream, kNoAllocStageRecs);
 }

@@ -98,3 +98,23 @@ def test_bench_legs_are_defined():
 
     missing = {name for name in called - local - defined if not hasattr(builtins, name)}
     assert not missing, missing
+
+
+def test_rates_and_codec_roofline():
+    # 1 GB in, 0.75 GB stream: the codec moves 1.75 GB per call; at 1 ms per
+    # encode and 0.5 ms per decode against a 7,000 GB/s copy peak.
+    r = bench.rates(10 ** 9, 750_000_000, 0.001, 0.0005, 7000.0)
+    assert r["encode_gbs"] == pytest.approx(1000.0) and r["decode_gbs"] == pytest.approx(2000.0)
+    assert r["encode_frac_of_codec_roofline"] == pytest.approx(1750.0 / 7000.0)
+    assert r["decode_frac_of_codec_roofline"] == pytest.approx(3500.0 / 7000.0)
+    assert r["codec_roofline_gbs"] == pytest.approx(7000.0 / 1.75)
+
+
+def test_default_run_headlines_the_largest_graded_workload():
+    from lossless_kv_cache_bf16_gb300 import workloads as W
+
+    largest = max(bench.GRADED, key=lambda name: W.CONFIGS[name].numel * (2 if W.CONFIGS[name].dtype == "bf16" else 1))
+    assert largest == "long_ctx_gqa"
+    import inspect
+
+    assert '"--config", default="long_ctx_gqa"' in inspect.getsource(bench.main)
