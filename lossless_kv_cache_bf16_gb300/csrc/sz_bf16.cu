@@ -436,14 +436,15 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
 //
 // One block barrier per tile.  The escapes are gathered one tile ahead into
 // the other of two bitmap/table buffers: while tile t is decoded from buffer
-// t % 2, every thread takes up to two of the next 512 records (cursor + tid
-// and cursor + 256 + tid) and, for each that lies below tile t+1's end,
-// checks it and enters it into buffer (t+1) % 2.  The tile's closing barrier
-// (count_taken_sync) both publishes those entries and counts them, which
-// advances the cursor; only a tile with more than 512 escapes takes further
-// counted steps.  A bitmap word is read only
-// by its owning thread, which clears it right after reading.  Chunk headers
-// are read two tiles ahead, also ahead of a closing barrier.
+// t % 2, every thread takes up to four of the next 1,024 records (cursor +
+// tid + 256 k) and, for each that lies below tile t+1's end, checks it and
+// enters it into buffer (t+1) % 2.  The tile's closing barrier
+// (count_prefix_sync) both publishes those entries and counts them, which
+// advances the cursor; only a tile with more than 1,024 escapes takes further
+// counted steps.  The record windows keep two windows of copies in flight
+// ahead of the walk.  A bitmap word is read only by its owning thread, which
+// clears it right after reading.  Chunk headers are read two tiles ahead,
+// also ahead of a closing barrier.
 //
 // Validation: every record is consumed by exactly one tile and checked there
 // (position inside the tile, above the previous one); a chunk's last tile
@@ -455,7 +456,8 @@ namespace {
 
 constexpr uint32_t kDecStages = 2;
 constexpr uint32_t kDecThreads = kBf16Threads;  // 256
-constexpr uint32_t kDecR = 2;                   // records a thread takes per step
+constexpr uint32_t kDecR = 4;                   // records a thread takes per step
+constexpr uint32_t kDecWindows = 4;             // record windows: two resident, two in flight
 constexpr uint32_t kStepRecs = kDecR * kDecThreads;
 
 struct DecodeSmem {
@@ -465,8 +467,9 @@ struct DecodeSmem {
     uint32_t lut[256];
     uint32_t bits[2][kDecThreads];  // escape bitmaps: word tid belongs to thread tid
     uint8_t patch[2][kBf16Tile];    // escape exponents by position in the tile
-    alignas(16) uint8_t win[3][kWinBytes];  // record windows (RecordWindow)
+    alignas(16) uint8_t win[kDecWindows][kWinBytes];  // record windows (RecordWindow)
     uint32_t hdr[2][2];             // {offset, count} of a chunk, by chunk parity
+    uint32_t taken[2][kDecThreads / 32];  // per-warp step counts (count_prefix_sync)
     uint32_t scratch[8];
     int bad;
     int abort;
@@ -543,7 +546,9 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
     // Record windows and the walk state (the chunk of the tile whose escapes
     // are gathered next).  All of it is block-uniform, so every thread
     // reaches the same barriers.
-    RecordWindow<kDecThreads> W(S.win, rec, p.n_esc);
+    RecordWindow<kDecThreads, kDecWindows> W(S.win, rec, p.n_esc);
+    uint32_t parity = 0;  // count_prefix_sync's slot parity (block-uniform)
+    auto count_step = [&](uint32_t took) { return count_prefix_sync<kDecThreads, kDecR>(took, &S.taken[0][0], parity); };
     uint32_t chunk_o = 0, chunk_end = 0, cursor = 0;
     // The next step's records [cursor, cursor + kStepRecs), and record
     // cursor - 1 when the step continues a tile, must be resident.
@@ -586,7 +591,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
         uint32_t took = 0;
 #pragma unroll
         for (uint32_t k = 0; k < kDecR; k++) {
-            // 64-bit: cursor + 511 may pass 2^32 near the end of 2^32 records.
+            // 64-bit: cursor + 1023 may pass 2^32 near the end of 2^32 records.
             const uint64_t r64 = (uint64_t)cursor + tid + k * kDecThreads;
             if (r64 >= chunk_end) break;
             const uint32_t r = (uint32_t)r64;
@@ -612,7 +617,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
         while (k == kStepRecs && cursor < chunk_end) {
             const uint32_t prev = W.pos(cursor - 1);  // still resident
             cover(true);
-            k = count_taken_sync<kDecThreads>(gather(tw, b, prev));
+            k = count_step(gather(tw, b, prev));
             cursor += k;
         }
         if (last_of_chunk(tw) && cursor != chunk_end && tid == 0) S.bad = 1;
@@ -652,7 +657,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
             }
         }
         cover(false);
-        end_tile(t_begin, 0, count_taken_sync<kDecThreads>(gather(t_begin, 0, 0xFFFFFFFFu)));
+        end_tile(t_begin, 0, count_step(gather(t_begin, 0, 0xFFFFFFFFu)));
     }
 
     bool aborted = false;
@@ -779,7 +784,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
         if (failed_wait) S.abort = 1;
         // Closing barrier: stage slot and buffer buf free, buffer buf ^ 1 and
         // the next header published, the step counted.
-        const uint32_t k = count_taken_sync<kDecThreads>(mine);
+        const uint32_t k = count_step(mine);
         if (S.abort) {
             aborted = true;
             break;
