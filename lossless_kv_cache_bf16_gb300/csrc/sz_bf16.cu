@@ -37,10 +37,10 @@ constexpr uint32_t kWarps = kBf16Threads / 32;
 //    round-robin order.  Sub-tiles arrive through a 2-stage ring of TMA bulk
 //    copies; per sub-tile the block splits, codes and packs, stores the dense
 //    streams, and ranks the escapes (ballot/popc warp scans, then a block
-//    scan).  Each scan tile's escape count, the count of each of its
-//    1,024-element units (one per warp and sub-tile) and its first ws_cap
-//    records, in element order, go to the workspace.  Blocks never wait for
-//    each other.
+//    scan).  Each scan tile's escape count and its first ws_cap records, in
+//    element order, go to the workspace, and, for a scan tile with more
+//    escapes than that, the count of each of its 1,024-element units (one per
+//    warp and sub-tile).  Blocks never wait for each other.
 // 2. finish_kernel (sz_finish.cu) turns the counts into escape offsets,
 //    copies the staged records into the stream, writes the chunk headers and
 //    the stream size, and re-derives the records of any scan tile beyond its
@@ -66,7 +66,7 @@ static_assert(kBf16Tile / kWarps == kUnitElems, "a unit is one warp's share of a
 struct EncodeSmem {
     alignas(128) uint8_t in[kEncStages][kTileBytes];
     uint64_t full[kEncStages];        // TMA -> compute: sub-tile landed
-    alignas(16) uint32_t warp_esc[2][kWarps];
+    alignas(16) uint32_t warp_esc[kSubsPerScan][kWarps];  // warp totals of the scan tile's sub-tiles
     alignas(16) uint8_t rec[3 * kStageRecsBf16];  // the scan tile's staged records
     uint8_t code[256];                // exponent -> code; 0x10 marks an escape
 };
@@ -344,11 +344,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
             }
             uint32_t off[4];
             const uint32_t warp_total = warp_escape_ranks(esc, lane, off);
-            if (lane == 0) {
-                S.warp_esc[i & 1][warp] = warp_total;
-                // The warp's 1,024 elements are unit part * 8 + warp of the scan tile.
-                p.ws_unit[(uint64_t)st * kUnitsPerScan + part * kWarps + warp] = (uint16_t)warp_total;
-            }
+            if (lane == 0) S.warp_esc[part][warp] = warp_total;
             // Block barrier: warp totals visible, the ring slot consumed by
             // every thread (its words were used by the stores above).
             if (__syncthreads_or(failed_wait)) {
@@ -362,8 +358,8 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
                 // offset is the one before it, picked by the warp index bits
                 // (fixed per thread, so the tests leave the loop).
                 static_assert(kWarps == 8, "eight warp totals");
-                const uint4 a = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][0]);
-                const uint4 b = *reinterpret_cast<const uint4*>(&S.warp_esc[i & 1][4]);
+                const uint4 a = *reinterpret_cast<const uint4*>(&S.warp_esc[part][0]);
+                const uint4 b = *reinterpret_cast<const uint4*>(&S.warp_esc[part][4]);
                 const uint32_t p0 = a.x, p1 = p0 + a.y, p2 = p1 + a.z, p3 = p2 + a.w;
                 const uint32_t p4 = p3 + b.x, p5 = p4 + b.y, p6 = p5 + b.z, p7 = p6 + b.w;
                 const uint32_t lo = (warp & 2u) ? ((warp & 1u) ? p2 : p1) : ((warp & 1u) ? p0 : 0u);
@@ -381,6 +377,11 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
         if (aborted) break;  // block-uniform
         if (tid == 0) p.ws_count[st] = run;
         __syncthreads();  // every record of the scan tile is in S.rec
+        // A scan tile with more escapes than it stages also leaves the escape
+        // count of each unit (warp w of sub-tile part is unit part * 8 + w),
+        // from which the finish kernel re-derives the rest; others need none.
+        if (run > p.ws_cap && tid < subs * kWarps)
+            p.ws_unit[(uint64_t)st * kUnitsPerScan + tid] = (uint16_t)S.warp_esc[tid / kWarps][tid % kWarps];
         {
             // The workspace region (3 ws_cap bytes, a multiple of 16) starts
             // 16-byte aligned, so whole 16-byte pieces stay inside it.

@@ -28,7 +28,7 @@ namespace sz {
 namespace {
 
 static_assert(kChunk % kE5Tile == 0, "tiles must not straddle chunks");
-static_assert(8 * kE5PerThread == kUnitElems, "a unit is eight encoder threads' elements");
+static_assert(32 * kE5PerThread == kUnitElemsE5, "an E5M2 unit is one encoder warp's elements");
 constexpr uint32_t kWarpElems = 32 * kE5PerThread;     // 4096
 constexpr uint32_t kEncThreads = kScanTile / kE5PerThread;  // 256: one scan tile per encode block
 constexpr uint32_t kEncWarps = kEncThreads / 32;
@@ -106,10 +106,11 @@ __device__ __forceinline__ void code_group(uint32_t a, uint32_t b, uint32_t add,
 // loads stay coalesced while each thread codes its own 128 contiguous bytes.
 // The packed bytes (7 pieces of 16 bytes per thread) reuse the same buffer
 // once the whole warp has read its rows, and leave with coalesced stores.
-// Before that, the tile's escape count, the counts of its 1,024-element
-// units and its first ws_cap records (element order: thread, then element;
-// exponents read back from the rows) go to the workspace; finish_kernel
-// (sz_finish.cu) places the records.
+// Before that, the tile's escape count and its first ws_cap records
+// (element order: thread, then element; exponents read back from the rows)
+// go to the workspace, and, when the tile has more escapes than that, the
+// count of each warp's 4,096 elements; finish_kernel (sz_finish.cu) places
+// the records.
 // ---------------------------------------------------------------------------
 struct EncodeE5Smem {
     uint4 buf[kEncWarps][256];  // input: 8 swizzled pieces per thread; then output: 7 pieces per thread
@@ -168,13 +169,6 @@ __device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5
         if (lane >= (uint32_t)d) incl += a;
     }
     if (lane == 31) s_warp_esc[warp] = incl;
-    {
-        // Escapes of each 1,024-element unit (8 lanes of 128 elements):
-        // unit warp * 4 + lane / 8 of the scan tile.
-        const uint32_t prev8 = __shfl_up_sync(0xFFFFFFFFu, incl, 8);
-        if ((lane & 7u) == 7u)
-            p.ws_unit[(uint64_t)st * kUnitsPerScan + warp * 4u + (lane >> 3)] = (uint16_t)(incl - (lane >= 8 ? prev8 : 0u));
-    }
     __syncthreads();
     uint32_t rank = incl - mine, tile_esc = 0;
 #pragma unroll
@@ -184,6 +178,10 @@ __device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5
         tile_esc += c;
     }
     if (tid == 0) p.ws_count[st] = tile_esc;
+    // Only a scan tile with more escapes than it stages leaves the escape
+    // count of each of its units (one warp's 4,096 elements each), from
+    // which the finish kernel re-derives the rest.
+    if (tile_esc > p.ws_cap && tid < kEncWarps) p.ws_unit[(uint64_t)st * kUnitsPerScan + tid] = (uint16_t)s_warp_esc[tid];
     // Stage this thread's records (those ranked below ws_cap); the exponents
     // come from the thread's input row, still in shared memory.
     // They are gathered in shared memory and leave in 16-byte stores.

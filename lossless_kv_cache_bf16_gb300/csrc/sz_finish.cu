@@ -13,8 +13,9 @@
 //    most 3 single bytes at either end;
 //  * a scan tile with more than ws_cap escapes has its ws_cap staged records
 //    copied the same way; the rest are re-derived from the input unit by
-//    unit (1,024 elements each, whose escape counts the encoders also left
-//    in the workspace, so every unit's first record index is known).  The
+//    unit (1,024 elements each for BF16, 4,096 for E5M2, whose escape counts
+//    the encoders also left in the workspace, so every unit's first record
+//    index is known).  The
 //    units holding unstaged records are spread over all warps of the block:
 //    a warp loads its unit with all 16-byte loads in flight, finds and ranks
 //    the escapes (a warp scan), assembles their records in its staging
@@ -99,16 +100,17 @@ __device__ __forceinline__ void put_full_group(uint8_t* buf, uint32_t a, uint32_
     }
 }
 
-// The records of one 1,024-element unit of a scan tile that did not fit the
-// staged ones, re-derived from the input and written by one warp at byte
-// offset dst of the stream, in element order: the unit's records of
-// unit-local rank >= skip (those below are among the staged records).  The
+// The records of 1,024 elements of a scan tile that did not fit the staged
+// ones, re-derived from the input and written by one warp at byte offset dst
+// of the stream, in element order: those of local rank >= skip (the ones
+// below are among the staged records).  Returns how many escapes the 1,024
+// elements hold.  The
 // unit is kU pieces of 16 bytes per lane (piece u * 32 + lane), all loaded
 // before any is examined.  buf: the warp's staging buffer (kStageBytes + 16
 // bytes, 16-byte aligned), which holds the 1,024 records a unit can have.
 template <bool BF16, bool PAGED>
-__device__ void rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
-                              const uint8_t* s_member, uint8_t* buf) {
+__device__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
+                                  const uint8_t* s_member, uint8_t* buf) {
     constexpr uint32_t kPer = BF16 ? 8u : 16u;  // elements in 16 bytes
     constexpr uint32_t kEsize = BF16 ? 2u : 1u;
     constexpr uint32_t kU = kUnitElems / (32 * kPer);  // 4 (BF16) or 2 (E5M2)
@@ -202,6 +204,7 @@ __device__ void rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t sk
     __syncwarp();
     copy_out(buf, before > skip ? 3 * (before - skip) : 0u, p.out, dst, p.capacity, lane, 32);
     __syncwarp();  // buf is reused by the warp's next unit
+    return before;  // the escapes of these 1,024 elements
 }
 
 }  // namespace
@@ -211,8 +214,7 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
     __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 16];  // +16: realignment reads past the end
     __shared__ uint32_t s_sum[kFinWarps];
     __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
-    __shared__ uint16_t s_units[kFinThreads][kUnitsPerScan];  // unit escape counts of the heavy tiles
-    __shared__ uint8_t s_heavy[kFinThreads];                 // the batch's heavy tiles, in order
+    __shared__ uint8_t s_heavy[kFinThreads];  // the batch's heavy tiles, in order
     __shared__ uint32_t s_nheavy[kFinWarps];
     __shared__ uint8_t s_member[256];  // exponent is in the codebook
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -289,27 +291,25 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
                 if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
             }
         }
-        __syncthreads();
-        // The batch's heavy tiles (more escapes than staged), in order, and
-        // the escape counts of their units (units past n were never
-        // written: 0), loaded once for all warps.
+        // The batch's heavy tiles (more escapes than staged), in order.
         const uint32_t batch = min(kFinThreads, t1 - c0);
         const bool is_heavy = tid < batch && cnt > p.ws_cap;
-        const uint32_t hb = __ballot_sync(0xFFFFFFFFu, is_heavy);
-        if (lane == 0) s_nheavy[warp] = __popc(hb);
-        __syncthreads();
-        uint32_t nheavy = 0, hbefore = 0;
+        // The barrier that publishes s_prefix and s_count (and lets s_sum be
+        // rewritten) also tells whether the batch has heavy tiles at all (the
+        // common case has none).
+        const bool any_heavy = __syncthreads_or(is_heavy);
+        uint32_t nheavy = 0;
+        if (any_heavy) {
+            const uint32_t hb = __ballot_sync(0xFFFFFFFFu, is_heavy);
+            if (lane == 0) s_nheavy[warp] = __popc(hb);
+            __syncthreads();
+            uint32_t hbefore = 0;
 #pragma unroll
-        for (uint32_t v = 0; v < kFinWarps; v++) {
-            hbefore += v < warp ? s_nheavy[v] : 0u;
-            nheavy += s_nheavy[v];
-        }
-        if (is_heavy) s_heavy[hbefore + __popc(hb & ((1u << lane) - 1u))] = (uint8_t)tid;
-        __syncthreads();
-        for (uint32_t i = tid; i < nheavy * kUnitsPerScan; i += kFinThreads) {
-            const uint32_t h = i / kUnitsPerScan, u = i % kUnitsPerScan, st = c0 + s_heavy[h];
-            const bool in_range = (uint64_t)st * kScanTile + (uint64_t)u * kUnitElems < p.L.n;
-            s_units[h][u] = in_range ? p.ws_unit[(uint64_t)st * kUnitsPerScan + u] : (uint16_t)0;
+            for (uint32_t v = 0; v < kFinWarps; v++) {
+                hbefore += v < warp ? s_nheavy[v] : 0u;
+                nheavy += s_nheavy[v];
+            }
+            if (is_heavy) s_heavy[hbefore + __popc(hb & ((1u << lane) - 1u))] = (uint8_t)tid;
         }
         // One warp per scan tile: copy its staged records (all of them, or
         // the first ws_cap of a heavier tile), 1,024 records at a time.
@@ -333,17 +333,31 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
                 __syncwarp();  // the buffer is reused next
             }
         }
-        __syncthreads();  // s_units complete
+        if (any_heavy) __syncthreads();  // s_heavy complete (block-uniform)
         // The units that hold the heavy tiles' remaining records are
         // re-derived, spread over all warps of the block.  Every warp walks
         // the same list of such units in the same order (heavy tiles in tile
         // order, units in element order) and takes every kFinWarps-th one, so
         // the units of one tile run side by side.
+        // Lane u of the warp holds the escape count of unit u of a heavy tile
+        // (32 units of 1,024 elements for BF16, 8 of 4,096 for E5M2; units
+        // past n were never written: 0); the next tile's counts are loaded
+        // while this one's units are re-derived.
+        constexpr uint32_t kUnit = BF16 ? kUnitElems : kUnitElemsE5;
+        constexpr uint32_t kUnits = kScanTile / kUnit;
+        auto unit_count = [&](uint32_t h) -> uint32_t {
+            if (h >= nheavy) return 0u;
+            const uint32_t st = c0 + s_heavy[h];
+            const bool in_range = lane < kUnits && (uint64_t)st * kScanTile + (uint64_t)lane * kUnit < p.L.n;
+            return in_range ? (uint32_t)p.ws_unit[(uint64_t)st * kUnitsPerScan + lane] : 0u;
+        };
         uint32_t k = 0;  // running index of the units walked so far
+        uint32_t uc_next = unit_count(0);
         for (uint32_t h = 0; h < nheavy; h++) {
             const uint32_t j = s_heavy[h];
             const uint64_t tbase = (uint64_t)(c0 + j) * kScanTile;
-            const uint32_t uc = s_units[h][lane];
+            const uint32_t uc = uc_next;
+            uc_next = unit_count(h + 1);
             uint32_t incl = uc;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
@@ -363,9 +377,15 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
                 const uint32_t u = __ffs(units) - 1;
                 for (uint32_t q = 0; q < kFinWarps && units; q++) units &= units - 1;  // the next one is 8 on
                 const uint32_t f = __shfl_sync(0xFFFFFFFFu, ufirst, u);
-                const uint32_t skip = p.ws_cap > f ? p.ws_cap - f : 0u;
-                const uint64_t dst = p.L.rec_off + 3ull * ((uint64_t)s_prefix[j] + f + skip);
-                rederive_unit<BF16, PAGED>(p, tbase + (uint64_t)u * kUnitElems, skip, dst, s_member, stage);
+                // The unit's records of tile-local rank >= ws_cap go out, in
+                // steps of 1,024 elements (one step for a BF16 unit).
+                uint32_t done = 0;  // escapes of the unit's earlier steps
+                for (uint32_t e = 0; e < kUnit; e += kUnitElems) {
+                    const uint32_t at = f + done;  // tile-local rank of the step's first escape
+                    const uint32_t skip = p.ws_cap > at ? p.ws_cap - at : 0u;
+                    const uint64_t dst = p.L.rec_off + 3ull * ((uint64_t)s_prefix[j] + at + skip);
+                    done += rederive_unit<BF16, PAGED>(p, tbase + (uint64_t)u * kUnit + e, skip, dst, s_member, stage);
+                }
             }
         }
         base += total;

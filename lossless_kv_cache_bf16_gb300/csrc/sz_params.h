@@ -99,10 +99,13 @@ constexpr uint32_t kScanTile = 32768;
 // so that every tile's staged run starts 16-byte aligned.
 constexpr uint32_t kStageRecsBf16 = 2048;
 constexpr uint32_t kStageRecsE5 = 1024;
-// A scan tile is 32 units of 1,024 consecutive elements; the encoders record
-// each unit's escape count, so that the records of a scan tile beyond its
-// staged ones can be re-derived unit by unit, in parallel, at known offsets.
+// A scan tile is 32 units of 1,024 consecutive elements (BF16) or 8 units of
+// 4,096 (E5M2, one encoder warp's share); for a scan tile with more escapes
+// than it stages, the encoders record each unit's escape count, so that the
+// remaining records can be re-derived unit by unit, in parallel, at known
+// offsets.  The workspace has room for 32 counts per scan tile.
 constexpr uint32_t kUnitElems = 1024;
+constexpr uint32_t kUnitElemsE5 = 4096;
 constexpr uint32_t kUnitsPerScan = kScanTile / kUnitElems;  // 32
 
 // Launches kern as a programmatic dependent of the kernel before it in the
