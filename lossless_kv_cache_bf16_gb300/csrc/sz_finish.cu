@@ -28,6 +28,7 @@
 // "Metodologia: SplitZip" > "Flujo de Escape").
 #include "sz_device.cuh"
 #include "sz_params.h"
+#include "sz_pipeline.cuh"
 
 namespace sz {
 
@@ -36,10 +37,13 @@ namespace {
 constexpr uint32_t kFinThreads = 256;
 constexpr uint32_t kFinWarps = kFinThreads / 32;
 constexpr uint32_t kScansPerChunk = kChunk / kScanTile;
-constexpr uint32_t kPieceRecs = 1024;                     // records a warp moves at a time
+constexpr uint32_t kPieceRecs = 1024;                     // records a warp re-derives at a time
 constexpr uint32_t kStageBytes = 3 * kPieceRecs;          // a warp's staging buffer
-constexpr uint32_t kStageLoads = kStageBytes / 512;       // 16-byte loads per lane
-static_assert(kStageBytes % 512 == 0, "whole warp-wide 16-byte loads");
+constexpr uint32_t kHalfRecs = kPieceRecs / 2;            // staged records per half of it
+constexpr uint32_t kHalfStride = 3 * kHalfRecs + 16;      // second half: 16-byte aligned, a gap after the first
+constexpr uint32_t kHalfLoads = 3 * kHalfRecs / 512;      // 16-byte loads per lane for a half
+static_assert((3 * kHalfRecs) % 512 == 0 && kHalfStride % 16 == 0, "whole warp-wide 16-byte loads");
+static_assert(kHalfStride + 3 * kHalfRecs + 16 <= kStageBytes + 32, "both halves, and the reads past them, fit");
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
 
 // Copy nbytes from shared memory (src, 4-byte aligned, readable up to 4 bytes
@@ -106,7 +110,7 @@ __device__ __forceinline__ void put_full_group(uint8_t* buf, uint32_t a, uint32_
 // below are among the staged records).  Returns how many escapes the 1,024
 // elements hold.  The
 // unit is kU pieces of 16 bytes per lane (piece u * 32 + lane), all loaded
-// before any is examined.  buf: the warp's staging buffer (kStageBytes + 16
+// before any is examined.  buf: the warp's staging buffer (kStageBytes + 32
 // bytes, 16-byte aligned), which holds the 1,024 records a unit can have.
 template <bool BF16, bool PAGED>
 __device__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
@@ -211,7 +215,7 @@ __device__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_
 
 template <bool BF16, bool PAGED>
 __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodeParams p) {
-    __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 16];  // +16: realignment reads past the end
+    __shared__ __align__(16) uint8_t s_stage[kFinWarps][kStageBytes + 32];  // +32: realignment reads past the end
     __shared__ uint32_t s_sum[kFinWarps];
     __shared__ uint32_t s_prefix[kFinThreads], s_count[kFinThreads];
     __shared__ uint8_t s_heavy[kFinThreads];  // the batch's heavy tiles, in order
@@ -312,26 +316,57 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
             if (is_heavy) s_heavy[hbefore + __popc(hb & ((1u << lane) - 1u))] = (uint8_t)tid;
         }
         // One warp per scan tile: copy its staged records (all of them, or
-        // the first ws_cap of a heavier tile), 1,024 records at a time.
+        // the first ws_cap of a heavier tile).  The warp's staging buffer has
+        // two halves of 512 records: a run that fits one (the common case)
+        // arrives there by asynchronous copies while the warp writes out the
+        // run before it, so a warp's runs cost one memory round trip instead
+        // of one each.  A longer run goes through its half 512 records at a
+        // time.
+        auto fits = [&](uint32_t j) { return min(s_count[j], p.ws_cap) <= kHalfRecs; };
+        auto prefetch = [&](uint32_t j, uint32_t h) {  // whole warp; one commit group
+            const uint32_t nbytes = 3 * min(s_count[j], p.ws_cap);
+            const uint8_t* run = p.ws_rec + (uint64_t)(c0 + j) * 3 * p.ws_cap;
+            // Whole 16-byte pieces stay inside the run's region (3 ws_cap
+            // bytes, a multiple of 16, starting 16-byte aligned).
+            for (uint32_t b = 16 * lane; b < nbytes; b += 512) cp_async16(stage + h * kHalfStride + b, run + b, 16);
+            cp_async_commit();
+        };
+        uint32_t h = 0;
+        bool ready = warp < batch && fits(warp);  // run j is on its way into half h
+        if (ready) prefetch(warp, 0);
         for (uint32_t j = warp; j < batch; j += kFinWarps) {
-            const uint32_t st = c0 + j, c = min(s_count[j], p.ws_cap);
-            // The staged run starts 16-byte aligned inside a region of
-            // 3 * ws_cap bytes (a multiple of 16); so does every piece.
-            const uint8_t* run = p.ws_rec + (uint64_t)st * 3 * p.ws_cap;
-            for (uint32_t q = 0; q < c; q += kPieceRecs) {
-                const uint32_t nbytes = 3 * min(kPieceRecs, c - q);
-                const uint4* src = reinterpret_cast<const uint4*>(run + 3 * q);
-                uint4 v[kStageLoads];
-#pragma unroll
-                for (uint32_t k = 0; k < kStageLoads; k++)
-                    if (16 * lane + 512 * k < nbytes) v[k] = src[lane + 32 * k];
-#pragma unroll
-                for (uint32_t k = 0; k < kStageLoads; k++)
-                    if (16 * lane + 512 * k < nbytes) reinterpret_cast<uint4*>(stage)[lane + 32 * k] = v[k];
+            const uint32_t c = min(s_count[j], p.ws_cap);
+            const uint64_t dst = p.L.rec_off + 3ull * s_prefix[j];
+            const uint32_t jn = j + kFinWarps;
+            const bool next = jn < batch && fits(jn);
+            if (next) prefetch(jn, h ^ 1u);
+            uint8_t* const half = stage + h * kHalfStride;
+            if (ready) {
+                if (next)
+                    cp_async_wait_group<1>();
+                else
+                    cp_async_wait_all();
                 __syncwarp();
-                copy_out(stage, nbytes, p.out, p.L.rec_off + 3ull * ((uint64_t)s_prefix[j] + q), p.capacity, lane, 32);
-                __syncwarp();  // the buffer is reused next
+                copy_out(half, 3 * c, p.out, dst, p.capacity, lane, 32);
+                __syncwarp();  // the half is refilled two runs later
+            } else {
+                for (uint32_t q = 0; q < c; q += kHalfRecs) {
+                    const uint32_t nbytes = 3 * min(kHalfRecs, c - q);
+                    const uint4* src = reinterpret_cast<const uint4*>(p.ws_rec + (uint64_t)(c0 + j) * 3 * p.ws_cap + 3 * q);
+                    uint4 v[kHalfLoads];
+#pragma unroll
+                    for (uint32_t k = 0; k < kHalfLoads; k++)
+                        if (16 * lane + 512 * k < nbytes) v[k] = src[lane + 32 * k];
+#pragma unroll
+                    for (uint32_t k = 0; k < kHalfLoads; k++)
+                        if (16 * lane + 512 * k < nbytes) reinterpret_cast<uint4*>(half)[lane + 32 * k] = v[k];
+                    __syncwarp();
+                    copy_out(half, nbytes, p.out, dst + 3ull * q, p.capacity, lane, 32);
+                    __syncwarp();  // the half is reused next
+                }
             }
+            h ^= 1u;
+            ready = next;
         }
         if (any_heavy) __syncthreads();  // s_heavy complete (block-uniform)
         // The units that hold the heavy tiles' remaining records are
