@@ -95,11 +95,11 @@ typedef struct sz_codebook {
 size_t sz_encoded_size(sz_dtype dt, size_t n, size_t n_escapes);
 
 /* Bytes of device workspace that sz_encode needs for n elements: for every
- * 32,768-element scan tile its escape count, the escape counts of its 32
- * units of 1,024 elements, and up to 2,048 (BF16) or 1,024 (E5M2) staged
- * escape records of 3 bytes -- about 9.6% of the input bytes for either
- * dtype.  A scan tile with more escapes than it stages has the rest of its
- * records re-derived from the input (same stream, more time).  The
+ * 32,768-element scan tile its escape count, an error word, the escape
+ * counts of its units, and up to 2,048 (BF16) or 1,024 (E5M2) staged escape
+ * records of 3 bytes -- about 9.6% of the input bytes for either dtype.  A
+ * scan tile with more escapes than it stages has the rest of its records
+ * re-derived from the input (same stream, more time).  The
  * workspace is scratch: its contents on entry do not matter (every count is
  * written before it is read), and it must not be shared by encodes that can
  * run at the same time.  Host only; returns 0 for an unknown dtype. */
@@ -182,7 +182,9 @@ sz_status sz_calibrate(sz_dtype dt, const void* d_sample, size_t n,
  *                host thread can read once the stream has passed the call
  *                without a copy
  *  d_status      device int or NULL: SZ_OK, SZ_ERR_CAPACITY or SZ_ERR_TIMEOUT
- *                (sz_encode_dcb also SZ_ERR_INVALID_ARG for a bad codebook)
+ *                (sz_encode_dcb also SZ_ERR_INVALID_ARG for a bad codebook).
+ *                Written once, by the call's last kernel; what it held before
+ *                the call does not matter
  *  d_ws          device workspace of ws_bytes >= sz_workspace_size(dt, n)
  * Asynchronous; the stream is byte-for-byte the layout above. */
 sz_status sz_encode(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, size_t n,
@@ -316,8 +318,8 @@ const char* sz_status_string(int status);
  * almost all device memory to its KV-cache pool and forbids further
  * allocations, or a latency-critical path that must not take cudaMalloc's
  * implicit device synchronisation -- and so cannot provide the workspace
- * that sz_encode takes.  This call uses a workspace of 6,848,512 bytes
- * (6.53 MiB) held in a static device array inside the library instead, and
+ * that sz_encode takes.  This call uses a workspace of 6,881,280 bytes
+ * (6.56 MiB) held in a static device array inside the library instead, and
  * otherwise behaves exactly like sz_encode (same arguments, stream bytes,
  * d_out_bytes and d_status semantics).  It allocates nothing and calls no
  * allocating routine.

@@ -39,10 +39,11 @@ uint64_t scan_tiles_for(uint64_t n) { return std::max<uint64_t>(1, cdiv(n, kScan
 uint32_t stage_recs_for(sz_dtype dt) { return dt == SZ_BF16 ? kStageRecsBf16 : kStageRecsE5; }
 static_assert(kStageRecsBf16 % 16 == 0 && kStageRecsE5 % 16 == 0, "staged runs start 16-byte aligned");
 uint64_t align16(uint64_t x) { return (x + 15) & ~15ull; }
-// Workspace: [u32 count per scan tile][u16 count per 1,024-element unit,
-// 32 per scan tile][3 * cap bytes of records per scan tile].  Each section
-// starts 16-byte aligned.
-uint64_t unit_counts_offset(uint64_t tiles) { return align16(4 * tiles); }
+// Workspace: [u32 count per scan tile][i32 error code per encode block (at
+// most one block per scan tile)][u16 count per unit, 32 per scan tile][3 *
+// cap bytes of records per scan tile].  Each section starts 16-byte aligned.
+uint64_t error_words_offset(uint64_t tiles) { return align16(4 * tiles); }
+uint64_t unit_counts_offset(uint64_t tiles) { return error_words_offset(tiles) + align16(4 * tiles); }
 uint64_t staged_records_offset(uint64_t tiles) { return unit_counts_offset(tiles) + 2ull * kUnitsPerScan * tiles; }
 uint64_t workspace_bytes(uint64_t n, uint32_t cap) {
     const uint64_t tiles = scan_tiles_for(n);
@@ -114,6 +115,7 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     p.capacity = out_capacity;
     p.num_tiles = (uint32_t)scan_tiles_for(n);
     p.ws_count = static_cast<uint32_t*>(d_ws);
+    p.ws_err = reinterpret_cast<int*>(static_cast<uint8_t*>(d_ws) + error_words_offset(p.num_tiles));
     p.ws_unit = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(d_ws) + unit_counts_offset(p.num_tiles));
     p.ws_rec = static_cast<uint8_t*>(d_ws) + staged_records_offset(p.num_tiles);
     p.ws_cap = stage_recs;
@@ -133,11 +135,12 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
     else
         p.vec = aligned(d_in, 16) && aligned(d_out, 16);
 
-    // The workspace needs no clearing: the encoders write every count that
-    // the finish kernel reads.
-    cudaError_t err = d_status ? cudaMemsetAsync(d_status, 0, sizeof(int), stream) : cudaSuccess;
-    if (err != cudaSuccess) return from_cuda(err);
-    err = dt == SZ_BF16 ? launch_encode_bf16(p, stream) : launch_encode_e5m2(p, stream);
+    // Neither the workspace nor *d_status needs clearing: the encoders
+    // write every count and error word that the finish kernel reads, and the
+    // finish kernel's last block writes *d_status once, after every other
+    // block of the encode has reported.  (A reset of the status word would
+    // cost the GPU an operation of its own, about 2.7 us.)
+    const cudaError_t err = dt == SZ_BF16 ? launch_encode_bf16(p, stream) : launch_encode_e5m2(p, stream);
     return from_cuda(err);
 }
 
@@ -146,13 +149,14 @@ sz_status encode_impl(sz_dtype dt, const sz_codebook* h_cb, const void* d_in, si
 // instead of taking one from the caller.  Every GPU that loads the library
 // holds the array until the process exits.  Sized for n up to 2^28 elements
 // of either dtype, staging up to 256 escape records per scan tile (the rest
-// are re-derived): 8,192 scan tiles x (4 + 64 + 768) bytes = 6,848,512 bytes.
+// are re-derived): 8,192 scan tiles x (4 + 4 + 64 + 768) bytes = 6,881,280
+// bytes.
 constexpr uint64_t kNoAllocMaxElems = 1ull << 28;
 constexpr uint32_t kNoAllocStageRecs = 256;
 static_assert(kNoAllocStageRecs <= kStageRecsE5 && kNoAllocStageRecs % 16 == 0, "within both encoders' staging");
 constexpr uint64_t kNoAllocScratchBytes =
-    (kNoAllocMaxElems / kScanTile) * (4 + 2ull * kUnitsPerScan + 3ull * kNoAllocStageRecs);
-static_assert(kNoAllocScratchBytes == 6848512, "the size the header states");
+    (kNoAllocMaxElems / kScanTile) * (4 + 4 + 2ull * kUnitsPerScan + 3ull * kNoAllocStageRecs);
+static_assert(kNoAllocScratchBytes == 6881280, "the size the header states");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Host code cannot use g_noalloc_scratch as a device address (in host code the

@@ -69,6 +69,7 @@ struct EncodeSmem {
     alignas(16) uint32_t warp_esc[kSubsPerScan][kWarps];  // warp totals of the scan tile's sub-tiles
     alignas(16) uint8_t rec[3 * kStageRecsBf16];  // the scan tile's staged records
     uint8_t code[256];                // exponent -> code; 0x10 marks an escape
+    int err;                          // the block's error code (paged input: bad page ids)
 };
 
 struct GroupOut {
@@ -175,13 +176,13 @@ __device__ __forceinline__ uint32_t warp_escape_ranks(const uint32_t (&esc)[4], 
 // elements), so one page lookup serves the whole group.
 template <bool PAGED>
 __device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64_t base, uint32_t lane,
-                                                   uint32_t (&w)[4][4], uint32_t (&cnt)[4]) {
+                                                   uint32_t (&w)[4][4], uint32_t (&cnt)[4], int* err) {
     const uint64_t n = p.L.n;
 #pragma unroll
     for (int k = 0; k < 4; k++) {
         const uint64_t i0 = base + k * 256u + lane * 8u;
         cnt[k] = i0 >= n ? 0u : (n - i0 >= 8 ? 8u : (uint32_t)(n - i0));
-        const uint8_t* g = p.in + (cnt[k] ? elem_offset<PAGED>(p.pm, i0, 2, p.status) : 2 * i0);
+        const uint8_t* g = p.in + (cnt[k] ? elem_offset<PAGED>(p.pm, i0, 2, err) : 2 * i0);
         if (p.vec && cnt[k] == 8) {
             const uint4 v = ld_stream_v4(g);
             w[k][0] = v.x, w[k][1] = v.y, w[k][2] = v.z, w[k][3] = v.w;
@@ -231,8 +232,10 @@ __device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const
     }
 }
 
+// bad_codebook: the device codebook failed its check (SZ_ERR_INVALID_ARG).
+// At its end the block writes its error code to ws_err[blockIdx.x].
 template <bool CONTIG, bool PAGED>
-__device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const uint8_t (&cb)[16]) {
+__device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const uint8_t (&cb)[16], bool bad_codebook) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
@@ -255,6 +258,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
 
     if (tid == 0) {
         for (uint32_t s = 0; s < kEncStages; s++) mbar_init(&S.full[s], 1);
+        S.err = 0;  // reported to only after the barrier below
         fence_mbar_init();
     }
     {
@@ -279,7 +283,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
             if (PAGED) {
                 const uint32_t piece = 1u << piece_lg;  // elements per copy
                 for (uint32_t e = 0; e < kBf16Tile; e += piece)
-                    bulk_g2s(S.in[slot] + 2 * e, p.in + elem_offset<true>(p.pm, (uint64_t)u * kBf16Tile + e, 2, p.status),
+                    bulk_g2s(S.in[slot] + 2 * e, p.in + elem_offset<true>(p.pm, (uint64_t)u * kBf16Tile + e, 2, &S.err),
                              2 * piece, &S.full[slot]);
             } else {
                 bulk_g2s(S.in[slot], p.in + (uint64_t)u * kTileBytes, kTileBytes, &S.full[slot]);
@@ -324,7 +328,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
                     st_stream_u32(o_nib + k * 128, o.nib);
                 }
             } else {
-                load_groups_global<PAGED>(p, wbase, lane, w, cnt);
+                load_groups_global<PAGED>(p, wbase, lane, w, cnt, &S.err);
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
                     const uint64_t i0 = wbase + k * 256u + lane * 8u;
@@ -394,17 +398,21 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
         // barrier, which every thread reaches after this copy.
     }
     if (aborted && tid == 0) {
-        if (p.status) atomicMax(p.status, kStatusTimeout);
         // Copies in flight must land before the block exits (bounded).
         for (uint32_t k = waited; k < issued; k++)
             if (!(p.skip_first && blockIdx.x == 0 && k == 0))
                 mbar_wait(&S.full[k % kEncStages], (k / kEncStages) & 1u, p.wait_limit_ns);
     }
+    // The block's error code for the finish kernel: a timed-out wait, a bad
+    // device codebook, or (paged input, reported by any thread) a bad page id.
+    if (PAGED) __syncthreads();
+    if (tid == 0)
+        p.ws_err[blockIdx.x] = aborted ? kStatusTimeout : (bad_codebook ? kStatusInvalid : (PAGED ? S.err : 0));
 }
 
 // MODE 0: codebook in the parameters, table coding; 1: in the parameters,
-// contiguous; 2: in device memory, checked (a bad one sets SZ_ERR_INVALID_ARG
-// in *status) and the coding chosen on the device.
+// contiguous; 2: in device memory, checked (a bad one is reported as
+// SZ_ERR_INVALID_ARG) and the coding chosen on the device.
 // PAGED: the input is a paged tensor (EncodeParams::pm).
 template <int MODE, bool PAGED = false>
 __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf16_kernel(const EncodeParams p) {
@@ -412,13 +420,12 @@ __global__ void __launch_bounds__(kComputeThreads, SZ_ENC_MIN_BLOCKS) encode_bf1
     bool contig;
     const bool ok = load_codebook(p.cb, MODE == 2 ? p.cb_dev : nullptr, 256u, cb, contig);
     if (MODE == 2) {
-        if (!ok && blockIdx.x == 0 && threadIdx.x == 0 && p.status) atomicMax(p.status, kStatusInvalid);
         if (contig)
-            encode_bf16_body<true, false>(p, cb);
+            encode_bf16_body<true, false>(p, cb, !ok);
         else
-            encode_bf16_body<false, false>(p, cb);
+            encode_bf16_body<false, false>(p, cb, !ok);
     } else {
-        encode_bf16_body<MODE == 1, PAGED>(p, cb);
+        encode_bf16_body<MODE == 1, PAGED>(p, cb, false);
     }
 }
 

@@ -116,15 +116,19 @@ struct EncodeE5Smem {
     uint4 buf[kEncWarps][256];  // input: 8 swizzled pieces per thread; then output: 7 pieces per thread
     alignas(16) uint8_t rec[3 * kStageRecsE5];  // the scan tile's staged records
     uint32_t warp_esc[kEncWarps];
+    int werr[kEncWarps];        // paged input: each warp's error code (bad page ids)
     uint8_t field[256];         // byte -> field; 0x80 marks an escape
 };
 
 // Everything after the input rows are in shared memory: coding, escape
 // ranks, staged records, packed output.
-template <bool CONTIG>
+// The block's error goes out with the tile's escape count, as its bit 31
+// (kCountError): a bad device codebook (bad_codebook), or, with PAGED input,
+// a bad page id reported by any warp in S.werr.
+template <bool CONTIG, bool PAGED>
 __device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5Smem& S, const uint8_t (&cb)[16],
                                                  uint64_t warp_base, uint64_t thread_base, bool warp_full,
-                                                 uint32_t cnt) {
+                                                 uint32_t cnt, bool bad_codebook) {
     auto& s_field = S.field;
     auto& s_in = S.buf;
     auto& s_out = S.buf;
@@ -177,7 +181,14 @@ __device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5
         if (v < warp) rank += c;
         tile_esc += c;
     }
-    if (tid == 0) p.ws_count[st] = tile_esc;
+    if (tid == 0) {
+        bool bad = bad_codebook;
+        if (PAGED) {
+#pragma unroll
+            for (uint32_t v = 0; v < kEncWarps; v++) bad |= S.werr[v] != 0;
+        }
+        p.ws_count[st] = tile_esc | (bad ? kCountError : 0u);
+    }
     // Only a scan tile with more escapes than it stages leaves the escape
     // count of each of its units (one warp's 4,096 elements each), from
     // which the finish kernel re-derives the rest.
@@ -240,8 +251,8 @@ __device__ __forceinline__ void encode_e5m2_code(const EncodeParams& p, EncodeE5
 }
 
 // MODE 0: codebook in the parameters, table coding; 1: in the parameters,
-// contiguous; 2: in device memory, checked (a bad one sets
-// SZ_ERR_INVALID_ARG in *status), the coding chosen per block.  The device
+// contiguous; 2: in device memory, checked (a bad one is reported as
+// SZ_ERR_INVALID_ARG), the coding chosen per block.  The device
 // codebook is loaded first and examined only once this thread's input loads
 // are in flight, so its latency hides behind theirs.
 // PAGED: the input is a paged tensor (EncodeParams::pm).
@@ -258,16 +269,22 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
     const uint64_t thread_base = warp_base + lane * kE5PerThread;
     const bool warp_full = p.vec && warp_base + kWarpElems <= n;
     const uint32_t cnt = thread_base >= n ? 0u : (n - thread_base >= kE5PerThread ? kE5PerThread : (uint32_t)(n - thread_base));
+    // Paged input: the warp's error word, cleared before any lane can report to it.
+    int* const werr = PAGED ? &S.werr[warp] : nullptr;
+    if (PAGED) {
+        if (lane == 0) *werr = 0;
+        __syncwarp();
+    }
 
     // Input bytes into this thread's row.
     if (warp_full) {
         // A 16-element piece never straddles a page; the warp's 4,096
         // elements in one page take one lookup.
-        const RunOffset<PAGED> run(p.pm, warp_base, 12, 1, p.status);
+        const RunOffset<PAGED> run(p.pm, warp_base, 12, 1, werr);
 #pragma unroll
         for (uint32_t i = 0; i < 8; i++) {
             const uint32_t piece = lane + 32 * i;
-            s_in[warp][swz8(piece >> 3, piece & 7u)] = ld_stream_v4(p.in + run.at(p.pm, warp_base, 16 * piece, 1, p.status));
+            s_in[warp][swz8(piece >> 3, piece & 7u)] = ld_stream_v4(p.in + run.at(p.pm, warp_base, 16 * piece, 1, werr));
         }
     }
     uint8_t cb[16];
@@ -294,7 +311,6 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
     } else {
         ok = load_codebook(p.cb, nullptr, 32u, cb, contig);
     }
-    if (MODE == 2 && !ok && blockIdx.x == 0 && tid == 0 && p.status) atomicMax(p.status, kStatusInvalid);
     if (blockIdx.x == 0 && tid == 0) {
 #pragma unroll
         for (int k = 0; k < kCodes; k++) p.out[p.L.cb_off + k] = cb[k];
@@ -311,7 +327,7 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
 #pragma unroll
                 for (uint32_t t = 0; t < 4; t++) {
                     const uint32_t j = 16 * s + 4 * q + t;
-                    v |= (j < cnt ? (uint32_t)p.in[elem_offset<PAGED>(p.pm, thread_base + j, 1, p.status)] : pad)
+                    v |= (j < cnt ? (uint32_t)p.in[elem_offset<PAGED>(p.pm, thread_base + j, 1, werr)] : pad)
                          << (8 * t);
                 }
                 w[q] = v;
@@ -323,7 +339,7 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
     // A contiguous run must also stay within 5 bits for the byte-parallel coding.
     const bool use_contig = MODE == 1 || (MODE == 2 && contig && cb[0] <= 16);
     if (use_contig) {
-        encode_e5m2_code<true>(p, S, cb, warp_base, thread_base, warp_full, cnt);
+        encode_e5m2_code<true, PAGED>(p, S, cb, warp_base, thread_base, warp_full, cnt, MODE == 2 && !ok);
     } else {
         // The byte -> field table (block-uniform branch).
         const uint32_t x = tid, e = (x >> 2) & 31u;
@@ -334,7 +350,7 @@ __global__ void __launch_bounds__(kEncThreads, MODE == 0 ? 3 : 4) encode_e5m2_ke
         const uint32_t sm3 = ((x >> 7) << 2) | (x & 3u);
         S.field[x] = (uint8_t)(code == 0xFFu ? (0x80u | (sm3 << 4)) : (code | (sm3 << 4)));
         __syncthreads();
-        encode_e5m2_code<false>(p, S, cb, warp_base, thread_base, warp_full, cnt);
+        encode_e5m2_code<false, PAGED>(p, S, cb, warp_base, thread_base, warp_full, cnt, MODE == 2 && !ok);
     }
 }
 
@@ -717,7 +733,9 @@ cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s) {
     kern<<<p.num_tiles, kEncThreads, smem, s>>>(p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    return launch_finish(p, false, s);
+    EncodeParams q = p;
+    q.grid = 0;  // no error words: the E5M2 blocks flag errors in their counts
+    return launch_finish(q, false, s);
 }
 
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s) {

@@ -132,13 +132,14 @@ __device__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_
         if (vec && valid[u] == kPer) {
             // A piece of 16 bytes never straddles a page (pages are a power
             // of two of at least 16 elements).
-            const uint4 v = ld_stream_v4(p.in + elem_offset<PAGED>(p.pm, i0, kEsize, p.status));
+            // A bad page id was already reported by the encode kernel.
+            const uint4 v = ld_stream_v4(p.in + elem_offset<PAGED>(p.pm, i0, kEsize, nullptr));
             w[u][0] = v.x, w[u][1] = v.y, w[u][2] = v.z, w[u][3] = v.w;
         } else {
 #pragma unroll
             for (uint32_t j = 0; j < kPer; j++) {
                 if (j < valid[u]) {
-                    const uint8_t* e = p.in + elem_offset<PAGED>(p.pm, i0 + j, kEsize, p.status);
+                    const uint8_t* e = p.in + elem_offset<PAGED>(p.pm, i0 + j, kEsize, nullptr);
                     const uint32_t v = BF16 ? ((uint32_t)e[0] | ((uint32_t)e[1] << 8)) : (uint32_t)e[0];
                     w[u][j / (4 / kEsize)] |= v << (8 * kEsize * (j % (4 / kEsize)));
                 }
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
     __shared__ uint8_t s_heavy[kFinThreads];  // the batch's heavy tiles, in order
     __shared__ uint32_t s_nheavy[kFinWarps];
     __shared__ uint8_t s_member[256];  // exponent is in the codebook
+    __shared__ int s_err;              // last block: the capacity error, then the call's status
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint32_t T = p.num_tiles, F = gridDim.x;
     const uint32_t t0 = (uint32_t)((uint64_t)blockIdx.x * T / F), t1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * T / F);
@@ -232,23 +234,30 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
 #pragma unroll
         for (int k = 0; k < kCodes; k++) member |= cb[k] == tid;
         s_member[tid] = (uint8_t)member;
+        if (tid == 0) s_err = 0;
     }
     // The kernel is launched as a programmatic dependent of the encode
     // kernel, so the lines above overlap its tail; everything below reads
     // what it wrote, once it has finished (no wait without that launch).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // Escapes in all scan tiles before this block's range.  ws_count is
-    // 16-byte aligned.
-    uint32_t part = 0;
+    // 16-byte aligned.  Bit 31 of a count is the E5M2 encoder's error flag
+    // (kCountError); the last block, which reads every count, collects it.
+    uint32_t part = 0, flags = 0;
     {
         const uint4* c4 = reinterpret_cast<const uint4*>(p.ws_count);
         const uint32_t q_end = t0 / 4;
 #pragma unroll 8
         for (uint32_t q = tid; q < q_end; q += kFinThreads) {
             const uint4 v = c4[q];
-            part += v.x + v.y + v.z + v.w;
+            part += (v.x & ~kCountError) + (v.y & ~kCountError) + (v.z & ~kCountError) + (v.w & ~kCountError);
+            flags |= v.x | v.y | v.z | v.w;
         }
-        if (tid < (t0 & 3u)) part += p.ws_count[(t0 & ~3u) + tid];
+        if (tid < (t0 & 3u)) {
+            const uint32_t v = p.ws_count[(t0 & ~3u) + tid];
+            part += v & ~kCountError;
+            flags |= v;
+        }
     }
     part = __reduce_add_sync(0xFFFFFFFFu, part);
     if (lane == 0) s_sum[warp] = part;
@@ -261,7 +270,9 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
     uint8_t* const stage = s_stage[warp];
     for (uint32_t c0 = t0; c0 < t1; c0 += kFinThreads) {
         const uint32_t t = c0 + tid;
-        const uint32_t cnt = t < t1 ? p.ws_count[t] : 0u;
+        const uint32_t cword = t < t1 ? p.ws_count[t] : 0u;
+        const uint32_t cnt = cword & ~kCountError;
+        flags |= cword;
         uint32_t incl = cnt;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
             if ((t % kScansPerChunk == kScansPerChunk - 1 || last) && p.L.num_chunks > 0) {
                 // The chunk's earlier scan tiles: at most kScansPerChunk - 1.
                 uint32_t before = 0;
-                for (uint32_t k = t - t % kScansPerChunk; k < t; k++) before += p.ws_count[k];
+                for (uint32_t k = t - t % kScansPerChunk; k < t; k++) before += p.ws_count[k] & ~kCountError;
                 const uint32_t c = t / kScansPerChunk;
                 store_u32_le(p.out + p.L.hdr_off + 8ull * c, prefix - before);
                 store_u32_le(p.out + p.L.hdr_off + 8ull * c + 4, before + cnt);
@@ -292,7 +303,7 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
             if (last) {
                 const unsigned long long size = p.L.rec_off + 3ull * (prefix + cnt);
                 *p.out_bytes = size;
-                if (size > p.capacity && p.status) atomicMax(p.status, kStatusCapacity);
+                if (size > p.capacity) s_err = kStatusCapacity;  // the last block's own
             }
         }
         // The batch's heavy tiles (more escapes than staged), in order.
@@ -425,6 +436,20 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
         }
         base += total;
         __syncthreads();
+    }
+    // The call's status, written once, by the last block: the largest error
+    // code of the encode (a timed-out wait, a bad device codebook, a bad page
+    // id) and its own (capacity).  So the status word needs no reset before
+    // the call.
+    if (blockIdx.x == F - 1 && p.status) {
+        // BF16: one error word per encode block (p.grid of them, a few
+        // hundred); E5M2: the flags in the counts (p.grid is 0).
+        int e = (flags & kCountError) ? kStatusInvalid : 0;
+        for (uint32_t b = tid; b < p.grid; b += kFinThreads) e = max(e, p.ws_err[b]);
+        e = __reduce_max_sync(0xFFFFFFFFu, e);
+        if (lane == 0 && e) atomicMax(&s_err, e);
+        __syncthreads();
+        if (tid == 0) *p.status = s_err;
     }
 }
 

@@ -35,13 +35,15 @@ struct EncodeParams {
     uint64_t capacity;
     uint32_t num_tiles;      // scan tiles
     unsigned long long* out_bytes;
-    int* status;             // nullable
+    int* status;             // nullable; written once, by the finish kernel
     uint64_t wait_limit_ns;
     int vec;                 // 1 when the aligned vector path may be used
-    uint32_t grid;           // persistent kernels: blocks in the launch
+    uint32_t grid;           // blocks of the encode kernel's launch
     uint32_t skip_first;     // test hook: a wait that never completes
     int contig;              // codebook is 16 consecutive exponents cb[0]..cb[0]+15
     uint32_t* ws_count;      // workspace: escapes per scan tile
+    int* ws_err;             // workspace: each BF16 encode block's error code (0 = none); the
+                             // finish kernel's last block turns them into *status
     uint16_t* ws_unit;       // workspace: escapes per 1,024-element unit, kUnitsPerScan per scan tile
     uint8_t* ws_rec;         // workspace: staged records, ws_cap per scan tile
     uint32_t ws_cap;         // records staged per scan tile
@@ -104,6 +106,9 @@ constexpr uint32_t kStageRecsE5 = 1024;
 // than it stages, the encoders record each unit's escape count, so that the
 // remaining records can be re-derived unit by unit, in parallel, at known
 // offsets.  The workspace has room for 32 counts per scan tile.
+// The E5M2 encoder flags an error of its scan tile (a bad page id or device
+// codebook) in bit 31 of the tile's escape count, which never exceeds 2^15.
+constexpr uint32_t kCountError = 0x80000000u;
 constexpr uint32_t kUnitElems = 1024;
 constexpr uint32_t kUnitElemsE5 = 4096;
 constexpr uint32_t kUnitsPerScan = kScanTile / kUnitElems;  // 32

@@ -45,11 +45,11 @@ def test_encoded_size_matches_oracle(S, orc):
 
 
 def test_workspace_size(S):
-    # Per 32,768-element scan tile: a u32 count (a 16-byte aligned block of
-    # them), 32 u16 counts of its 1,024-element units, and 2,048 (BF16) or
-    # 1,024 (E5M2) staged 3-byte records.
+    # Per 32,768-element scan tile: a u32 count and an i32 error word (each
+    # a 16-byte aligned block), 32 u16 unit counts, and 2,048 (BF16) or 1,024
+    # (E5M2) staged 3-byte records.
     for dt, staged in ((S.SZ_BF16, 2048), (S.SZ_FP8_E5M2, 1024)):
-        ws = lambda tiles: ((4 * tiles + 15) // 16) * 16 + 64 * tiles + 3 * staged * tiles
+        ws = lambda tiles: 2 * (((4 * tiles + 15) // 16) * 16) + 64 * tiles + 3 * staged * tiles
         assert S.sz_workspace_size(dt, 0) == ws(1)
         assert S.sz_workspace_size(dt, 32768) == ws(1)
         assert S.sz_workspace_size(dt, 32769) == ws(2)

@@ -203,3 +203,32 @@ def test_scan_tiles_beyond_staging(orc, kind, seed, densities):
     cb = CB_MID if kind == "bf16" else CB_E5_MID
     x = _unit_density_tensor(kind, n, seed, densities)
     roundtrip_vs_oracle(orc, kind, cb, x)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e5m2"])
+def test_encode_status_needs_no_reset(orc, kind):
+    """The encode writes its status word once, at its end, from what every
+    block of the encode reported: whatever the word held before (another
+    call's error, garbage) does not matter, and an error of one call does not
+    stay for the next call on the same word and workspace."""
+    from lossless_kv_cache_bf16_gb300 import splitzip as S
+
+    dt = G.DT[kind]
+    cb = CB_MID if kind == "bf16" else CB_E5_MID
+    x = _unit_density_tensor(kind, 3 * 65536 + 777, 41, (0.0, 0.01, 0.5))
+    n = G.elements(dt, x)
+    want = orc.encode(ODT[kind], cb, G.as_bytes(x))
+    ws = torch.empty(S.sz_workspace_size(dt, n), dtype=torch.uint8, device="cuda")
+    ob = torch.zeros(1, dtype=torch.int64, device="cuda")
+    st = torch.empty(1, dtype=torch.int32, device="cuda")
+    full = torch.empty(S.sz_encoded_size(dt, n, n), dtype=torch.uint8, device="cuda")
+    short = torch.empty(S.sz_encoded_size(dt, n, 0) + 30, dtype=torch.uint8, device="cuda")
+    for before, out, expect in ((-1, full, S.SZ_OK), (99, short, S.SZ_ERR_CAPACITY), (S.SZ_ERR_CAPACITY, full, S.SZ_OK),
+                                (S.SZ_ERR_TIMEOUT, short, S.SZ_ERR_CAPACITY), (0, full, S.SZ_OK)):
+        st.fill_(before)
+        S.sz_encode(dt, cb, x, out, ob, st, ws)
+        torch.cuda.synchronize()
+        assert int(st.item()) == expect, (before, expect)
+        assert int(ob.item()) == want.size
+        if expect == S.SZ_OK:
+            assert np.array_equal(out[: want.size].cpu().numpy(), want)
