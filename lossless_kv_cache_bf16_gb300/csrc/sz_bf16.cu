@@ -201,33 +201,30 @@ __device__ __forceinline__ void load_groups_global(const EncodeParams& p, uint64
 }
 
 // Writes the records of lane's escapes among one warp's 1,024 elements
-// starting at element `base`: record index first + off[k] + rank in group.
-// One loop over all of the lane's escape bits (group k = bit / 8), so the
-// warp iterates as often as its busiest lane has escapes, not once per group.
+// starting at element `base`: record index first + off[k] + rank in group k,
+// for indexes below cap.  One loop per group, so that each group's exponent
+// words and offset are fixed registers: an iteration is a handful of
+// instructions, and the warp iterates as often as the busiest lane of each
+// group has escapes.
 __device__ __forceinline__ void emit_records(uint64_t base, uint32_t lane, const uint32_t (&ex)[4][2],
-                                             const uint32_t (&esc)[4], const uint32_t (&off)[4], uint64_t first,
-                                             uint8_t* dst, uint64_t limit) {
-    const uint32_t all = esc[0] | (esc[1] << 8) | (esc[2] << 16) | (esc[3] << 24);
-    uint32_t m = all;
+                                             const uint32_t (&esc)[4], const uint32_t (&off)[4], uint32_t first,
+                                             uint8_t* dst, uint32_t cap) {
     const uint32_t pos_base = (uint32_t)(base + lane * 8u) & 0xFFFFu;  // a warp never straddles a chunk
-    while (m) {
-        const uint32_t b = __ffs(m) - 1;
-        m &= m - 1;
-        const uint32_t k = b >> 3, jj = b & 7u;
-        const uint32_t offk = k < 2 ? (k == 0 ? off[0] : off[1]) : (k == 2 ? off[2] : off[3]);
-        const uint32_t before = __popc(all & ((1u << b) - 1u) & (0xFFu << (8 * k)));  // earlier in the group
-        // Exponent of element jj of group k: byte jj & 3 of its exponent word.
-        const bool hi = jj >= 4;
-        const uint32_t w0 = hi ? ex[0][1] : ex[0][0], w1 = hi ? ex[1][1] : ex[1][0];
-        const uint32_t w2 = hi ? ex[2][1] : ex[2][0], w3 = hi ? ex[3][1] : ex[3][0];
-        const uint32_t word = k < 2 ? (k == 0 ? w0 : w1) : (k == 2 ? w2 : w3);
-        const uint32_t e = (word >> (8 * (jj & 3u))) & 0xFFu;
-        const uint32_t pos = pos_base + k * 256u + jj;
-        const uint64_t at = 3ull * (first + offk + before);
-        if (at + 3 <= limit) {
-            dst[at] = (uint8_t)pos;
-            dst[at + 1] = (uint8_t)(pos >> 8);
-            dst[at + 2] = (uint8_t)e;
+#pragma unroll
+    for (uint32_t k = 0; k < 4; k++) {
+        uint32_t m = esc[k], idx = first + off[k];
+        while (m) {
+            const uint32_t jj = __ffs(m) - 1;
+            m &= m - 1;
+            // Byte jj of the group's exponent bytes (the low byte is stored).
+            const uint32_t e = __byte_perm(ex[k][0], ex[k][1], jj);
+            const uint32_t pos = pos_base + k * 256u + jj;
+            if (idx < cap) {
+                dst[3 * idx] = (uint8_t)pos;
+                dst[3 * idx + 1] = (uint8_t)(pos >> 8);
+                dst[3 * idx + 2] = (uint8_t)e;
+            }
+            idx++;
         }
     }
 }
@@ -375,7 +372,7 @@ __device__ __forceinline__ void encode_bf16_body(const EncodeParams& p, const ui
             // that scan tile's records from the input.  They are gathered in
             // shared memory and leave once per scan tile, in 16-byte stores.
             if (warp_total && run + warp_off < p.ws_cap)
-                emit_records(wbase, lane, ex, esc, off, run + warp_off, S.rec, 3ull * p.ws_cap);
+                emit_records(wbase, lane, ex, esc, off, run + warp_off, S.rec, p.ws_cap);
             run += sub_esc;
         }
         if (aborted) break;  // block-uniform
