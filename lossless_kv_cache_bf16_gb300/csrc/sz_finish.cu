@@ -112,9 +112,15 @@ __device__ __forceinline__ void put_full_group(uint8_t* buf, uint32_t a, uint32_
 // unit is kU pieces of 16 bytes per lane (piece u * 32 + lane), all loaded
 // before any is examined.  buf: the warp's staging buffer (kStageBytes + 32
 // bytes, 16-byte aligned), which holds the 1,024 records a unit can have.
+// cb_test (shared memory): {the codebook is cb0 .. cb0 + 15, cbk}.  With a
+// contiguous codebook membership is tested with byte arithmetic instead of
+// lookups in s_member (a byte per exponent, whose random banks conflict);
+// cbk is (256 - cb0) mod 256 (BF16) or cb0 (E5M2) in every byte.
+// Not inlined: it runs only for scan tiles beyond their staging, and kept
+// apart it leaves the registers of the kernel's common path alone.
 template <bool BF16, bool PAGED>
-__device__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
-                                  const uint8_t* s_member, uint8_t* buf) {
+__device__ __noinline__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
+                                               const uint8_t* s_member, const uint32_t* cb_test, uint8_t* buf) {
     constexpr uint32_t kPer = BF16 ? 8u : 16u;  // elements in 16 bytes
     constexpr uint32_t kEsize = BF16 ? 2u : 1u;
     constexpr uint32_t kU = kUnitElems / (32 * kPer);  // 4 (BF16) or 2 (E5M2)
@@ -165,9 +171,30 @@ __device__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_
             for (uint32_t g = 0; g < 4; g++) ex[g] = (w[u][g] >> 2) & 0x1F1F1F1Fu;
         }
         uint32_t mask = 0;
+        if (cb_test[0]) {
+            const uint32_t cbk = cb_test[1];
+            // Per byte x = 128 + (exponent - cb0 modulo 256): the element is
+            // in the codebook iff x lies in 128 .. 143, that is bit 7 set and
+            // bits 4..6 clear.
 #pragma unroll
-        for (uint32_t j = 0; j < kPer; j++)
-            if (j < valid[u] && !s_member[(ex[j >> 2] >> (8 * (j & 3))) & 0xFFu]) mask |= 1u << j;
+            for (uint32_t g = 0; g < kPer / 4; g++) {
+                const uint32_t e = ex[g];
+                // BF16: a byte-wise add of (256 - cb0) without carries between
+                // bytes (low 7 bits added, bit 7 by exclusive or), then bit 7
+                // flipped.  E5M2: exponents <= 31 and cb0 <= 16 leave no
+                // borrow.
+                const uint32_t x = BF16 ? (((e & 0x7F7F7F7Fu) + (cbk & 0x7F7F7F7Fu)) ^ ((e ^ cbk) & 0x80808080u)) ^ 0x80808080u
+                                        : (e | 0x80808080u) - cbk;
+                const uint32_t hi3 = ((x & 0x70707070u) + 0x70707070u) & 0x80808080u;  // bits 4..6 not all clear
+                const uint32_t out = (~x | hi3) & 0x80808080u;                            // bit 7: an escape
+                mask |= (((out >> 7) * 0x00204081u) >> 21 & 0xFu) << (4 * g);            // bits 0, 8, 16, 24 -> 0..3
+            }
+            if (valid[u] < kPer) mask &= (1u << valid[u]) - 1u;
+        } else {
+#pragma unroll
+            for (uint32_t j = 0; j < kPer; j++)
+                if (j < valid[u] && !s_member[(ex[j >> 2] >> (8 * (j & 3))) & 0xFFu]) mask |= 1u << j;
+        }
         const uint32_t c = __popc(mask);
         uint32_t x = c;
 #pragma unroll
@@ -226,10 +253,17 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint32_t T = p.num_tiles, F = gridDim.x;
     const uint32_t t0 = (uint32_t)((uint64_t)blockIdx.x * T / F), t1 = (uint32_t)((uint64_t)(blockIdx.x + 1) * T / F);
+    // The re-derivation's membership test: {contiguous codebook, its constant}
+    // (see rederive_unit).
+    __shared__ uint32_t s_cb_test[2];
     {
         uint8_t cb[16];
         bool contig;
         load_codebook(p.cb, p.cb_dev, BF16 ? 256u : 32u, cb, contig);
+        if (tid == 0) {
+            s_cb_test[0] = contig;
+            s_cb_test[1] = 0x01010101u * (BF16 ? (256u - cb[0]) & 0xFFu : (uint32_t)cb[0]);
+        }
         uint32_t member = 0;
 #pragma unroll
         for (int k = 0; k < kCodes; k++) member |= cb[k] == tid;
@@ -430,7 +464,7 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
                     const uint32_t at = f + done;  // tile-local rank of the step's first escape
                     const uint32_t skip = p.ws_cap > at ? p.ws_cap - at : 0u;
                     const uint64_t dst = p.L.rec_off + 3ull * ((uint64_t)s_prefix[j] + at + skip);
-                    done += rederive_unit<BF16, PAGED>(p, tbase + (uint64_t)u * kUnit + e, skip, dst, s_member, stage);
+                    done += rederive_unit<BF16, PAGED>(p, tbase + (uint64_t)u * kUnit + e, skip, dst, s_member, s_cb_test, stage);
                 }
             }
         }
