@@ -116,10 +116,8 @@ __device__ __forceinline__ void put_full_group(uint8_t* buf, uint32_t a, uint32_
 // contiguous codebook membership is tested with byte arithmetic instead of
 // lookups in s_member (a byte per exponent, whose random banks conflict);
 // cbk is (256 - cb0) mod 256 (BF16) or cb0 (E5M2) in every byte.
-// Not inlined: it runs only for scan tiles beyond their staging, and kept
-// apart it leaves the registers of the kernel's common path alone.
 template <bool BF16, bool PAGED>
-__device__ __noinline__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
+__device__ __forceinline__ uint32_t rederive_unit(const EncodeParams& p, uint64_t ubase, uint32_t skip, uint64_t dst,
                                                const uint8_t* s_member, const uint32_t* cb_test, uint8_t* buf) {
     constexpr uint32_t kPer = BF16 ? 8u : 16u;  // elements in 16 bytes
     constexpr uint32_t kEsize = BF16 ? 2u : 1u;
@@ -237,6 +235,32 @@ __device__ __noinline__ uint32_t rederive_unit(const EncodeParams& p, uint64_t u
     copy_out(buf, before > skip ? 3 * (before - skip) : 0u, p.out, dst, p.capacity, lane, 32);
     __syncwarp();  // buf is reused by the warp's next unit
     return before;  // the escapes of these 1,024 elements
+}
+
+// The units of one heavy scan tile that this warp takes (every kFinWarps-th
+// of those set in `units`, from the lowest): each unit's records of
+// tile-local rank >= ws_cap go out, in steps of 1,024 elements (one step
+// for a BF16 unit).  ufirst (lane u): the tile's escapes before unit u;
+// prefix: the tile's first record index in the stream.  Not inlined: it
+// runs only for scan tiles beyond their staging, and kept apart it leaves
+// the registers of the kernel's common path alone.
+template <bool BF16, bool PAGED>
+__device__ __noinline__ void rederive_units(const EncodeParams& p, uint64_t tbase, uint32_t units, uint32_t ufirst,
+                                            uint32_t prefix, const uint8_t* s_member, const uint32_t* cb_test,
+                                            uint8_t* stage) {
+    constexpr uint32_t kUnit = BF16 ? kUnitElems : kUnitElemsE5;
+    while (units) {
+        const uint32_t u = __ffs(units) - 1;
+        for (uint32_t q = 0; q < kFinWarps && units; q++) units &= units - 1;  // the next one is 8 on
+        const uint32_t f = __shfl_sync(0xFFFFFFFFu, ufirst, u);
+        uint32_t done = 0;  // escapes of the unit's earlier steps
+        for (uint32_t e = 0; e < kUnit; e += kUnitElems) {
+            const uint32_t at = f + done;  // tile-local rank of the step's first escape
+            const uint32_t skip = p.ws_cap > at ? p.ws_cap - at : 0u;
+            const uint64_t dst = p.L.rec_off + 3ull * ((uint64_t)prefix + at + skip);
+            done += rederive_unit<BF16, PAGED>(p, tbase + (uint64_t)u * kUnit + e, skip, dst, s_member, cb_test, stage);
+        }
+    }
 }
 
 }  // namespace
@@ -453,20 +477,7 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
                 units &= units - 1;
                 skip_units--;
             }
-            while (units) {
-                const uint32_t u = __ffs(units) - 1;
-                for (uint32_t q = 0; q < kFinWarps && units; q++) units &= units - 1;  // the next one is 8 on
-                const uint32_t f = __shfl_sync(0xFFFFFFFFu, ufirst, u);
-                // The unit's records of tile-local rank >= ws_cap go out, in
-                // steps of 1,024 elements (one step for a BF16 unit).
-                uint32_t done = 0;  // escapes of the unit's earlier steps
-                for (uint32_t e = 0; e < kUnit; e += kUnitElems) {
-                    const uint32_t at = f + done;  // tile-local rank of the step's first escape
-                    const uint32_t skip = p.ws_cap > at ? p.ws_cap - at : 0u;
-                    const uint64_t dst = p.L.rec_off + 3ull * ((uint64_t)s_prefix[j] + at + skip);
-                    done += rederive_unit<BF16, PAGED>(p, tbase + (uint64_t)u * kUnit + e, skip, dst, s_member, s_cb_test, stage);
-                }
-            }
+            if (units) rederive_units<BF16, PAGED>(p, tbase, units, ufirst, s_prefix[j], s_member, s_cb_test, stage);
         }
         base += total;
         __syncthreads();
