@@ -41,7 +41,6 @@ constexpr uint32_t kPieceRecs = 1024;                     // records a warp re-d
 constexpr uint32_t kStageBytes = 3 * kPieceRecs;          // a warp's staging buffer
 constexpr uint32_t kHalfRecs = kPieceRecs / 2;            // staged records per half of it
 constexpr uint32_t kHalfStride = 3 * kHalfRecs + 16;      // second half: 16-byte aligned, a gap after the first
-constexpr uint32_t kHalfLoads = 3 * kHalfRecs / 512;      // 16-byte loads per lane for a half
 static_assert((3 * kHalfRecs) % 512 == 0 && kHalfStride % 16 == 0, "whole warp-wide 16-byte loads");
 static_assert(kHalfStride + 3 * kHalfRecs + 16 <= kStageBytes + 32, "both halves, and the reads past them, fit");
 static_assert(kChunk % kScanTile == 0, "scan tiles must not straddle chunks");
@@ -74,6 +73,25 @@ __device__ __forceinline__ void copy_out(const uint8_t* src, uint32_t nbytes, ui
     for (uint32_t e = tid; e < head + tail; e += step) {
         const uint32_t off = e < head ? e : head + 16 * pieces + (e - head);
         if (dst + off < capacity) o[off] = src[off];
+    }
+}
+
+// One warp copies a staged run of c records (run: 16-byte aligned, readable
+// in whole 16-byte pieces up to 3 c rounded up) to out + dst, 1,024 records
+// at a time through buf (the warp's whole staging buffer): every piece of a
+// round is in flight at once.  Not inlined, like the re-derivation: it
+// serves only runs longer than half the buffer.
+__device__ __noinline__ void copy_run(const uint8_t* run, uint32_t c, uint8_t* out, uint64_t dst, uint64_t capacity,
+                                      uint8_t* buf) {
+    const uint32_t lane = threadIdx.x & 31u;
+    for (uint32_t q = 0; q < c; q += kPieceRecs) {
+        const uint32_t nbytes = 3 * min(kPieceRecs, c - q);
+        for (uint32_t b = 16 * lane; b < nbytes; b += 512) cp_async16(buf + b, run + 3ull * q + b, 16);
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncwarp();
+        copy_out(buf, nbytes, out, dst + 3ull * q, capacity, lane, 32);
+        __syncwarp();  // buf is reused next
     }
 }
 
@@ -389,8 +407,8 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
         // two halves of 512 records: a run that fits one (the common case)
         // arrives there by asynchronous copies while the warp writes out the
         // run before it, so a warp's runs cost one memory round trip instead
-        // of one each.  A longer run goes through its half 512 records at a
-        // time.
+        // of one each.  A longer run takes the whole buffer, 1,024 records
+        // (one round trip) at a time.
         auto fits = [&](uint32_t j) { return min(s_count[j], p.ws_cap) <= kHalfRecs; };
         auto prefetch = [&](uint32_t j, uint32_t h) {  // whole warp; one commit group
             const uint32_t nbytes = 3 * min(s_count[j], p.ws_cap);
@@ -408,33 +426,24 @@ __global__ void __launch_bounds__(kFinThreads, 4) finish_kernel(const EncodePara
             const uint64_t dst = p.L.rec_off + 3ull * s_prefix[j];
             const uint32_t jn = j + kFinWarps;
             const bool next = jn < batch && fits(jn);
-            if (next) prefetch(jn, h ^ 1u);
-            uint8_t* const half = stage + h * kHalfStride;
             if (ready) {
+                if (next) prefetch(jn, h ^ 1u);
                 if (next)
                     cp_async_wait_group<1>();
                 else
                     cp_async_wait_all();
                 __syncwarp();
-                copy_out(half, 3 * c, p.out, dst, p.capacity, lane, 32);
+                copy_out(stage + h * kHalfStride, 3 * c, p.out, dst, p.capacity, lane, 32);
                 __syncwarp();  // the half is refilled two runs later
+                h ^= 1u;
             } else {
-                for (uint32_t q = 0; q < c; q += kHalfRecs) {
-                    const uint32_t nbytes = 3 * min(kHalfRecs, c - q);
-                    const uint4* src = reinterpret_cast<const uint4*>(p.ws_rec + (uint64_t)(c0 + j) * 3 * p.ws_cap + 3 * q);
-                    uint4 v[kHalfLoads];
-#pragma unroll
-                    for (uint32_t k = 0; k < kHalfLoads; k++)
-                        if (16 * lane + 512 * k < nbytes) v[k] = src[lane + 32 * k];
-#pragma unroll
-                    for (uint32_t k = 0; k < kHalfLoads; k++)
-                        if (16 * lane + 512 * k < nbytes) reinterpret_cast<uint4*>(half)[lane + 32 * k] = v[k];
-                    __syncwarp();
-                    copy_out(half, nbytes, p.out, dst + 3ull * q, p.capacity, lane, 32);
-                    __syncwarp();  // the half is reused next
-                }
+                // A longer run takes the whole buffer (no copy is in flight
+                // into it), 1,024 records at a time; the next run is fetched
+                // afterwards.
+                copy_run(p.ws_rec + (uint64_t)(c0 + j) * 3 * p.ws_cap, c, p.out, dst, p.capacity, stage);
+                if (next) prefetch(jn, 0);
+                h = 0;
             }
-            h ^= 1u;
             ready = next;
         }
         if (any_heavy) __syncthreads();  // s_heavy complete (block-uniform)
