@@ -121,6 +121,29 @@ def test_all_escape_and_no_escape(orc):
     assert s.size == 7 * ((n + 7) // 8) + 3 * n + 16 + 8 * 4
 
 
+@pytest.mark.parametrize("escapes", ["quarter_minus_one", "quarter", "sixty_percent"])
+def test_escape_dense_streams(orc, escapes):
+    """Streams in which a quarter or more of the elements are escapes, at
+    exact counts spread uniformly over four and a fraction chunks: the
+    stream is the oracle's byte for byte, and decoding gives the input back
+    bit for bit, also into an output that is only 2-byte aligned (no vector
+    stores) from an input at an odd address."""
+    n = 4 * 65536 + 400                      # a multiple of 4: a quarter is exact
+    k = {"quarter_minus_one": n // 4 - 1, "quarter": n // 4, "sixty_percent": (3 * n) // 5}[escapes]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(41)
+    x = _gauss(n, scale_sigma=0.1, seed=42).view(torch.int16).to(torch.int32) & 0xFFFF
+    inside = torch.randint(120, 136, (n,), generator=g, device="cuda", dtype=torch.int32)
+    x = (x & 0x807F) | (inside << 7)
+    idx = torch.randperm(n, generator=g, device="cuda")[:k]
+    outside = torch.randint(10, 110, (k,), generator=g, device="cuda", dtype=torch.int32)
+    x[idx] = (x[idx] & 0x807F) | (outside << 7)
+    x = x.to(torch.int16).view(torch.bfloat16)
+    s = roundtrip_vs_oracle(orc, "bf16", CB_MID, x)
+    assert s.size == n + n // 2 + 16 + 8 * 5 + 3 * k
+    roundtrip_vs_oracle(orc, "bf16", CB_MID, x, dec_out_offset=2, dec_in_offset=1)
+
+
 def test_calibration_matches_oracle(orc):
     from lossless_kv_cache_bf16_gb300 import workloads as W
 
