@@ -8,21 +8,26 @@
 //    per thread), then scans its own counts in batches of 256, giving every
 //    scan tile its escape offset;
 //  * one warp per scan tile copies the staged records to offset * 3 in the
-//    escape stream: 16-byte loads of the whole staged run into shared memory,
-//    then aligned 4-byte stores (a funnel shift realigns the bytes) with at
-//    most 3 single bytes at either end;
+//    escape stream: asynchronous 16-byte copies of the staged run into
+//    shared memory (the next run's while this one leaves), then aligned
+//    16-byte stores (funnel shifts realign the bytes) with at most 15 single
+//    bytes at either end;
 //  * a scan tile with more than ws_cap escapes has its ws_cap staged records
 //    copied the same way; the rest are re-derived from the input unit by
 //    unit (1,024 elements each for BF16, 4,096 for E5M2, whose escape counts
 //    the encoders also left in the workspace, so every unit's first record
-//    index is known).  The
-//    units holding unstaged records are spread over all warps of the block:
-//    a warp loads its unit with all 16-byte loads in flight, finds and ranks
-//    the escapes (a warp scan), assembles their records in its staging
-//    buffer and writes them with the same aligned word stores;
+//    index is known).  The units holding unstaged records are spread over
+//    all warps of the block: a warp loads its unit with all 16-byte loads in
+//    flight, finds the escapes (byte arithmetic for a contiguous codebook,
+//    a membership table otherwise) and ranks them (a warp scan), assembles
+//    their records in its staging buffer and writes them with the same
+//    aligned stores.  This path runs out of line, one call per heavy scan
+//    tile and warp, so that it leaves the common path's registers alone;
 //  * a chunk's last scan tile writes the chunk's header (offset = escapes
 //    before the chunk, count = escapes in it); the last scan tile writes the
-//    stream size.
+//    stream size;
+//  * the last block writes the call's status word once: the largest error
+//    code of the encode blocks and its own capacity check.
 // Escapes are (u16 position in the 65,536-element chunk, u8 exponent) pairs
 // in element order (SplitZip technical summary, gist.science/es,
 // "Metodologia: SplitZip" > "Flujo de Escape").
