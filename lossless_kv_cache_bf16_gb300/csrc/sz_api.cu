@@ -370,6 +370,10 @@ sz_status sz_debug_encode_stalled(sz_dtype dt, const sz_codebook* h_cb, const vo
                        wait_limit_ns, stream);
 }
 
+// Streams with at least one escape per kDenseDecodeDiv elements count as
+// dense in escapes for the decoder (a measured crossover: 2.5%).
+constexpr uint64_t kDenseDecodeDiv = 40;
+
 sz_status decode_impl(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, void* d_out, int* d_status,
                       cudaStream_t stream, PageMap pm) {
     if (!dtype_ok(dt) || !d_in || (n > 0 && !d_out) || (uint64_t)n >= (1ull << 32)) return SZ_ERR_INVALID_ARG;
@@ -398,7 +402,11 @@ sz_status decode_impl(sz_dtype dt, const void* d_in, size_t in_bytes, size_t n, 
         const cudaError_t err = cudaMemsetAsync(d_status, 0, sizeof(int), stream);
         if (err != cudaSuccess) return from_cuda(err);
     }
-    return from_cuda(dt == SZ_BF16 ? launch_decode_bf16(p, stream) : launch_decode_e5m2(p, stream));
+    // A BF16 stream with escapes in at least 1 / kDenseDecodeDiv of its
+    // elements (known here from its size) takes the decoder variant that
+    // computes exponents by byte adds (decode_bf16_kernel's ADDS).
+    const bool adds = dt == SZ_BF16 && !pm.ids && n_esc * kDenseDecodeDiv >= n;
+    return from_cuda(dt == SZ_BF16 ? launch_decode_bf16(p, stream, false, adds) : launch_decode_e5m2(p, stream));
 }
 
 // A page pool: page_elems a power of two in [16, 2^30], the pool 16-byte

@@ -18,6 +18,7 @@
 #include "sz_records.cuh"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace sz {
 
@@ -488,7 +489,13 @@ static_assert(sizeof(DecodeSmem) <= 56 * 1024, "decode shared memory");
 // PAGED: the output is a paged tensor (DecodeParams::pm).
 // TOP8: the Top-8 layout of the codebook ablation (3-bit codes, 8 per 3
 // bytes, an 8-entry codebook); everything else is shared.
-template <bool PAGED, bool TOP8 = false>
+// ADDS: for streams dense in escapes (the host picks it from the escape
+// count): with a codebook of 16 consecutive exponents cb0 .. cb0 + 15, whole
+// tiles take their exponents from code + cb0 instead of the 256-entry table.
+// A table lookup per two elements reads shared memory at random banks, and
+// where the escape tables are busy too that costs more than the adds; on
+// sparse streams the table measured faster, so they keep it.
+template <bool PAGED, bool TOP8 = false, bool ADDS = false>
 __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const DecodeParams p) {
     constexpr uint32_t kCodeBytes = TOP8 ? kBf16Tile / 8 * 3 : kBf16Tile / 2;  // code bytes per tile
     constexpr int kEntries = TOP8 ? 8 : kCodes;
@@ -525,7 +532,15 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
         for (int k = 0; k < kEntries; k++) dup |= (k != (int)tid) && cb[k] == cb[tid];
         if (dup) S.bad = 1;  // ordered before the reads by the barriers below
     }
-    __syncthreads();
+    // Consecutive codebook (no wrap): exponent = code + cb0 (ADDS only).
+    bool contig = false;
+    if (ADDS && !TOP8) {
+        const bool mine = tid >= (uint32_t)kCodes || ((uint32_t)cb[0] + 15u <= 255u && cb[tid] == cb[0] + tid);
+        contig = __syncthreads_and(mine) != 0;
+    } else {
+        __syncthreads();
+    }
+    const uint32_t add7 = ((uint32_t)cb[0] * 0x10001u) << 7;  // cb0 at bits 7 and 23
 
     auto full_tile = [&](uint32_t t) { return tma && (uint64_t)(t + 1) * kBf16Tile <= n; };
     auto issue = [&](uint32_t slot, uint32_t t) {  // thread 0 only
@@ -690,14 +705,26 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
             S.bits[buf][tid] = 0;  // only this thread reads this word
             const uint32_t qt = warp * 1024u + lane * 8u;  // the thread's first element in the tile
             // Group k of the thread: sm bytes (2 words), nibbles (1 word) -> 4 output words.
-            auto decode_group = [&](int k, uint2 smv, uint32_t nibv, uint32_t (&y)[4]) {
+            // CONTIG (a std::bool_constant): exponents by byte adds, else by
+            // the table.
+            auto decode_group = [&](auto CONTIG, int k, uint2 smv, uint32_t nibv, uint32_t (&y)[4]) {
+                // The low and the high code of every nibble byte, one per byte.
+                const uint32_t c_lo = nibv & 0x0F0F0F0Fu, c_hi = (nibv >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     // Each sm byte twice per 16-bit half: the high copy keeps the
                     // sign (bit 15), the low copy the mantissa (bits 0..6).
                     const uint32_t smw = q < 2 ? smv.x : smv.y;
                     const uint32_t tt = __byte_perm(smw, 0, (q & 1) ? 0x3322 : 0x1100);
-                    y[q] = (tt & 0x807F807Fu) | S.lut[TOP8 ? (nibv >> (6 * q)) & 63u : (nibv >> (8 * q)) & 0xFFu];
+                    uint32_t e;
+                    if (decltype(CONTIG)::value) {
+                        // Byte q of c_lo and of c_hi into bytes 0 and 2; bytes 1
+                        // and 3 are the (zero) sign of a code byte.
+                        e = prmt(c_lo, c_hi, 0xC480u + 0x1111u * q) * 128u + add7;
+                    } else {
+                        e = S.lut[TOP8 ? (nibv >> (6 * q)) & 63u : (nibv >> (8 * q)) & 0xFFu];
+                    }
+                    y[q] = (tt & 0x807F807Fu) | e;
                 }
                 const uint32_t gb = (bits >> (8 * k)) & 0xFFu;
                 if (gb) {
@@ -711,8 +738,8 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     }
                 }
             };
-            if (full_tile(t)) {
-                // Whole tile in the stage slot: no bounds to check.
+            // Whole tile in the stage slot: no bounds to check.
+            auto whole_tile = [&](auto CONTIG) {
                 const RunOffset<PAGED> tile_off(p.pm, base, 13, 2, p.status);  // 8,192-element tile
                 const uint8_t* ssm = S.sm[slot] + qt;
                 const uint8_t* snb = S.nib[slot] + qt / 2;
@@ -729,12 +756,18 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                     } else {
                         codes = *reinterpret_cast<const uint32_t*>(snb + k * 128);
                     }
-                    decode_group(k, *reinterpret_cast<const uint2*>(ssm + k * 256), codes, y);
+                    decode_group(CONTIG, k, *reinterpret_cast<const uint2*>(ssm + k * 256), codes, y);
                     // A group of 8 never straddles a page; a tile in one page
                     // takes one lookup.
                     uint8_t* dst = PAGED ? p.out + tile_off.at(p.pm, base, qt + k * 256u, 2, p.status) : o + k * 512;
                     st_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
                 }
+            };
+            if (full_tile(t)) {
+                if (ADDS && contig)
+                    whole_tile(std::true_type{});
+                else
+                    whole_tile(std::false_type{});
             } else {
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
@@ -760,7 +793,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) decode_bf16_kernel(const Decod
                         nibv = nb;
                     }
                     uint32_t y[4];
-                    decode_group(k, smv, nibv, y);
+                    decode_group(std::false_type{}, k, smv, nibv, y);
                     uint8_t* dst = p.out + (cnt ? elem_offset<PAGED>(p.pm, i0, 2, p.status) : 2 * i0);
                     if (p.vec && cnt == 8) {
                         st_v4(dst, make_uint4(y[0], y[1], y[2], y[3]));
@@ -824,9 +857,12 @@ cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s) {
     return launch_finish(q, true, s);
 }
 
-cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8) {
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8, bool adds) {
     const size_t smem = sizeof(DecodeSmem);
-    auto kern = top8 ? decode_bf16_kernel<false, true> : p.pm.ids ? decode_bf16_kernel<true> : decode_bf16_kernel<false>;
+    auto kern = top8      ? decode_bf16_kernel<false, true>
+                : p.pm.ids ? decode_bf16_kernel<true>
+                : adds     ? decode_bf16_kernel<false, false, true>
+                           : decode_bf16_kernel<false>;
     int sms = 0, per_sm = 0;
     cudaError_t err = kernel_fit((const void*)kern, kDecThreads, smem, &sms, &per_sm);
     if (err != cudaSuccess) return err;

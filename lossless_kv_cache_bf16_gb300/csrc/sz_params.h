@@ -142,7 +142,8 @@ cudaError_t kernel_fit(const void* kern, int threads, size_t smem, int* sms, int
 
 cudaError_t launch_encode_bf16(const EncodeParams& p, cudaStream_t s);
 // top8: the Top-8 layout of the codebook ablation (see sz_ablation_decode).
-cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8 = false);
+// adds: the stream is dense in escapes (decode_bf16_kernel's ADDS).
+cudaError_t launch_decode_bf16(const DecodeParams& p, cudaStream_t s, bool top8 = false, bool adds = false);
 cudaError_t launch_encode_e5m2(const EncodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_e5m2(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_histogram(const HistogramParams& p, cudaStream_t s);
