@@ -121,15 +121,18 @@ def test_all_escape_and_no_escape(orc):
     assert s.size == 7 * ((n + 7) // 8) + 3 * n + 16 + 8 * 4
 
 
-@pytest.mark.parametrize("escapes", ["quarter_minus_one", "quarter", "sixty_percent"])
+@pytest.mark.parametrize("escapes", ["fortieth_minus_one", "fortieth", "quarter", "sixty_percent"])
 def test_escape_dense_streams(orc, escapes):
-    """Streams in which a quarter or more of the elements are escapes, at
-    exact counts spread uniformly over four and a fraction chunks: the
-    stream is the oracle's byte for byte, and decoding gives the input back
-    bit for bit, also into an output that is only 2-byte aligned (no vector
-    stores) from an input at an odd address."""
-    n = 4 * 65536 + 400                      # a multiple of 4: a quarter is exact
-    k = {"quarter_minus_one": n // 4 - 1, "quarter": n // 4, "sixty_percent": (3 * n) // 5}[escapes]
+    """Streams with escapes in 1/40 of the elements and more, at exact counts
+    spread uniformly over four and a fraction chunks.  From 1/40 on the
+    decoder runs its escape-dense variant (exponents by byte adds for a
+    contiguous codebook); one escape fewer keeps the other.  On both sides
+    the stream is the oracle's byte for byte, and decoding gives the input
+    back bit for bit, also into an output that is only 2-byte aligned (no
+    vector stores) from an input at an odd address."""
+    n = 4 * 65536 + 416                      # a multiple of 40: 1/40 is exact
+    k = {"fortieth_minus_one": n // 40 - 1, "fortieth": n // 40, "quarter": n // 4,
+         "sixty_percent": (3 * n) // 5}[escapes]
     g = torch.Generator(device="cuda")
     g.manual_seed(41)
     x = _gauss(n, scale_sigma=0.1, seed=42).view(torch.int16).to(torch.int32) & 0xFFFF
